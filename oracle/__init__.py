@@ -1,0 +1,254 @@
+"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle of the routed SwiGLU expert layer.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference arm may
+import this package.  The CUDA library never does, and the two share no code.
+
+This module is argument marshalling over ``mok_oracle.c`` (plain C, fp64 loops); every function
+cites, in the C source, the page passage it follows.  Arrays cross as numpy arrays:
+bf16 tensors as ``uint16`` bit patterns, E4M3 / E8M0 as ``uint8``.
+
+Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against closed forms,
+library routines (numpy / torch CPU float8 / torch autograd) or finite differences.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mok_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MT = 128  # GEMM row tile used for the padded expert-grouped layout
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mok_oracle.c`` into ``liboracle.so`` with gcc (OpenMP, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i64, i32 = ctypes.c_int64, ctypes.c_int32
+            lib.orc_bf16_value.restype = ctypes.c_double
+            lib.orc_bf16_value.argtypes = [ctypes.c_uint16]
+            lib.orc_e4m3_value.restype = ctypes.c_double
+            lib.orc_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_encode.restype = ctypes.c_uint8
+            lib.orc_e4m3_encode.argtypes = [ctypes.c_double]
+            lib.orc_e8m0_value.restype = ctypes.c_double
+            lib.orc_e8m0_value.argtypes = [ctypes.c_uint8]
+            lib.orc_mxfp8_quantize.restype = ctypes.c_int
+            lib.orc_mxfp8_quantize.argtypes = [P, i64, i64, P, P]
+            lib.orc_rpad_max.restype = i64
+            lib.orc_rpad_max.argtypes = [i64, i32, i32, i32]
+            lib.orc_schedule.restype = ctypes.c_int
+            lib.orc_schedule.argtypes = [i64, i32, i32, P, i32, i32, i32, P, P, P, P, i64, P, P, i64, P, P, i64,
+                                         P, P]
+            lib.orc_forward.restype = None
+            lib.orc_forward.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
+            lib.orc_backward.restype = None
+            lib.orc_backward.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P]
+            lib.orc_forward_tokens.restype = None
+            lib.orc_forward_tokens.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, i64, P, P]
+            lib.orc_backward_tokens.restype = None
+            lib.orc_backward_tokens.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i64, P, P, P]
+            lib.orc_dw_entries.restype = None
+            lib.orc_dw_entries.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, P, P]
+            lib.orc_num_threads.restype = ctypes.c_int
+            lib.orc_num_threads.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16, a.dtype
+    return a
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+# ----------------------------------------------------------------------------------------------
+# number formats
+# ----------------------------------------------------------------------------------------------
+def bf16_value(bits: int) -> float:
+    return _load().orc_bf16_value(int(bits))
+
+
+def bf16_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact value of bf16 bit patterns (vectorised form of ``orc_bf16_value``)."""
+    with np.errstate(invalid="ignore"):
+        return (_u16(a).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def e4m3_value(code: int) -> float:
+    return _load().orc_e4m3_value(int(code))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(_load().orc_e4m3_encode(float(v)))
+
+
+def e8m0_value(b: int) -> float:
+    return _load().orc_e8m0_value(int(b))
+
+
+def mxfp8_quantize(x_bf16: np.ndarray):
+    """MXFP8 (E4M3 + one E8M0 scale per 32 along the last axis) of a 2-D bf16 matrix."""
+    x = _u16(x_bf16)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    sc = np.empty((rows, cols // 32), np.uint8)
+    rc = _load().orc_mxfp8_quantize(_p(x), rows, cols, _p(q), _p(sc))
+    if rc != 0:
+        raise ValueError("cols must be a multiple of 32")
+    return q, sc
+
+
+def mxfp8_dequantize(q: np.ndarray, sc: np.ndarray) -> np.ndarray:
+    """Exact value of an MXFP8 matrix: e4m3 * 2^(e8m0 - 127)."""
+    lib = _load()
+    lut = np.array([lib.orc_e4m3_value(c) for c in range(256)], np.float64)
+    sv = np.array([lib.orc_e8m0_value(b) for b in range(256)], np.float64)
+    return lut[q] * np.repeat(sv[sc], 32, axis=1)
+
+
+# ----------------------------------------------------------------------------------------------
+# schedule
+# ----------------------------------------------------------------------------------------------
+def rpad_max(T: int, K: int, E: int, mt: int = MT) -> int:
+    return int(_load().orc_rpad_max(T, K, E, mt))
+
+
+def schedule(ids: np.ndarray, E: int, mb: int, MB: int, mt: int = MT) -> dict:
+    """Expert-grouped schedule of the flat slots of ``ids`` [T, K] (see ``orc_schedule``)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, K = ids.shape
+    R = T * K
+    cap = rpad_max(T, K, E, mt)
+    tcap = (R + mb - 1) // mb + E
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    poff = np.empty(E + 1, np.int32)
+    perm = np.empty(cap, np.int32)
+    inv = np.empty(max(R, 1), np.int32)
+    tiles = np.empty((tcap, 4), np.int32)
+    mblocks = np.empty((max(cap // mt, 1), 4), np.int32)
+    ntiles = np.zeros(1, np.int64)
+    nmb = np.zeros(1, np.int64)
+    rp = np.zeros(1, np.int64)
+    rc = _load().orc_schedule(T, K, E, _p(ids), mt, mb, MB, _p(counts), _p(offsets), _p(poff), _p(perm), cap,
+                              _p(inv), _p(tiles), tcap, _p(ntiles), _p(mblocks), mblocks.shape[0], _p(nmb), _p(rp))
+    if rc == 1:
+        raise ValueError("expert id out of range")
+    if rc == 2:
+        raise ValueError("capacity exceeded")
+    Rp = int(rp[0])
+    return dict(counts=counts, offsets=offsets, poff=poff, perm=perm[:Rp].copy(), inv=inv[:R].copy(),
+                tiles=tiles[: int(ntiles[0])].copy(), mblocks=mblocks[: int(nmb[0])].copy(), rpad=Rp)
+
+
+# ----------------------------------------------------------------------------------------------
+# layer forward / backward (fp64)
+# ----------------------------------------------------------------------------------------------
+def _layer_args(ids, s, x, Wg, Wu, Wd):
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    x, Wg, Wu, Wd = _u16(x), _u16(Wg), _u16(Wu), _u16(Wd)
+    T, K = ids.shape
+    E, I, H = Wg.shape
+    assert x.shape == (T, H) and Wu.shape == (E, I, H) and Wd.shape == (E, H, I) and s.shape == (T, K)
+    return ids, s, x, Wg, Wu, Wd, T, H, I, E, K
+
+
+def forward(ids, s, x, Wg, Wu, Wd, intermediates: bool = False):
+    """out [T, H] fp64; with ``intermediates`` also g, u, a [R, I] and y [R, H] in slot order."""
+    ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
+    R = T * K
+    out = np.empty((T, H), np.float64)
+    if intermediates:
+        g, u, a, y = (np.empty((R, I)), np.empty((R, I)), np.empty((R, I)), np.empty((R, H)))
+        ptrs = [_p(g), _p(u), _p(a), _p(y)]
+    else:
+        ptrs = [None] * 4
+    _load().orc_forward(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(out), *ptrs)
+    if intermediates:
+        return out, dict(g=g, u=u, a=a, y=y)
+    return out
+
+
+def backward(ids, s, x, Wg, Wu, Wd, dY, check: bool = False):
+    """dict(dX [T,H], dWg, dWu [E,I,H], dWd [E,H,I], dS [T,K]) in fp64 (+ dS_check = <dY, y>)."""
+    ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
+    dY = _u16(dY)
+    assert dY.shape == (T, H)
+    dX = np.empty((T, H))
+    dWg = np.empty((E, I, H))
+    dWu = np.empty((E, I, H))
+    dWd = np.empty((E, H, I))
+    dS = np.empty((T, K))
+    dSc = np.empty((T, K)) if check else None
+    _load().orc_backward(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), _p(dX), _p(dWg),
+                         _p(dWu), _p(dWd), _p(dS), _p(dSc) if check else None)
+    r = dict(dX=dX, dWg=dWg, dWu=dWu, dWd=dWd, dS=dS)
+    if check:
+        r["dS_check"] = dSc
+    return r
+
+
+def forward_tokens(ids, s, x, Wg, Wu, Wd, tokens):
+    ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
+    tok = np.ascontiguousarray(tokens, dtype=np.int64)
+    out = np.empty((tok.size, H))
+    _load().orc_forward_tokens(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), tok.size, _p(tok),
+                               _p(out))
+    return out
+
+
+def backward_tokens(ids, s, x, Wg, Wu, Wd, dY, tokens):
+    ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
+    dY = _u16(dY)
+    tok = np.ascontiguousarray(tokens, dtype=np.int64)
+    dX = np.empty((tok.size, H))
+    dS = np.empty((tok.size, K))
+    _load().orc_backward_tokens(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), tok.size,
+                                _p(tok), _p(dX), _p(dS))
+    return dX, dS
+
+
+def dw_entries(ids, s, x, Wg, Wu, Wd, dY, which, e, m, c):
+    """Single entries of dWg (which 0), dWu (1) [e, m<I, c<H] and dWd (2) [e, m<H, c<I]."""
+    ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
+    dY = _u16(dY)
+    which = np.ascontiguousarray(which, np.int32)
+    e = np.ascontiguousarray(e, np.int32)
+    m = np.ascontiguousarray(m, np.int32)
+    c = np.ascontiguousarray(c, np.int32)
+    val = np.empty(which.size)
+    _load().orc_dw_entries(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), which.size,
+                           _p(which), _p(e), _p(m), _p(c), _p(val))
+    return val
