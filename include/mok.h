@@ -1,0 +1,205 @@
+/*
+ * mok.h -- C ABI of libmok: the deterministic top-k routed SwiGLU expert layer (Mixture-of-Kittens
+ * style), forward and backward, on one GB300 GPU (sm_103a).
+ *
+ * The calls follow the functional API the project card describes ("Mixture-of-Kittens (MoK)"
+ * project card, agentlenshq: "Functional API" block -- get_workspace, build_schedule(topk_experts),
+ * forward, backward -- and "Key concepts" table -- ops.mxfp8_quantize, the MoKConfig knobs).
+ * With one GPU the expert-parallel dispatch and combine of the pages become on-device gathers and
+ * a fixed-order weighted reduction.
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers unless a comment says otherwise.  bf16 tensors are row-major
+ *    arrays of 16-bit patterns; fp32 is IEEE binary32; E4M3 / E8M0 are bytes.
+ *  - Ownership: the caller allocates and frees every buffer (inputs, outputs, the workspace and
+ *    the forward context).  The library never allocates device memory and keeps no state
+ *    between calls beyond a per-device cache of the SM count and one driver entry point.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Every
+ *    call only enqueues work on it and returns; none synchronises, except
+ *    mok_read_device_status.  Inputs must stay valid until the enqueued work has run.
+ *  - Errors: argument, shape, alignment and size problems are detected on the host and returned
+ *    before anything is enqueued.  Data-dependent problems found on the device (an expert id
+ *    outside [0, E), a bounded wait that timed out) set bits (1 << code) in the schedule's device
+ *    status word; the kernels skip the offending work and return normally.  Read the word with
+ *    mok_read_device_status.
+ *  - Determinism: for the same inputs every output is bitwise identical from run to run, for any
+ *    num_ctas, minibatch or macrobatch setting; no floating-point atomics are used.
+ *  - Re-entrancy: calls on distinct workspaces may run concurrently.
+ */
+#ifndef MOK_H
+#define MOK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOK_API __attribute__((visibility("default")))
+#else
+#define MOK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOK_OK = 0,
+  MOK_ERR_INVALID_ARG = 1,          /* null pointer, bad shape, misaligned pointer */
+  MOK_ERR_UNSUPPORTED = 2,          /* a shape or mode this build does not implement */
+  MOK_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace or forward context smaller than required */
+  MOK_ERR_CUDA = 4,                 /* a CUDA runtime / driver call failed */
+  MOK_ERR_BAD_EXPERT_ID = 5,        /* device status: a top-k id outside [0, E); that slot is skipped */
+  MOK_ERR_CAPACITY = 6,             /* device status: a schedule table overflowed (cannot happen
+                                       with a workspace of mok_workspace_bytes) */
+  MOK_ERR_TIMEOUT = 7               /* device status: a bounded in-kernel wait gave up */
+} mok_status;
+
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
+
+/* Layer knobs (the project card's MoKConfig: minibatch granularity and macrobatch size; the
+ * communication-SM count has no meaning on one GPU).
+ *  minibatch_rows  rows of one minibatch tile of the schedule; a multiple of 128, >= 128.  Tiles
+ *                  never cross experts.  It sets the order in which GEMM tiles are visited (all
+ *                  tiles of one minibatch are visited together, weights then stay in L2); it
+ *                  never changes a result.
+ *  macrobatch_rows a multiple of minibatch_rows; each tile records first_row / macrobatch_rows.
+ *  num_ctas        persistent grid size of the GEMM kernels; 0 = one CTA per SM.
+ *  precision       mok_precision.
+ *  debug_flags     must be 0. */
+typedef struct {
+  int32_t minibatch_rows;
+  int32_t macrobatch_rows;
+  int32_t num_ctas;
+  int32_t precision;
+  uint32_t debug_flags;
+} mok_config;
+
+/* T tokens, hidden size H, expert intermediate size I, E experts, top-K.
+ * Supported: T >= 0; H and I multiples of 128; 1 <= K <= E <= 1024; T * K < 2^31. */
+typedef struct {
+  int64_t T;
+  int32_t H, I, E, K;
+} mok_shape;
+
+/* Filled by mok_build_schedule: device pointers into the caller's workspace (all int32 unless
+ * noted).  R = T*K routed slots, slot j = t*K + k; rows are positions in the expert-grouped
+ * layout, each expert's segment padded to a multiple of 128 rows.
+ *   counts[E]            slots routed to each expert
+ *   offsets[E+1]         exclusive prefix sum of counts
+ *   poff[E+1]            exclusive prefix sum of counts rounded up to 128 (poff[E] = Rpad)
+ *   perm[rpad_max]       slot held by each row, -1 on padding rows (valid for row < Rpad)
+ *   inv[R]               row holding each slot
+ *   tiles[tiles_max][4]  minibatch tiles {expert, first row, valid rows, first row / MB}
+ *   mblocks[mblocks_max][4]  128-row blocks {expert, first row, valid rows, tile index}
+ *   meta[16]             meta[0] = Rpad, meta[1] = number of tiles, meta[2] = number of blocks
+ *   row_weight[rpad_max] fp32 combine weight of each row (0 on padding rows)
+ *   row_token[rpad_max]  token of each row (-1 on padding rows)
+ *   status               device status word (bit (1 << mok_status code) per problem seen) */
+typedef struct {
+  mok_shape shape;
+  mok_config config;
+  int64_t rpad_max, tiles_max, mblocks_max;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* poff;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* tiles;
+  int32_t* mblocks;
+  int32_t* meta;
+  float* row_weight;
+  int32_t* row_token;
+  uint32_t* status;
+  const float* topk_weights; /* the caller's [T, K] fp32 weights, read by the combine */
+  void* ws;                  /* the workspace the schedule lives in (start of the carve) */
+  size_t ws_bytes;
+} mok_schedule;
+
+/* Expert weights in the PyTorch [out, in] convention.
+ *   w_gate, w_up [E, I, H] bf16; w_down [E, H, I] bf16.
+ * MXFP8 mode (precision == MOK_MXFP8) additionally reads pre-quantised copies made with
+ * mok_mxfp8_quantize (the project card: "weights are pre-quantised with ops.mxfp8_quantize"):
+ *   q_gate, q_up [E*I, H] E4M3 with s_gate, s_up [E*I, H/32] E8M0;
+ *   q_down [E*H, I] E4M3 with s_down [E*H, I/32] E8M0.
+ * Unused fields may be NULL. */
+typedef struct {
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const uint8_t* q_gate;
+  const uint8_t* s_gate;
+  const uint8_t* q_up;
+  const uint8_t* s_up;
+  const uint8_t* q_down;
+  const uint8_t* s_down;
+} mok_weights;
+
+/* Gradients, overwritten (not accumulated):
+ *   dx [T, H] bf16; dw_gate, dw_up [E, I, H] fp32; dw_down [E, H, I] fp32 (experts that received
+ *   no slot get exact zeros); d_topk_weights [T, K] fp32 = dL/ds for the renormalised weights. */
+typedef struct {
+  void* dx;
+  float* dw_gate;
+  float* dw_up;
+  float* dw_down;
+  float* d_topk_weights;
+} mok_grads;
+
+/* Library version string (the project card's `mok.__version__`).  Host pointer, static. */
+MOK_API const char* mok_version(void);
+
+/* Human-readable name of a status code.  Host pointer, static. */
+MOK_API const char* mok_status_string(mok_status s);
+
+/* Bytes of device workspace needed by mok_build_schedule / mok_forward / mok_backward for this
+ * shape and config (the project card's get_workspace).  0 when the arguments are invalid. */
+MOK_API size_t mok_workspace_bytes(const mok_config* cfg, const mok_shape* shape);
+
+/* Bytes of the forward context (activations saved by mok_forward for mok_backward). */
+MOK_API size_t mok_fwd_ctx_bytes(const mok_config* cfg, const mok_shape* shape);
+
+/* MXFP8 quantisation (the project card's ops.mxfp8_quantize; MXFP8 mode of "Cursor Open-Sources
+ * Mixture-of-Kittens (MoK) ...", English summary).  in_bf16 [rows, cols] row-major, cols a
+ * multiple of 32; out_e4m3 [rows, cols]; out_e8m0 [rows, cols/32].  Per 32 consecutive elements of
+ * a row: shared = floor(log2(amax)) - 8 clamped to [-127, 127] (amax = 0 gives -127), scale byte =
+ * shared + 127, element = E4M3 round-to-nearest-even of v / 2^shared saturating to +-448.  A block
+ * holding NaN or Inf gets scale 0xFF and elements 0x7F.  All three pointers 16-byte aligned. */
+MOK_API mok_status mok_mxfp8_quantize(const void* in_bf16, int64_t rows, int64_t cols, uint8_t* out_e4m3,
+                              uint8_t* out_e8m0, void* stream);
+
+/* Build the schedule ("Mixture-of-Kittens(MoK)란? ..." (alltoptrend), section 4 (1): one schedule
+ * table drives dispatch and combine of both passes; section 4 (3): no token is dropped).
+ * topk_ids [T, K] int32, topk_weights [T, K] fp32 (both device, kept by reference in *sched_out
+ * and read by later calls).  ws: device workspace of at least mok_workspace_bytes bytes, 256-byte
+ * aligned.  sched_out: HOST struct, filled here.  The schedule is a stable counting sort of the
+ * slots by expert (ascending slot index within an expert), padded per expert to 128 rows,
+ * cut into minibatch tiles. */
+MOK_API mok_status mok_build_schedule(const mok_config* cfg, const mok_shape* shape, const int32_t* topk_ids,
+                              const float* topk_weights, void* ws, size_t ws_bytes, mok_schedule* sched_out,
+                              void* stream);
+
+/* Forward: out[t] = sum over k ascending of s[t,k] * Wd[e] (silu(Wg[e] x[t]) * (Wu[e] x[t])),
+ * e = ids[t,k], computed in fp32 on the tensor cores and rounded once to bf16 ("Cursor
+ * Open-Sources Mixture-of-Kittens (MoK) ...", English summary: SwiGLU experts, BF16 / MXFP8).
+ * x [T, H] bf16; out [T, H] bf16; fwd_ctx: device buffer of mok_fwd_ctx_bytes bytes that
+ * mok_backward reads (gathered x, gate/up pre-activations, SwiGLU output). */
+MOK_API mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weights* w, void* out, void* fwd_ctx,
+                       size_t fwd_ctx_bytes, void* stream);
+
+/* Backward for upstream gradient dy [T, H] bf16 = dL/dout.  Writes every field of *g.  The
+ * router-weight gradient d_topk_weights[t,k] = <Wd[e]^T dy[t], a(t,k)> is formed inside the
+ * SwiGLU backward ("Cursor Open-Sources ...", English summary: SonicMoE-style router-weight
+ * gradient fused into the SwiGLU backward).  fwd_ctx must hold the matching mok_forward's
+ * context; sched must be the schedule both calls used. */
+MOK_API mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const void* dy, const mok_weights* w,
+                        const mok_grads* g, void* stream);
+
+/* Copy the schedule's device status word to *out (host pointer) after synchronising the stream.
+ * The only call that blocks. */
+MOK_API mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H */

@@ -1,0 +1,320 @@
+// mok_api.cu -- the C ABI: host-side validation, workspace carving, TMA descriptors and the launch
+// sequence of each call.  The calls follow the functional API of the "Mixture-of-Kittens (MoK)"
+// project card (agentlenshq), "Functional API" block: get_workspace -> mok_workspace_bytes,
+// build_schedule(topk_experts) -> mok_build_schedule, forward -> mok_forward, backward ->
+// mok_backward, and ops.mxfp8_quantize -> mok_mxfp8_quantize.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "mok_gemm.cuh"
+#include "mok_internal.cuh"
+
+namespace mok {
+
+namespace {
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Carver {
+  char* base;
+  size_t off = 0;
+  template <class T>
+  T* take(int64_t n) {
+    off = align_up(off);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += static_cast<size_t>(n > 0 ? n : 0) * sizeof(T);
+    return p;
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+mok_status from_cuda(int rc) { return rc == 0 ? MOK_OK : MOK_ERR_CUDA; }
+}  // namespace
+
+bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s) {
+  if (!cfg || !shape) return false;
+  const mok_shape& p = *shape;
+  if (p.T < 0 || p.H <= 0 || p.I <= 0 || p.K <= 0 || p.E <= 0) return false;
+  if (p.H % 128 != 0 || p.I % 128 != 0) return false;
+  if (p.K > p.E || p.E > 1024) return false;
+  if (p.T * static_cast<int64_t>(p.K) >= (int64_t(1) << 31)) return false;
+  if (cfg->minibatch_rows < kRowTile || cfg->minibatch_rows % kRowTile != 0) return false;
+  if (cfg->macrobatch_rows < cfg->minibatch_rows || cfg->macrobatch_rows % cfg->minibatch_rows != 0) return false;
+  if (cfg->num_ctas < 0 || cfg->debug_flags != 0) return false;
+  if (cfg->precision != MOK_BF16 && cfg->precision != MOK_MXFP8) return false;
+  s->T = p.T;
+  s->H = p.H;
+  s->I = p.I;
+  s->E = p.E;
+  s->K = p.K;
+  s->mb = cfg->minibatch_rows;
+  s->MB = cfg->macrobatch_rows;
+  s->R = p.T * p.K;
+  s->rpad_max = s->R + static_cast<int64_t>(p.E) * (kRowTile - 1);
+  s->tiles_max = (s->R + s->mb - 1) / s->mb + p.E;
+  s->mblocks_max = s->rpad_max / kRowTile;
+  s->nchunks = (s->R + kSchedChunk - 1) / kSchedChunk;
+  if (s->rpad_max >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st) {
+  Carver c{base};
+  mok_schedule d{};
+  d.counts = c.take<int32_t>(z.E);
+  d.offsets = c.take<int32_t>(z.E + 1);
+  d.poff = c.take<int32_t>(z.E + 1);
+  d.perm = c.take<int32_t>(z.rpad_max);
+  d.inv = c.take<int32_t>(z.R);
+  d.tiles = c.take<int32_t>(4 * z.tiles_max);
+  d.mblocks = c.take<int32_t>(4 * z.mblocks_max);
+  d.meta = c.take<int32_t>(16);
+  d.status = reinterpret_cast<uint32_t*>(d.meta ? d.meta + 15 : nullptr);
+  d.row_weight = c.take<float>(z.rpad_max);
+  d.row_token = c.take<int32_t>(z.rpad_max);
+  Staging t{};
+  t.chunk_hist = c.take<int32_t>(z.nchunks * (z.E + 1));
+  t.ybuf = c.take<uint16_t>(z.rpad_max * z.H);
+  t.dyg = c.take<uint16_t>(z.rpad_max * z.H);
+  t.dgdu = c.take<uint16_t>(z.rpad_max * 2 * z.I);
+  t.as = c.take<uint16_t>(z.rpad_max * z.I);
+  t.dspart = c.take<float>(z.rpad_max * (z.I / 128));
+  if (s) {
+    s->counts = d.counts;
+    s->offsets = d.offsets;
+    s->poff = d.poff;
+    s->perm = d.perm;
+    s->inv = d.inv;
+    s->tiles = d.tiles;
+    s->mblocks = d.mblocks;
+    s->meta = d.meta;
+    s->status = d.status;
+    s->row_weight = d.row_weight;
+    s->row_token = d.row_token;
+  }
+  if (st) *st = t;
+  return align_up(c.off);
+}
+
+size_t carve_ctx(const Sizes& z, char* base, Ctx* ctx) {
+  Carver c{base};
+  Ctx x{};
+  x.xg = c.take<uint16_t>(z.rpad_max * z.H);
+  x.gu = c.take<uint16_t>(z.rpad_max * 2 * z.I);
+  x.a = c.take<uint16_t>(z.rpad_max * z.I);
+  if (ctx) *ctx = x;
+  return align_up(c.off);
+}
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] (inner contiguous), 128-byte swizzled boxes [box_outer, box_inner].
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                    uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || !base || !aligned16(base)) return false;
+  if (outer == 0) outer = 1;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace mok
+
+using namespace mok;
+
+extern "C" {
+
+const char* mok_version(void) { return "0.1.0"; }
+
+const char* mok_status_string(mok_status s) {
+  switch (s) {
+    case MOK_OK: return "ok";
+    case MOK_ERR_INVALID_ARG: return "invalid argument";
+    case MOK_ERR_UNSUPPORTED: return "unsupported";
+    case MOK_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOK_ERR_CUDA: return "CUDA error";
+    case MOK_ERR_BAD_EXPERT_ID: return "expert id out of range";
+    case MOK_ERR_CAPACITY: return "schedule capacity exceeded";
+    case MOK_ERR_TIMEOUT: return "bounded device wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t mok_workspace_bytes(const mok_config* cfg, const mok_shape* shape) {
+  Sizes z;
+  if (!make_sizes(cfg, shape, &z)) return 0;
+  return carve_workspace(z, nullptr, nullptr, nullptr);
+}
+
+size_t mok_fwd_ctx_bytes(const mok_config* cfg, const mok_shape* shape) {
+  Sizes z;
+  if (!make_sizes(cfg, shape, &z)) return 0;
+  return carve_ctx(z, nullptr, nullptr);
+}
+
+mok_status mok_mxfp8_quantize(const void* in_bf16, int64_t rows, int64_t cols, uint8_t* out_e4m3,
+                              uint8_t* out_e8m0, void* stream) {
+  if (rows < 0 || cols < 0 || cols % 32 != 0) return MOK_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MOK_OK;
+  if (!in_bf16 || !out_e4m3 || !out_e8m0) return MOK_ERR_INVALID_ARG;
+  if (!aligned16(in_bf16) || !aligned16(out_e4m3)) return MOK_ERR_INVALID_ARG;
+  return from_cuda(launch_mxfp8_quantize(static_cast<const uint16_t*>(in_bf16), rows, cols, out_e4m3, out_e8m0,
+                                         as_stream(stream)));
+}
+
+mok_status mok_build_schedule(const mok_config* cfg, const mok_shape* shape, const int32_t* topk_ids,
+                              const float* topk_weights, void* ws, size_t ws_bytes, mok_schedule* out,
+                              void* stream) {
+  Sizes z;
+  if (!out || !make_sizes(cfg, shape, &z)) return MOK_ERR_INVALID_ARG;
+  if (cfg->precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return MOK_ERR_INVALID_ARG;
+  if (z.R > 0 && (!topk_ids || !topk_weights)) return MOK_ERR_INVALID_ARG;
+  Staging st;
+  mok_schedule s{};
+  const size_t need = carve_workspace(z, static_cast<char*>(ws), &s, &st);
+  if (ws_bytes < need) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  s.shape = *shape;
+  s.config = *cfg;
+  s.rpad_max = z.rpad_max;
+  s.tiles_max = z.tiles_max;
+  s.mblocks_max = z.mblocks_max;
+  s.topk_weights = topk_weights;
+  s.ws = ws;
+  s.ws_bytes = ws_bytes;
+  const int rc = launch_schedule(z, topk_ids, topk_weights, s, st, as_stream(stream));
+  if (rc) return MOK_ERR_CUDA;
+  *out = s;
+  return MOK_OK;
+}
+
+static mok_status check_sched(const mok_schedule* s, Sizes* z, Staging* st) {
+  if (!s || !s->ws) return MOK_ERR_INVALID_ARG;
+  if (!make_sizes(&s->config, &s->shape, z)) return MOK_ERR_INVALID_ARG;
+  mok_schedule again{};
+  const size_t need = carve_workspace(*z, static_cast<char*>(s->ws), &again, st);
+  if (s->ws_bytes < need || again.meta != s->meta) return MOK_ERR_INVALID_ARG;
+  return MOK_OK;
+}
+
+static int grid_of(const mok_schedule* s) {
+  const int n = s->config.num_ctas;
+  return n > 0 ? n : sm_count();
+}
+
+mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weights* w, void* out, void* fwd_ctx,
+                       size_t fwd_ctx_bytes, void* stream) {
+  Sizes z;
+  Staging st;
+  mok_status rc = check_sched(sched, &z, &st);
+  if (rc != MOK_OK) return rc;
+  if (sched->config.precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (!w || !fwd_ctx) return MOK_ERR_INVALID_ARG;
+  Ctx ctx;
+  if (fwd_ctx_bytes < carve_ctx(z, static_cast<char*>(fwd_ctx), &ctx)) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(fwd_ctx) % kAlign) return MOK_ERR_INVALID_ARG;
+  if (z.T > 0 && (!x || !out || !aligned16(x) || !aligned16(out))) return MOK_ERR_INVALID_ARG;
+  if (!w->w_gate || !w->w_up || !w->w_down || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
+      !aligned16(w->w_down))
+    return MOK_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H, ctx.xg, s))
+    return MOK_ERR_CUDA;
+  const int g = grid_of(sched);
+  int e = launch_fwd_gemms(z, *sched, ctx, st, *w, g, s);
+  if (e < 0) return MOK_ERR_INVALID_ARG;
+  if (e) return MOK_ERR_CUDA;
+  return from_cuda(launch_combine(st.ybuf, sched->inv, sched->topk_weights, z.T, z.K, z.H,
+                                  static_cast<uint16_t*>(out), s));
+}
+
+mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const void* dy, const mok_weights* w,
+                        const mok_grads* g, void* stream) {
+  Sizes z;
+  Staging st;
+  mok_status rc = check_sched(sched, &z, &st);
+  if (rc != MOK_OK) return rc;
+  if (sched->config.precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (!w || !g || !fwd_ctx || (reinterpret_cast<uintptr_t>(fwd_ctx) % kAlign)) return MOK_ERR_INVALID_ARG;
+  if (!g->dw_gate || !g->dw_up || !g->dw_down || !aligned16(g->dw_gate) || !aligned16(g->dw_up) ||
+      !aligned16(g->dw_down))
+    return MOK_ERR_INVALID_ARG;
+  if (z.T > 0 && (!dy || !g->dx || !g->d_topk_weights || !aligned16(dy) || !aligned16(g->dx)))
+    return MOK_ERR_INVALID_ARG;
+  if (!w->w_gate || !w->w_up || !w->w_down || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
+      !aligned16(w->w_down))
+    return MOK_ERR_INVALID_ARG;
+  Ctx ctx;
+  carve_ctx(z, static_cast<char*>(const_cast<void*>(fwd_ctx)), &ctx);
+  cudaStream_t s = as_stream(stream);
+  const int grid = grid_of(sched);
+  if (launch_gather_rows(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H, st.dyg,
+                         s))
+    return MOK_ERR_CUDA;
+  int e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 1, s);
+  if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
+  const int n_tiles1 = z.I / (z.I % 256 == 0 ? 256 : 128);
+  if (launch_ds_reduce(st.dspart, sched->inv, z.R, n_tiles1, g->d_topk_weights, s)) return MOK_ERR_CUDA;
+  e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 2, s);
+  if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
+  if (launch_combine(st.ybuf, sched->inv, nullptr, z.T, z.K, z.H, static_cast<uint16_t*>(g->dx), s))
+    return MOK_ERR_CUDA;
+  e = launch_wgrad_gemms(z, *sched, ctx, st, *g, grid, s);
+  if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
+  return MOK_OK;
+}
+
+mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream) {
+  if (!sched || !sched->status || !out) return MOK_ERR_INVALID_ARG;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, sched->status, sizeof v, cudaMemcpyDeviceToHost, as_stream(stream)) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOK_ERR_CUDA;
+  *out = v;
+  return MOK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,467 @@
+// mok_gemm.cuh -- the grouped expert GEMMs of the layer on the 5th-generation tensor cores.
+//
+// One persistent, warp-specialised kernel template serves all six contractions of the layer
+// ("Cursor Open-Sources Mixture-of-Kittens (MoK) ...", English summary: SwiGLU experts, forward
+// and backward, router-weight gradient inside the SwiGLU backward):
+//   FWD_GATEUP  [g|u] = Xg Wg_e^T | Xg Wu_e^T, epilogue a = silu(g) u          (K = H)
+//   FWD_DOWN    y = a Wd_e^T                                                   (K = I)
+//   DGRAD1      dA' = dYg Wd_e, epilogue: dS partials, SwiGLU backward, s*a     (K = H, B MN-major)
+//   DGRAD2      dXg = [dg|du] [Wg_e;Wu_e]                                       (K = 2I, B MN-major)
+//   WGRAD_GU    [dWg;dWu]_e = [dg|du]_e^T Xg_e                                  (K = rows of e, A,B MN-major)
+//   WGRAD_D     dWd_e = dYg_e^T (s a)_e                                         (K = rows of e, A,B MN-major)
+//
+// Roles (192 threads): warp 0 lane 0 issues TMA tile loads into a ring of shared-memory stages;
+// warp 1 owns the tensor memory and its lane 0 issues tcgen05.mma (M = 128, N = BN, K = 16) into
+// one of two TMEM accumulators; warps 2..5 drain the other accumulator (tcgen05.ld), apply the
+// epilogue and store to global memory.  Every output element is produced by exactly one CTA with a
+// fixed K order, so results are bitwise independent of the grid size and of the tile order.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "mok_internal.cuh"
+#include "mok_ptx.cuh"
+
+namespace mok {
+
+enum GemmVariant : int {
+  V_FWD_GATEUP = 0,
+  V_FWD_DOWN = 1,
+  V_DGRAD1 = 2,
+  V_DGRAD2 = 3,
+  V_WGRAD_GU = 4,
+  V_WGRAD_D = 5,
+};
+
+constexpr int kBM = 128;      // MMA M (rows of the accumulator = TMEM lanes)
+constexpr int kBK = 64;       // bf16 elements per K block: one 128-byte swizzle row
+constexpr int kUmmaK = 16;    // K of one tcgen05.mma.kind::f16
+constexpr int kGemmThreads = 192;
+
+struct GemmArgs {
+  // work enumeration
+  const int32_t* mblocks;  // row-tiled variants: 128-row blocks {expert, first row, valid, tile}
+  const int32_t* tiles;    // minibatch tiles {expert, first row, valid, macro}
+  const int32_t* meta;     // meta[2] = number of 128-row blocks
+  const int32_t* poff;     // weight-gradient variants: padded expert offsets
+  int32_t E, I, H;
+  int32_t n_tiles;         // N / BN
+  int32_t m_tiles;         // weight-gradient variants: M / 128
+  int32_t k_blocks;        // row-tiled variants: K / 64
+  int32_t kb_split;        // DGRAD2: K blocks read from Wg before switching to Wu (I / 64)
+  // epilogue operands
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* in0;
+  const void* in1;
+  const float* row_weight;
+  uint32_t* status;
+};
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr uint32_t kABytes = kBM * kBK * 2;
+  static constexpr uint32_t kBBytes = BN * kBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 2 * BN;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + 256;
+};
+
+struct Unit {
+  int e, row0, nt, mt, kblocks;
+};
+
+template <int VAR>
+__device__ __forceinline__ int gemm_num_units(const GemmArgs& a) {
+  if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) return a.E * a.m_tiles * a.n_tiles;
+  else return a.meta[2] * a.n_tiles;
+}
+
+// Row-tiled variants: all units of one minibatch tile are consecutive, N tile outer and 128-row
+// block inner, so a weight tile is reused by the tile's blocks while it sits in L2.
+template <int VAR>
+__device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
+  Unit w;
+  if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) {
+    const int per_e = a.m_tiles * a.n_tiles;
+    w.e = u / per_e;
+    const int r = u - w.e * per_e;
+    w.mt = r / a.n_tiles;
+    w.nt = r - w.mt * a.n_tiles;
+    const int p0 = __ldg(a.poff + w.e), p1 = __ldg(a.poff + w.e + 1);
+    w.row0 = p0;
+    w.kblocks = (p1 - p0) / kBK;
+  } else {
+    const int bq = u / a.n_tiles;
+    const int4 mbk = __ldg(reinterpret_cast<const int4*>(a.mblocks) + bq);
+    const int4 tl = __ldg(reinterpret_cast<const int4*>(a.tiles) + mbk.w);
+    const int mb0 = tl.y / kBM;
+    const int nmb = (tl.z + kBM - 1) / kBM;
+    const int local = u - mb0 * a.n_tiles;
+    w.nt = local / nmb;
+    w.row0 = (mb0 + (local - w.nt * nmb)) * kBM;
+    w.e = mbk.x;
+    w.mt = 0;
+    w.kblocks = a.k_blocks;
+  }
+  return w;
+}
+
+// Issue the TMA loads of one K block into stage (sa, sb), all completing on barrier `bar`.
+template <int VAR, int BN>
+__device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
+                                          uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
+                                          const CUtensorMap* tB2) {
+  const int k0 = kb * kBK;
+  if constexpr (VAR == V_FWD_GATEUP) {
+    tma_load_2d(sa, tA, bar, k0, w.row0);
+    const int n0 = w.e * a.I + w.nt * (BN / 2);
+    tma_load_2d(sb, tB, bar, k0, n0);
+    tma_load_2d(sb + (BN / 2) * 128, tB2, bar, k0, n0);
+  } else if constexpr (VAR == V_FWD_DOWN) {
+    tma_load_2d(sa, tA, bar, k0, w.row0);
+    tma_load_2d(sb, tB, bar, k0, w.e * a.H + w.nt * BN);
+  } else if constexpr (VAR == V_DGRAD1) {
+    tma_load_2d(sa, tA, bar, k0, w.row0);
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, tB, bar, w.nt * BN + j * 64, w.e * a.H + k0);
+  } else if constexpr (VAR == V_DGRAD2) {
+    tma_load_2d(sa, tA, bar, k0, w.row0);
+    const bool first = kb < a.kb_split;
+    const CUtensorMap* tm = first ? tB : tB2;
+    const int krow = w.e * a.I + (first ? k0 : k0 - a.kb_split * kBK);
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, tm, bar, w.nt * BN + j * 64, krow);
+  } else {  // weight gradients: both operands MN-major, K runs over the expert's rows
+    const int krow = w.row0 + k0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tma_load_2d(sa + j * 8192, tA, bar, w.mt * kBM + j * 64, krow);
+#pragma unroll
+    for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, tB, bar, w.nt * BN + j * 64, krow);
+  }
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ void load_bf16x32(const uint16_t* p, float (&v)[32]) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 x = q[i];
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = bf16_lo(w[j]);
+      v[8 * i + 2 * j + 1] = bf16_hi(w[j]);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* p, const float (&v)[32]) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    q[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+
+// Epilogue of one unit for one accumulator row (`r` = row within the 128-row tile).
+template <int VAR, int BN>
+__device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int r, uint32_t taddr) {
+  const bool empty = w.kblocks == 0;
+  if constexpr (VAR == V_FWD_GATEUP) {
+    const int64_t row = w.row0 + r;
+    const int i0 = w.nt * (BN / 2);
+    uint16_t* gu = static_cast<uint16_t*>(a.out0) + row * (2 * static_cast<int64_t>(a.I));
+    uint16_t* av = static_cast<uint16_t*>(a.out1) + row * static_cast<int64_t>(a.I);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t rg[32], ru[32];
+      tmem_ld_32x32b_x32(taddr + c, rg);
+      tmem_ld_32x32b_x32(taddr + BN / 2 + c, ru);
+      tmem_ld_wait();
+      float g[32], u[32], o[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        g[i] = __uint_as_float(rg[i]);
+        u[i] = __uint_as_float(ru[i]);
+        o[i] = silu_f(g[i]) * u[i];
+      }
+      store_bf16x32(gu + i0 + c, g);
+      store_bf16x32(gu + a.I + i0 + c, u);
+      store_bf16x32(av + i0 + c, o);
+    }
+  } else if constexpr (VAR == V_FWD_DOWN || VAR == V_DGRAD2) {
+    const int64_t row = w.row0 + r;
+    uint16_t* out = static_cast<uint16_t*>(a.out0) + row * static_cast<int64_t>(a.H) + w.nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t rv[32];
+      tmem_ld_32x32b_x32(taddr + c, rv);
+      tmem_ld_wait();
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rv[i]);
+      store_bf16x32(out + c, v);
+    }
+  } else if constexpr (VAR == V_DGRAD1) {
+    // dA' = dY Wd (this tile's BN columns of I); the forward's g, u, a come from the context.
+    const int64_t row = w.row0 + r;
+    const int64_t I = a.I;
+    const int i0 = w.nt * BN;
+    const uint16_t* gu = static_cast<const uint16_t*>(a.in0) + row * 2 * I;
+    const uint16_t* av = static_cast<const uint16_t*>(a.in1) + row * I;
+    uint16_t* dgdu = static_cast<uint16_t*>(a.out0) + row * 2 * I;
+    uint16_t* as = static_cast<uint16_t*>(a.out1) + row * I;
+    const float s = __ldg(a.row_weight + row);
+    float part = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t rv[32];
+      tmem_ld_32x32b_x32(taddr + c, rv);
+      tmem_ld_wait();
+      float g[32], u[32], av32[32], dg[32], du[32], sa[32];
+      load_bf16x32(gu + i0 + c, g);
+      load_bf16x32(gu + I + i0 + c, u);
+      load_bf16x32(av + i0 + c, av32);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float dap = __uint_as_float(rv[i]);
+        part = fmaf(dap, av32[i], part);
+        const float da = s * dap;
+        const float sg = sigmoid_f(g[i]);
+        dg[i] = da * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+        du[i] = da * g[i] * sg;
+        sa[i] = s * av32[i];
+      }
+      store_bf16x32(dgdu + i0 + c, dg);
+      store_bf16x32(dgdu + I + i0 + c, du);
+      store_bf16x32(as + i0 + c, sa);
+    }
+    static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
+  } else {  // weight gradients, fp32 out
+    const int m = w.mt * kBM + r;
+    float* dst;
+    int64_t ld;
+    if constexpr (VAR == V_WGRAD_GU) {
+      ld = a.H;
+      dst = m < a.I ? static_cast<float*>(a.out0) + (static_cast<int64_t>(w.e) * a.I + m) * ld
+                    : static_cast<float*>(a.out1) + (static_cast<int64_t>(w.e) * a.I + (m - a.I)) * ld;
+    } else {
+      ld = a.I;
+      dst = static_cast<float*>(a.out0) + (static_cast<int64_t>(w.e) * a.H + m) * ld;
+    }
+    dst += w.nt * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t rv[32];
+      if (!empty) {
+        tmem_ld_32x32b_x32(taddr + c, rv);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rv[i] = 0u;
+      }
+      float4* q = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        q[i] = make_float4(__uint_as_float(rv[4 * i]), __uint_as_float(rv[4 * i + 1]),
+                           __uint_as_float(rv[4 * i + 2]), __uint_as_float(rv[4 * i + 3]));
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used only while winding down.
+__device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity, uint32_t* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs / 4) {
+      record_status(status, MOK_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int VAR, int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+  using C = GemmCfg<BN>;
+  constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);
+  constexpr bool kBmn = (VAR >= V_DGRAD1);
+  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
+  constexpr int S = C::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+  uint8_t* gbase = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * C::kStageBytes);
+  // bars[0..S) full, [S..2S) empty, [2S, 2S+2) accumulator full, [2S+2, 2S+4) accumulator empty,
+  // [2S+4] drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmB2);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_units = gemm_num_units<VAR>(args);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_parity[S];
+      for (int s = 0; s < S; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        const Unit w = gemm_decode<VAR>(args, u);
+        for (int kb = 0; kb < w.kblocks; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+          const uint32_t sa = base + stage * C::kStageBytes;
+          gemm_load<VAR, BN>(args, w, kb, sa, sa + C::kABytes, full_bar(stage), &tmA, &tmB, &tmB2);
+          last_parity[stage] = static_cast<int>(phase);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // wind down: let the copies already issued land before the CTA exits
+        for (int s = 0; s < S; ++s)
+          if (last_parity[s] >= 0) mbar_wait_final(full_bar(s), static_cast<uint32_t>(last_parity[s]), args.status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
+        const Unit w = gemm_decode<VAR>(args, u);
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < w.kblocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * C::kStageBytes, sb = sa + C::kABytes;
+#pragma unroll
+          for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
+            const uint64_t ad = kAmn ? sdesc_sw128(sa + ks * 2048, 8192, 1024) : sdesc_sw128(sa + ks * 32, 16, 1024);
+            const uint64_t bd = kBmn ? sdesc_sw128(sb + ks * 2048, 8192, 1024) : sdesc_sw128(sb + ks * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued by this thread has completed before TMEM is released
+      umma_commit(drain_bar);
+      mbar_wait_final(drain_bar, 0, args.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const Unit w = gemm_decode<VAR>(args, u);
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      gemm_epilogue<VAR, BN>(args, w, q * 32 + lane, taddr);
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                    uint32_t box_outer);
+
+template <int VAR, int BN>
+int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmArgs& args, int grid,
+                cudaStream_t stream) {
+  using C = GemmCfg<BN>;
+  static bool configured = false;  // per process; the attribute is per function, set once
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    configured = true;
+  }
+  if (grid <= 0) return 0;
+  gemm_kernel<VAR, BN><<<grid, kGemmThreads, C::kSmemBytes, stream>>>(a, b, b2, args);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace mok

@@ -1,0 +1,48 @@
+// mok_gemm_wgrad.cu -- weight-gradient expert GEMMs.  Each output tile of dW is reduced by one CTA
+// over its expert's rows in ascending row order (K = the expert's padded rows; padding rows are
+// zero), so the reduction order is fixed and no atomics are used.  Experts without rows get zeros.
+#include "mok_gemm.cuh"
+
+namespace mok {
+
+int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
+                       const mok_grads& g, int num_ctas, cudaStream_t stream) {
+  CUtensorMap tA, tB;
+  GemmArgs a{};
+  a.poff = s.poff;
+  a.E = z.E;
+  a.I = z.I;
+  a.H = z.H;
+  a.status = s.status;
+  // [dWg ; dWu]_e = [dg | du]_e^T Xg_e   (M = 2I, N = H)
+  {
+    const int BN = z.H % 256 == 0 ? 256 : 128;
+    if (!make_tmap_bf16(&tA, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 64)) return -1;
+    if (!make_tmap_bf16(&tB, ctx.xg, z.H, z.rpad_max, 64, 64)) return -1;
+    a.m_tiles = 2 * z.I / kBM;
+    a.n_tiles = z.H / BN;
+    a.out0 = g.dw_gate;
+    a.out1 = g.dw_up;
+    const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
+    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256>(tA, tB, tB, a, grid, stream)
+                             : launch_gemm<V_WGRAD_GU, 128>(tA, tB, tB, a, grid, stream);
+    if (rc) return rc;
+  }
+  // dWd_e = dYg_e^T (s a)_e   (M = H, N = I)
+  {
+    const int BN = z.I % 256 == 0 ? 256 : 128;
+    if (!make_tmap_bf16(&tA, st.dyg, z.H, z.rpad_max, 64, 64)) return -1;
+    if (!make_tmap_bf16(&tB, st.as, z.I, z.rpad_max, 64, 64)) return -1;
+    a.m_tiles = z.H / kBM;
+    a.n_tiles = z.I / BN;
+    a.out0 = g.dw_down;
+    a.out1 = nullptr;
+    const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
+    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    return BN == 256 ? launch_gemm<V_WGRAD_D, 256>(tA, tB, tB, a, grid, stream)
+                     : launch_gemm<V_WGRAD_D, 128>(tA, tB, tB, a, grid, stream);
+  }
+}
+
+}  // namespace mok

@@ -1,0 +1,61 @@
+// mok_internal.cuh -- declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mok.h"
+
+namespace mok {
+
+constexpr int kRowTile = 128;       // GEMM row tile: each expert's segment is padded to it
+constexpr int kSchedChunk = 512;    // slots per warp in the schedule histogram / scatter
+constexpr int kSchedWarps = 8;      // warps per CTA in the schedule kernels
+
+// Derived sizes of one (shape, config) pair.
+struct Sizes {
+  int64_t T, R, rpad_max, tiles_max, mblocks_max, nchunks;
+  int32_t H, I, E, K, mb, MB;
+};
+bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s);
+
+// Staging buffers inside the workspace (after the schedule tables) and the forward context.
+struct Staging {
+  uint16_t* ybuf;    // [rpad_max, H] bf16: expert outputs y (forward), then dX per row (backward)
+  uint16_t* dyg;     // [rpad_max, H] bf16: gathered upstream gradient rows
+  uint16_t* dgdu;    // [rpad_max, 2I] bf16: [dg | du]
+  uint16_t* as;      // [rpad_max, I] bf16: s * a
+  float* dspart;     // [rpad_max, I/128] fp32: router-gradient partial sums per N tile
+  int32_t* chunk_hist;  // [nchunks, E+1]
+};
+struct Ctx {
+  uint16_t* xg;      // [rpad_max, H] bf16: gathered x rows (zero on padding rows)
+  uint16_t* gu;      // [rpad_max, 2I] bf16: [g | u]
+  uint16_t* a;       // [rpad_max, I] bf16: silu(g) * u
+};
+size_t carve_workspace(const Sizes& z, char* base, mok_schedule* sched, Staging* st);  // returns bytes
+size_t carve_ctx(const Sizes& z, char* base, Ctx* ctx);
+
+int sm_count();
+
+// launchers (return a cudaError_t as int)
+int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mok_schedule& s, const Staging& st,
+                    cudaStream_t stream);
+int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+                       int32_t H, uint16_t* dst, cudaStream_t stream);
+int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
+                   uint16_t* out, cudaStream_t stream);
+int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, float* ds,
+                     cudaStream_t stream);
+int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sc,
+                          cudaStream_t stream);
+
+// GEMM phases
+int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st, const mok_weights& w,
+                     int num_ctas, cudaStream_t stream);
+int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
+                       const mok_weights& w, int num_ctas, int phase, cudaStream_t stream);
+int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
+                       const mok_grads& g, int num_ctas, cudaStream_t stream);
+
+}  // namespace mok

@@ -1,0 +1,239 @@
+// mok_move.cu -- the HBM-bound steps: dispatch gather, fixed-order weighted combine / dX reduce,
+// router-gradient reduce, and MXFP8 quantisation.
+//
+// Dispatch and combine are the one-GPU form of the pages' pull dispatch and push combine
+// ("Mixture-of-Kittens(MoK)란? ..." (alltoptrend), section 4 (1)): token rows are gathered into the
+// expert-grouped layout, and each token's K expert outputs are summed back in ascending k in fp32
+// and rounded once to bf16, so the result does not depend on any scheduling order.
+#include "mok_internal.cuh"
+#include "mok_ptx.cuh"
+
+namespace mok {
+namespace {
+
+constexpr int kMoveThreads = 256;
+
+// dst[row] = src[row_token[row]] for row < Rpad (= meta[0]); zero rows where row_token < 0.
+// One warp per row, 16-byte vectors, lanes striding along the row (coalesced).
+__global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* __restrict__ src,
+                                                                  const int32_t* __restrict__ row_token,
+                                                                  const int32_t* __restrict__ meta, int64_t vecs,
+                                                                  uint4* __restrict__ dst) {
+  const int64_t rpad = meta[0];
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); row < rpad;
+       row += nwarps) {
+    const int t = row_token[row];
+    uint4* d = dst + row * vecs;
+    if (t >= 0) {
+      const uint4* s = src + static_cast<int64_t>(t) * vecs;
+      int64_t c = lane;
+      for (; c + 96 < vecs; c += 128) {
+        const uint4 v0 = __ldg(s + c), v1 = __ldg(s + c + 32), v2 = __ldg(s + c + 64), v3 = __ldg(s + c + 96);
+        d[c] = v0;
+        d[c + 32] = v1;
+        d[c + 64] = v2;
+        d[c + 96] = v3;
+      }
+      for (; c < vecs; c += 32) d[c] = __ldg(s + c);
+    } else {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int64_t c = lane; c < vecs; c += 32) d[c] = z;
+    }
+  }
+}
+
+// out[t] = bf16( sum_{k = 0..K-1 ascending} w[t,k] * y[inv[t*K+k]] ), fp32 accumulation; w == nullptr
+// means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.
+__global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __restrict__ y,
+                                                              const int32_t* __restrict__ inv,
+                                                              const float* __restrict__ w, int64_t T, int K,
+                                                              int64_t vecs, uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); t < T;
+       t += nwarps) {
+    for (int64_t c = lane; c < vecs; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        const int row = __ldg(inv + t * K + k);
+        if (row < 0) continue;
+        const float wk = w ? __ldg(w + t * K + k) : 1.0f;
+        const uint4 v = __ldg(y + static_cast<int64_t>(row) * vecs + c);
+        const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wk, bf16_lo(p[i]), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wk, bf16_hi(p[i]), acc[2 * i + 1]);
+        }
+      }
+      out[t * vecs + c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
+// ds[j] = sum over N tiles (ascending) of part[inv[j], :]; 0 for skipped slots.
+__global__ void __launch_bounds__(kMoveThreads) ds_reduce_kernel(const float* __restrict__ part,
+                                                                const int32_t* __restrict__ inv, int64_t R,
+                                                                int n_tiles, float* __restrict__ ds) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x;
+  if (j >= R) return;
+  const int row = inv[j];
+  float acc = 0.0f;
+  if (row >= 0) {
+    const float* p = part + static_cast<int64_t>(row) * n_tiles;
+    for (int n = 0; n < n_tiles; ++n) acc += p[n];
+  }
+  ds[j] = acc;
+}
+
+// ---------------------------------------------------------------------------------------------
+// MXFP8: E4M3 elements with one E8M0 scale per 32 consecutive values ("Mixture-of-Kittens (MoK)"
+// project card, "Key concepts": ops.mxfp8_quantize).  Integer arithmetic on the bf16 bit pattern:
+// |v| = M * 2^X exactly (M < 256), so every rounding decision below is exact.
+// ---------------------------------------------------------------------------------------------
+
+// floor(log2 |v|) of a finite nonzero bf16 magnitude (15 bits).
+__device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
+  const uint32_t eb = mag >> 7, m = mag & 0x7Fu;
+  if (eb != 0) return static_cast<int>(eb) - 127;
+  return (31 - __clz(m)) - 133;  // subnormal: m * 2^-133
+}
+
+// E4M3 code (without sign) of |v| * 2^-shared, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_code(uint32_t mag, int shared) {
+  const uint32_t eb = mag >> 7, mf = mag & 0x7Fu;
+  if (eb == 0 && mf == 0) return 0;
+  uint32_t M;
+  int X;
+  if (eb != 0) {
+    M = 0x80u | mf;
+    X = static_cast<int>(eb) - 134;
+  } else {
+    M = mf;
+    X = -133;
+  }
+  const int Y = X - shared;                          // value = M * 2^Y
+  const int p = 31 - __clz(M);                       // leading bit of M
+  const int Ep = p + Y;                              // unbiased exponent of the value
+  const int qe = (Ep > -6 ? Ep : -6) - 3;            // quantum: 2^qe (subnormal quantum 2^-9)
+  const int d = qe - Y;                              // right shift of M onto the quantum grid
+  uint32_t n;
+  if (d <= 0) {
+    n = M << (-d);                                   // exact (d >= -7 here)
+  } else if (d > 20) {
+    n = 0;                                           // far below half a quantum
+  } else {
+    n = M >> d;
+    const uint32_t rem = M & ((1u << d) - 1u), half = 1u << (d - 1);
+    if (rem > half || (rem == half && (n & 1u))) ++n;
+  }
+  int q = qe;
+  if (n == 16u) {                                    // mantissa overflow: next binade
+    n = 8u;
+    ++q;
+  }
+  if (q == -9 && n < 8u) return n;                   // subnormal (includes 0)
+  const int E = q + 10;                              // value = n * 2^q = (1 + (n-8)/8) * 2^(E-7)
+  if (E > 15) return 0x7Eu;
+  const uint32_t code = (static_cast<uint32_t>(E) << 3) | (n - 8u);
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+// One thread per 32-element block; 64 bytes read, 32 + 1 bytes written.
+__global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint4* __restrict__ in,
+                                                                     int64_t nblocks, uint4* __restrict__ q,
+                                                                     uint8_t* __restrict__ sc) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; b < nblocks; b += stride) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(in + b * 4 + i);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    uint32_t amax = 0;
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t mag = (i & 1 ? (w[i >> 1] >> 16) : w[i >> 1]) & 0x7FFFu;
+      bad |= mag >= 0x7F80u;
+      amax = mag > amax ? mag : amax;
+    }
+    uint32_t out[8];
+    uint8_t sbyte;
+    if (bad) {
+      sbyte = 0xFF;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = 0x7F7F7F7Fu;
+    } else {
+      int shared = amax == 0 ? -127 : bf16_floor_log2(amax) - 8;
+      shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
+      sbyte = static_cast<uint8_t>(shared + 127);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) out[i] = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t h = (i & 1 ? (w[i >> 1] >> 16) : w[i >> 1]) & 0xFFFFu;
+        const uint32_t c = e4m3_code(h & 0x7FFFu, shared) | ((h >> 8) & 0x80u);
+        out[i >> 2] |= c << (8 * (i & 3));
+      }
+    }
+    q[b * 2] = make_uint4(out[0], out[1], out[2], out[3]);
+    q[b * 2 + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+    sc[b] = sbyte;
+  }
+}
+
+int grid_for(int64_t items, int per_block) {
+  const int64_t want = (items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+
+int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+                       int32_t H, uint16_t* dst, cudaStream_t stream) {
+  if (rpad_max <= 0) return 0;
+  const int grid = grid_for(rpad_max, kMoveThreads / 32);
+  gather_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), row_token, meta,
+                                                        H / 8, reinterpret_cast<uint4*>(dst));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
+                   uint16_t* out, cudaStream_t stream) {
+  if (T <= 0) return 0;
+  const int grid = grid_for(T, kMoveThreads / 32);
+  combine_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(y), inv, s, T, K, H / 8,
+                                                    reinterpret_cast<uint4*>(out));
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, float* ds,
+                     cudaStream_t stream) {
+  if (R <= 0) return 0;
+  const int grid = static_cast<int>((R + kMoveThreads - 1) / kMoveThreads);
+  ds_reduce_kernel<<<grid, kMoveThreads, 0, stream>>>(part, inv, R, n_tiles, ds);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sc,
+                          cudaStream_t stream) {
+  const int64_t nblocks = rows * (cols / 32);
+  if (nblocks <= 0) return 0;
+  const int grid = grid_for(nblocks, kMoveThreads);
+  mxfp8_quantize_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(in), nblocks,
+                                                           reinterpret_cast<uint4*>(q), sc);
+  return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace mok

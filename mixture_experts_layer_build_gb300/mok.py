@@ -1,0 +1,289 @@
+"""Thin Python binding of ``libmok.so`` (see ``include/mok.h``): argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module only checks tensor
+dtypes / devices / contiguity, passes ``data_ptr()``s and the current CUDA stream, and turns
+status codes into exceptions.  PyTorch provides device memory and streams.
+
+Importing this module loads the library and raises ``ImportError`` when it is missing: there is
+no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmok.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libmok.so not found at {LIB_PATH}; build it with __graft_entry__.build() "
+                      "(nvcc, sm_103a). There is no CPU fallback.")
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOK_OK = 0
+MOK_ERR_INVALID_ARG = 1
+MOK_ERR_UNSUPPORTED = 2
+MOK_ERR_WORKSPACE_TOO_SMALL = 3
+MOK_ERR_CUDA = 4
+MOK_ERR_BAD_EXPERT_ID = 5
+MOK_ERR_CAPACITY = 6
+MOK_ERR_TIMEOUT = 7
+MOK_BF16 = 0
+MOK_MXFP8 = 1
+
+
+class MokError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _lib.mok_status_string(code).decode()
+        super().__init__(f"{where}: {msg} (status {code})")
+
+
+class mok_config(ctypes.Structure):
+    _fields_ = [("minibatch_rows", ctypes.c_int32), ("macrobatch_rows", ctypes.c_int32),
+                ("num_ctas", ctypes.c_int32), ("precision", ctypes.c_int32), ("debug_flags", ctypes.c_uint32)]
+
+
+class mok_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("K", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+
+
+class mok_schedule(ctypes.Structure):
+    _fields_ = [("shape", mok_shape), ("config", mok_config), ("rpad_max", ctypes.c_int64),
+                ("tiles_max", ctypes.c_int64), ("mblocks_max", ctypes.c_int64), ("counts", _P), ("offsets", _P),
+                ("poff", _P), ("perm", _P), ("inv", _P), ("tiles", _P), ("mblocks", _P), ("meta", _P),
+                ("row_weight", _P), ("row_token", _P), ("status", _P), ("topk_weights", _P), ("ws", _P),
+                ("ws_bytes", ctypes.c_size_t)]
+
+
+class mok_weights(ctypes.Structure):
+    _fields_ = [("w_gate", _P), ("w_up", _P), ("w_down", _P), ("q_gate", _P), ("s_gate", _P), ("q_up", _P),
+                ("s_up", _P), ("q_down", _P), ("s_down", _P)]
+
+
+class mok_grads(ctypes.Structure):
+    _fields_ = [("dx", _P), ("dw_gate", _P), ("dw_up", _P), ("dw_down", _P), ("d_topk_weights", _P)]
+
+
+_lib.mok_version.restype = ctypes.c_char_p
+_lib.mok_version.argtypes = []
+_lib.mok_status_string.restype = ctypes.c_char_p
+_lib.mok_status_string.argtypes = [ctypes.c_int]
+_lib.mok_workspace_bytes.restype = ctypes.c_size_t
+_lib.mok_workspace_bytes.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape)]
+_lib.mok_fwd_ctx_bytes.restype = ctypes.c_size_t
+_lib.mok_fwd_ctx_bytes.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape)]
+_lib.mok_mxfp8_quantize.restype = ctypes.c_int
+_lib.mok_mxfp8_quantize.argtypes = [_P, ctypes.c_int64, ctypes.c_int64, _P, _P, _P]
+_lib.mok_build_schedule.restype = ctypes.c_int
+_lib.mok_build_schedule.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape), _P, _P, _P,
+                                    ctypes.c_size_t, ctypes.POINTER(mok_schedule), _P]
+_lib.mok_forward.restype = ctypes.c_int
+_lib.mok_forward.argtypes = [ctypes.POINTER(mok_schedule), _P, ctypes.POINTER(mok_weights), _P, _P,
+                             ctypes.c_size_t, _P]
+_lib.mok_backward.restype = ctypes.c_int
+_lib.mok_backward.argtypes = [ctypes.POINTER(mok_schedule), _P, _P, ctypes.POINTER(mok_weights),
+                              ctypes.POINTER(mok_grads), _P]
+_lib.mok_read_device_status.restype = ctypes.c_int
+_lib.mok_read_device_status.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(ctypes.c_uint32), _P]
+
+EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
+            "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status")
+
+
+def _check(rc: int, where: str):
+    if rc != MOK_OK:
+        raise MokError(rc, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def mok_version() -> str:
+    return _lib.mok_version().decode()
+
+
+def make_config(minibatch_rows=512, macrobatch_rows=2048, num_ctas=0, precision=MOK_BF16) -> mok_config:
+    return mok_config(minibatch_rows, macrobatch_rows, num_ctas, precision, 0)
+
+
+def make_shape(T, H, I, E, K) -> mok_shape:
+    return mok_shape(T, H, I, E, K)
+
+
+def mok_workspace_bytes(cfg: mok_config, shape: mok_shape) -> int:
+    n = _lib.mok_workspace_bytes(ctypes.byref(cfg), ctypes.byref(shape))
+    if n == 0:
+        raise MokError(MOK_ERR_INVALID_ARG, "mok_workspace_bytes")
+    return n
+
+
+def mok_fwd_ctx_bytes(cfg: mok_config, shape: mok_shape) -> int:
+    n = _lib.mok_fwd_ctx_bytes(ctypes.byref(cfg), ctypes.byref(shape))
+    if n == 0:
+        raise MokError(MOK_ERR_INVALID_ARG, "mok_fwd_ctx_bytes")
+    return n
+
+
+def mok_mxfp8_quantize(x: torch.Tensor, out_q: torch.Tensor | None = None, out_s: torch.Tensor | None = None,
+                       stream=None):
+    """MXFP8 of a 2-D bf16 tensor: (E4M3 bytes [rows, cols] uint8, E8M0 scales [rows, cols/32] uint8)."""
+    rows, cols = x.shape
+    if out_q is None:
+        out_q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if out_s is None:
+        out_s = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+    _check(_lib.mok_mxfp8_quantize(_ptr(x, torch.bfloat16, "x"), rows, cols, _ptr(out_q, torch.uint8, "out_q"),
+                                   _ptr(out_s, torch.uint8, "out_s"), _stream(stream)), "mok_mxfp8_quantize")
+    return out_q, out_s
+
+
+@dataclass
+class Schedule:
+    """A built schedule plus the tensors it refers to (kept alive here)."""
+    c: mok_schedule
+    ws: torch.Tensor
+    topk_ids: torch.Tensor
+    topk_weights: torch.Tensor
+
+    def _view(self, field, n, dtype=torch.int32):
+        """Device tensor view of one schedule table (for tests and inspection)."""
+        ptr = getattr(self.c, field)
+        base = self.ws.data_ptr()
+        off = ptr - base
+        esz = torch.tensor([], dtype=dtype).element_size()
+        assert off % esz == 0 and off >= 0
+        return self.ws.view(torch.uint8)[off:off + n * esz].view(dtype)
+
+    def tables(self) -> dict:
+        E = self.c.shape.E
+        R = self.c.shape.T * self.c.shape.K
+        return dict(counts=self._view("counts", E), offsets=self._view("offsets", E + 1),
+                    poff=self._view("poff", E + 1), perm=self._view("perm", self.c.rpad_max),
+                    inv=self._view("inv", R), tiles=self._view("tiles", 4 * self.c.tiles_max).view(-1, 4),
+                    mblocks=self._view("mblocks", 4 * self.c.mblocks_max).view(-1, 4),
+                    meta=self._view("meta", 16), row_weight=self._view("row_weight", self.c.rpad_max, torch.float32),
+                    row_token=self._view("row_token", self.c.rpad_max))
+
+
+def alloc_workspace(cfg: mok_config, shape: mok_shape, device="cuda") -> torch.Tensor:
+    return torch.empty(mok_workspace_bytes(cfg, shape), dtype=torch.uint8, device=device)
+
+
+def alloc_fwd_ctx(cfg: mok_config, shape: mok_shape, device="cuda") -> torch.Tensor:
+    return torch.empty(mok_fwd_ctx_bytes(cfg, shape), dtype=torch.uint8, device=device)
+
+
+def mok_build_schedule(cfg: mok_config, shape: mok_shape, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                       ws: torch.Tensor, stream=None) -> Schedule:
+    s = mok_schedule()
+    _check(_lib.mok_build_schedule(ctypes.byref(cfg), ctypes.byref(shape), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                   _ptr(topk_weights, torch.float32, "topk_weights"), _ptr(ws, None, "ws"),
+                                   ws.numel() * ws.element_size(), ctypes.byref(s), _stream(stream)),
+           "mok_build_schedule")
+    return Schedule(s, ws, topk_ids, topk_weights)
+
+
+def weights_struct(Wg, Wu, Wd, mx: dict | None = None) -> mok_weights:
+    w = mok_weights()
+    w.w_gate = _ptr(Wg, torch.bfloat16, "w_gate")
+    w.w_up = _ptr(Wu, torch.bfloat16, "w_up")
+    w.w_down = _ptr(Wd, torch.bfloat16, "w_down")
+    if mx:
+        for k in ("q_gate", "s_gate", "q_up", "s_up", "q_down", "s_down"):
+            setattr(w, k, _ptr(mx.get(k), torch.uint8, k))
+    return w
+
+
+def mok_forward(sched: Schedule, x: torch.Tensor, weights: mok_weights, out: torch.Tensor, fwd_ctx: torch.Tensor,
+                stream=None) -> torch.Tensor:
+    _check(_lib.mok_forward(ctypes.byref(sched.c), _ptr(x, torch.bfloat16, "x"), ctypes.byref(weights),
+                            _ptr(out, torch.bfloat16, "out"), _ptr(fwd_ctx, None, "fwd_ctx"),
+                            fwd_ctx.numel() * fwd_ctx.element_size(), _stream(stream)), "mok_forward")
+    return out
+
+
+@dataclass
+class Grads:
+    dx: torch.Tensor
+    dw_gate: torch.Tensor
+    dw_up: torch.Tensor
+    dw_down: torch.Tensor
+    d_topk_weights: torch.Tensor
+
+    @staticmethod
+    def empty(T, H, I, E, K, device="cuda") -> "Grads":
+        return Grads(torch.empty((T, H), dtype=torch.bfloat16, device=device),
+                     torch.empty((E, I, H), dtype=torch.float32, device=device),
+                     torch.empty((E, I, H), dtype=torch.float32, device=device),
+                     torch.empty((E, H, I), dtype=torch.float32, device=device),
+                     torch.empty((T, K), dtype=torch.float32, device=device))
+
+    def struct(self) -> mok_grads:
+        g = mok_grads()
+        g.dx = _ptr(self.dx, torch.bfloat16, "dx")
+        g.dw_gate = _ptr(self.dw_gate, torch.float32, "dw_gate")
+        g.dw_up = _ptr(self.dw_up, torch.float32, "dw_up")
+        g.dw_down = _ptr(self.dw_down, torch.float32, "dw_down")
+        g.d_topk_weights = _ptr(self.d_topk_weights, torch.float32, "d_topk_weights")
+        return g
+
+
+def mok_backward(sched: Schedule, fwd_ctx: torch.Tensor, dy: torch.Tensor, weights: mok_weights, grads: Grads,
+                 stream=None) -> Grads:
+    gs = grads.struct()
+    _check(_lib.mok_backward(ctypes.byref(sched.c), _ptr(fwd_ctx, None, "fwd_ctx"), _ptr(dy, torch.bfloat16, "dy"),
+                             ctypes.byref(weights), ctypes.byref(gs), _stream(stream)), "mok_backward")
+    return grads
+
+
+def mok_read_device_status(sched: Schedule, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(_lib.mok_read_device_status(ctypes.byref(sched.c), ctypes.byref(v), _stream(stream)),
+           "mok_read_device_status")
+    return v.value
+
+
+class Layer:
+    """Convenience owner of the workspace and forward context of one (shape, config) pair."""
+
+    def __init__(self, T, H, I, E, K, cfg: mok_config | None = None, device="cuda"):
+        self.shape = make_shape(T, H, I, E, K)
+        self.cfg = cfg or make_config()
+        self.ws = alloc_workspace(self.cfg, self.shape, device)
+        self.ctx = alloc_fwd_ctx(self.cfg, self.shape, device)
+        self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        self.grads = Grads.empty(T, H, I, E, K, device)
+        self.sched = None
+
+    def schedule(self, topk_ids, topk_weights, stream=None) -> Schedule:
+        self.sched = mok_build_schedule(self.cfg, self.shape, topk_ids, topk_weights, self.ws, stream)
+        return self.sched
+
+    def forward(self, x, weights: mok_weights, stream=None):
+        return mok_forward(self.sched, x, weights, self.out, self.ctx, stream)
+
+    def backward(self, dy, weights: mok_weights, stream=None) -> Grads:
+        return mok_backward(self.sched, self.ctx, dy, weights, self.grads, stream)

@@ -1,0 +1,148 @@
+"""GPU forward / backward of the routed SwiGLU expert layer vs the fp64 oracle.
+
+Tolerance (BF16): max|gpu - oracle| / max|oracle| <= 2e-2 per output tensor; the GPU computes
+with bf16 operands, fp32 accumulation and bf16 intermediates (g, u, a, y, dg, du, dX rows), each
+rounding contributing about 2^-9 relative.  Small cases compare every element; the full-size
+workload compares sampled tokens and sampled weight-gradient entries the oracle computes one by
+one.  Determinism: repeats, grid sizes and minibatch settings must agree bitwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import TOL_BF16, ctx_views, rel_err, to_f64
+from mixture_experts_layer_build_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mok():
+    from mixture_experts_layer_build_gb300 import mok as m
+    return m
+
+
+def _run(mok, d, w, cfg, dev="cuda"):
+    x, ids, s, dY = (d[k].to(dev) for k in ("x", "topk_ids", "topk_weights", "dY"))
+    Wg, Wu, Wd = (d[k].to(dev) for k in ("Wg", "Wu", "Wd"))
+    layer = mok.Layer(w.T, w.H, w.I, w.E, w.K, cfg)
+    weights = mok.weights_struct(Wg, Wu, Wd)
+    layer.schedule(ids, s)
+    out = layer.forward(x, weights)
+    g = layer.backward(dY, weights)
+    torch.cuda.synchronize()
+    assert mok.mok_read_device_status(layer.sched) == 0
+    return layer, out, g
+
+
+def _np_args(d):
+    return (d["topk_ids"].numpy(), d["topk_weights"].numpy(), inputs.bits(d["x"]), inputs.bits(d["Wg"].cpu()),
+            inputs.bits(d["Wu"].cpu()), inputs.bits(d["Wd"].cpu()))
+
+
+SMALL = [
+    ("tiny", inputs.WORKLOADS["tiny"]),
+    ("ragged", inputs.custom(T=100, H=256, I=256, E=5, K=3)),
+    ("multi_tile", inputs.custom(T=700, H=512, I=384, E=3, K=2)),
+    ("one_expert", inputs.custom(T=64, H=128, I=128, E=1, K=1)),
+    ("wide", inputs.custom(T=96, H=1024, I=512, E=6, K=2)),
+]
+
+
+@pytest.mark.parametrize("name,w", SMALL, ids=[n for n, _ in SMALL])
+def test_forward_backward_full_parity(mok, name, w):
+    d = inputs.make(w, seed=1)
+    layer, out, g = _run(mok, d, w, mok.make_config(128, 256))
+    args = _np_args(d)
+    ref_out, it = oracle.forward(*args, intermediates=True)
+    ref = oracle.backward(*args, inputs.bits(d["dY"]))
+    errs = dict(out=rel_err(to_f64(out), ref_out), dX=rel_err(to_f64(g.dx), ref["dX"]),
+                dWg=rel_err(to_f64(g.dw_gate), ref["dWg"]), dWu=rel_err(to_f64(g.dw_up), ref["dWu"]),
+                dWd=rel_err(to_f64(g.dw_down), ref["dWd"]), dS=rel_err(to_f64(g.d_topk_weights), ref["dS"]))
+    # saved activations in the forward context, row inv[j] <-> slot j
+    inv = layer.sched.tables()["inv"].cpu().numpy().astype(np.int64)
+    cv = ctx_views(layer.ctx, layer.sched.c.rpad_max, w.H, w.I)
+    gu = to_f64(cv["gu"])[inv]
+    errs["g"] = rel_err(gu[:, :w.I], it["g"])
+    errs["u"] = rel_err(gu[:, w.I:], it["u"])
+    errs["a"] = rel_err(to_f64(cv["a"])[inv], it["a"])
+    errs["xg"] = rel_err(to_f64(cv["xg"])[inv], oracle.bf16_to_f64(args[2])[np.arange(w.R) // w.K])
+    bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
+    assert not bad, errs
+    assert errs["xg"] == 0.0  # the gather is a copy
+
+
+def test_unused_experts_get_exact_zero_gradients(mok):
+    w = inputs.custom(T=50, H=128, I=128, E=7, K=2)
+    d = inputs.make(w, seed=2)
+    ids = d["topk_ids"]
+    ids[ids == 3] = 4
+    ids[ids == 6] = 0
+    d["topk_ids"] = ids
+    _, _, g = _run(mok, d, w, mok.make_config(128, 128))
+    for e in (3, 6):
+        assert not g.dw_gate[e].any() and not g.dw_up[e].any() and not g.dw_down[e].any()
+
+
+def test_empty_batch(mok):
+    w = inputs.custom(T=0, H=128, I=128, E=4, K=2)
+    d = inputs.make(w, seed=0)
+    _, out, g = _run(mok, d, w, mok.make_config(128, 128))
+    assert out.numel() == 0
+    assert not g.dw_gate.any() and not g.dw_down.any()
+
+
+@pytest.fixture(scope="module")
+def full_size(mok):
+    """The T=4096, H=2048, I=1024, E=64, top-6 BF16 workload, run once."""
+    w = inputs.WORKLOADS["bf16_e64"]
+    d = inputs.make(w, seed=0)
+    layer, out, g = _run(mok, d, w, mok.make_config(512, 2048))
+    res = dict(out=out.clone(), dx=g.dx.clone(), dwg=g.dw_gate.clone(), dwu=g.dw_up.clone(), dwd=g.dw_down.clone(),
+               ds=g.d_topk_weights.clone())
+    return w, d, res
+
+
+def test_full_size_sampled_parity(mok, full_size):
+    w, d, r = full_size
+    args = _np_args(d)
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(w.T, size=48, replace=False))
+    ref_out = oracle.forward_tokens(*args, tok)
+    dX, dS = oracle.backward_tokens(*args, inputs.bits(d["dY"]), tok)
+    tk = torch.from_numpy(tok).cuda()
+    errs = dict(out=rel_err(to_f64(r["out"][tk]), ref_out), dX=rel_err(to_f64(r["dx"][tk]), dX),
+                dS=rel_err(to_f64(r["ds"][tk]), dS))
+    n = 96
+    for which, key, M, N in ((0, "dwg", w.I, w.H), (1, "dwu", w.I, w.H), (2, "dwd", w.H, w.I)):
+        t = r[key]
+        # the sample always holds the entry where the GPU tensor peaks, so a wrong peak cannot
+        # hide behind the denominator
+        flat = int(t.abs().argmax())
+        pe, pm, pc = np.unravel_index(flat, t.shape)
+        e = np.concatenate([[pe], rng.integers(0, w.E, n)])
+        m = np.concatenate([[pm], rng.integers(0, M, n)])
+        c = np.concatenate([[pc], rng.integers(0, N, n)])
+        ref = oracle.dw_entries(*args, inputs.bits(d["dY"]), np.full(n + 1, which), e, m, c)
+        got = t[torch.from_numpy(e).cuda(), torch.from_numpy(m).cuda(), torch.from_numpy(c).cuda()]
+        errs[key] = rel_err(to_f64(got), ref)
+    bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
+    assert not bad, errs
+
+
+def test_full_size_properties(full_size):
+    w, d, r = full_size
+    # every output finite, no expert gradient left unwritten (NaN from uninitialised memory)
+    for k, v in r.items():
+        assert torch.isfinite(v).all(), k
+
+
+def test_determinism_repeats_grids_and_minibatches(mok, full_size):
+    w, d, r = full_size
+    cfgs = [mok.make_config(512, 2048)] * 9 + [mok.make_config(128, 256, 37), mok.make_config(2048, 4096, 1),
+                                                 mok.make_config(256, 256, 300)]
+    for i, cfg in enumerate(cfgs):
+        _, out, g = _run(mok, d, w, cfg)
+        for k, v in dict(out=out, dx=g.dx, dwg=g.dw_gate, dwu=g.dw_up, dwd=g.dw_down, ds=g.d_topk_weights).items():
+            assert torch.equal(v, r[k]), (i, k)
