@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of the routed SwiGLU expert layer: one step = schedule + forward + backward.
+
+Default workload: T=4096 tokens, H=2048, I=1024, E=64 experts, top-6, BF16 (near-uniform softmax
+routing), synthetic seeded inputs.  Prints ONE JSON line (rank 0):
+  value     tokens/s of the whole job (all ranks), inputs resident in HBM, CUDA events on the
+            launching stream, max over ranks;
+  e2e       the same metric through the C ABI with host (pinned) inputs: H2D of x, ids, weights,
+            dY and D2H of out, dX, d_topk_weights inside every timed step;
+  roofline  the dominant kernel's algorithmic flops (or bytes) per launch over its average launch
+            time, measured live with per-launch CUDA events (the library's trace hook), against
+            the measured peak;
+  cpu_baseline  the fp64 CPU oracle as it stands, timed on a bounded token sample.
+``--impl reference`` times the oracle alone (the reference arm; rank 0 only).
+
+Multi-GPU (torchrun): every rank runs an independent data-parallel shard of the same shape (its
+own tokens); the layer has no collective, so N ranks are N replicas (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd+bwd tokens/s on 1×GB300 (BF16, MXFP8); % of tensor/HBM peak"
+UNIT = "tokens/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_PEAKS = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="bf16_e64")
+    p.add_argument("--minibatch", type=int, default=512)
+    p.add_argument("--macrobatch", type=int, default=2048)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU seconds of the oracle sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing
+# ------------------------------------------------------------------------------------------------
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+    return 0, 1, 0
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int, device) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.marks = {}
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="mok_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + \
+                    float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+            except ValueError:
+                ts = 0.0
+            try:
+                rows.append(dict(ts=ts, sm=float(parts[2]), smax=float(parts[3]), power=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        t0, t1 = self.marks.get("t0"), self.marks.get("t1")
+        timed = [r for r in rows if t0 is not None and t0 - 0.05 <= r["ts"] <= t1 + 0.05]
+        window = "timed region"
+        if len(timed) < 3:  # short timed region: use every sample of the benchmark run
+            timed, window = rows, "whole benchmark run (timed region shorter than the sampling period)"
+        if not timed:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = set()
+        for r in timed:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        loaded = [r["sm"] for r in timed if r["power"] > 200.0] or [r["sm"] for r in timed]
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": max(r["smax"] for r in timed),
+                "reasons": sorted(reasons), "samples": len(timed), "window": window,
+                "power_w_max": max(r["power"] for r in timed)}
+
+
+# ------------------------------------------------------------------------------------------------
+# algorithmic work per kernel (flops for tensor-core kernels, bytes for the HBM-bound ones)
+# ------------------------------------------------------------------------------------------------
+def kernel_work(w) -> dict:
+    R, H, I, T, K = w.R, w.H, w.I, w.T, w.K
+    f = lambda c: ("tensor", c * R * H * I)  # noqa: E731
+    return {
+        "gemm_fwd_gateup": f(4), "gemm_fwd_down": f(2), "gemm_dgrad1": f(2), "gemm_dgrad2": f(4),
+        "gemm_wgrad_gu": f(4), "gemm_wgrad_d": f(2),
+        # gather: unique token rows read once + routed rows written
+        "gather_x": ("hbm", T * H * 2 + R * H * 2), "gather_dy": ("hbm", T * H * 2 + R * H * 2),
+        # combine / dX reduce: routed rows read + weights/indices + token rows written
+        "combine": ("hbm", R * H * 2 + T * K * 8 + T * H * 2), "dx_reduce": ("hbm", R * H * 2 + T * K * 4 + T * H * 2),
+    }
+
+
+def src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_layer_build_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "mok.h"), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def traffic_for(kernel: str, workload: str):
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None, "no ncu capture committed"
+    d = json.load(open(PROFILE_TRAFFIC))
+    e = d.get(workload, {}).get(kernel)
+    if not e:
+        return None, "kernel not captured"
+    if e.get("src_hash") != src_hash():
+        return None, "kernel changed since the counters were taken"
+    return e["dram_bytes_per_launch"], e.get("note", "")
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle timing
+# ------------------------------------------------------------------------------------------------
+def oracle_sample_args(d, tokens: int):
+    from mixture_experts_layer_build_gb300 import inputs
+    ids = d["topk_ids"][:tokens].numpy()
+    s = d["topk_weights"][:tokens].numpy()
+    x = inputs.bits(d["x"][:tokens])
+    dY = inputs.bits(d["dY"][:tokens])
+    return ids, s, x, dY
+
+
+def time_oracle_step(d, wbits, tokens: int) -> float:
+    import oracle
+    ids, s, x, dY = oracle_sample_args(d, tokens)
+    Wg, Wu, Wd = wbits
+    t0 = time.perf_counter()
+    oracle.forward(ids, s, x, Wg, Wu, Wd)
+    oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
+    return time.perf_counter() - t0
+
+
+def calibrate_oracle_tokens(d, wbits, target_s: float, T: int) -> tuple[int, float]:
+    """Token count whose oracle fwd+bwd takes about target_s, from a linear fit through 8- and
+    32-token runs (the oracle's fixed cost is the dense dW initialisation)."""
+    a, b = min(8, T), min(32, T)
+    ta = time_oracle_step(d, wbits, a)
+    tb = time_oracle_step(d, wbits, b)
+    slope = (tb - ta) / (b - a) if b > a else tb / max(b, 1)
+    if slope <= 0:
+        slope = tb / b
+    fixed = max(ta - slope * a, 0.0)
+    tokens = int(max(a, min(T, (target_s - fixed) / slope)))
+    return tokens, tb
+
+
+def cores_used():
+    import oracle
+    return oracle.num_threads()
+
+
+# ------------------------------------------------------------------------------------------------
+def reference_arm(args, rank, ws):
+    """The oracle timed as it stands (fp64 C loops, all host cores), step = fwd + bwd of a bounded
+    token sample of the workload."""
+    if rank != 0:
+        return
+    from mixture_experts_layer_build_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    d = inputs.make(w, seed=0)
+    wbits = (inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+    per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    tokens, _ = calibrate_oracle_tokens(d, wbits, per_step_budget, w.T)
+    for _ in range(args.warmup):
+        time_oracle_step(d, wbits, tokens)
+    times = [time_oracle_step(d, wbits, tokens) for _ in range(args.steps)]
+    t = float(np.mean(times))
+    value = tokens / t
+    cores = cores_used()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"fwd+bwd of the first {tokens} of {w.T} tokens per step (all their routed "
+                                   f"rows, full dW), fp64 C loops with OpenMP"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, args, n):
+    wbytes = 3 * w.E * w.H * w.I * 2
+    return {"workload": f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} top-{w.K} {w.precision.upper()}, router "
+                        f"{w.router}, seeded synthetic", "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
+            "global_batch": w.T * n, "minibatch_rows": args.minibatch, "macrobatch_rows": args.macrobatch,
+            "parallelism": f"replicas x{n} (independent data-parallel shards; the layer has no collective)",
+            "l2": f"inputs larger than L2: {wbytes / 1e6:.0f} MB of expert weights streamed every step, no flush"}
+
+
+def ours(args, rank, ws, local_rank):
+    from mixture_experts_layer_build_gb300 import inputs, mok
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = inputs.WORKLOADS[args.workload]
+    d = inputs.make(w, seed=rank, weight_device=str(dev))
+    x, ids, s, dY = (d[k].to(dev) for k in ("x", "topk_ids", "topk_weights", "dY"))
+    Wg, Wu, Wd = d["Wg"], d["Wu"], d["Wd"]
+    cfg = mok.make_config(args.minibatch, args.macrobatch)
+    layer = mok.Layer(w.T, w.H, w.I, w.E, w.K, cfg, device=dev)
+    weights = mok.weights_struct(Wg, Wu, Wd)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(xx=x, ii=ids, ss=s, dd=dY):
+        layer.schedule(ii, ss, stream)
+        layer.forward(xx, weights, stream)
+        layer.backward(dd, weights, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+
+    # ---- timed region: inputs resident in HBM ----
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier(ws)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, ws, dev)
+    status = mok.mok_read_device_status(layer.sched, stream)
+
+    # ---- per-kernel times: the same K steps with the library's event trace ----
+    tr = mok.Tracer(capacity=20 * args.steps + 64)
+    with tr:
+        for _ in range(args.steps):
+            step()
+    recs = tr.records()
+    launches_per_step = len(recs) / args.steps
+    per = {}
+    for name, t in recs:
+        p = per.setdefault(name, [0.0, 0])
+        p[0] += t
+        p[1] += 1
+    traced_total = sum(v[0] for v in per.values())
+    kernels = {k: {"avg_ms": v[0] / v[1], "launches": v[1], "share": v[0] / traced_total} for k, v in per.items()}
+    work = kernel_work(w)
+    peaks, peak_src = load_peaks()
+    for k, v in kernels.items():
+        if k in work:
+            kind, amount = work[k]
+            if kind == "tensor":
+                v["tflops"] = amount / (v["avg_ms"] * 1e-3) / 1e12
+            else:
+                v["gbs"] = amount / (v["avg_ms"] * 1e-3) / 1e9
+    dom = max((k for k in kernels if k in work), key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
+    kind, amount = work[dom]
+    achieved_per_s = amount / (kernels[dom]["avg_ms"] * 1e-3)
+    traffic, tnote = traffic_for(dom, args.workload)
+    if kind == "tensor":
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved_per_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved_per_s / 1e12 / peak, "traffic": traffic}
+    else:
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved_per_s / 1e9, "peak": peak, "unit": "GB/s",
+                "frac": achieved_per_s / 1e9 / peak, "traffic": traffic}
+    roof.update({"kernel": dom, "peak_source": f"{peak_src} (burst bf16 GEMM / STREAM copy)"
+                 if peak_src == "measured" else "fallback", "traffic_note": tnote,
+                 "algorithmic_per_launch": amount})
+
+    # ---- end to end through the C ABI with host buffers ----
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    hx, hids, hs, hdy = pin(d["x"]), pin(d["topk_ids"]), pin(d["topk_weights"]), pin(d["dY"])
+    hout = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    hds = torch.empty((w.T, w.K), dtype=torch.float32).pin_memory()
+    dx_, dids, ds_, ddy = (torch.empty_like(t, device=dev) for t in (x, ids, s, dY))
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hs, hdy))
+    d2h = sum(t.numel() * t.element_size() for t in (hout, hdx, hds))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            dx_.copy_(hx, non_blocking=True)
+            dids.copy_(hids, non_blocking=True)
+            ds_.copy_(hs, non_blocking=True)
+            ddy.copy_(hdy, non_blocking=True)
+            step(dx_, dids, ds_, ddy)
+            hout.copy_(layer.out, non_blocking=True)
+            hdx.copy_(layer.grads.dx, non_blocking=True)
+            hds.copy_(layer.grads.d_topk_weights, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+    clk = clocks.stop()
+
+    result = None
+    if rank == 0:
+        tokens_per_s = w.T * ws / (ms_max * 1e-3)
+        result = {
+            "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init expert weights)",
+            "config": config_of(w, args, ws),
+            "tflops": w.flops() / (ms_max * 1e-3) / 1e12,
+            "roofline": roof,
+            "kernels": kernels,
+            "e2e": {"value": w.T * ws / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "launches_per_step": launches_per_step,
+            "clocks": clk,
+            "device_status": status,
+        }
+    return result, d, w
+
+
+def main():
+    args = parse()
+    rank, ws, local_rank = dist_init()
+    if args.impl == "reference":
+        reference_arm(args, rank, ws)
+        return
+    res, d, w = ours(args, rank, ws, local_rank)
+    if rank == 0:
+        if ws == 1 and not args.no_cpu_baseline:
+            from mixture_experts_layer_build_gb300 import inputs
+            wbits = (inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+            tokens, _ = calibrate_oracle_tokens(d, wbits, args.cpu_seconds, w.T)
+            t = time_oracle_step(d, wbits, tokens)
+            res["cpu_baseline"] = {"value": tokens / t, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                                   "sample": f"fp64 oracle fwd+bwd of the first {tokens} of {w.T} tokens (all their "
+                                             f"routed rows, full dW), {t:.1f} s"}
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -194,6 +194,26 @@ MOK_API mok_status mok_forward(const mok_schedule* sched, const void* x, const m
 MOK_API mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const void* dy, const mok_weights* w,
                         const mok_grads* g, void* stream);
 
+/* Kernel-level tracing for profiling.  Every kernel the library launches while a trace is set
+ * is bracketed by two cudaEventRecord calls on its stream, into caller-created events:
+ *   events    HOST array of 2 * capacity cudaEvent_t handles (as void*), created by the caller
+ *             (timing enabled); launch i uses events[2i] (before) and events[2i+1] (after).
+ *   kinds     HOST array of capacity int32: the kernel kind of launch i (mok_kernel_name).
+ *   count     launches recorded so far; the library increments it and stops at capacity.
+ * Pass NULL to stop tracing.  The trace is process-wide and not thread-safe: set it only around
+ * single-threaded profiling runs.  Event records add a stream operation per launch boundary. */
+typedef struct {
+  void** events;
+  int32_t* kinds;
+  int32_t capacity;
+  int32_t count;
+} mok_trace;
+
+MOK_API mok_status mok_set_trace(mok_trace* trace);
+
+/* Name of a kernel kind recorded in mok_trace.kinds (static host string; "?" when unknown). */
+MOK_API const char* mok_kernel_name(int32_t kind);
+
 /* Copy the schedule's device status word to *out (host pointer) after synchronising the stream.
  * The only call that blocks. */
 MOK_API mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream);

@@ -47,7 +47,9 @@ def build(verbose: bool = False, extra=None) -> str:
     objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
     if jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        r = subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+        cudalib = os.path.join(os.path.dirname(os.path.dirname(NVCC)), "lib64")
+        r = subprocess.run([NVCC, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", f"-rpath,{cudalib}", "-o", tmp,
+                            *objs], capture_output=True, text=True)
         if r.returncode:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link of libmok.so failed")

@@ -161,6 +161,22 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
   return r == CUDA_SUCCESS;
 }
 
+static mok_trace* g_trace = nullptr;
+
+void trace_begin(cudaStream_t s, int kind) {
+  mok_trace* t = g_trace;
+  if (!t || t->count >= t->capacity) return;
+  t->kinds[t->count] = kind;
+  cudaEventRecord(static_cast<cudaEvent_t>(t->events[2 * t->count]), s);
+}
+
+void trace_end(cudaStream_t s) {
+  mok_trace* t = g_trace;
+  if (!t || t->count >= t->capacity) return;
+  cudaEventRecord(static_cast<cudaEvent_t>(t->events[2 * t->count + 1]), s);
+  ++t->count;
+}
+
 }  // namespace mok
 
 using namespace mok;
@@ -261,14 +277,15 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
       !aligned16(w->w_down))
     return MOK_ERR_INVALID_ARG;
   cudaStream_t s = as_stream(stream);
-  if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H, ctx.xg, s))
+  if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H, ctx.xg,
+                         K_GATHER_X, s))
     return MOK_ERR_CUDA;
   const int g = grid_of(sched);
   int e = launch_fwd_gemms(z, *sched, ctx, st, *w, g, s);
   if (e < 0) return MOK_ERR_INVALID_ARG;
   if (e) return MOK_ERR_CUDA;
   return from_cuda(launch_combine(st.ybuf, sched->inv, sched->topk_weights, z.T, z.K, z.H,
-                                  static_cast<uint16_t*>(out), s));
+                                  static_cast<uint16_t*>(out), K_COMBINE, s));
 }
 
 mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const void* dy, const mok_weights* w,
@@ -292,7 +309,7 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   cudaStream_t s = as_stream(stream);
   const int grid = grid_of(sched);
   if (launch_gather_rows(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H, st.dyg,
-                         s))
+                         K_GATHER_DY, s))
     return MOK_ERR_CUDA;
   int e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 1, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
@@ -300,11 +317,26 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   if (launch_ds_reduce(st.dspart, sched->inv, z.R, n_tiles1, g->d_topk_weights, s)) return MOK_ERR_CUDA;
   e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 2, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
-  if (launch_combine(st.ybuf, sched->inv, nullptr, z.T, z.K, z.H, static_cast<uint16_t*>(g->dx), s))
+  if (launch_combine(st.ybuf, sched->inv, nullptr, z.T, z.K, z.H, static_cast<uint16_t*>(g->dx), K_DX_REDUCE, s))
     return MOK_ERR_CUDA;
   e = launch_wgrad_gemms(z, *sched, ctx, st, *g, grid, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
   return MOK_OK;
+}
+
+mok_status mok_set_trace(mok_trace* trace) {
+  if (trace && (!trace->events || !trace->kinds || trace->capacity < 0 || trace->count < 0))
+    return MOK_ERR_INVALID_ARG;
+  g_trace = trace;
+  return MOK_OK;
+}
+
+const char* mok_kernel_name(int32_t kind) {
+  static const char* names[K_NUM_KINDS] = {
+      "sched_hist",      "sched_scan",    "sched_scatter", "gather_x",       "gemm_fwd_gateup",
+      "gemm_fwd_down",   "combine",       "gather_dy",     "gemm_dgrad1",    "ds_reduce",
+      "gemm_dgrad2",     "dx_reduce",     "gemm_wgrad_gu", "gemm_wgrad_d",   "mxfp8_quantize"};
+  return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "?";
 }
 
 mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream) {

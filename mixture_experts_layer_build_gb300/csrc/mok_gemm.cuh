@@ -460,7 +460,15 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
     configured = true;
   }
   if (grid <= 0) return 0;
+  constexpr int kKind = VAR == V_FWD_GATEUP  ? K_GEMM_FWD_GATEUP
+                        : VAR == V_FWD_DOWN  ? K_GEMM_FWD_DOWN
+                        : VAR == V_DGRAD1    ? K_GEMM_DGRAD1
+                        : VAR == V_DGRAD2    ? K_GEMM_DGRAD2
+                        : VAR == V_WGRAD_GU  ? K_GEMM_WGRAD_GU
+                                             : K_GEMM_WGRAD_D;
+  trace_begin(stream, kKind);
   gemm_kernel<VAR, BN><<<grid, kGemmThreads, C::kSmemBytes, stream>>>(a, b, b2, args);
+  trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -38,13 +38,35 @@ size_t carve_ctx(const Sizes& z, char* base, Ctx* ctx);
 
 int sm_count();
 
+// Kernel kinds reported through mok_trace.
+enum KernelKind : int {
+  K_SCHED_HIST = 0,
+  K_SCHED_SCAN,
+  K_SCHED_SCATTER,
+  K_GATHER_X,
+  K_GEMM_FWD_GATEUP,
+  K_GEMM_FWD_DOWN,
+  K_COMBINE,
+  K_GATHER_DY,
+  K_GEMM_DGRAD1,
+  K_DS_REDUCE,
+  K_GEMM_DGRAD2,
+  K_DX_REDUCE,
+  K_GEMM_WGRAD_GU,
+  K_GEMM_WGRAD_D,
+  K_MXFP8_QUANTIZE,
+  K_NUM_KINDS
+};
+void trace_begin(cudaStream_t s, int kind);  // no-ops unless a trace is set
+void trace_end(cudaStream_t s);
+
 // launchers (return a cudaError_t as int)
 int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mok_schedule& s, const Staging& st,
                     cudaStream_t stream);
 int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                       int32_t H, uint16_t* dst, cudaStream_t stream);
+                       int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
 int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
-                   uint16_t* out, cudaStream_t stream);
+                   uint16_t* out, int kind, cudaStream_t stream);
 int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, float* ds,
                      cudaStream_t stream);
 int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sc,

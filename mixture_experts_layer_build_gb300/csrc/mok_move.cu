@@ -201,20 +201,24 @@ int grid_for(int64_t items, int per_block) {
 }  // namespace
 
 int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                       int32_t H, uint16_t* dst, cudaStream_t stream) {
+                       int32_t H, uint16_t* dst, int kind, cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
   const int grid = grid_for(rpad_max, kMoveThreads / 32);
+  trace_begin(stream, kind);
   gather_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), row_token, meta,
                                                         H / 8, reinterpret_cast<uint4*>(dst));
+  trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
 
 int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
-                   uint16_t* out, cudaStream_t stream) {
+                   uint16_t* out, int kind, cudaStream_t stream) {
   if (T <= 0) return 0;
   const int grid = grid_for(T, kMoveThreads / 32);
+  trace_begin(stream, kind);
   combine_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(y), inv, s, T, K, H / 8,
                                                     reinterpret_cast<uint4*>(out));
+  trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -222,7 +226,9 @@ int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n
                      cudaStream_t stream) {
   if (R <= 0) return 0;
   const int grid = static_cast<int>((R + kMoveThreads - 1) / kMoveThreads);
+  trace_begin(stream, K_DS_REDUCE);
   ds_reduce_kernel<<<grid, kMoveThreads, 0, stream>>>(part, inv, R, n_tiles, ds);
+  trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -231,8 +237,10 @@ int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_
   const int64_t nblocks = rows * (cols / 32);
   if (nblocks <= 0) return 0;
   const int grid = grid_for(nblocks, kMoveThreads);
+  trace_begin(stream, K_MXFP8_QUANTIZE);
   mxfp8_quantize_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(in), nblocks,
                                                            reinterpret_cast<uint4*>(q), sc);
+  trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
 

@@ -189,16 +189,22 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
   const int blocks = static_cast<int>((nchunks + kSchedWarps - 1) / kSchedWarps);
   if (blocks > 0) {
     const size_t sh = sizeof(int32_t) * kSchedWarps * (z.E + 1);
+    trace_begin(stream, K_SCHED_HIST);
     sched_hist_kernel<<<blocks, kSchedWarps * 32, sh, stream>>>(ids, z.R, z.E, nchunks, st.chunk_hist);
+    trace_end(stream);
   }
+  trace_begin(stream, K_SCHED_SCAN);
   sched_scan_kernel<<<1, 1024, 0, stream>>>(z.E, nchunks, st.chunk_hist, z.mb, z.MB, z.rpad_max, z.tiles_max,
                                             z.mblocks_max, s.counts, s.offsets, s.poff, s.perm, s.row_token,
                                             s.row_weight, s.tiles, s.mblocks, s.meta);
+  trace_end(stream);
   if (blocks > 0) {
     const size_t sh = sizeof(int32_t) * kSchedWarps * z.E;
+    trace_begin(stream, K_SCHED_SCATTER);
     sched_scatter_kernel<<<blocks, kSchedWarps * 32, sh, stream>>>(ids, w, z.R, z.K, z.E, nchunks, st.chunk_hist,
                                                                     s.poff, s.meta, s.perm, s.inv, s.row_token,
                                                                     s.row_weight);
+    trace_end(stream);
   }
   return static_cast<int>(cudaGetLastError());
 }

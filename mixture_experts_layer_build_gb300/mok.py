@@ -91,11 +91,23 @@ _lib.mok_forward.argtypes = [ctypes.POINTER(mok_schedule), _P, ctypes.POINTER(mo
 _lib.mok_backward.restype = ctypes.c_int
 _lib.mok_backward.argtypes = [ctypes.POINTER(mok_schedule), _P, _P, ctypes.POINTER(mok_weights),
                               ctypes.POINTER(mok_grads), _P]
+
+
+class mok_trace(ctypes.Structure):
+    _fields_ = [("events", ctypes.POINTER(ctypes.c_void_p)), ("kinds", ctypes.POINTER(ctypes.c_int32)),
+                ("capacity", ctypes.c_int32), ("count", ctypes.c_int32)]
+
+
+_lib.mok_set_trace.restype = ctypes.c_int
+_lib.mok_set_trace.argtypes = [ctypes.POINTER(mok_trace)]
+_lib.mok_kernel_name.restype = ctypes.c_char_p
+_lib.mok_kernel_name.argtypes = [ctypes.c_int32]
 _lib.mok_read_device_status.restype = ctypes.c_int
 _lib.mok_read_device_status.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(ctypes.c_uint32), _P]
 
 EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
-            "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status")
+            "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status", "mok_set_trace",
+            "mok_kernel_name")
 
 
 def _check(rc: int, where: str):
@@ -287,3 +299,43 @@ class Layer:
 
     def backward(self, dy, weights: mok_weights, stream=None) -> Grads:
         return mok_backward(self.sched, self.ctx, dy, weights, self.grads, stream)
+
+
+def mok_kernel_name(kind: int) -> str:
+    return _lib.mok_kernel_name(kind).decode()
+
+
+def mok_set_trace(trace: "mok_trace | None"):
+    _check(_lib.mok_set_trace(ctypes.byref(trace) if trace is not None else None), "mok_set_trace")
+
+
+class Tracer:
+    """Records a CUDA event pair around every kernel the library launches while active
+    (``with Tracer(n) as tr: ...``), then reports per-launch device times in ms."""
+
+    def __init__(self, capacity: int):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:
+            e.record()  # creates the underlying cudaEvent_t
+        torch.cuda.synchronize()
+        self._handles = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
+        self._kinds = (ctypes.c_int32 * capacity)()
+        self.trace = mok_trace(self._handles, self._kinds, capacity, 0)
+
+    def __enter__(self):
+        self.trace.count = 0
+        mok_set_trace(self.trace)
+        return self
+
+    def __exit__(self, *exc):
+        mok_set_trace(None)
+        return False
+
+    def records(self):
+        """[(kernel name, ms)] in launch order (synchronises)."""
+        torch.cuda.synchronize()
+        out = []
+        for i in range(self.trace.count):
+            out.append((mok_kernel_name(self._kinds[i]),
+                        self.events[2 * i].elapsed_time(self.events[2 * i + 1])))
+        return out
