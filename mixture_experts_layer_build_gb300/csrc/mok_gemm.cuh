@@ -66,7 +66,8 @@ struct GemmCfg {
   static constexpr uint32_t kBBytes = BN * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + 256;
+  static constexpr uint32_t kStagingBytes = 4 * 2 * 4096;  // 4 epilogue warps x 2 tiles of 4 KB
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + kStagingBytes + 256;
 };
 
 struct Unit {
@@ -146,115 +147,172 @@ __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 __device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
 
-__device__ __forceinline__ void load_bf16x32(const uint16_t* p, float (&v)[32]) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ uint4 ldg_v4(const uint16_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+
+// Per-warp output stager: two shared-memory tiles (4 KB apart) of 32 rows x ROW bytes in the TMA
+// swizzle layout of that row size -- 128-byte rows: 16-byte chunk j of row r sits at chunk
+// j ^ (r & 7); 64-byte rows: at j ^ ((r >> 1) & 3).  Both keep the 32 lanes' row writes free of
+// bank conflicts.  Each filled tile leaves as one asynchronous TMA tile store; a tile is refilled
+// only after its previous store has finished reading it.
+template <int ROW>
+struct Stager {
+  static constexpr int kChunks = ROW / 16;
+  uint32_t buf0;
+  int cur;
+  int lane;
+  __device__ __forceinline__ uint32_t acquire() {
+    if (lane == 0) bulk_wait_read_le1();
+    __syncwarp();
+    const uint32_t b = buf0 + (static_cast<uint32_t>(cur) << 12);
+    cur ^= 1;
+    return b;
+  }
+  // Lane r writes its row (kChunks chunks of 16 bytes) and the warp stores the tile at (c0, c1).
+  __device__ __forceinline__ void put_and_store(const uint4* ch, const CUtensorMap* tm, int c0, int c1) {
+    const uint32_t b = acquire();
+    const uint32_t row = b + static_cast<uint32_t>(lane) * ROW;
+    const int sw = ROW == 128 ? (lane & 7) : ((lane >> 1) & 3);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 x = q[i];
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[8 * i + 2 * j] = bf16_lo(w[j]);
-      v[8 * i + 2 * j + 1] = bf16_hi(w[j]);
+    for (int j = 0; j < kChunks; ++j) st_shared_v4(row + (static_cast<uint32_t>(j ^ sw) << 4), ch[j]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm, b, c0, c1);
+      bulk_commit();
     }
+  }
+  __device__ __forceinline__ void drain() {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+template <int N>
+__device__ __forceinline__ void pack_bf16(const float* v, uint4* ch) {
+#pragma unroll
+  for (int j = 0; j < N / 8; ++j)
+    ch[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                       pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r0[32], r1[32];
+  tmem_ld_32x32b_x32(taddr, r0);
+  tmem_ld_32x32b_x32(taddr + 32, r1);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __uint_as_float(r0[i]);
+    v[32 + i] = __uint_as_float(r1[i]);
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(uint16_t* p, const float (&v)[32]) {
-  uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    q[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+__device__ __forceinline__ void unpack8(uint4 x, float* v) {
+  v[0] = bf16_lo(x.x); v[1] = bf16_hi(x.x); v[2] = bf16_lo(x.y); v[3] = bf16_hi(x.y);
+  v[4] = bf16_lo(x.z); v[5] = bf16_hi(x.z); v[6] = bf16_lo(x.w); v[7] = bf16_hi(x.w);
 }
 
-// Epilogue of one unit for one accumulator row (`r` = row within the 128-row tile).
+template <int VAR>
+constexpr int epi_row_bytes() { return VAR == V_DGRAD1 ? 64 : 128; }
+
+// Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab.
+// tO0 / tO1 are the output tensor maps of the variant.
 template <int VAR, int BN>
-__device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int r, uint32_t taddr) {
-  const bool empty = w.kblocks == 0;
+__device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int lane, uint32_t taddr,
+                                              Stager<epi_row_bytes<VAR>()>& stg, const CUtensorMap* tO0,
+                                              const CUtensorMap* tO1) {
   if constexpr (VAR == V_FWD_GATEUP) {
-    const int64_t row = w.row0 + r;
+    // columns [0, BN/2) of the accumulator are gate, [BN/2, BN) up, for I columns i0 ...
     const int i0 = w.nt * (BN / 2);
-    uint16_t* gu = static_cast<uint16_t*>(a.out0) + row * (2 * static_cast<int64_t>(a.I));
-    uint16_t* av = static_cast<uint16_t*>(a.out1) + row * static_cast<int64_t>(a.I);
+    const int rowc = w.row0 + q * 32;
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
-      uint32_t rg[32], ru[32];
-      tmem_ld_32x32b_x32(taddr + c, rg);
-      tmem_ld_32x32b_x32(taddr + BN / 2 + c, ru);
-      tmem_ld_wait();
-      float g[32], u[32], o[32];
+    for (int c = 0; c < BN / 2; c += 64) {
+      float g[64], u[64];
+      tmem_ld64(taddr + c, g);
+      tmem_ld64(taddr + BN / 2 + c, u);
+      uint4 ch[8];
+      pack_bf16<64>(g, ch);
+      stg.put_and_store(ch, tO0, i0 + c, rowc);
+      pack_bf16<64>(u, ch);
+      stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        g[i] = __uint_as_float(rg[i]);
-        u[i] = __uint_as_float(ru[i]);
-        o[i] = silu_f(g[i]) * u[i];
-      }
-      store_bf16x32(gu + i0 + c, g);
-      store_bf16x32(gu + a.I + i0 + c, u);
-      store_bf16x32(av + i0 + c, o);
+      for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
+      pack_bf16<64>(g, ch);
+      stg.put_and_store(ch, tO1, i0 + c, rowc);
     }
   } else if constexpr (VAR == V_FWD_DOWN || VAR == V_DGRAD2) {
-    const int64_t row = w.row0 + r;
-    uint16_t* out = static_cast<uint16_t*>(a.out0) + row * static_cast<int64_t>(a.H) + w.nt * BN;
+    const int rowc = w.row0 + q * 32;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t rv[32];
-      tmem_ld_32x32b_x32(taddr + c, rv);
-      tmem_ld_wait();
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rv[i]);
-      store_bf16x32(out + c, v);
+    for (int c = 0; c < BN; c += 64) {
+      float v[64];
+      tmem_ld64(taddr + c, v);
+      uint4 ch[8];
+      pack_bf16<64>(v, ch);
+      stg.put_and_store(ch, tO0, w.nt * BN + c, rowc);
     }
   } else if constexpr (VAR == V_DGRAD1) {
     // dA' = dY Wd (this tile's BN columns of I); the forward's g, u, a come from the context.
-    const int64_t row = w.row0 + r;
+    // 32-column chunks: dg, du and s*a leave as 32 x 64-byte tiles.
+    const int64_t row = w.row0 + q * 32 + lane;
     const int64_t I = a.I;
     const int i0 = w.nt * BN;
     const uint16_t* gu = static_cast<const uint16_t*>(a.in0) + row * 2 * I;
     const uint16_t* av = static_cast<const uint16_t*>(a.in1) + row * I;
-    uint16_t* dgdu = static_cast<uint16_t*>(a.out0) + row * 2 * I;
-    uint16_t* as = static_cast<uint16_t*>(a.out1) + row * I;
     const float s = __ldg(a.row_weight + row);
+    const int rowc = w.row0 + q * 32;
     float part = 0.0f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t rv[32];
       tmem_ld_32x32b_x32(taddr + c, rv);
-      tmem_ld_wait();
-      float g[32], u[32], av32[32], dg[32], du[32], sa[32];
-      load_bf16x32(gu + i0 + c, g);
-      load_bf16x32(gu + I + i0 + c, u);
-      load_bf16x32(av + i0 + c, av32);
+      uint4 pg[4], pu[4], pa[4];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float dap = __uint_as_float(rv[i]);
-        part = fmaf(dap, av32[i], part);
-        const float da = s * dap;
-        const float sg = sigmoid_f(g[i]);
-        dg[i] = da * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
-        du[i] = da * g[i] * sg;
-        sa[i] = s * av32[i];
+      for (int j = 0; j < 4; ++j) {
+        pg[j] = ldg_v4(gu + i0 + c + 8 * j);
+        pu[j] = ldg_v4(gu + I + i0 + c + 8 * j);
+        pa[j] = ldg_v4(av + i0 + c + 8 * j);
       }
-      store_bf16x32(dgdu + i0 + c, dg);
-      store_bf16x32(dgdu + I + i0 + c, du);
-      store_bf16x32(as + i0 + c, sa);
+      tmem_ld_wait();
+      float dg[32], du[32], sa[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float g8[8], u8[8], a8[8];
+        unpack8(pg[j], g8);
+        unpack8(pu[j], u8);
+        unpack8(pa[j], a8);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int i = 8 * j + k;
+          const float dap = __uint_as_float(rv[i]);
+          part = fmaf(dap, a8[k], part);
+          const float da = s * dap;
+          const float sg = sigmoid_f(g8[k]);
+          dg[i] = da * u8[k] * sg * (1.0f + g8[k] * (1.0f - sg));
+          du[i] = da * g8[k] * sg;
+          sa[i] = s * a8[k];
+        }
+      }
+      uint4 ch[4];
+      pack_bf16<32>(dg, ch);
+      stg.put_and_store(ch, tO0, i0 + c, rowc);
+      pack_bf16<32>(du, ch);
+      stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
+      pack_bf16<32>(sa, ch);
+      stg.put_and_store(ch, tO1, i0 + c, rowc);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
-  } else {  // weight gradients, fp32 out
-    const int m = w.mt * kBM + r;
-    float* dst;
-    int64_t ld;
+  } else {  // weight gradients, fp32 out, 32-column tiles
+    const bool empty = w.kblocks == 0;
+    const int m0 = w.mt * kBM + q * 32;  // first of this warp's 32 output rows
+    const CUtensorMap* tm;
+    int r0;
     if constexpr (VAR == V_WGRAD_GU) {
-      ld = a.H;
-      dst = m < a.I ? static_cast<float*>(a.out0) + (static_cast<int64_t>(w.e) * a.I + m) * ld
-                    : static_cast<float*>(a.out1) + (static_cast<int64_t>(w.e) * a.I + (m - a.I)) * ld;
+      tm = m0 < a.I ? tO0 : tO1;
+      r0 = w.e * a.I + (m0 < a.I ? m0 : m0 - a.I);
     } else {
-      ld = a.I;
-      dst = static_cast<float*>(a.out0) + (static_cast<int64_t>(w.e) * a.H + m) * ld;
+      tm = tO0;
+      r0 = w.e * a.H + m0;
     }
-    dst += w.nt * BN;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t rv[32];
@@ -265,11 +323,10 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
 #pragma unroll
         for (int i = 0; i < 32; ++i) rv[i] = 0u;
       }
-      float4* q = reinterpret_cast<float4*>(dst + c);
+      uint4 ch[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        q[i] = make_float4(__uint_as_float(rv[4 * i]), __uint_as_float(rv[4 * i + 1]),
-                           __uint_as_float(rv[4 * i + 2]), __uint_as_float(rv[4 * i + 3]));
+      for (int j = 0; j < 8; ++j) ch[j] = make_uint4(rv[4 * j], rv[4 * j + 1], rv[4 * j + 2], rv[4 * j + 3]);
+      stg.put_and_store(ch, tm, w.nt * BN + c, r0);
     }
   }
 }
@@ -289,7 +346,8 @@ __device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity, u
 template <int VAR, int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
+                const __grid_constant__ CUtensorMap tmO1, const GemmArgs args) {
   using C = GemmCfg<BN>;
   constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);
   constexpr bool kBmn = (VAR >= V_DGRAD1);
@@ -300,7 +358,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
   uint8_t* gbase = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * C::kStageBytes);
+  const uint32_t staging = base + S * C::kStageBytes;  // 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * C::kStageBytes + C::kStagingBytes);
   // bars[0..S) full, [S..2S) empty, [2S, 2S+2) accumulator full, [2S+2, 2S+4) accumulator empty,
   // [2S+4] drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
@@ -328,6 +387,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmB2);
+    tma_prefetch_desc(&tmO0);
+    tma_prefetch_desc(&tmO1);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -415,6 +476,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    Stager<epi_row_bytes<VAR>()> stg{staging + static_cast<uint32_t>(warp - 2) * 8192u, 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
@@ -425,7 +487,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      gemm_epilogue<VAR, BN>(args, w, q * 32 + lane, taddr);
+      gemm_epilogue<VAR, BN>(args, w, q, lane, taddr, stg, &tmO0, &tmO1);
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       if (++acc == 2) {
@@ -433,6 +495,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    stg.drain();
   }
   tc_fence_before();
   __syncthreads();
@@ -447,10 +510,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ---------------------------------------------------------------------------------------------
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                     uint32_t box_outer);
+bool make_tmap_bf16_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                         uint32_t box_outer);
+bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                   uint32_t box_outer);
 
 template <int VAR, int BN>
-int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmArgs& args, int grid,
-                cudaStream_t stream) {
+int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o0,
+                const CUtensorMap& o1, const GemmArgs& args, int grid, cudaStream_t stream) {
   using C = GemmCfg<BN>;
   static bool configured = false;  // per process; the attribute is per function, set once
   if (!configured) {
@@ -467,7 +534,7 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
                         : VAR == V_WGRAD_GU  ? K_GEMM_WGRAD_GU
                                              : K_GEMM_WGRAD_D;
   trace_begin(stream, kKind);
-  gemm_kernel<VAR, BN><<<grid, kGemmThreads, C::kSmemBytes, stream>>>(a, b, b2, args);
+  gemm_kernel<VAR, BN><<<grid, kGemmThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, args);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

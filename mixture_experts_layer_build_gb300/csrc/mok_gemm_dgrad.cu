@@ -27,7 +27,7 @@ static int clamp_grid(int num_ctas, int64_t units) {
 
 int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                        const mok_weights& w, int num_ctas, int phase, cudaStream_t stream) {
-  CUtensorMap tA, tB, tB2;
+  CUtensorMap tA, tB, tB2, tO0, tO1;
   GemmArgs a = common_args(z, s);
   if (phase == 1) {
     const int BN = z.I % 256 == 0 ? 256 : 128;
@@ -40,9 +40,11 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.out0 = st.dgdu;
     a.out1 = st.as;
     a.out2 = st.dspart;
+    if (!make_tmap_bf16_sw64(&tO0, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
+    if (!make_tmap_bf16_sw64(&tO1, st.as, z.I, z.rpad_max, 32, 32)) return -1;
     const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
-    return BN == 256 ? launch_gemm<V_DGRAD1, 256>(tA, tB, tB, a, grid, stream)
-                     : launch_gemm<V_DGRAD1, 128>(tA, tB, tB, a, grid, stream);
+    return BN == 256 ? launch_gemm<V_DGRAD1, 256>(tA, tB, tB, tO0, tO1, a, grid, stream)
+                     : launch_gemm<V_DGRAD1, 128>(tA, tB, tB, tO0, tO1, a, grid, stream);
   }
   const int BN = z.H % 256 == 0 ? 256 : 128;
   if (!make_tmap_bf16(&tA, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 128)) return -1;
@@ -52,9 +54,10 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   a.k_blocks = 2 * z.I / kBK;
   a.kb_split = z.I / kBK;
   a.out0 = st.ybuf;
+  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
-  return BN == 256 ? launch_gemm<V_DGRAD2, 256>(tA, tB, tB2, a, grid, stream)
-                   : launch_gemm<V_DGRAD2, 128>(tA, tB, tB2, a, grid, stream);
+  return BN == 256 ? launch_gemm<V_DGRAD2, 256>(tA, tB, tB2, tO0, tO0, a, grid, stream)
+                   : launch_gemm<V_DGRAD2, 128>(tA, tB, tB2, tO0, tO0, a, grid, stream);
 }
 
 }  // namespace mok

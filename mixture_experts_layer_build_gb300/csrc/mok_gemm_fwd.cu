@@ -24,7 +24,7 @@ static int clamp_grid(int num_ctas, int64_t units) {
 
 int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st, const mok_weights& w,
                      int num_ctas, cudaStream_t stream) {
-  CUtensorMap tA, tB, tB2;
+  CUtensorMap tA, tB, tB2, tO0, tO1;
   GemmArgs a = common_args(z, s);
   // [g | u] = Xg [Wg_e | Wu_e]^T : 128 gate columns and the same 128 up columns per tile
   if (!make_tmap_bf16(&tA, ctx.xg, z.H, z.rpad_max, 64, 128)) return -1;
@@ -34,7 +34,10 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   a.k_blocks = z.H / kBK;
   a.out0 = ctx.gu;
   a.out1 = ctx.a;
-  int rc = launch_gemm<V_FWD_GATEUP, 256>(tA, tB, tB2, a, clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
+  if (!make_tmap_bf16(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 32)) return -1;
+  if (!make_tmap_bf16(&tO1, ctx.a, z.I, z.rpad_max, 64, 32)) return -1;
+  int rc = launch_gemm<V_FWD_GATEUP, 256>(tA, tB, tB2, tO0, tO1, a, clamp_grid(num_ctas, z.mblocks_max * a.n_tiles),
+                                          stream);
   if (rc) return rc;
   // y = a Wd_e^T
   const int BN = z.H % 256 == 0 ? 256 : 128;
@@ -44,9 +47,10 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   a.k_blocks = z.I / kBK;
   a.out0 = st.ybuf;
   a.out1 = nullptr;
+  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
-  return BN == 256 ? launch_gemm<V_FWD_DOWN, 256>(tA, tB, tB, a, grid, stream)
-                   : launch_gemm<V_FWD_DOWN, 128>(tA, tB, tB, a, grid, stream);
+  return BN == 256 ? launch_gemm<V_FWD_DOWN, 256>(tA, tB, tB, tO0, tO0, a, grid, stream)
+                   : launch_gemm<V_FWD_DOWN, 128>(tA, tB, tB, tO0, tO0, a, grid, stream);
 }
 
 }  // namespace mok

@@ -7,7 +7,7 @@ namespace mok {
 
 int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                        const mok_grads& g, int num_ctas, cudaStream_t stream) {
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tO0, tO1;
   GemmArgs a{};
   a.poff = s.poff;
   a.E = z.E;
@@ -23,10 +23,12 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.n_tiles = z.H / BN;
     a.out0 = g.dw_gate;
     a.out1 = g.dw_up;
+    if (!make_tmap_f32(&tO0, g.dw_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 32, 32)) return -1;
+    if (!make_tmap_f32(&tO1, g.dw_up, z.H, static_cast<uint64_t>(z.E) * z.I, 32, 32)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
     const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
-    const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256>(tA, tB, tB, a, grid, stream)
-                             : launch_gemm<V_WGRAD_GU, 128>(tA, tB, tB, a, grid, stream);
+    const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256>(tA, tB, tB, tO0, tO1, a, grid, stream)
+                             : launch_gemm<V_WGRAD_GU, 128>(tA, tB, tB, tO0, tO1, a, grid, stream);
     if (rc) return rc;
   }
   // dWd_e = dYg_e^T (s a)_e   (M = H, N = I)
@@ -38,10 +40,11 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.n_tiles = z.I / BN;
     a.out0 = g.dw_down;
     a.out1 = nullptr;
+    if (!make_tmap_f32(&tO0, g.dw_down, z.I, static_cast<uint64_t>(z.E) * z.H, 32, 32)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
     const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
-    return BN == 256 ? launch_gemm<V_WGRAD_D, 256>(tA, tB, tB, a, grid, stream)
-                     : launch_gemm<V_WGRAD_D, 128>(tA, tB, tB, a, grid, stream);
+    return BN == 256 ? launch_gemm<V_WGRAD_D, 256>(tA, tB, tB, tO0, tO0, a, grid, stream)
+                     : launch_gemm<V_WGRAD_D, 128>(tA, tB, tB, tO0, tO0, a, grid, stream);
   }
 }
 
