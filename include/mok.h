@@ -214,6 +214,29 @@ MOK_API mok_status mok_set_trace(mok_trace* trace);
 /* Name of a kernel kind recorded in mok_trace.kinds (static host string; "?" when unknown). */
 MOK_API const char* mok_kernel_name(int32_t kind);
 
+/* Schedule build for callers that cannot allocate device memory.  The pages have no counterpart
+ * to this call: it exists for code that may not call cudaMalloc (or any allocating routine) while
+ * it runs, e.g. a runtime that only hands out fixed, pre-sized buffers.  It computes exactly the
+ * tables of mok_build_schedule, but its scratch (the per-chunk expert histogram) lives in a
+ * fixed array inside the library: 2 MiB of device memory per GPU that loads the library, held
+ * until the process exits.
+ *   sched   HOST struct.  On entry the caller sets these DEVICE pointers to its own buffers:
+ *           counts [E], offsets [E+1], poff [E+1], perm [rpad_max], inv [T*K], tiles
+ *           [tiles_max*4], mblocks [mblocks_max*4], meta [16], row_weight [rpad_max] (fp32),
+ *           row_token [rpad_max], with rpad_max = T*K + 127*E, tiles_max = ceil(T*K / mb) + E,
+ *           mblocks_max = floor(rpad_max / 128).  The call fills the remaining fields (status
+ *           points at meta[15]; ws is NULL).  Such a schedule holds no workspace, so it serves
+ *           inspection and the caller's own kernels, not mok_forward / mok_backward.
+ * Limit: ceil(T*K / 512) * (E + 1) <= 524288, else MOK_ERR_UNSUPPORTED is returned before any
+ * work is enqueued.  The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls share the one
+ * array, so calls whose work overlaps on the GPU (different streams, or different host threads)
+ * race; serialise them.  Nothing needs clearing between calls: every scratch entry a call reads,
+ * it has written first. */
+MOK_API mok_status mok_build_schedule_noalloc(const mok_config* cfg, const mok_shape* shape,
+                                              const int32_t* topk_ids, const float* topk_weights,
+                                              mok_schedule* sched, void* stream);
+
 /* Copy the schedule's device status word to *out (host pointer) after synchronising the stream.
  * The only call that blocks. */
 MOK_API mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream);

@@ -107,7 +107,10 @@ _lib.mok_read_device_status.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POI
 
 EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
             "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status", "mok_set_trace",
-            "mok_kernel_name")
+            "mok_kernel_name", "mok_build_schedule_noalloc")
+_lib.mok_build_schedule_noalloc.restype = ctypes.c_int
+_lib.mok_build_schedule_noalloc.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape), _P, _P,
+                                            ctypes.POINTER(mok_schedule), _P]
 
 
 def _check(rc: int, where: str):
