@@ -10,11 +10,13 @@
 //   WGRAD_GU    [dWg;dWu]_e = [dg|du]_e^T Xg_e                                  (K = rows of e, A,B MN-major)
 //   WGRAD_D     dWd_e = dYg_e^T (s a)_e                                         (K = rows of e, A,B MN-major)
 //
-// Roles (192 threads): warp 0 lane 0 issues TMA tile loads into a ring of shared-memory stages;
-// warp 1 owns the tensor memory and its lane 0 issues tcgen05.mma (M = 128, N = BN, K = 16) into
-// one of two TMEM accumulators; warps 2..5 drain the other accumulator (tcgen05.ld), apply the
-// epilogue and store to global memory.  Every output element is produced by exactly one CTA with a
-// fixed K order, so results are bitwise independent of the grid size and of the tile order.
+// Roles: warp 0 lane 0 issues TMA tile loads into a ring of shared-memory stages; warp 1 owns the
+// tensor memory and its lane 0 issues tcgen05.mma (M = 128, N = BN, K = 16) into one of two TMEM
+// accumulators; four epilogue warps (one per TMEM lane quarter) drain the other accumulator
+// (tcgen05.ld), apply the epilogue math and write through swizzled shared tiles with TMA tile
+// stores.  Every output element is produced by
+// exactly one CTA with a fixed K order, so results are bitwise independent of the grid size and of
+// the tile order.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -36,7 +38,6 @@ enum GemmVariant : int {
 constexpr int kBM = 128;      // MMA M (rows of the accumulator = TMEM lanes)
 constexpr int kBK = 64;       // bf16 elements per K block: one 128-byte swizzle row
 constexpr int kUmmaK = 16;    // K of one tcgen05.mma.kind::f16
-constexpr int kGemmThreads = 192;
 
 struct GemmArgs {
   // work enumeration
@@ -59,14 +60,17 @@ struct GemmArgs {
   uint32_t* status;
 };
 
-template <int BN>
+template <int VAR, int BN>
 struct GemmCfg {
   static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kStageBufs = 2;  // staging tiles per epilogue warp
+  static constexpr int kEpiWarps = 4;   // one warp per TMEM lane quarter
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = kBM * kBK * 2;
   static constexpr uint32_t kBBytes = BN * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;
-  static constexpr uint32_t kStagingBytes = 4 * 2 * 4096;  // 4 epilogue warps x 2 tiles of 4 KB
+  static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * 4096;  // per warp: tiles of 4 KB
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + kStagingBytes + 256;
 };
 
@@ -144,27 +148,29 @@ __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int 
   }
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
-__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + __expf(-g)); }
+// SwiGLU pieces in fp32 with the fast approximate division (about 2 ulp; the results are rounded to
+// bf16 next, 2^-9).
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 __device__ __forceinline__ uint4 ldg_v4(const uint16_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
-// Per-warp output stager: two shared-memory tiles (4 KB apart) of 32 rows x ROW bytes in the TMA
+// Per-warp output stager: NBUF shared-memory tiles (4 KB apart) of 32 rows x ROW bytes in the TMA
 // swizzle layout of that row size -- 128-byte rows: 16-byte chunk j of row r sits at chunk
 // j ^ (r & 7); 64-byte rows: at j ^ ((r >> 1) & 3).  Both keep the 32 lanes' row writes free of
 // bank conflicts.  Each filled tile leaves as one asynchronous TMA tile store; a tile is refilled
-// only after its previous store has finished reading it.
-template <int ROW>
+// only after its previous store has finished reading it, so up to NBUF stores are in flight.
+template <int ROW, int NBUF>
 struct Stager {
   static constexpr int kChunks = ROW / 16;
   uint32_t buf0;
   int cur;
   int lane;
   __device__ __forceinline__ uint32_t acquire() {
-    if (lane == 0) bulk_wait_read_le1();
+    if (lane == 0) bulk_wait_read<NBUF - 1>();
     __syncwarp();
     const uint32_t b = buf0 + (static_cast<uint32_t>(cur) << 12);
-    cur ^= 1;
+    cur = cur + 1 == NBUF ? 0 : cur + 1;
     return b;
   }
   // Lane r writes its row (kChunks chunks of 16 bytes) and the warp stores the tile at (c0, c1).
@@ -212,15 +218,39 @@ __device__ __forceinline__ void unpack8(uint4 x, float* v) {
   v[4] = bf16_lo(x.z); v[5] = bf16_hi(x.z); v[6] = bf16_lo(x.w); v[7] = bf16_hi(x.w);
 }
 
+// Hand the accumulator back to the MMA warp once this thread has read its last TMEM column.
+__device__ __forceinline__ void release_acc(uint32_t tempty) {
+  tc_fence_before();
+  mbar_arrive(tempty);
+}
+
+// The forward context's g, u, a for one 32-column chunk of one row (DGRAD1 epilogue operand).
+struct Dg1Chunk {
+  uint4 g[4], u[4], a[4];
+};
+__device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, int q, int lane, int c, Dg1Chunk& d) {
+  const int64_t row = w.row0 + q * 32 + lane;
+  const int64_t I = a.I;
+  const uint16_t* gu = static_cast<const uint16_t*>(a.in0) + row * 2 * I + c;
+  const uint16_t* av = static_cast<const uint16_t*>(a.in1) + row * I + c;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    d.g[j] = ldg_v4(gu + 8 * j);
+    d.u[j] = ldg_v4(gu + I + 8 * j);
+    d.a[j] = ldg_v4(av + 8 * j);
+  }
+}
+
 template <int VAR>
 constexpr int epi_row_bytes() { return VAR == V_DGRAD1 ? 64 : 128; }
 
 // Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab.
-// tO0 / tO1 are the output tensor maps of the variant.
-template <int VAR, int BN>
+// tO0 / tO1 are the output tensor maps of the variant; `tempty` is released as soon as the last
+// accumulator column has been read.  `pre` holds DGRAD1's first prefetched context chunk.
+template <int VAR, int BN, class Stg>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int lane, uint32_t taddr,
-                                              Stager<epi_row_bytes<VAR>()>& stg, const CUtensorMap* tO0,
-                                              const CUtensorMap* tO1) {
+                                              Stg& stg, const CUtensorMap* tO0, const CUtensorMap* tO1,
+                                              uint32_t tempty, Dg1Chunk& pre) {
   if constexpr (VAR == V_FWD_GATEUP) {
     // columns [0, BN/2) of the accumulator are gate, [BN/2, BN) up, for I columns i0 ...
     const int i0 = w.nt * (BN / 2);
@@ -230,6 +260,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       float g[64], u[64];
       tmem_ld64(taddr + c, g);
       tmem_ld64(taddr + BN / 2 + c, u);
+      if (c + 64 >= BN / 2) release_acc(tempty);
       uint4 ch[8];
       pack_bf16<64>(g, ch);
       stg.put_and_store(ch, tO0, i0 + c, rowc);
@@ -246,59 +277,51 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     for (int c = 0; c < BN; c += 64) {
       float v[64];
       tmem_ld64(taddr + c, v);
+      if (c + 64 >= BN) release_acc(tempty);
       uint4 ch[8];
       pack_bf16<64>(v, ch);
       stg.put_and_store(ch, tO0, w.nt * BN + c, rowc);
     }
   } else if constexpr (VAR == V_DGRAD1) {
-    // dA' = dY Wd (this tile's BN columns of I); the forward's g, u, a come from the context.
-    // 32-column chunks: dg, du and s*a leave as 32 x 64-byte tiles.
+    // dA' = dY Wd (this tile's BN columns of I); the forward's g, u, a come from the context,
+    // fetched one 32-column chunk ahead.  dg, du and s*a leave as 32 x 64-byte tiles.
     const int64_t row = w.row0 + q * 32 + lane;
-    const int64_t I = a.I;
     const int i0 = w.nt * BN;
-    const uint16_t* gu = static_cast<const uint16_t*>(a.in0) + row * 2 * I;
-    const uint16_t* av = static_cast<const uint16_t*>(a.in1) + row * I;
     const float s = __ldg(a.row_weight + row);
     const int rowc = w.row0 + q * 32;
     float part = 0.0f;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
+      const Dg1Chunk cur = pre;
+      if (c + 32 < BN) dgrad1_fetch(a, w, q, lane, i0 + c + 32, pre);
       uint32_t rv[32];
       tmem_ld_32x32b_x32(taddr + c, rv);
-      uint4 pg[4], pu[4], pa[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        pg[j] = ldg_v4(gu + i0 + c + 8 * j);
-        pu[j] = ldg_v4(gu + I + i0 + c + 8 * j);
-        pa[j] = ldg_v4(av + i0 + c + 8 * j);
-      }
       tmem_ld_wait();
-      float dg[32], du[32], sa[32];
+      if (c + 32 >= BN) release_acc(tempty);
+      uint4 cdg[4], cdu[4], csa[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float g8[8], u8[8], a8[8];
-        unpack8(pg[j], g8);
-        unpack8(pu[j], u8);
-        unpack8(pa[j], a8);
+        float g8[8], u8[8], a8[8], dg[8], du[8], sa[8];
+        unpack8(cur.g[j], g8);
+        unpack8(cur.u[j], u8);
+        unpack8(cur.a[j], a8);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const int i = 8 * j + k;
-          const float dap = __uint_as_float(rv[i]);
+          const float dap = __uint_as_float(rv[8 * j + k]);
           part = fmaf(dap, a8[k], part);
           const float da = s * dap;
           const float sg = sigmoid_f(g8[k]);
-          dg[i] = da * u8[k] * sg * (1.0f + g8[k] * (1.0f - sg));
-          du[i] = da * g8[k] * sg;
-          sa[i] = s * a8[k];
+          dg[k] = da * u8[k] * sg * (1.0f + g8[k] * (1.0f - sg));
+          du[k] = da * g8[k] * sg;
+          sa[k] = s * a8[k];
         }
+        pack_bf16<8>(dg, cdg + j);
+        pack_bf16<8>(du, cdu + j);
+        pack_bf16<8>(sa, csa + j);
       }
-      uint4 ch[4];
-      pack_bf16<32>(dg, ch);
-      stg.put_and_store(ch, tO0, i0 + c, rowc);
-      pack_bf16<32>(du, ch);
-      stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
-      pack_bf16<32>(sa, ch);
-      stg.put_and_store(ch, tO1, i0 + c, rowc);
+      stg.put_and_store(cdg, tO0, i0 + c, rowc);
+      stg.put_and_store(cdu, tO0, a.I + i0 + c, rowc);
+      stg.put_and_store(csa, tO1, i0 + c, rowc);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else {  // weight gradients, fp32 out, 32-column tiles
@@ -313,12 +336,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       tm = tO0;
       r0 = w.e * a.H + m0;
     }
+    if (empty) release_acc(tempty);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t rv[32];
       if (!empty) {
         tmem_ld_32x32b_x32(taddr + c, rv);
         tmem_ld_wait();
+        if (c + 32 >= BN) release_acc(tempty);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) rv[i] = 0u;
@@ -344,11 +369,11 @@ __device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity, u
 }
 
 template <int VAR, int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
                 const __grid_constant__ CUtensorMap tmO1, const GemmArgs args) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<VAR, BN>;
   constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);
   constexpr bool kBmn = (VAR >= V_DGRAD1);
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
@@ -379,7 +404,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), 32 * C::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -476,20 +501,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    Stager<epi_row_bytes<VAR>()> stg{staging + static_cast<uint32_t>(warp - 2) * 8192u, 0, lane};
+    Stager<epi_row_bytes<VAR>(), C::kStageBufs> stg{
+        staging + static_cast<uint32_t>(warp - 2) * (C::kStageBufs * 4096u), 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       const Unit w = gemm_decode<VAR>(args, u);
+      Dg1Chunk pre;
+      if constexpr (VAR == V_DGRAD1) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);  // before the wait
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      gemm_epilogue<VAR, BN>(args, w, q, lane, taddr, stg, &tmO0, &tmO1);
-      tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      gemm_epilogue<VAR, BN>(args, w, q, lane, taddr, stg, &tmO0, &tmO1, tempty_bar(acc), pre);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -518,7 +544,7 @@ bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
 template <int VAR, int BN>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o0,
                 const CUtensorMap& o1, const GemmArgs& args, int grid, cudaStream_t stream) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<VAR, BN>;
   static bool configured = false;  // per process; the attribute is per function, set once
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -534,7 +560,7 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
                         : VAR == V_WGRAD_GU  ? K_GEMM_WGRAD_GU
                                              : K_GEMM_WGRAD_D;
   trace_begin(stream, kKind);
-  gemm_kernel<VAR, BN><<<grid, kGemmThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, args);
+  gemm_kernel<VAR, BN><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, args);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

@@ -45,11 +45,13 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* 
 }
 
 // out[t] = bf16( sum_{k = 0..K-1 ascending} w[t,k] * y[inv[t*K+k]] ), fp32 accumulation; w == nullptr
-// means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.
+// means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.  The K
+// row loads of a vector are issued together (8 at a time) before the fixed-order FMA chain.
 __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __restrict__ y,
                                                               const int32_t* __restrict__ inv,
                                                               const float* __restrict__ w, int64_t T, int K,
                                                               int64_t vecs, uint4* __restrict__ out) {
+  constexpr int kBatch = 8;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); t < T;
@@ -58,16 +60,27 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __re
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      for (int k = 0; k < K; ++k) {
-        const int row = __ldg(inv + t * K + k);
-        if (row < 0) continue;
-        const float wk = w ? __ldg(w + t * K + k) : 1.0f;
-        const uint4 v = __ldg(y + static_cast<int64_t>(row) * vecs + c);
-        const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+      for (int k0 = 0; k0 < K; k0 += kBatch) {
+        uint4 v[kBatch];
+        float wk[kBatch];
+        bool use[kBatch];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] = fmaf(wk, bf16_lo(p[i]), acc[2 * i]);
-          acc[2 * i + 1] = fmaf(wk, bf16_hi(p[i]), acc[2 * i + 1]);
+        for (int b = 0; b < kBatch; ++b) {
+          const int k = k0 + b;
+          const int row = k < K ? __ldg(inv + t * K + k) : -1;
+          use[b] = row >= 0;
+          wk[b] = (use[b] && w) ? __ldg(w + t * K + k) : 1.0f;
+          v[b] = use[b] ? __ldg(y + static_cast<int64_t>(row) * vecs + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          if (!use[b]) continue;
+          const uint32_t p[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wk[b], bf16_lo(p[i]), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wk[b], bf16_hi(p[i]), acc[2 * i + 1]);
+          }
         }
       }
       out[t * vecs + c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),

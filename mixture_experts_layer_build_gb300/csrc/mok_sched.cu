@@ -6,33 +6,49 @@
 // step is needed (every size here is bounded on the host, nothing is read back).
 //
 // Three launches, all integer work, bit-exact by construction:
-//   1. per-warp histograms of 512-slot chunks (shared-memory integer atomics: order-free);
-//   2. one CTA: per-expert exclusive scan over chunks, block-wide warp-shuffle scans over experts
-//      (offsets, padded offsets, tile starts), the tile and block tables, padding rows;
-//   3. per-warp stable scatter: chunks walked in 32-slot pieces in order, equal experts ranked
-//      by lane with __match_any_sync, so slots keep ascending order inside each expert.
+//   1. per-warp histograms of 512-slot chunks (shared-memory integer atomics: order-free), all of
+//      a warp's id loads in flight together;
+//   2. one CTA: a two-level scan -- 32 chunk groups x experts summed with loads coalesced across
+//      experts, a per-expert scan over the groups, block-wide warp-shuffle scans over experts
+//      (offsets, padded offsets, tile starts) -- then the tile and block tables, the padding rows,
+//      and every chunk's absolute first row per expert written back;
+//   3. per-warp stable scatter: a chunk walked in 32-slot pieces in order, equal experts ranked
+//      by lane with __match_any_sync, so slots keep ascending order inside each expert.  Two warps
+//      per CTA spread the scattered row writes over many SMs.
+#include <climits>
+
 #include "mok_internal.cuh"
 #include "mok_ptx.cuh"
 
 namespace mok {
 namespace {
 
-__global__ void __launch_bounds__(kSchedWarps * 32) sched_hist_kernel(const int32_t* __restrict__ ids, int64_t R,
-                                                                     int E, int64_t nchunks,
-                                                                     int32_t* __restrict__ chunk_hist) {
+constexpr int kHistWarps = 2;                    // warps per CTA of the histogram / scatter launches
+constexpr int kPieces = kSchedChunk / 32;        // 32-slot pieces per chunk
+constexpr int kBatch = 8;                        // pieces whose loads are in flight together
+
+__global__ void __launch_bounds__(kHistWarps * 32) sched_hist_kernel(const int32_t* __restrict__ ids, int64_t R,
+                                                                    int E, int64_t nchunks,
+                                                                    int32_t* __restrict__ chunk_hist) {
   extern __shared__ int32_t sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kSchedWarps + warp;
+  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kHistWarps + warp;
   int32_t* h = sh + warp * (E + 1);
   for (int e = lane; e <= E; e += 32) h[e] = 0;
   __syncwarp();
   if (chunk >= nchunks) return;
   const int64_t j0 = chunk * kSchedChunk;
-  for (int i = lane; i < kSchedChunk; i += 32) {
-    const int64_t j = j0 + i;
-    if (j < R) {
-      int e = ids[j];
-      if (e < 0 || e >= E) e = E;  // column E counts invalid ids
+  for (int p0 = 0; p0 < kPieces; p0 += kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t j = j0 + (p0 + b) * 32 + lane;
+      ev[b] = j < R ? __ldg(ids + j) : INT32_MIN;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (ev[b] == INT32_MIN) continue;
+      const int e = (ev[b] < 0 || ev[b] >= E) ? E : ev[b];  // column E counts invalid ids
       atomicAdd(&h[e], 1);
     }
   }
@@ -82,20 +98,32 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
                                                          int32_t* __restrict__ perm, int32_t* __restrict__ row_token,
                                                          float* __restrict__ row_weight, int32_t* __restrict__ tiles,
                                                          int32_t* __restrict__ mblocks, int32_t* __restrict__ meta) {
+  extern __shared__ int32_t part[];  // [32 chunk groups][E + 1]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int W = E + 1;
+  const int64_t L = (nchunks + 31) / 32;  // chunks per group; group g = warp g
+  const int64_t c0 = warp * L, c1 = min(nchunks, c0 + L);
+  // level 1: per (group, expert) sums; lanes read consecutive experts of one chunk (coalesced)
+  for (int e = lane; e < W; e += 32) {
+    int sum = 0;
+    for (int64_t c = c0; c < c1; ++c) sum += chunk_hist[c * W + e];
+    part[warp * W + e] = sum;
+  }
+  __syncthreads();
+  // level 2: per expert, exclusive over the groups
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
-    for (int64_t c = 0; c < nchunks; ++c) {
-      int32_t* p = chunk_hist + c * (E + 1) + e;
-      const int v = *p;
-      *p = cnt;  // becomes the count of expert e in the chunks before c
+    for (int g = 0; g < 32; ++g) {
+      const int v = part[g * W + e];
+      part[g * W + e] = cnt;
       cnt += v;
     }
   }
   __shared__ int s_bad;
   if (threadIdx.x == 0) {
     int bad = 0;
-    for (int64_t c = 0; c < nchunks; ++c) bad += chunk_hist[c * (E + 1) + E];
+    for (int g = 0; g < 32; ++g) bad += part[g * W + E];
     s_bad = bad;
   }
   const int padded = (cnt + kRowTile - 1) / kRowTile * kRowTile;
@@ -103,7 +131,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
   int v[3] = {cnt, padded, ntile}, tot[3];
   block_excl_scan3(v, tot);
   const int off = v[0], pof = v[1], tst = v[2];
-  bool overflow = (tot[1] > rpad_max) || (tot[2] > tiles_max) || (tot[1] / kRowTile > mblocks_max);
+  const bool overflow = (tot[1] > rpad_max) || (tot[2] > tiles_max) || (tot[1] / kRowTile > mblocks_max);
   if (e < E && !overflow) {
     counts[e] = cnt;
     offsets[e] = off;
@@ -128,6 +156,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
       row_token[r] = -1;
       row_weight[r] = 0.0f;
     }
+    for (int g = 0; g < 32; ++g) part[g * W + e] += pof;  // first row of group g's slots of e
   }
   if (e == 0) {
     offsets[E] = tot[0];
@@ -140,44 +169,66 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
     if (overflow) st |= 1u << MOK_ERR_CAPACITY;
     meta[15] = static_cast<int32_t>(st);  // the device status word; later kernels only OR into it
   }
+  __syncthreads();
+  if (overflow) return;
+  // every chunk's first row per expert, in place
+  for (int ex = lane; ex < E; ex += 32) {
+    int run = part[warp * W + ex];
+    for (int64_t c = c0; c < c1; ++c) {
+      const int vv = chunk_hist[c * W + ex];
+      chunk_hist[c * W + ex] = run;
+      run += vv;
+    }
+  }
 }
 
-__global__ void __launch_bounds__(kSchedWarps * 32) sched_scatter_kernel(
+__global__ void __launch_bounds__(kHistWarps * 32) sched_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t R, int K, int E, int64_t nchunks,
-    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ poff, const int32_t* __restrict__ meta,
-    int32_t* __restrict__ perm, int32_t* __restrict__ inv, int32_t* __restrict__ row_token,
-    float* __restrict__ row_weight) {
+    const int32_t* __restrict__ chunk_first, const int32_t* __restrict__ meta, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv, int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
   extern __shared__ int32_t sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kSchedWarps + warp;
+  const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kHistWarps + warp;
   if (chunk >= nchunks) return;  // whole warp leaves together
   if (meta[15] & (1 << MOK_ERR_CAPACITY)) return;
   int32_t* run = sh + warp * E;
-  for (int e = lane; e < E; e += 32) run[e] = poff[e] + chunk_base[chunk * (E + 1) + e];
+  for (int e = lane; e < E; e += 32) run[e] = chunk_first[chunk * (E + 1) + e];
   __syncwarp();
   const int64_t j0 = chunk * kSchedChunk;
-  for (int p = 0; p < kSchedChunk / 32; ++p) {
-    const int64_t j = j0 + p * 32 + lane;
-    int e = -1;
-    if (j < R) {
-      e = ids[j];
-      if (e < 0 || e >= E) e = -1;
+  for (int p0 = 0; p0 < kPieces; p0 += kBatch) {
+    int ev[kBatch];
+    float wv[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t j = j0 + (p0 + b) * 32 + lane;
+      ev[b] = -1;
+      wv[b] = 0.0f;
+      if (j < R) {
+        const int e0 = __ldg(ids + j);
+        ev[b] = (e0 < 0 || e0 >= E) ? -1 : e0;
+        wv[b] = __ldg(w + j);
+      }
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int base = (e >= 0) ? run[e] : 0;
-    __syncwarp();
-    if (e >= 0) {
-      const int row = base + rank;
-      perm[row] = static_cast<int32_t>(j);
-      inv[j] = row;
-      row_token[row] = static_cast<int32_t>(j / K);
-      row_weight[row] = w[j];
-      if (lane == 31 - __clz(peers)) run[e] = base + __popc(peers);
-    } else if (j < R) {
-      inv[j] = -1;  // an invalid id: the slot is skipped (status word says so)
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t j = j0 + (p0 + b) * 32 + lane;
+      const int e = ev[b];
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int base = (e >= 0) ? run[e] : 0;
+      __syncwarp();
+      if (e >= 0) {
+        const int row = base + rank;
+        perm[row] = static_cast<int32_t>(j);
+        inv[j] = row;
+        row_token[row] = static_cast<int32_t>(j / K);
+        row_weight[row] = wv[b];
+        if (lane == 31 - __clz(peers)) run[e] = base + __popc(peers);
+      } else if (j < R) {
+        inv[j] = -1;  // an invalid id: the slot is skipped (status word says so)
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
 }
 
@@ -185,25 +236,31 @@ __global__ void __launch_bounds__(kSchedWarps * 32) sched_scatter_kernel(
 
 int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mok_schedule& s, const Staging& st,
                     cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {  // the scan's group sums need up to 32 x 1025 int32 of shared memory
+    const cudaError_t e = cudaFuncSetAttribute(sched_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(sizeof(int32_t) * 32 * 1025));
+    if (e != cudaSuccess) return static_cast<int>(e);
+    configured = true;
+  }
   const int64_t nchunks = z.nchunks;
-  const int blocks = static_cast<int>((nchunks + kSchedWarps - 1) / kSchedWarps);
+  const int blocks = static_cast<int>((nchunks + kHistWarps - 1) / kHistWarps);
   if (blocks > 0) {
-    const size_t sh = sizeof(int32_t) * kSchedWarps * (z.E + 1);
+    const size_t sh = sizeof(int32_t) * kHistWarps * (z.E + 1);
     trace_begin(stream, K_SCHED_HIST);
-    sched_hist_kernel<<<blocks, kSchedWarps * 32, sh, stream>>>(ids, z.R, z.E, nchunks, st.chunk_hist);
+    sched_hist_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(ids, z.R, z.E, nchunks, st.chunk_hist);
     trace_end(stream);
   }
   trace_begin(stream, K_SCHED_SCAN);
-  sched_scan_kernel<<<1, 1024, 0, stream>>>(z.E, nchunks, st.chunk_hist, z.mb, z.MB, z.rpad_max, z.tiles_max,
-                                            z.mblocks_max, s.counts, s.offsets, s.poff, s.perm, s.row_token,
-                                            s.row_weight, s.tiles, s.mblocks, s.meta);
+  sched_scan_kernel<<<1, 1024, sizeof(int32_t) * 32 * (z.E + 1), stream>>>(
+      z.E, nchunks, st.chunk_hist, z.mb, z.MB, z.rpad_max, z.tiles_max, z.mblocks_max, s.counts, s.offsets, s.poff,
+      s.perm, s.row_token, s.row_weight, s.tiles, s.mblocks, s.meta);
   trace_end(stream);
   if (blocks > 0) {
-    const size_t sh = sizeof(int32_t) * kSchedWarps * z.E;
+    const size_t sh = sizeof(int32_t) * kHistWarps * z.E;
     trace_begin(stream, K_SCHED_SCATTER);
-    sched_scatter_kernel<<<blocks, kSchedWarps * 32, sh, stream>>>(ids, w, z.R, z.K, z.E, nchunks, st.chunk_hist,
-                                                                    s.poff, s.meta, s.perm, s.inv, s.row_token,
-                                                                    s.row_weight);
+    sched_scatter_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(ids, w, z.R, z.K, z.E, nchunks, st.chunk_hist,
+                                                                   s.meta, s.perm, s.inv, s.row_token, s.row_weight);
     trace_end(stream);
   }
   return static_cast<int>(cudaGetLastError());

@@ -112,3 +112,14 @@ def test_schedule_repeat_bitwise(mok):
                 assert np.array_equal(first[k][:n], again[k][:n]), k
             elif k not in ("tiles", "mblocks"):
                 assert np.array_equal(first[k], again[k]), k
+
+
+def test_schedule_large_batch(mok):
+    # 320,000 slots: 625 chunks, so the scan's 32 chunk groups hold up to 20 chunks each
+    rng = np.random.default_rng(11)
+    T, K, E = 40000, 8, 96
+    ids = np.minimum(rng.zipf(1.3, size=(T, K)) - 1, E - 1).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    g, st = _gpu_schedule(mok, ids, w, E, mb=512, MB=2048)
+    assert st == 0
+    _compare(ids, w, E, 512, 2048, g)
