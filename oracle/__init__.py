@@ -21,6 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mok_oracle.c")
+_SRC_MX = os.path.join(_HERE, "mok_oracle_mx.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -30,10 +31,11 @@ MT = 128  # GEMM row tile used for the padded expert-grouped layout
 
 def build(force: bool = False) -> str:
     """Compile ``mok_oracle.c`` into ``liboracle.so`` with gcc (OpenMP, no fast-math)."""
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_MX))
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, _SRC_MX, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -71,6 +73,16 @@ def _load():
             lib.orc_backward_tokens.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i64, P, P, P]
             lib.orc_dw_entries.restype = None
             lib.orc_dw_entries.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, P, P]
+            lib.orc_mx_set_quant.restype = None
+            lib.orc_mx_set_quant.argtypes = [ctypes.c_int]
+            lib.orc_mx_fakequant.restype = None
+            lib.orc_mx_fakequant.argtypes = [P, i64]
+            lib.orc_layer_mx.restype = None
+            lib.orc_layer_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P]
+            lib.orc_tokens_mx.restype = None
+            lib.orc_tokens_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i64, P, P, P, P]
+            lib.orc_dw_block_mx.restype = None
+            lib.orc_dw_block_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i32, i32, i64, P, P, P, P]
             lib.orc_num_threads.restype = ctypes.c_int
             lib.orc_num_threads.argtypes = []
             _lib = lib
@@ -252,3 +264,90 @@ def dw_entries(ids, s, x, Wg, Wu, Wd, dY, which, e, m, c):
     _load().orc_dw_entries(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), which.size,
                            _p(which), _p(e), _p(m), _p(c), _p(val))
     return val
+
+
+# ----------------------------------------------------------------------------------------------
+# MXFP8 mode (mok_oracle_mx.c)
+# ----------------------------------------------------------------------------------------------
+MX_KEYS = ("q_gate", "s_gate", "q_up", "s_up", "q_down", "s_down",
+           "qt_gate", "st_gate", "qt_up", "st_up", "qt_down", "st_down")
+
+
+def mx_fakequant(v: np.ndarray) -> np.ndarray:
+    """MX quantise-dequantise of an fp64 array along its last axis (blocks of 32)."""
+    a = np.array(v, dtype=np.float64, copy=True, order="C")
+    _load().orc_mx_fakequant(_p(a), a.size)
+    return a
+
+
+def mx_set_quant(on: bool):
+    _load().orc_mx_set_quant(1 if on else 0)
+
+
+def mx_weights(Wg, Wu, Wd) -> dict:
+    """The pre-quantised weight copies of the MXFP8 mode, from bf16 weights [E,I,H], [E,H,I]:
+    forward copies along each GEMM's K (Wg, Wu along H; Wd along I) and backward copies of the
+    transposes (Wg^T, Wu^T along I; Wd^T along H)."""
+    Wg, Wu, Wd = _u16(Wg), _u16(Wu), _u16(Wd)
+    E, I, H = Wg.shape
+    out = {}
+    out["q_gate"], out["s_gate"] = mxfp8_quantize(Wg.reshape(E * I, H))
+    out["q_up"], out["s_up"] = mxfp8_quantize(Wu.reshape(E * I, H))
+    out["q_down"], out["s_down"] = mxfp8_quantize(Wd.reshape(E * H, I))
+    out["qt_gate"], out["st_gate"] = mxfp8_quantize(np.ascontiguousarray(Wg.transpose(0, 2, 1)).reshape(E * H, I))
+    out["qt_up"], out["st_up"] = mxfp8_quantize(np.ascontiguousarray(Wu.transpose(0, 2, 1)).reshape(E * H, I))
+    out["qt_down"], out["st_down"] = mxfp8_quantize(np.ascontiguousarray(Wd.transpose(0, 2, 1)).reshape(E * I, H))
+    return out
+
+
+def _mx_ptrs(mx: dict):
+    arrs = [np.ascontiguousarray(mx[k]) for k in MX_KEYS]
+    ptrs = (ctypes.c_void_p * 12)(*[a.ctypes.data for a in arrs])
+    return arrs, ptrs
+
+
+def layer_mx(ids, s, x, dY, mx: dict, E: int, I: int, with_aq: bool = False) -> dict:
+    """Full MXFP8-mode forward + backward (fp64 apart from the quantisation points)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    x, dY = _u16(x), _u16(dY)
+    T, K = ids.shape
+    H = x.shape[1]
+    arrs, ptrs = _mx_ptrs(mx)
+    r = dict(out=np.empty((T, H)), dX=np.empty((T, H)), dWg=np.empty((E, I, H)), dWu=np.empty((E, I, H)),
+             dWd=np.empty((E, H, I)), dS=np.empty((T, K)))
+    aq = np.empty((T * K, I)) if with_aq else None
+    _load().orc_layer_mx(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(dY), ptrs, _p(r["out"]), _p(r["dX"]),
+                         _p(r["dWg"]), _p(r["dWu"]), _p(r["dWd"]), _p(r["dS"]), _p(aq) if with_aq else None)
+    if with_aq:
+        r["aq"] = aq
+    return r
+
+
+def tokens_mx(ids, s, x, dY, mx: dict, E: int, I: int, tokens):
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    x, dY = _u16(x), _u16(dY)
+    T, K = ids.shape
+    H = x.shape[1]
+    tok = np.ascontiguousarray(tokens, dtype=np.int64)
+    arrs, ptrs = _mx_ptrs(mx)
+    out, dX, dS = np.empty((tok.size, H)), np.empty((tok.size, H)), np.empty((tok.size, K))
+    _load().orc_tokens_mx(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(dY), ptrs, tok.size, _p(tok), _p(out), _p(dX),
+                          _p(dS))
+    return out, dX, dS
+
+
+def dw_block_mx(ids, s, x, dY, mx: dict, E: int, I: int, e: int, i0: int, hs):
+    """dWg, dWu [32, nh] and dWd [nh, 32] of expert e on I columns [i0, i0+32) and hidden columns hs."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    x, dY = _u16(x), _u16(dY)
+    T, K = ids.shape
+    H = x.shape[1]
+    hs = np.ascontiguousarray(hs, dtype=np.int32)
+    arrs, ptrs = _mx_ptrs(mx)
+    dwg, dwu, dwd = np.empty((32, hs.size)), np.empty((32, hs.size)), np.empty((hs.size, 32))
+    _load().orc_dw_block_mx(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(dY), ptrs, int(e), int(i0), hs.size, _p(hs),
+                            _p(dwg), _p(dwu), _p(dwd))
+    return dwg, dwu, dwd

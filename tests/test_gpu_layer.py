@@ -146,3 +146,48 @@ def test_determinism_repeats_grids_and_minibatches(mok, full_size):
         _, out, g = _run(mok, d, w, cfg)
         for k, v in dict(out=out, dx=g.dx, dwg=g.dw_gate, dwu=g.dw_up, dwd=g.dw_down, ds=g.d_topk_weights).items():
             assert torch.equal(v, r[k]), (i, k)
+
+
+def _sampled_errors(d, w, r, ntok=16, n=64, seed=0):
+    """Sampled parity of one full-size run: tokens for out / dX / dS, entries of every dW tensor
+    (always including the GPU tensor's peak entry)."""
+    args = _np_args(d)
+    dy = inputs.bits(d["dY"])
+    rng = np.random.default_rng(seed)
+    tok = np.sort(rng.choice(w.T, size=ntok, replace=False))
+    tk = torch.from_numpy(tok).cuda()
+    ref_out = oracle.forward_tokens(*args, tok)
+    dX, dS = oracle.backward_tokens(*args, dy, tok)
+    errs = dict(out=rel_err(to_f64(r["out"][tk]), ref_out), dX=rel_err(to_f64(r["dx"][tk]), dX),
+                dS=rel_err(to_f64(r["ds"][tk]), dS))
+    ids = d["topk_ids"].numpy().reshape(-1)
+    used = np.unique(ids)
+    for which, key, M, N in ((0, "dwg", w.I, w.H), (1, "dwu", w.I, w.H), (2, "dwd", w.H, w.I)):
+        t = r[key]
+        pe, pm, pc = np.unravel_index(int(t.abs().argmax()), t.shape)
+        e = np.concatenate([[pe], rng.choice(used, n)])
+        m = np.concatenate([[pm], rng.integers(0, M, n)])
+        c = np.concatenate([[pc], rng.integers(0, N, n)])
+        ref = oracle.dw_entries(*args, dy, np.full(n + 1, which), e, m, c)
+        got = t[torch.from_numpy(e).cuda(), torch.from_numpy(m).cuda(), torch.from_numpy(c).cuda()]
+        errs[key] = rel_err(to_f64(got), ref)
+    return errs
+
+
+@pytest.mark.parametrize("name", ["dsv3_e256", "sweep_zipf0", "sweep_zipf2"])
+def test_workload_sampled_parity_and_grid_determinism(mok, name):
+    w = inputs.WORKLOADS[name]
+    d = inputs.make(w, seed=0, weight_device="cuda")
+    _, out, g = _run(mok, d, w, mok.make_config(512, 2048))
+    r = dict(out=out.clone(), dx=g.dx.clone(), dwg=g.dw_gate.clone(), dwu=g.dw_up.clone(), dwd=g.dw_down.clone(),
+             ds=g.d_topk_weights.clone())
+    del g
+    errs = _sampled_errors(d, w, r)
+    bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
+    assert not bad, errs
+    # a different grid and minibatch size must give the same bits
+    _, out2, g2 = _run(mok, d, w, mok.make_config(128, 1024, 61))
+    for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down, ds=g2.d_topk_weights).items():
+        assert torch.equal(v, r[k]), k
+    del g2, r, d
+    torch.cuda.empty_cache()

@@ -1,0 +1,130 @@
+"""Pins of the oracle's MXFP8 mode (mok_oracle_mx.c).
+
+The MXFP8 mode is the BF16 layer with MX quantise-dequantise steps at fixed points (x and dY along
+H, a and dg/du along I, weights pre-quantised along each GEMM's K).  Pins:
+  * the fp64 quantise-dequantise equals the byte-level quantiser (itself pinned against torch's
+    float8 conversion) on bf16 inputs, and is idempotent;
+  * with quantisation switched off and weights already on the MX grid, the MXFP8 dataflow equals
+    the BF16 oracle (pinned against torch autograd and finite differences);
+  * with quantisation on, the saved a_q is exactly the quantised SwiGLU output of the BF16 oracle
+    run on the quantised inputs;
+  * the sampled entry points agree with the full one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_build_gb300 import inputs
+
+
+def _bits(a):
+    return inputs.bits(torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16))
+
+
+def test_fakequant_matches_byte_quantiser_and_is_idempotent():
+    rng = np.random.default_rng(0)
+    x = _bits(rng.standard_normal((16, 256)) * 2.0 ** rng.integers(-20, 20, size=(16, 1)))
+    q, sc = oracle.mxfp8_quantize(x)
+    deq = oracle.mxfp8_dequantize(q, sc)
+    fq = oracle.mx_fakequant(oracle.bf16_to_f64(x))
+    assert np.array_equal(fq, deq)
+    assert np.array_equal(oracle.mx_fakequant(fq), fq)
+    # fp64 inputs that are not bf16: within half a quantum of the block's top binade (quantum
+    # 2^(floor(log2 amax) - 3)), except values beyond 448 * 2^shared, which saturate
+    v = rng.standard_normal((4, 64))
+    f = oracle.mx_fakequant(v).reshape(4, 2, 32)
+    blocks = v.reshape(4, 2, 32)
+    _, ex = np.frexp(np.abs(blocks).max(axis=2))
+    shared = (ex - 1 - 8)[:, :, None]
+    quantum = 2.0 ** (ex - 1 - 3)[:, :, None]
+    sat = np.abs(blocks) >= 448.0 * 2.0 ** shared
+    assert np.all(np.abs(f - blocks)[~sat] <= (quantum / 2 * np.ones_like(blocks))[~sat])
+    assert np.all(np.abs(f[sat]) == (448.0 * 2.0 ** shared * np.ones_like(blocks))[sat])
+
+
+def _grid_weights(rng, E, I, H):
+    """bf16 weights whose values are already on their MX grids along both axes: signed powers of
+    two in [2^-9, 2^-3], so any 32-block holds them at most 2^6 below its top, exactly in E4M3."""
+    w = rng.standard_normal((E, I, H)) * 0.02
+    signs = np.sign(w)
+    e = np.clip(np.round(np.log2(np.abs(w) + 1e-30)), -9, -3)
+    return _bits(signs * 2.0 ** e)
+
+
+def test_dataflow_without_quantisation_equals_bf16_oracle():
+    rng = np.random.default_rng(1)
+    T, H, I, E, K = 24, 64, 64, 3, 2
+    ids = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    s = rng.random((T, K)).astype(np.float32)
+    x = _bits(rng.standard_normal((T, H)))
+    dY = _bits(rng.standard_normal((T, H)))
+    Wg, Wu = _grid_weights(rng, E, I, H), _grid_weights(rng, E, I, H)
+    Wd = _grid_weights(rng, E, H, I)
+    mx = oracle.mx_weights(Wg, Wu, Wd)
+    # the grid weights decode exactly from every copy
+    assert np.array_equal(oracle.mxfp8_dequantize(mx["q_gate"], mx["s_gate"]).reshape(E, I, H),
+                          oracle.bf16_to_f64(Wg))
+    assert np.array_equal(oracle.mxfp8_dequantize(mx["qt_down"], mx["st_down"]).reshape(E, I, H),
+                          oracle.bf16_to_f64(Wd).transpose(0, 2, 1))
+    oracle.mx_set_quant(False)
+    try:
+        r = oracle.layer_mx(ids, s, x, dY, mx, E, I)
+    finally:
+        oracle.mx_set_quant(True)
+    out = oracle.forward(ids, s, x, Wg, Wu, Wd)
+    ref = oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
+    np.testing.assert_allclose(r["out"], out, rtol=1e-12, atol=1e-14)
+    for k in ("dX", "dWg", "dWu", "dWd", "dS"):
+        np.testing.assert_allclose(r[k], ref[k], rtol=1e-11, atol=1e-13, err_msg=k)
+
+
+def test_quantisation_point_of_a():
+    rng = np.random.default_rng(2)
+    T, H, I, E, K = 16, 64, 64, 2, 1
+    ids = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    s = np.ones((T, K), np.float32)
+    x = _bits(rng.standard_normal((T, H)))
+    Wg, Wu = _grid_weights(rng, E, I, H), _grid_weights(rng, E, I, H)
+    Wd = _grid_weights(rng, E, H, I)
+    mx = oracle.mx_weights(Wg, Wu, Wd)
+    r = oracle.layer_mx(ids, s, x, x, mx, E, I, with_aq=True)
+    xq = _bits(oracle.mx_fakequant(oracle.bf16_to_f64(x)))  # E4M3 x 2^k values are bf16-exact
+    _, it = oracle.forward(ids, s, xq, Wg, Wu, Wd, intermediates=True)
+    np.testing.assert_allclose(r["aq"], oracle.mx_fakequant(it["a"]), rtol=0, atol=1e-15)
+    assert not np.array_equal(r["aq"], it["a"])  # the quantisation really happened
+
+
+def test_sampled_entry_points_agree_with_full():
+    rng = np.random.default_rng(3)
+    w = inputs.custom(T=40, H=128, I=64, E=3, K=2)
+    d = inputs.make(w, seed=5)
+    args = (d["topk_ids"].numpy(), d["topk_weights"].numpy(), inputs.bits(d["x"]), inputs.bits(d["dY"]))
+    mx = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+    full = oracle.layer_mx(*args, mx, w.E, w.I)
+    tok = np.array([0, 11, 39])
+    out, dX, dS = oracle.tokens_mx(*args, mx, w.E, w.I, tok)
+    np.testing.assert_allclose(out, full["out"][tok], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dX, full["dX"][tok], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dS, full["dS"][tok], rtol=1e-12, atol=1e-14)
+    hs = np.array([0, 5, 127, 64])
+    for e in range(w.E):
+        dwg, dwu, dwd = oracle.dw_block_mx(*args, mx, w.E, w.I, e, 32, hs)
+        np.testing.assert_allclose(dwg, full["dWg"][e, 32:64][:, hs], rtol=1e-11, atol=1e-14)
+        np.testing.assert_allclose(dwu, full["dWu"][e, 32:64][:, hs], rtol=1e-11, atol=1e-14)
+        np.testing.assert_allclose(dwd, full["dWd"][e][hs, 32:64], rtol=1e-11, atol=1e-14)
+
+
+def test_mx_mode_is_close_to_bf16():
+    w = inputs.custom(T=32, H=128, I=64, E=4, K=2)
+    d = inputs.make(w, seed=6)
+    ids, s = d["topk_ids"].numpy(), d["topk_weights"].numpy()
+    x, dY = inputs.bits(d["x"]), inputs.bits(d["dY"])
+    Wg, Wu, Wd = inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"])
+    r = oracle.layer_mx(ids, s, x, dY, oracle.mx_weights(Wg, Wu, Wd), w.E, w.I)
+    out = oracle.forward(ids, s, x, Wg, Wu, Wd)
+    ref = oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
+    rel = lambda a, b: np.abs(a - b).max() / np.abs(b).max()  # noqa: E731
+    assert rel(r["out"], out) < 0.15
+    for k in ("dX", "dWg", "dWd", "dS"):
+        assert rel(r[k], ref[k]) < 0.2, k
