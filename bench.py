@@ -164,6 +164,8 @@ def kernel_work(w) -> dict:
         "gather_x": ("hbm", T * H * 2 + R * H * 2), "gather_dy": ("hbm", T * H * 2 + R * H * 2),
         # combine / dX reduce: routed rows read + weights/indices + token rows written
         "combine": ("hbm", R * H * 2 + T * K * 8 + T * H * 2), "dx_reduce": ("hbm", R * H * 2 + T * K * 4 + T * H * 2),
+        # MXFP8: exact decode of one pre-quantised weight copy (1 + 1/32 bytes read, 2 written per element)
+        "mx_dequant": ("hbm", w.E * H * I * (1 + 1 / 32 + 2)),
     }
 
 
@@ -210,12 +212,18 @@ def oracle_sample_args(d, tokens: int):
 
 
 def time_oracle_step(d, wbits, tokens: int) -> float:
+    """One oracle fwd + bwd of the first `tokens` tokens.  wbits = (Wg, Wu, Wd) bf16 bit patterns
+    for the BF16 oracle, or a dict of pre-quantised copies for the MXFP8 oracle."""
     import oracle
     ids, s, x, dY = oracle_sample_args(d, tokens)
-    Wg, Wu, Wd = wbits
     t0 = time.perf_counter()
-    oracle.forward(ids, s, x, Wg, Wu, Wd)
-    oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
+    if isinstance(wbits, dict):
+        E, I = d["Wg"].shape[0], d["Wg"].shape[1]
+        oracle.layer_mx(ids, s, x, dY, wbits, E, I)
+    else:
+        Wg, Wu, Wd = wbits
+        oracle.forward(ids, s, x, Wg, Wu, Wd)
+        oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
     return time.perf_counter() - t0
 
 
@@ -248,6 +256,9 @@ def reference_arm(args, rank, ws):
     w = inputs.WORKLOADS[args.workload]
     d = inputs.make(w, seed=0)
     wbits = (inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+    if w.precision == "mxfp8":
+        import oracle
+        wbits = oracle.mx_weights(*wbits)
     per_step_budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
     tokens, _ = calibrate_oracle_tokens(d, wbits, per_step_budget, w.T)
     for _ in range(args.warmup):
@@ -287,9 +298,14 @@ def ours(args, rank, ws, local_rank):
     d = inputs.make(w, seed=rank, weight_device=str(dev))
     x, ids, s, dY = (d[k].to(dev) for k in ("x", "topk_ids", "topk_weights", "dY"))
     Wg, Wu, Wd = d["Wg"], d["Wu"], d["Wd"]
-    cfg = mok.make_config(args.minibatch, args.macrobatch)
+    mxfp8 = w.precision == "mxfp8"
+    cfg = mok.make_config(args.minibatch, args.macrobatch, precision=mok.MOK_MXFP8 if mxfp8 else mok.MOK_BF16)
     layer = mok.Layer(w.T, w.H, w.I, w.E, w.K, cfg, device=dev)
-    weights = mok.weights_struct(Wg, Wu, Wd)
+    if mxfp8:  # weights are pre-quantised once, outside the step (the caller's optimiser step)
+        mx = mok.quantize_weights(Wg.to(dev), Wu.to(dev), Wd.to(dev))
+        weights = mok.weights_struct(mx=mx)
+    else:
+        weights = mok.weights_struct(Wg, Wu, Wd)
     stream = torch.cuda.Stream(device=dev)
 
     def step(xx=x, ii=ids, ss=s, dd=dY):
@@ -400,7 +416,8 @@ def ours(args, rank, ws, local_rank):
         result = {
             "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init expert weights)",
+            "vs_baseline": None, "dtype": "mxfp8 operands, bf16 tensor-core arithmetic" if mxfp8 else "bf16",
+            "data": "synthetic (seeded; random-init expert weights)",
             "config": config_of(w, args, ws),
             "tflops": w.flops() / (ms_max * 1e-3) / 1e12,
             "roofline": roof,
@@ -426,6 +443,9 @@ def main():
         if ws == 1 and not args.no_cpu_baseline:
             from mixture_experts_layer_build_gb300 import inputs
             wbits = (inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+            if w.precision == "mxfp8":
+                import oracle
+                wbits = oracle.mx_weights(*wbits)
             tokens, _ = calibrate_oracle_tokens(d, wbits, args.cpu_seconds, w.T)
             t = time_oracle_step(d, wbits, tokens)
             res["cpu_baseline"] = {"value": tokens / t, "unit": UNIT, "cores": cores_used(), "kind": "oracle",

@@ -116,12 +116,15 @@ typedef struct {
 } mok_schedule;
 
 /* Expert weights in the PyTorch [out, in] convention.
- *   w_gate, w_up [E, I, H] bf16; w_down [E, H, I] bf16.
- * MXFP8 mode (precision == MOK_MXFP8) additionally reads pre-quantised copies made with
- * mok_mxfp8_quantize (the project card: "weights are pre-quantised with ops.mxfp8_quantize"):
- *   q_gate, q_up [E*I, H] E4M3 with s_gate, s_up [E*I, H/32] E8M0;
- *   q_down [E*H, I] E4M3 with s_down [E*H, I/32] E8M0.
- * Unused fields may be NULL. */
+ * BF16 mode: w_gate, w_up [E, I, H] bf16; w_down [E, H, I] bf16.
+ * MXFP8 mode (precision == MOK_MXFP8) reads only pre-quantised copies made with mok_mxfp8_quantize
+ * (the project card, "Key concepts": weights are pre-quantised with ops.mxfp8_quantize), each
+ * quantised along the K axis of the GEMM that consumes it:
+ *   forward   q_gate, q_up [E*I, H] E4M3 + s_gate, s_up [E*I, H/32] E8M0   (Wg, Wu along H)
+ *             q_down [E*H, I] + s_down [E*H, I/32]                         (Wd along I)
+ *   backward  qt_gate, qt_up [E*H, I] + st_gate, st_up [E*H, I/32]          (Wg^T, Wu^T along I)
+ *             qt_down [E*I, H] + st_down [E*I, H/32]                        (Wd^T along H)
+ * Fields a mode does not read may be NULL. */
 typedef struct {
   const void* w_gate;
   const void* w_up;
@@ -132,6 +135,12 @@ typedef struct {
   const uint8_t* s_up;
   const uint8_t* q_down;
   const uint8_t* s_down;
+  const uint8_t* qt_gate;
+  const uint8_t* st_gate;
+  const uint8_t* qt_up;
+  const uint8_t* st_up;
+  const uint8_t* qt_down;
+  const uint8_t* st_down;
 } mok_weights;
 
 /* Gradients, overwritten (not accumulated):

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "mok_gemm.cuh"
@@ -60,6 +61,7 @@ bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s) {
   s->tiles_max = (s->R + s->mb - 1) / s->mb + p.E;
   s->mblocks_max = s->rpad_max / kRowTile;
   s->nchunks = (s->R + kSchedChunk - 1) / kSchedChunk;
+  s->mx = cfg->precision == MOK_MXFP8;
   if (s->rpad_max >= (int64_t(1) << 31)) return false;
   return true;
 }
@@ -85,6 +87,15 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
   t.dgdu = c.take<uint16_t>(z.rpad_max * 2 * z.I);
   t.as = c.take<uint16_t>(z.rpad_max * z.I);
   t.dspart = c.take<float>(z.rpad_max * (z.I / 128));
+  if (z.mx) {
+    const int64_t n = static_cast<int64_t>(z.E) * z.H * z.I;
+    t.wg_f = c.take<uint16_t>(n);
+    t.wu_f = c.take<uint16_t>(n);
+    t.wd_f = c.take<uint16_t>(n);
+    t.wg_b = c.take<uint16_t>(n);
+    t.wu_b = c.take<uint16_t>(n);
+    t.wd_b = c.take<uint16_t>(n);
+  }
   if (s) {
     s->counts = d.counts;
     s->offsets = d.offsets;
@@ -106,7 +117,8 @@ size_t carve_ctx(const Sizes& z, char* base, Ctx* ctx) {
   Carver c{base};
   Ctx x{};
   x.xg = c.take<uint16_t>(z.rpad_max * z.H);
-  x.gu = c.take<uint16_t>(z.rpad_max * 2 * z.I);
+  x.gu = z.mx ? static_cast<void*>(c.take<float>(z.rpad_max * 2 * z.I))
+              : static_cast<void*>(c.take<uint16_t>(z.rpad_max * 2 * z.I));
   x.a = c.take<uint16_t>(z.rpad_max * z.I);
   if (ctx) *ctx = x;
   return align_up(c.off);
@@ -242,7 +254,6 @@ mok_status mok_build_schedule(const mok_config* cfg, const mok_shape* shape, con
                               void* stream) {
   Sizes z;
   if (!out || !make_sizes(cfg, shape, &z)) return MOK_ERR_INVALID_ARG;
-  if (cfg->precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return MOK_ERR_INVALID_ARG;
   if (z.R > 0 && (!topk_ids || !topk_weights)) return MOK_ERR_INVALID_ARG;
   Staging st;
@@ -277,25 +288,42 @@ static int grid_of(const mok_schedule* s) {
   return n > 0 ? n : sm_count();
 }
 
+static bool all16(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return false;
+  return true;
+}
+
 mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weights* w, void* out, void* fwd_ctx,
                        size_t fwd_ctx_bytes, void* stream) {
   Sizes z;
   Staging st;
   mok_status rc = check_sched(sched, &z, &st);
   if (rc != MOK_OK) return rc;
-  if (sched->config.precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (!w || !fwd_ctx) return MOK_ERR_INVALID_ARG;
   Ctx ctx;
   if (fwd_ctx_bytes < carve_ctx(z, static_cast<char*>(fwd_ctx), &ctx)) return MOK_ERR_WORKSPACE_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(fwd_ctx) % kAlign) return MOK_ERR_INVALID_ARG;
   if (z.T > 0 && (!x || !out || !aligned16(x) || !aligned16(out))) return MOK_ERR_INVALID_ARG;
-  if (!w->w_gate || !w->w_up || !w->w_down || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
-      !aligned16(w->w_down))
+  if (z.mx) {
+    if (!all16({w->q_gate, w->q_up, w->q_down}) || !w->s_gate || !w->s_up || !w->s_down) return MOK_ERR_INVALID_ARG;
+  } else if (!all16({w->w_gate, w->w_up, w->w_down})) {
     return MOK_ERR_INVALID_ARG;
+  }
   cudaStream_t s = as_stream(stream);
-  if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H, ctx.xg,
-                         K_GATHER_X, s))
+  if (z.mx) {  // exact bf16 decodes of the pre-quantised forward copies
+    const int64_t EI = static_cast<int64_t>(z.E) * z.I, EH = static_cast<int64_t>(z.E) * z.H;
+    if (launch_mx_dequant(w->q_gate, w->s_gate, EI, z.H, st.wg_f, s) ||
+        launch_mx_dequant(w->q_up, w->s_up, EI, z.H, st.wu_f, s) ||
+        launch_mx_dequant(w->q_down, w->s_down, EH, z.I, st.wd_f, s))
+      return MOK_ERR_CUDA;
+    if (launch_gather_rows_mx(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
+                              ctx.xg, K_GATHER_X, s))
+      return MOK_ERR_CUDA;
+  } else if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
+                                ctx.xg, K_GATHER_X, s)) {
     return MOK_ERR_CUDA;
+  }
   const int g = grid_of(sched);
   int e = launch_fwd_gemms(z, *sched, ctx, st, *w, g, s);
   if (e < 0) return MOK_ERR_INVALID_ARG;
@@ -310,23 +338,33 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   Staging st;
   mok_status rc = check_sched(sched, &z, &st);
   if (rc != MOK_OK) return rc;
-  if (sched->config.precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (!w || !g || !fwd_ctx || (reinterpret_cast<uintptr_t>(fwd_ctx) % kAlign)) return MOK_ERR_INVALID_ARG;
-  if (!g->dw_gate || !g->dw_up || !g->dw_down || !aligned16(g->dw_gate) || !aligned16(g->dw_up) ||
-      !aligned16(g->dw_down))
-    return MOK_ERR_INVALID_ARG;
+  if (!all16({g->dw_gate, g->dw_up, g->dw_down})) return MOK_ERR_INVALID_ARG;
   if (z.T > 0 && (!dy || !g->dx || !g->d_topk_weights || !aligned16(dy) || !aligned16(g->dx)))
     return MOK_ERR_INVALID_ARG;
-  if (!w->w_gate || !w->w_up || !w->w_down || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
-      !aligned16(w->w_down))
+  if (z.mx) {
+    if (!all16({w->qt_gate, w->qt_up, w->qt_down}) || !w->st_gate || !w->st_up || !w->st_down)
+      return MOK_ERR_INVALID_ARG;
+  } else if (!all16({w->w_gate, w->w_up, w->w_down})) {
     return MOK_ERR_INVALID_ARG;
+  }
   Ctx ctx;
   carve_ctx(z, static_cast<char*>(const_cast<void*>(fwd_ctx)), &ctx);
   cudaStream_t s = as_stream(stream);
   const int grid = grid_of(sched);
-  if (launch_gather_rows(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H, st.dyg,
-                         K_GATHER_DY, s))
+  if (z.mx) {  // exact bf16 decodes of the pre-quantised backward copies
+    const int64_t EI = static_cast<int64_t>(z.E) * z.I, EH = static_cast<int64_t>(z.E) * z.H;
+    if (launch_mx_dequant(w->qt_gate, w->st_gate, EH, z.I, st.wg_b, s) ||
+        launch_mx_dequant(w->qt_up, w->st_up, EH, z.I, st.wu_b, s) ||
+        launch_mx_dequant(w->qt_down, w->st_down, EI, z.H, st.wd_b, s))
+      return MOK_ERR_CUDA;
+    if (launch_gather_rows_mx(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
+                              st.dyg, K_GATHER_DY, s))
+      return MOK_ERR_CUDA;
+  } else if (launch_gather_rows(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
+                                st.dyg, K_GATHER_DY, s)) {
     return MOK_ERR_CUDA;
+  }
   int e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 1, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
   const int n_tiles1 = z.I / (z.I % 256 == 0 ? 256 : 128);
@@ -351,7 +389,8 @@ const char* mok_kernel_name(int32_t kind) {
   static const char* names[K_NUM_KINDS] = {
       "sched_hist",      "sched_scan",    "sched_scatter", "gather_x",       "gemm_fwd_gateup",
       "gemm_fwd_down",   "combine",       "gather_dy",     "gemm_dgrad1",    "ds_reduce",
-      "gemm_dgrad2",     "dx_reduce",     "gemm_wgrad_gu", "gemm_wgrad_d",   "mxfp8_quantize"};
+      "gemm_dgrad2",     "dx_reduce",     "gemm_wgrad_gu", "gemm_wgrad_d",   "mxfp8_quantize",
+      "mx_dequant"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "?";
 }
 

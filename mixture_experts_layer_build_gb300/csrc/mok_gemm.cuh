@@ -114,12 +114,25 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
   return w;
 }
 
-// Issue the TMA loads of one K block into stage (sa, sb), all completing on barrier `bar`.
-template <int VAR, int BN>
+// Issue the TMA loads of one K block into stage (sa, sb), all completing on barrier `bar`.  With MX
+// the dgrad variants read B from K-major transposed weight copies ([E*I, H] for dgrad1, [E*H, I]
+// for dgrad2) instead of the MN-major forward layout.
+template <int VAR, int BN, bool MX>
 __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
                                           uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
                                           const CUtensorMap* tB2) {
   const int k0 = kb * kBK;
+  if constexpr (MX && VAR == V_DGRAD1) {
+    tma_load_2d(sa, tA, bar, k0, w.row0);
+    tma_load_2d(sb, tB, bar, k0, w.e * a.I + w.nt * BN);
+    return;
+  }
+  if constexpr (MX && VAR == V_DGRAD2) {
+    tma_load_2d(sa, tA, bar, k0, w.row0);
+    const bool first = kb < a.kb_split;
+    tma_load_2d(sb, first ? tB : tB2, bar, first ? k0 : k0 - a.kb_split * kBK, w.e * a.H + w.nt * BN);
+    return;
+  }
   if constexpr (VAR == V_FWD_GATEUP) {
     tma_load_2d(sa, tA, bar, k0, w.row0);
     const int n0 = w.e * a.I + w.nt * (BN / 2);
@@ -247,7 +260,7 @@ constexpr int epi_row_bytes() { return VAR == V_DGRAD1 ? 64 : 128; }
 // Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab.
 // tO0 / tO1 are the output tensor maps of the variant; `tempty` is released as soon as the last
 // accumulator column has been read.  `pre` holds DGRAD1's first prefetched context chunk.
-template <int VAR, int BN, class Stg>
+template <int VAR, int BN, bool MX, class Stg>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int lane, uint32_t taddr,
                                               Stg& stg, const CUtensorMap* tO0, const CUtensorMap* tO1,
                                               uint32_t tempty, Dg1Chunk& pre) {
@@ -262,12 +275,32 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       tmem_ld64(taddr + BN / 2 + c, u);
       if (c + 64 >= BN / 2) release_acc(tempty);
       uint4 ch[8];
-      pack_bf16<64>(g, ch);
-      stg.put_and_store(ch, tO0, i0 + c, rowc);
-      pack_bf16<64>(u, ch);
-      stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
+      if constexpr (MX) {  // g, u kept in fp32 for the backward's re-quantisation of dg, du
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ch[j] = make_uint4(__float_as_uint(g[32 * h + 4 * j]), __float_as_uint(g[32 * h + 4 * j + 1]),
+                               __float_as_uint(g[32 * h + 4 * j + 2]), __float_as_uint(g[32 * h + 4 * j + 3]));
+          stg.put_and_store(ch, tO0, i0 + c + 32 * h, rowc);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ch[j] = make_uint4(__float_as_uint(u[32 * h + 4 * j]), __float_as_uint(u[32 * h + 4 * j + 1]),
+                               __float_as_uint(u[32 * h + 4 * j + 2]), __float_as_uint(u[32 * h + 4 * j + 3]));
+          stg.put_and_store(ch, tO0, a.I + i0 + c + 32 * h, rowc);
+        }
+      } else {
+        pack_bf16<64>(g, ch);
+        stg.put_and_store(ch, tO0, i0 + c, rowc);
+        pack_bf16<64>(u, ch);
+        stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
+      }
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
+      if constexpr (MX) {  // a leaves MX-quantised along I (two blocks of 32)
+        mx_fakequant32(g);
+        mx_fakequant32(g + 32);
+      }
       pack_bf16<64>(g, ch);
       stg.put_and_store(ch, tO1, i0 + c, rowc);
     }
@@ -282,6 +315,62 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       pack_bf16<64>(v, ch);
       stg.put_and_store(ch, tO0, w.nt * BN + c, rowc);
     }
+  } else if constexpr (VAR == V_DGRAD1 && MX) {
+    // MXFP8: as below, with g, u read in fp32 and dg, du quantise-dequantised per block of 32.
+    const int64_t row = w.row0 + q * 32 + lane;
+    const int64_t I = a.I;
+    const int i0 = w.nt * BN;
+    const float* gu = static_cast<const float*>(a.in0) + row * 2 * I;
+    const uint16_t* av = static_cast<const uint16_t*>(a.in1) + row * I;
+    const float s = __ldg(a.row_weight + row);
+    const int rowc = w.row0 + q * 32;
+    float part = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      float4 g4[8], u4[8];
+      const float4* gp = reinterpret_cast<const float4*>(gu + i0 + c);
+      const float4* up = reinterpret_cast<const float4*>(gu + I + i0 + c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        g4[j] = __ldg(gp + j);
+        u4[j] = __ldg(up + j);
+      }
+      uint32_t rv[32];
+      tmem_ld_32x32b_x32(taddr + c, rv);
+      tmem_ld_wait();
+      if (c + 32 >= BN) release_acc(tempty);
+      const float* g = reinterpret_cast<const float*>(g4);
+      const float* u = reinterpret_cast<const float*>(u4);
+      float dg[32], du[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float da = s * __uint_as_float(rv[i]);
+        const float sg = sigmoid_f(g[i]);
+        dg[i] = da * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+        du[i] = da * g[i] * sg;
+      }
+      mx_fakequant32(dg);
+      mx_fakequant32(du);
+      uint4 ch[4];
+      pack_bf16<32>(dg, ch);
+      stg.put_and_store(ch, tO0, i0 + c, rowc);
+      pack_bf16<32>(du, ch);
+      stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
+      float sa[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float a8[8];
+        unpack8(ldg_v4(av + i0 + c + 8 * j), a8);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          part = fmaf(__uint_as_float(rv[8 * j + k]), a8[k], part);
+          sa[8 * j + k] = s * a8[k];
+        }
+      }
+      pack_bf16<32>(sa, ch);
+      stg.put_and_store(ch, tO1, i0 + c, rowc);
+    }
+    static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else if constexpr (VAR == V_DGRAD1) {
     // dA' = dY Wd (this tile's BN columns of I); the forward's g, u, a come from the context,
     // fetched one 32-column chunk ahead.  dg, du and s*a leave as 32 x 64-byte tiles.
@@ -299,25 +388,27 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       tmem_ld_wait();
       if (c + 32 >= BN) release_acc(tempty);
       uint4 cdg[4], cdu[4], csa[4];
+      {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float g8[8], u8[8], a8[8], dg[8], du[8], sa[8];
-        unpack8(cur.g[j], g8);
-        unpack8(cur.u[j], u8);
-        unpack8(cur.a[j], a8);
+        for (int j = 0; j < 4; ++j) {
+          float g8[8], u8[8], a8[8], dg[8], du[8], sa[8];
+          unpack8(cur.g[j], g8);
+          unpack8(cur.u[j], u8);
+          unpack8(cur.a[j], a8);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float dap = __uint_as_float(rv[8 * j + k]);
-          part = fmaf(dap, a8[k], part);
-          const float da = s * dap;
-          const float sg = sigmoid_f(g8[k]);
-          dg[k] = da * u8[k] * sg * (1.0f + g8[k] * (1.0f - sg));
-          du[k] = da * g8[k] * sg;
-          sa[k] = s * a8[k];
+          for (int k = 0; k < 8; ++k) {
+            const float dap = __uint_as_float(rv[8 * j + k]);
+            part = fmaf(dap, a8[k], part);
+            const float da = s * dap;
+            const float sg = sigmoid_f(g8[k]);
+            dg[k] = da * u8[k] * sg * (1.0f + g8[k] * (1.0f - sg));
+            du[k] = da * g8[k] * sg;
+            sa[k] = s * a8[k];
+          }
+          pack_bf16<8>(dg, cdg + j);
+          pack_bf16<8>(du, cdu + j);
+          pack_bf16<8>(sa, csa + j);
         }
-        pack_bf16<8>(dg, cdg + j);
-        pack_bf16<8>(du, cdu + j);
-        pack_bf16<8>(sa, csa + j);
       }
       stg.put_and_store(cdg, tO0, i0 + c, rowc);
       stg.put_and_store(cdu, tO0, a.I + i0 + c, rowc);
@@ -368,14 +459,14 @@ __device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity, u
   return true;
 }
 
-template <int VAR, int BN>
+template <int VAR, int BN, bool MX>
 __global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
                 const __grid_constant__ CUtensorMap tmO1, const GemmArgs args) {
   using C = GemmCfg<VAR, BN>;
   constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);
-  constexpr bool kBmn = (VAR >= V_DGRAD1);
+  constexpr bool kBmn = (VAR >= V_DGRAD1) && !(MX && (VAR == V_DGRAD1 || VAR == V_DGRAD2));
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
   constexpr int S = C::kStages;
 
@@ -442,7 +533,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
           }
           mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
           const uint32_t sa = base + stage * C::kStageBytes;
-          gemm_load<VAR, BN>(args, w, kb, sa, sa + C::kABytes, full_bar(stage), &tmA, &tmB, &tmB2);
+          gemm_load<VAR, BN, MX>(args, w, kb, sa, sa + C::kABytes, full_bar(stage), &tmA, &tmB, &tmB2);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == S) {
             stage = 0;
@@ -508,14 +599,14 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       const Unit w = gemm_decode<VAR>(args, u);
       Dg1Chunk pre;
-      if constexpr (VAR == V_DGRAD1) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);  // before the wait
+      if constexpr (VAR == V_DGRAD1 && !MX) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);  // before the wait
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      gemm_epilogue<VAR, BN>(args, w, q, lane, taddr, stg, &tmO0, &tmO1, tempty_bar(acc), pre);
+      gemm_epilogue<VAR, BN, MX>(args, w, q, lane, taddr, stg, &tmO0, &tmO1, tempty_bar(acc), pre);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -541,13 +632,13 @@ bool make_tmap_bf16_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint6
 bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                    uint32_t box_outer);
 
-template <int VAR, int BN>
+template <int VAR, int BN, bool MX = false>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o0,
                 const CUtensorMap& o1, const GemmArgs& args, int grid, cudaStream_t stream) {
   using C = GemmCfg<VAR, BN>;
   static bool configured = false;  // per process; the attribute is per function, set once
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return static_cast<int>(e);
     configured = true;
@@ -560,7 +651,7 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
                         : VAR == V_WGRAD_GU  ? K_GEMM_WGRAD_GU
                                              : K_GEMM_WGRAD_D;
   trace_begin(stream, kKind);
-  gemm_kernel<VAR, BN><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, args);
+  gemm_kernel<VAR, BN, MX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, args);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

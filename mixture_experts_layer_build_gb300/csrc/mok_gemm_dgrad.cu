@@ -32,7 +32,11 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   if (phase == 1) {
     const int BN = z.I % 256 == 0 ? 256 : 128;
     if (!make_tmap_bf16(&tA, st.dyg, z.H, z.rpad_max, 64, 128)) return -1;
-    if (!make_tmap_bf16(&tB, w.w_down, z.I, static_cast<uint64_t>(z.E) * z.H, 64, 64)) return -1;
+    if (z.mx) {  // K-major B: Wd^T decoded from the copy quantised along H, [E*I, H]
+      if (!make_tmap_bf16(&tB, st.wd_b, z.H, static_cast<uint64_t>(z.E) * z.I, 64, BN)) return -1;
+    } else if (!make_tmap_bf16(&tB, w.w_down, z.I, static_cast<uint64_t>(z.E) * z.H, 64, 64)) {
+      return -1;
+    }
     a.n_tiles = z.I / BN;
     a.k_blocks = z.H / kBK;
     a.in0 = ctx.gu;
@@ -43,19 +47,30 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     if (!make_tmap_bf16_sw64(&tO0, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
     if (!make_tmap_bf16_sw64(&tO1, st.as, z.I, z.rpad_max, 32, 32)) return -1;
     const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+    if (z.mx)
+      return BN == 256 ? launch_gemm<V_DGRAD1, 256, true>(tA, tB, tB, tO0, tO1, a, grid, stream)
+                       : launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, a, grid, stream);
     return BN == 256 ? launch_gemm<V_DGRAD1, 256>(tA, tB, tB, tO0, tO1, a, grid, stream)
                      : launch_gemm<V_DGRAD1, 128>(tA, tB, tB, tO0, tO1, a, grid, stream);
   }
   const int BN = z.H % 256 == 0 ? 256 : 128;
   if (!make_tmap_bf16(&tA, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 128)) return -1;
-  if (!make_tmap_bf16(&tB, w.w_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
-  if (!make_tmap_bf16(&tB2, w.w_up, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
+  if (z.mx) {  // K-major B: Wg^T, Wu^T decoded from the copies quantised along I, [E*H, I]
+    if (!make_tmap_bf16(&tB, st.wg_b, z.I, static_cast<uint64_t>(z.E) * z.H, 64, BN)) return -1;
+    if (!make_tmap_bf16(&tB2, st.wu_b, z.I, static_cast<uint64_t>(z.E) * z.H, 64, BN)) return -1;
+  } else {
+    if (!make_tmap_bf16(&tB, w.w_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
+    if (!make_tmap_bf16(&tB2, w.w_up, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
+  }
   a.n_tiles = z.H / BN;
   a.k_blocks = 2 * z.I / kBK;
   a.kb_split = z.I / kBK;
   a.out0 = st.ybuf;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+  if (z.mx)
+    return BN == 256 ? launch_gemm<V_DGRAD2, 256, true>(tA, tB, tB2, tO0, tO0, a, grid, stream)
+                     : launch_gemm<V_DGRAD2, 128, true>(tA, tB, tB2, tO0, tO0, a, grid, stream);
   return BN == 256 ? launch_gemm<V_DGRAD2, 256>(tA, tB, tB2, tO0, tO0, a, grid, stream)
                    : launch_gemm<V_DGRAD2, 128>(tA, tB, tB2, tO0, tO0, a, grid, stream);
 }

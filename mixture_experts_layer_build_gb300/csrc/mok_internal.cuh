@@ -16,6 +16,7 @@ constexpr int kSchedWarps = 8;      // warps per CTA in the schedule kernels
 struct Sizes {
   int64_t T, R, rpad_max, tiles_max, mblocks_max, nchunks;
   int32_t H, I, E, K, mb, MB;
+  bool mx;  // MXFP8 mode
 };
 bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s);
 
@@ -27,10 +28,18 @@ struct Staging {
   uint16_t* as;      // [rpad_max, I] bf16: s * a
   float* dspart;     // [rpad_max, I/128] fp32: router-gradient partial sums per N tile
   int32_t* chunk_hist;  // [nchunks, E+1]
+  // MXFP8 mode only: exact bf16 decodes of the caller's pre-quantised weight copies
+  uint16_t* wg_f;    // [E*I, H]  Wg (quantised along H)
+  uint16_t* wu_f;    // [E*I, H]  Wu
+  uint16_t* wd_f;    // [E*H, I]  Wd (quantised along I)
+  uint16_t* wg_b;    // [E*H, I]  Wg^T (quantised along I)
+  uint16_t* wu_b;    // [E*H, I]  Wu^T
+  uint16_t* wd_b;    // [E*I, H]  Wd^T (quantised along H)
 };
 struct Ctx {
   uint16_t* xg;      // [rpad_max, H] bf16: gathered x rows (zero on padding rows)
-  uint16_t* gu;      // [rpad_max, 2I] bf16: [g | u]
+  void* gu;          // [rpad_max, 2I]: [g | u], bf16 (BF16 mode) or fp32 (MXFP8 mode, whose
+                     // backward re-quantises dg, du and needs g, u unrounded)
   uint16_t* a;       // [rpad_max, I] bf16: silu(g) * u
 };
 size_t carve_workspace(const Sizes& z, char* base, mok_schedule* sched, Staging* st);  // returns bytes
@@ -55,6 +64,7 @@ enum KernelKind : int {
   K_GEMM_WGRAD_GU,
   K_GEMM_WGRAD_D,
   K_MXFP8_QUANTIZE,
+  K_MX_DEQUANT,
   K_NUM_KINDS
 };
 void trace_begin(cudaStream_t s, int kind);  // no-ops unless a trace is set
@@ -65,6 +75,10 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
                     cudaStream_t stream);
 int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                        int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
+int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+                          int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
+int launch_mx_dequant(const uint8_t* q, const uint8_t* sc, int64_t rows, int64_t cols, uint16_t* dst,
+                      cudaStream_t stream);
 int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
                    uint16_t* out, int kind, cudaStream_t stream);
 int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, float* ds,
@@ -74,9 +88,9 @@ int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_
 
 // GEMM phases
 int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st, const mok_weights& w,
-                     int num_ctas, cudaStream_t stream);
+                     int num_ctas, cudaStream_t stream);  // MXFP8 mode (z.mx) reads st.w*_f
 int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
-                       const mok_weights& w, int num_ctas, int phase, cudaStream_t stream);
+                       const mok_weights& w, int num_ctas, int phase, cudaStream_t stream);  // MXFP8: st.w*_b
 int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                        const mok_grads& g, int num_ctas, cudaStream_t stream);
 

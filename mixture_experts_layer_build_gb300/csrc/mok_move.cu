@@ -205,6 +205,91 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
   }
 }
 
+// Value of an unsigned E4M3 code (7 bits): subnormal m * 2^-9, else (8 + m) * 2^(E - 10).
+__device__ __forceinline__ float e4m3_mag(uint32_t c) {
+  const int E = static_cast<int>(c >> 3), m = static_cast<int>(c & 7u);
+  return E ? ldexpf(static_cast<float>(8 + m), E - 10) : ldexpf(static_cast<float>(m), -9);
+}
+
+// Gather with MX quantise-dequantise of each row (blocks of 32 along the row), bit-exact with
+// mxfp8_quantize_kernel's rounding: dst[row] = MX(src[row_token[row]]), zero padding rows.
+// One warp per row; lane l handles the row's 32-element blocks l, l + 32, ...
+__global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint4* __restrict__ src,
+                                                                     const int32_t* __restrict__ row_token,
+                                                                     const int32_t* __restrict__ meta,
+                                                                     int64_t vecs, uint4* __restrict__ dst) {
+  const int64_t rpad = meta[0];
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
+  const int64_t nblk = vecs / 4;  // 32-element blocks per row
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); row < rpad;
+       row += nwarps) {
+    const int t = row_token[row];
+    uint4* d = dst + row * vecs;
+    for (int64_t b = lane; b < nblk; b += 32) {
+      if (t < 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[b * 4 + i] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const uint4* s = src + static_cast<int64_t>(t) * vecs + b * 4;
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldg(s + i);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+      }
+      uint32_t amax = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t mag = (i & 1 ? (w[i >> 1] >> 16) : w[i >> 1]) & 0x7FFFu;
+        amax = mag > amax ? mag : amax;
+      }
+      int shared = amax == 0 ? -127 : bf16_floor_log2(amax) - 8;
+      shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
+      // bf16 * 2^-shared is exact in fp32, so the hardware E4M3 rounding matches e4m3_code's
+      float o[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[2 * i] = bf16_lo(w[i]);
+        o[2 * i + 1] = bf16_hi(w[i]);
+      }
+      mx_qdq_pairs(o, 32, shared);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        d[b * 4 + i] = make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
+                                  pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
+    }
+  }
+}
+
+// Exact decode of an MXFP8 matrix to bf16: dst = e4m3 * 2^(scale - 127); one thread per block of 32.
+__global__ void __launch_bounds__(kMoveThreads) mx_dequant_kernel(const uint4* __restrict__ q,
+                                                                 const uint8_t* __restrict__ sc, int64_t nblocks,
+                                                                 uint4* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; b < nblocks; b += stride) {
+    const uint4 q0 = __ldg(q + 2 * b), q1 = __ldg(q + 2 * b + 1);
+    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const int sbyte = __ldg(sc + b);
+    float o[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t c = (words[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+      const float m = ((c & 0x7Fu) == 0x7Fu || sbyte == 0xFF) ? __int_as_float(0x7FC00000)
+                                                              : ldexpf(e4m3_mag(c & 0x7Fu), sbyte - 127);
+      o[i] = (c & 0x80u) ? -m : m;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      dst[b * 4 + i] = make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
+                                  pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
+  }
+}
+
 int grid_for(int64_t items, int per_block) {
   const int64_t want = (items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
@@ -220,6 +305,29 @@ int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int3
   trace_begin(stream, kind);
   gather_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), row_token, meta,
                                                         H / 8, reinterpret_cast<uint4*>(dst));
+  trace_end(stream);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+                          int32_t H, uint16_t* dst, int kind, cudaStream_t stream) {
+  if (rpad_max <= 0) return 0;
+  const int grid = grid_for(rpad_max, kMoveThreads / 32);
+  trace_begin(stream, kind);
+  gather_rows_mx_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), row_token, meta,
+                                                           H / 8, reinterpret_cast<uint4*>(dst));
+  trace_end(stream);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_mx_dequant(const uint8_t* q, const uint8_t* sc, int64_t rows, int64_t cols, uint16_t* dst,
+                      cudaStream_t stream) {
+  const int64_t nblocks = rows * (cols / 32);
+  if (nblocks <= 0) return 0;
+  const int grid = grid_for(nblocks, kMoveThreads);
+  trace_begin(stream, K_MX_DEQUANT);
+  mx_dequant_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(q), sc, nblocks,
+                                                       reinterpret_cast<uint4*>(dst));
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

@@ -7,6 +7,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "mok.h"
 
@@ -201,6 +202,48 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------------------------------------
+// MXFP8 helpers (OCP MX: E4M3 elements, one E8M0 scale per 32 values)
+// ------------------------------------------------------------------------------------------------
+// Two fp32 values -> E4M3 (round to nearest even, saturating to +-448) -> back to fp32, exactly.
+__device__ __forceinline__ void e4m3x2_round_trip(float& hi, float& lo) {
+  uint16_t q;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(hi), "f"(lo));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q));
+  hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+  lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// 2^e exactly, for e in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(1 << (e + 149));
+}
+
+// Quantise-dequantise 2n values of one MX block with shared exponent `shared` (in [-127, 127]):
+// E4M3(v * 2^-shared) * 2^shared, exact scalings, hardware round-to-nearest-even with saturation.
+__device__ __forceinline__ void mx_qdq_pairs(float* v, int n2, int shared) {
+  const float dn = pow2f(-shared), up = pow2f(shared);
+#pragma unroll
+  for (int i = 0; i < n2; i += 2) {
+    float hi = v[i] * dn, lo = v[i + 1] * dn;
+    e4m3x2_round_trip(hi, lo);
+    v[i] = hi * up;
+    v[i + 1] = lo * up;
+  }
+}
+
+// MX quantise-dequantise of 32 fp32 values in place: shared = floor(log2 amax) - 8 clamped at
+// -127 (amax 0 or subnormal), elements E4M3(v / 2^shared) * 2^shared.
+__device__ __forceinline__ void mx_fakequant32(float* v) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int shared = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
+  shared = shared < -127 ? -127 : shared;
+  mx_qdq_pairs(v, 32, shared);
 }
 
 // bf16 helpers (round to nearest even, no special-value surprises for finite inputs)

@@ -63,9 +63,12 @@ class mok_schedule(ctypes.Structure):
                 ("ws_bytes", ctypes.c_size_t)]
 
 
+MX_KEYS = ("q_gate", "s_gate", "q_up", "s_up", "q_down", "s_down",
+           "qt_gate", "st_gate", "qt_up", "st_up", "qt_down", "st_down")
+
+
 class mok_weights(ctypes.Structure):
-    _fields_ = [("w_gate", _P), ("w_up", _P), ("w_down", _P), ("q_gate", _P), ("s_gate", _P), ("q_up", _P),
-                ("s_up", _P), ("q_down", _P), ("s_down", _P)]
+    _fields_ = [("w_gate", _P), ("w_up", _P), ("w_down", _P)] + [(k, _P) for k in MX_KEYS]
 
 
 class mok_grads(ctypes.Structure):
@@ -221,15 +224,31 @@ def mok_build_schedule(cfg: mok_config, shape: mok_shape, topk_ids: torch.Tensor
     return Schedule(s, ws, topk_ids, topk_weights)
 
 
-def weights_struct(Wg, Wu, Wd, mx: dict | None = None) -> mok_weights:
+def weights_struct(Wg=None, Wu=None, Wd=None, mx: dict | None = None) -> mok_weights:
+    """bf16 weights for BF16 mode; ``mx`` = the pre-quantised copies (``quantize_weights``) for
+    MXFP8 mode.  The struct holds raw pointers: keep the tensors alive while it is used."""
     w = mok_weights()
     w.w_gate = _ptr(Wg, torch.bfloat16, "w_gate")
     w.w_up = _ptr(Wu, torch.bfloat16, "w_up")
     w.w_down = _ptr(Wd, torch.bfloat16, "w_down")
     if mx:
-        for k in ("q_gate", "s_gate", "q_up", "s_up", "q_down", "s_down"):
+        for k in MX_KEYS:
             setattr(w, k, _ptr(mx.get(k), torch.uint8, k))
     return w
+
+
+def quantize_weights(Wg: torch.Tensor, Wu: torch.Tensor, Wd: torch.Tensor, stream=None) -> dict:
+    """The MXFP8 weight copies of mok_weights, made with mok_mxfp8_quantize on the device: forward
+    copies along each GEMM's K and backward copies of the transposes."""
+    E, I, H = Wg.shape
+    out = {}
+    out["q_gate"], out["s_gate"] = mok_mxfp8_quantize(Wg.reshape(E * I, H), stream=stream)
+    out["q_up"], out["s_up"] = mok_mxfp8_quantize(Wu.reshape(E * I, H), stream=stream)
+    out["q_down"], out["s_down"] = mok_mxfp8_quantize(Wd.reshape(E * H, I), stream=stream)
+    out["qt_gate"], out["st_gate"] = mok_mxfp8_quantize(Wg.transpose(1, 2).contiguous().reshape(E * H, I), stream=stream)
+    out["qt_up"], out["st_up"] = mok_mxfp8_quantize(Wu.transpose(1, 2).contiguous().reshape(E * H, I), stream=stream)
+    out["qt_down"], out["st_down"] = mok_mxfp8_quantize(Wd.transpose(1, 2).contiguous().reshape(E * I, H), stream=stream)
+    return out
 
 
 def mok_forward(sched: Schedule, x: torch.Tensor, weights: mok_weights, out: torch.Tensor, fwd_ctx: torch.Tensor,

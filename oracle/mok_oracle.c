@@ -64,22 +64,22 @@ double orc_e4m3_value(uint8_t c) {
 }
 
 /* Round-to-nearest-even onto the E4M3 grid, saturating to +-448 (satfinite reading).
- * Brute force over the 127 non-negative finite codes: the nearest value wins, and on an exact
- * tie the code with the even mantissa (even code) wins.  NaN maps to 0x7F. */
+ * The 127 non-negative finite codes 0x00..0x7E have increasing values; bisection finds the code c
+ * with value(c) <= |v| < value(c + 1), then the nearer of the two wins, and on an exact tie the
+ * code with the even mantissa (even code).  NaN maps to 0x7F. */
 uint8_t orc_e4m3_encode(double v) {
     if (isnan(v)) return 0x7F;
     uint8_t sign = signbit(v) ? 0x80 : 0x00;
     double a = fabs(v);
     if (a >= 448.0) return (uint8_t)(sign | 0x7E);
-    int best = 0;
-    double best_d = INFINITY;
-    for (int c = 0; c <= 0x7E; ++c) {
-        double d = fabs(orc_e4m3_value((uint8_t)c) - a);
-        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
-            best = c;
-            best_d = d;
-        }
+    int lo = 0, hi = 0x7E; /* value(lo) <= a < value(hi) */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (orc_e4m3_value((uint8_t)mid) <= a) lo = mid;
+        else hi = mid;
     }
+    double dlo = a - orc_e4m3_value((uint8_t)lo), dhi = orc_e4m3_value((uint8_t)hi) - a;
+    int best = (dlo < dhi || (dlo == dhi && (lo & 1) == 0)) ? lo : hi;
     return (uint8_t)(sign | best);
 }
 

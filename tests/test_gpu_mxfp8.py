@@ -1,0 +1,129 @@
+"""GPU MXFP8 mode vs the fp64 MXFP8 oracle (mok_oracle_mx.c), through the C ABI.
+
+Tolerance (MXFP8): max|gpu - oracle| / max|oracle| <= 4e-2 per output tensor.  The pre-quantised
+weight bytes the GPU consumes come from mok_mxfp8_quantize and must equal the oracle's own
+quantisation bit for bit; activations are quantised inside the library (x, dY in the gather,
+a, dg, du in the GEMM epilogues) and the oracle mirrors those points in fp64.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import rel_err, to_f64
+from mixture_experts_layer_build_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_MX = 4e-2
+
+
+@pytest.fixture(scope="module")
+def mok():
+    from mixture_experts_layer_build_gb300 import mok as m
+    return m
+
+
+def _run_mx(mok, d, w, cfg, mx_gpu):
+    x, ids, s, dY = (d[k].cuda() for k in ("x", "topk_ids", "topk_weights", "dY"))
+    layer = mok.Layer(w.T, w.H, w.I, w.E, w.K, cfg)
+    weights = mok.weights_struct(mx=mx_gpu)
+    layer.schedule(ids, s)
+    out = layer.forward(x, weights)
+    g = layer.backward(dY, weights)
+    torch.cuda.synchronize()
+    assert mok.mok_read_device_status(layer.sched) == 0
+    return out, g
+
+
+def _mx_inputs(mok, d):
+    Wg, Wu, Wd = (d[k].cuda() for k in ("Wg", "Wu", "Wd"))
+    mx_gpu = mok.quantize_weights(Wg, Wu, Wd)
+    torch.cuda.synchronize()
+    return mx_gpu
+
+
+SMALL = [
+    ("tiny", inputs.WORKLOADS["tiny"]),
+    ("ragged", inputs.custom(T=100, H=256, I=256, E=5, K=3)),
+    ("multi_tile", inputs.custom(T=700, H=512, I=384, E=3, K=2)),
+]
+
+
+@pytest.mark.parametrize("name,w", SMALL, ids=[n for n, _ in SMALL])
+def test_mxfp8_full_parity(mok, name, w):
+    d = inputs.make(w, seed=2)
+    mx_gpu = _mx_inputs(mok, d)
+    mx_ref = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+    for k in oracle.MX_KEYS:  # the weight copies are bit-exact with the oracle's quantisation
+        assert np.array_equal(mx_gpu[k].cpu().numpy(), mx_ref[k]), k
+    cfg = mok.make_config(128, 256, precision=mok.MOK_MXFP8)
+    out, g = _run_mx(mok, d, w, cfg, mx_gpu)
+    ref = oracle.layer_mx(d["topk_ids"].numpy(), d["topk_weights"].numpy(), inputs.bits(d["x"]),
+                          inputs.bits(d["dY"]), mx_ref, w.E, w.I)
+    errs = dict(out=rel_err(to_f64(out), ref["out"]), dX=rel_err(to_f64(g.dx), ref["dX"]),
+                dWg=rel_err(to_f64(g.dw_gate), ref["dWg"]), dWu=rel_err(to_f64(g.dw_up), ref["dWu"]),
+                dWd=rel_err(to_f64(g.dw_down), ref["dWd"]), dS=rel_err(to_f64(g.d_topk_weights), ref["dS"]))
+    bad = {k: v for k, v in errs.items() if not v <= TOL_MX}
+    assert not bad, errs
+
+
+def test_mxfp8_ep64_shard_sampled_parity_and_determinism(mok):
+    """The per-GPU shard of an EP64 layer: 16,384 routed rows onto 4 experts (Zipf 1.2),
+    H=7168, I=2048, top-1."""
+    w = inputs.WORKLOADS["mxfp8_ep64_shard"]
+    d = inputs.make(w, seed=0)
+    mx_gpu = _mx_inputs(mok, d)
+    mx_ref = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+    for k in ("q_gate", "st_down"):  # spot-check two copies bit for bit
+        assert np.array_equal(mx_gpu[k].cpu().numpy(), mx_ref[k]), k
+    cfg = mok.make_config(512, 2048, precision=mok.MOK_MXFP8)
+    out, g = _run_mx(mok, d, w, cfg, mx_gpu)
+    r = dict(out=out.clone(), dx=g.dx.clone(), dwg=g.dw_gate.clone(), dwu=g.dw_up.clone(), dwd=g.dw_down.clone(),
+             ds=g.d_topk_weights.clone())
+    args = (d["topk_ids"].numpy(), d["topk_weights"].numpy(), inputs.bits(d["x"]), inputs.bits(d["dY"]))
+    rng = np.random.default_rng(0)
+    tok = np.sort(rng.choice(w.T, size=8, replace=False))
+    ro, rdx, rds = oracle.tokens_mx(*args, mx_ref, w.E, w.I, tok)
+    tk = torch.from_numpy(tok).cuda()
+    errs = dict(out=rel_err(to_f64(r["out"][tk]), ro), dX=rel_err(to_f64(r["dx"][tk]), rdx),
+                dS=rel_err(to_f64(r["ds"][tk]), rds))
+    counts = np.bincount(args[0].reshape(-1), minlength=w.E)
+    e = int(np.argmin(counts))
+    i0 = 32 * int(rng.integers(0, w.I // 32))
+    hs = np.sort(rng.choice(w.H, size=8, replace=False))
+    dwg, dwu, dwd = oracle.dw_block_mx(*args, mx_ref, w.E, w.I, e, i0, hs)
+    hk = torch.from_numpy(hs).cuda()
+    errs["dWg"] = rel_err(to_f64(r["dwg"][e, i0:i0 + 32][:, hk]), dwg)
+    errs["dWu"] = rel_err(to_f64(r["dwu"][e, i0:i0 + 32][:, hk]), dwu)
+    errs["dWd"] = rel_err(to_f64(r["dwd"][e][hk, i0:i0 + 32]), dwd)
+    bad = {k: v for k, v in errs.items() if not v <= TOL_MX}
+    assert not bad, errs
+    for k, v in r.items():
+        assert torch.isfinite(v).all(), k
+    # bitwise identical on another grid and minibatch size
+    out2, g2 = _run_mx(mok, d, w, mok.make_config(256, 512, 37, precision=mok.MOK_MXFP8), mx_gpu)
+    for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down, ds=g2.d_topk_weights).items():
+        assert torch.equal(v, r[k]), k
+
+
+def test_mxfp8_gather_quantises_x_bit_exactly(mok):
+    """The quantise-on-gather of x equals the oracle's MX quantisation of x, bit for bit."""
+    w = inputs.custom(T=200, H=512, I=128, E=4, K=2)
+    d = inputs.make(w, seed=4)
+    x = d["x"].clone()
+    x[3] = x[3] * 1e-30  # tiny block exponents
+    x[4] = x[4] * 1e30   # large ones
+    x[5, :64] = 0        # zero blocks
+    d["x"] = x
+    mx_gpu = _mx_inputs(mok, d)
+    cfg = mok.make_config(128, 256, precision=mok.MOK_MXFP8)
+    layer = mok.Layer(w.T, w.H, w.I, w.E, w.K, cfg)
+    layer.schedule(d["topk_ids"].cuda(), d["topk_weights"].cuda())
+    layer.forward(x.cuda(), mok.weights_struct(mx=mx_gpu))
+    torch.cuda.synchronize()
+    inv = layer.sched.tables()["inv"].cpu().numpy().astype(np.int64)
+    xg = layer.ctx.view(torch.uint8)[: layer.sched.c.rpad_max * w.H * 2].view(torch.bfloat16).view(-1, w.H)
+    got = to_f64(xg)[inv]
+    ref = oracle.mx_fakequant(oracle.bf16_to_f64(inputs.bits(x)))[np.arange(w.R) // w.K]
+    assert np.array_equal(got, ref)
