@@ -154,19 +154,39 @@ class ClockSampler:
 # ------------------------------------------------------------------------------------------------
 # algorithmic work per kernel (flops for tensor-core kernels, bytes for the HBM-bound ones)
 # ------------------------------------------------------------------------------------------------
-def kernel_work(w) -> dict:
-    R, H, I, T, K = w.R, w.H, w.I, w.T, w.K
-    f = lambda c: ("tensor", c * R * H * I)  # noqa: E731
+def kernel_work(w, e_active: int) -> dict:
+    """Algorithmic (flops, HBM bytes) of one launch of each kernel.  Bytes count each tensor the
+    kernel must read or write once: gathered rows R (not the padded rows), the weights of the
+    experts that received rows, the fp32 weight gradients of every expert."""
+    R, H, I, T, K, E = w.R, w.H, w.I, w.T, w.K, w.E
+    b16 = 2
+    gu_b = 4 if w.precision == "mxfp8" else 2  # saved g, u
+    wts = e_active * H * I * b16               # one weight matrix of the active experts
     return {
-        "gemm_fwd_gateup": f(4), "gemm_fwd_down": f(2), "gemm_dgrad1": f(2), "gemm_dgrad2": f(4),
-        "gemm_wgrad_gu": f(4), "gemm_wgrad_d": f(2),
+        "gemm_fwd_gateup": (4 * R * H * I, R * H * b16 + 2 * wts + R * 2 * I * gu_b + R * I * b16),
+        "gemm_fwd_down": (2 * R * H * I, R * I * b16 + wts + R * H * b16),
+        "gemm_dgrad1": (2 * R * H * I, R * H * b16 + wts + R * 2 * I * gu_b + R * I * b16 + R * 3 * I * b16),
+        "gemm_dgrad2": (4 * R * H * I, R * 2 * I * b16 + 2 * wts + R * H * b16),
+        "gemm_wgrad_gu": (4 * R * H * I, R * 2 * I * b16 + R * H * b16 + 2 * E * I * H * 4),
+        "gemm_wgrad_d": (2 * R * H * I, R * H * b16 + R * I * b16 + E * H * I * 4),
         # gather: unique token rows read once + routed rows written
-        "gather_x": ("hbm", T * H * 2 + R * H * 2), "gather_dy": ("hbm", T * H * 2 + R * H * 2),
+        "gather_x": (0, T * H * b16 + R * H * b16), "gather_dy": (0, T * H * b16 + R * H * b16),
         # combine / dX reduce: routed rows read + weights/indices + token rows written
-        "combine": ("hbm", R * H * 2 + T * K * 8 + T * H * 2), "dx_reduce": ("hbm", R * H * 2 + T * K * 4 + T * H * 2),
+        "combine": (0, R * H * b16 + T * K * 8 + T * H * b16), "dx_reduce": (0, R * H * b16 + T * K * 4 + T * H * b16),
         # MXFP8: exact decode of one pre-quantised weight copy (1 + 1/32 bytes read, 2 written per element)
-        "mx_dequant": ("hbm", w.E * H * I * (1 + 1 / 32 + 2)),
+        "mx_dequant": (0, E * H * I * (1 + 1 / 32 + 2)),
     }
+
+
+def roofline_of(flops, nbytes, ms, peaks):
+    """The kernel's bound is the larger of its tensor time and its HBM time at the measured peaks."""
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    sec = ms * 1e-3
+    if t_tensor >= t_hbm:
+        return dict(bound="tensor", achieved=flops / sec / 1e12, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=t_tensor / sec)
+    return dict(bound="hbm", achieved=nbytes / sec / 1e9, peak=peaks["hbm_gbs"], unit="GB/s", frac=t_hbm / sec)
 
 
 def src_hash() -> str:
@@ -351,30 +371,24 @@ def ours(args, rank, ws, local_rank):
         p[1] += 1
     traced_total = sum(v[0] for v in per.values())
     kernels = {k: {"avg_ms": v[0] / v[1], "launches": v[1], "share": v[0] / traced_total} for k, v in per.items()}
-    work = kernel_work(w)
+    e_active = int(torch.unique(ids).numel())
+    work = kernel_work(w, e_active)
     peaks, peak_src = load_peaks()
     for k, v in kernels.items():
         if k in work:
-            kind, amount = work[k]
-            if kind == "tensor":
-                v["tflops"] = amount / (v["avg_ms"] * 1e-3) / 1e12
-            else:
-                v["gbs"] = amount / (v["avg_ms"] * 1e-3) / 1e9
+            fl, nb = work[k]
+            if fl:
+                v["tflops"] = fl / (v["avg_ms"] * 1e-3) / 1e12
+            v["gbs"] = nb / (v["avg_ms"] * 1e-3) / 1e9
+            rf = roofline_of(fl, nb, v["avg_ms"], peaks)
+            v["bound"], v["frac"] = rf["bound"], rf["frac"]
     dom = max((k for k in kernels if k in work), key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
-    kind, amount = work[dom]
-    achieved_per_s = amount / (kernels[dom]["avg_ms"] * 1e-3)
+    fl, nb = work[dom]
     traffic, tnote = traffic_for(dom, args.workload)
-    if kind == "tensor":
-        peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved_per_s / 1e12, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved_per_s / 1e12 / peak, "traffic": traffic}
-    else:
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved_per_s / 1e9, "peak": peak, "unit": "GB/s",
-                "frac": achieved_per_s / 1e9 / peak, "traffic": traffic}
-    roof.update({"kernel": dom, "peak_source": f"{peak_src} (burst bf16 GEMM / STREAM copy)"
-                 if peak_src == "measured" else "fallback", "traffic_note": tnote,
-                 "algorithmic_per_launch": amount})
+    roof = roofline_of(fl, nb, kernels[dom]["avg_ms"], peaks)
+    roof.update({"traffic": traffic, "kernel": dom,
+                 "peak_source": f"{peak_src} (burst bf16 GEMM / STREAM copy)" if peak_src == "measured" else "fallback",
+                 "traffic_note": tnote, "algorithmic_flops_per_launch": fl, "algorithmic_bytes_per_launch": nb})
 
     # ---- end to end through the C ABI with host buffers ----
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
