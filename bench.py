@@ -6,7 +6,8 @@ routing), synthetic seeded inputs.  Prints ONE JSON line (rank 0):
   value     tokens/s of the whole job (all ranks), inputs resident in HBM, CUDA events on the
             launching stream, max over ranks;
   e2e       the same metric through the C ABI with host (pinned) inputs: H2D of x, ids, weights,
-            dY and D2H of out, dX, d_topk_weights inside every timed step;
+            dY and D2H of out, dX, d_topk_weights for every timed step, double-buffered over a
+            copy stream so transfers overlap the neighbouring steps' compute;
   roofline  the dominant kernel's algorithmic flops (or bytes) per launch over its average launch
             time, measured live with per-launch CUDA events (the library's trace hook), against
             the measured peak;
@@ -391,34 +392,70 @@ def ours(args, rank, ws, local_rank):
                  "traffic_note": tnote, "algorithmic_flops_per_launch": fl, "algorithmic_bytes_per_launch": nb})
 
     # ---- end to end through the C ABI with host buffers ----
+    # Every step copies its own inputs host->device and its results device->host inside the timed
+    # region.  Inputs and outputs are double-buffered over a copy stream, so step i+1's uploads and
+    # step i-1's downloads overlap step i's compute (the usual prefetching input pipeline).
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    hx, hids, hs, hdy = pin(d["x"]), pin(d["topk_ids"]), pin(d["topk_weights"]), pin(d["dY"])
-    hout = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-    hdx = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-    hds = torch.empty((w.T, w.K), dtype=torch.float32).pin_memory()
-    dx_, dids, ds_, ddy = (torch.empty_like(t, device=dev) for t in (x, ids, s, dY))
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hs, hdy))
-    d2h = sum(t.numel() * t.element_size() for t in (hout, hdx, hds))
+    host_in = [pin(d["x"]), pin(d["topk_ids"]), pin(d["topk_weights"]), pin(d["dY"])]
+    host_out = [[torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory(),
+                 torch.empty((w.T, w.K), dtype=torch.float32).pin_memory()] for _ in range(2)]
+    dev_in = [[torch.empty_like(t, device=dev) for t in (x, ids, s, dY)] for _ in range(2)]
+    dev_out = [dict(out=torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev),
+                    grads=mok.Grads.empty(w.T, w.H, w.I, w.E, w.K, device=dev)) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    copy_stream = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # uploads of buffer b landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # compute on buffer b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # downloads of buffer b finished
 
-    def e2e_step():
+    def upload(i):
+        b = i % 2
+        with torch.cuda.stream(copy_stream):
+            if i >= 2:
+                copy_stream.wait_event(ev_done[b])  # buffer b's previous step has consumed its inputs
+            for dst, src in zip(dev_in[b], host_in):
+                dst.copy_(src, non_blocking=True)
+            ev_in[b].record(copy_stream)
+
+    def compute(i):
+        b = i % 2
+        xx, ii, ss, dd = dev_in[b]
         with torch.cuda.stream(stream):
-            dx_.copy_(hx, non_blocking=True)
-            dids.copy_(hids, non_blocking=True)
-            ds_.copy_(hs, non_blocking=True)
-            ddy.copy_(hdy, non_blocking=True)
-            step(dx_, dids, ds_, ddy)
-            hout.copy_(layer.out, non_blocking=True)
-            hdx.copy_(layer.grads.dx, non_blocking=True)
-            hds.copy_(layer.grads.d_topk_weights, non_blocking=True)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])  # buffer b's previous results have been downloaded
+            sch = mok.mok_build_schedule(layer.cfg, layer.shape, ii, ss, layer.ws, stream)
+            mok.mok_forward(sch, xx, weights, dev_out[b]["out"], layer.ctx, stream)
+            mok.mok_backward(sch, layer.ctx, dd, weights, dev_out[b]["grads"], stream)
+            ev_done[b].record(stream)
 
-    for _ in range(2):
-        e2e_step()
+    def download(i):
+        b = i % 2
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_done[b])
+            o, g = dev_out[b]["out"], dev_out[b]["grads"]
+            for dst, src in zip(host_out[b], (o, g.dx, g.d_topk_weights)):
+                dst.copy_(src, non_blocking=True)
+            ev_out[b].record(copy_stream)
+
+    def e2e_run(n):
+        # issue order keeps both streams busy: upload(i+1) before compute(i)'s results are fetched
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            compute(i)
+            download(i)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     barrier(ws)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(copy_stream)
+    e2e_run(args.steps)
+    copy_stream.wait_stream(stream)
+    e1.record(copy_stream)
     torch.cuda.synchronize()
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)

@@ -57,6 +57,12 @@ WORKLOADS = {
     "sweep_zipf0": Workload("sweep_zipf0", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=0.0),
     "sweep_zipf1": Workload("sweep_zipf1", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=1.0),
     "sweep_zipf2": Workload("sweep_zipf2", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=2.0),
+    "sweep_zipf0_mx": Workload("sweep_zipf0_mx", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=0.0,
+                               precision="mxfp8"),
+    "sweep_zipf1_mx": Workload("sweep_zipf1_mx", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=1.0,
+                               precision="mxfp8"),
+    "sweep_zipf2_mx": Workload("sweep_zipf2_mx", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=2.0,
+                               precision="mxfp8"),
 }
 
 

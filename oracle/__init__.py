@@ -284,19 +284,27 @@ def mx_set_quant(on: bool):
     _load().orc_mx_set_quant(1 if on else 0)
 
 
-def mx_weights(Wg, Wu, Wd) -> dict:
+def mx_weights(Wg, Wu, Wd, experts=None) -> dict:
     """The pre-quantised weight copies of the MXFP8 mode, from bf16 weights [E,I,H], [E,H,I]:
     forward copies along each GEMM's K (Wg, Wu along H; Wd along I) and backward copies of the
-    transposes (Wg^T, Wu^T along I; Wd^T along H)."""
+    transposes (Wg^T, Wu^T along I; Wd^T along H).  With ``experts``, only those experts are
+    quantised (the others' bytes are zero and must not be read)."""
     Wg, Wu, Wd = _u16(Wg), _u16(Wu), _u16(Wd)
     E, I, H = Wg.shape
+    sel = range(E) if experts is None else sorted(set(int(e) for e in np.asarray(experts).reshape(-1)))
+    shapes = dict(gate=(I, H), up=(I, H), down=(H, I))
+    src = dict(gate=Wg, up=Wu, down=Wd)
     out = {}
-    out["q_gate"], out["s_gate"] = mxfp8_quantize(Wg.reshape(E * I, H))
-    out["q_up"], out["s_up"] = mxfp8_quantize(Wu.reshape(E * I, H))
-    out["q_down"], out["s_down"] = mxfp8_quantize(Wd.reshape(E * H, I))
-    out["qt_gate"], out["st_gate"] = mxfp8_quantize(np.ascontiguousarray(Wg.transpose(0, 2, 1)).reshape(E * H, I))
-    out["qt_up"], out["st_up"] = mxfp8_quantize(np.ascontiguousarray(Wu.transpose(0, 2, 1)).reshape(E * H, I))
-    out["qt_down"], out["st_down"] = mxfp8_quantize(np.ascontiguousarray(Wd.transpose(0, 2, 1)).reshape(E * I, H))
+    for name, W in src.items():
+        r, c = shapes[name]
+        q = np.zeros((E * r, c), np.uint8)
+        sc = np.zeros((E * r, c // 32), np.uint8)
+        qt = np.zeros((E * c, r), np.uint8)
+        st = np.zeros((E * c, r // 32), np.uint8)
+        for e in sel:
+            q[e * r:(e + 1) * r], sc[e * r:(e + 1) * r] = mxfp8_quantize(W[e])
+            qt[e * c:(e + 1) * c], st[e * c:(e + 1) * c] = mxfp8_quantize(np.ascontiguousarray(W[e].T))
+        out["q_" + name], out["s_" + name], out["qt_" + name], out["st_" + name] = q, sc, qt, st
     return out
 
 

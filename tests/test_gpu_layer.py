@@ -185,9 +185,16 @@ def test_workload_sampled_parity_and_grid_determinism(mok, name):
     errs = _sampled_errors(d, w, r)
     bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
     assert not bad, errs
-    # a different grid and minibatch size must give the same bits
-    _, out2, g2 = _run(mok, d, w, mok.make_config(128, 1024, 61))
-    for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down, ds=g2.d_topk_weights).items():
-        assert torch.equal(v, r[k]), k
-    del g2, r, d
+    # other grids and every minibatch size of the granularity sweep (128 .. 2048 rows) must give
+    # the same bits
+    cfgs = [mok.make_config(128, 1024, 61)]
+    if name.startswith("sweep"):
+        cfgs += [mok.make_config(mb, 2 * mb) for mb in (256, 1024, 2048)]
+    for cfg in cfgs:
+        _, out2, g2 = _run(mok, d, w, cfg)
+        for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down,
+                         ds=g2.d_topk_weights).items():
+            assert torch.equal(v, r[k]), (cfg.minibatch_rows, k)
+        del g2
+    del r, d
     torch.cuda.empty_cache()

@@ -127,3 +127,36 @@ def test_mxfp8_gather_quantises_x_bit_exactly(mok):
     got = to_f64(xg)[inv]
     ref = oracle.mx_fakequant(oracle.bf16_to_f64(inputs.bits(x)))[np.arange(w.R) // w.K]
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("name", ["sweep_zipf0_mx", "sweep_zipf2_mx"])
+def test_mxfp8_sweep_sampled_parity(mok, name):
+    """T=8192, H=4096, I=1536, E=128, top-8, Zipf-skewed routing, MXFP8.  The oracle quantises only
+    the experts its sampled tokens and its dW block touch."""
+    w = inputs.WORKLOADS[name]
+    d = inputs.make(w, seed=0, weight_device="cuda")
+    mx_gpu = _mx_inputs(mok, d)
+    out, g = _run_mx(mok, d, w, mok.make_config(512, 2048, precision=mok.MOK_MXFP8), mx_gpu)
+    ids = d["topk_ids"].numpy()
+    rng = np.random.default_rng(1)
+    tok = np.sort(rng.choice(w.T, size=4, replace=False))
+    counts = np.bincount(ids.reshape(-1), minlength=w.E)
+    e = int(np.argmax(counts))  # the heaviest expert for the weight-gradient block
+    experts = np.unique(np.concatenate([ids[tok].reshape(-1), [e]]))
+    mx_ref = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]), experts=experts)
+    args = (ids, d["topk_weights"].numpy(), inputs.bits(d["x"]), inputs.bits(d["dY"]))
+    ro, rdx, rds = oracle.tokens_mx(*args, mx_ref, w.E, w.I, tok)
+    tk = torch.from_numpy(tok).cuda()
+    errs = dict(out=rel_err(to_f64(out[tk]), ro), dX=rel_err(to_f64(g.dx[tk]), rdx),
+                dS=rel_err(to_f64(g.d_topk_weights[tk]), rds))
+    i0 = 32 * int(rng.integers(0, w.I // 32))
+    hs = np.sort(rng.choice(w.H, size=4, replace=False))
+    dwg, dwu, dwd = oracle.dw_block_mx(*args, mx_ref, w.E, w.I, e, i0, hs)
+    hk = torch.from_numpy(hs).cuda()
+    errs["dWg"] = rel_err(to_f64(g.dw_gate[e, i0:i0 + 32][:, hk]), dwg)
+    errs["dWu"] = rel_err(to_f64(g.dw_up[e, i0:i0 + 32][:, hk]), dwu)
+    errs["dWd"] = rel_err(to_f64(g.dw_down[e][hk, i0:i0 + 32]), dwd)
+    bad = {k: v for k, v in errs.items() if not v <= TOL_MX}
+    assert not bad, errs
+    del out, g
+    torch.cuda.empty_cache()
