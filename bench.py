@@ -156,37 +156,64 @@ class ClockSampler:
 # algorithmic work per kernel (flops for tensor-core kernels, bytes for the HBM-bound ones)
 # ------------------------------------------------------------------------------------------------
 def kernel_work(w, e_active: int) -> dict:
-    """Algorithmic (flops, HBM bytes) of one launch of each kernel.  Bytes count each tensor the
-    kernel must read or write once: gathered rows R (not the padded rows), the weights of the
-    experts that received rows, the fp32 weight gradients of every expert."""
+    """Algorithmic (flops, HBM bytes, operand type) of one launch of each kernel.  Bytes count each
+    tensor the kernel must read or write once: gathered rows R (not the padded rows), the weights of
+    the experts that received rows, the fp32 weight gradients of every expert.  MXFP8 operands
+    count 1 + 1/32 bytes per element (E4M3 code + its share of the E8M0 scale)."""
     R, H, I, T, K, E = w.R, w.H, w.I, w.T, w.K, w.E
     b16 = 2
-    gu_b = 4 if w.precision == "mxfp8" else 2  # saved g, u
-    wts = e_active * H * I * b16               # one weight matrix of the active experts
-    return {
-        "gemm_fwd_gateup": (4 * R * H * I, R * H * b16 + 2 * wts + R * 2 * I * gu_b + R * I * b16),
-        "gemm_fwd_down": (2 * R * H * I, R * I * b16 + wts + R * H * b16),
-        "gemm_dgrad1": (2 * R * H * I, R * H * b16 + wts + R * 2 * I * gu_b + R * I * b16 + R * 3 * I * b16),
-        "gemm_dgrad2": (4 * R * H * I, R * 2 * I * b16 + 2 * wts + R * H * b16),
-        "gemm_wgrad_gu": (4 * R * H * I, R * 2 * I * b16 + R * H * b16 + 2 * E * I * H * 4),
-        "gemm_wgrad_d": (2 * R * H * I, R * H * b16 + R * I * b16 + E * H * I * 4),
-        # gather: unique token rows read once + routed rows written
-        "gather_x": (0, T * H * b16 + R * H * b16), "gather_dy": (0, T * H * b16 + R * H * b16),
+    work = {
+        "gemm_wgrad_gu": (4 * R * H * I, R * 2 * I * b16 + R * H * b16 + 2 * E * I * H * 4, "bf16"),
+        "gemm_wgrad_d": (2 * R * H * I, R * H * b16 + R * I * b16 + E * H * I * 4, "bf16"),
         # combine / dX reduce: routed rows read + weights/indices + token rows written
-        "combine": (0, R * H * b16 + T * K * 8 + T * H * b16), "dx_reduce": (0, R * H * b16 + T * K * 4 + T * H * b16),
-        # MXFP8: exact decode of one pre-quantised weight copy (1 + 1/32 bytes read, 2 written per element)
-        "mx_dequant": (0, E * H * I * (1 + 1 / 32 + 2)),
+        "combine": (0, R * H * b16 + T * K * 8 + T * H * b16, None),
+        "dx_reduce": (0, R * H * b16 + T * K * 4 + T * H * b16, None),
     }
+    if w.precision == "mxfp8":
+        mx = 1 + 1 / 32
+        wts = e_active * H * I * mx  # one quantised weight matrix of the active experts
+        work.update({
+            # reads Xq, Wg, Wu; writes g, u (fp32), a (bf16) and its MX copy
+            "gemm_fwd_gateup": (4 * R * H * I, R * H * mx + 2 * wts + R * 2 * I * 4 + R * I * (b16 + mx), "e4m3"),
+            "gemm_fwd_down": (2 * R * H * I, R * I * mx + wts + R * H * b16, "e4m3"),
+            # reads dYq, Wd^T, g, u (fp32), a; writes dg, du (bf16 and MX), s*a, dS partials
+            "gemm_dgrad1": (2 * R * H * I, R * H * mx + wts + R * 2 * I * 4 + R * I * b16
+                            + R * 2 * I * (b16 + mx) + R * I * b16 + R * (I // 128) * 4, "e4m3"),
+            "gemm_dgrad2": (4 * R * H * I, R * 2 * I * mx + 2 * wts + R * H * b16, "e4m3"),
+            # gather: unique token rows read once; routed rows written in bf16 and MX
+            "gather_x": (0, T * H * b16 + R * H * (b16 + mx), None),
+            "gather_dy": (0, T * H * b16 + R * H * (b16 + mx), None),
+            # three weight-scale matrices re-tiled into atoms per launch (read + write)
+            "mx_scale_atoms": (0, 2 * 3 * E * H * I / 32, None),
+        })
+    else:
+        wts = e_active * H * I * b16
+        work.update({
+            "gemm_fwd_gateup": (4 * R * H * I, R * H * b16 + 2 * wts + R * 2 * I * b16 + R * I * b16, "bf16"),
+            "gemm_fwd_down": (2 * R * H * I, R * I * b16 + wts + R * H * b16, "bf16"),
+            "gemm_dgrad1": (2 * R * H * I, R * H * b16 + wts + R * 2 * I * b16 + R * I * b16 + R * 3 * I * b16,
+                            "bf16"),
+            "gemm_dgrad2": (4 * R * H * I, R * 2 * I * b16 + 2 * wts + R * H * b16, "bf16"),
+            "gather_x": (0, T * H * b16 + R * H * b16, None),
+            "gather_dy": (0, T * H * b16 + R * H * b16, None),
+        })
+    return work
 
 
-def roofline_of(flops, nbytes, ms, peaks):
-    """The kernel's bound is the larger of its tensor time and its HBM time at the measured peaks."""
-    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+# dense tensor-core peak of an operand type relative to bf16 (nominal 4.5 vs 2.25 PFLOP/s for e4m3)
+TENSOR_RATIO = {"bf16": 1.0, "e4m3": 2.0}
+
+
+def roofline_of(flops, nbytes, ms, peaks, kind="bf16"):
+    """The kernel's bound is the larger of its tensor time (at the measured bf16 peak times the
+    nominal ratio of its operand type) and its HBM time at the measured copy bandwidth."""
+    tpeak = peaks["bf16_tflops"] * TENSOR_RATIO[kind or "bf16"]
+    t_tensor = flops / (tpeak * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     sec = ms * 1e-3
     if t_tensor >= t_hbm:
-        return dict(bound="tensor", achieved=flops / sec / 1e12, peak=peaks["bf16_tflops"], unit="TFLOP/s",
-                    frac=t_tensor / sec)
+        return dict(bound="tensor", achieved=flops / sec / 1e12, peak=tpeak, unit="TFLOP/s",
+                    frac=t_tensor / sec, operands=kind)
     return dict(bound="hbm", achieved=nbytes / sec / 1e9, peak=peaks["hbm_gbs"], unit="GB/s", frac=t_hbm / sec)
 
 
@@ -377,18 +404,19 @@ def ours(args, rank, ws, local_rank):
     peaks, peak_src = load_peaks()
     for k, v in kernels.items():
         if k in work:
-            fl, nb = work[k]
+            fl, nb, kd = work[k]
             if fl:
                 v["tflops"] = fl / (v["avg_ms"] * 1e-3) / 1e12
             v["gbs"] = nb / (v["avg_ms"] * 1e-3) / 1e9
-            rf = roofline_of(fl, nb, v["avg_ms"], peaks)
+            rf = roofline_of(fl, nb, v["avg_ms"], peaks, kd)
             v["bound"], v["frac"] = rf["bound"], rf["frac"]
     dom = max((k for k in kernels if k in work), key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
-    fl, nb = work[dom]
+    fl, nb, kd = work[dom]
     traffic, tnote = traffic_for(dom, args.workload)
-    roof = roofline_of(fl, nb, kernels[dom]["avg_ms"], peaks)
+    roof = roofline_of(fl, nb, kernels[dom]["avg_ms"], peaks, kd)
     roof.update({"traffic": traffic, "kernel": dom,
-                 "peak_source": f"{peak_src} (burst bf16 GEMM / STREAM copy)" if peak_src == "measured" else "fallback",
+                 "peak_source": (f"{peak_src} (burst bf16 GEMM / STREAM copy)" if peak_src == "measured"
+                                 else "fallback") + (" x2 nominal e4m3/bf16" if kd == "e4m3" else ""),
                  "traffic_note": tnote, "algorithmic_flops_per_launch": fl, "algorithmic_bytes_per_launch": nb})
 
     # ---- end to end through the C ABI with host buffers ----
@@ -467,7 +495,7 @@ def ours(args, rank, ws, local_rank):
         result = {
             "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "mxfp8 operands, bf16 tensor-core arithmetic" if mxfp8 else "bf16",
+            "vs_baseline": None, "dtype": "mxfp8" if mxfp8 else "bf16",
             "data": "synthetic (seeded; random-init expert weights)",
             "config": config_of(w, args, ws),
             "tflops": w.flops() / (ms_max * 1e-3) / 1e12,

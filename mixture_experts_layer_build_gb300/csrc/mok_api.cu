@@ -88,13 +88,21 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
   t.as = c.take<uint16_t>(z.rpad_max * z.I);
   t.dspart = c.take<float>(z.rpad_max * (z.I / 128));
   if (z.mx) {
-    const int64_t n = static_cast<int64_t>(z.E) * z.H * z.I;
-    t.wg_f = c.take<uint16_t>(n);
-    t.wu_f = c.take<uint16_t>(n);
-    t.wd_f = c.take<uint16_t>(n);
-    t.wg_b = c.take<uint16_t>(n);
-    t.wu_b = c.take<uint16_t>(n);
-    t.wd_b = c.take<uint16_t>(n);
+    const int64_t rt = (z.rpad_max + kRowTile - 1) / kRowTile;  // 128-row tiles of the routed rows
+    const int64_t EH = static_cast<int64_t>(z.E) * z.H, EI = static_cast<int64_t>(z.E) * z.I;
+    t.xq = c.take<uint8_t>(z.rpad_max * z.H);
+    t.xs = c.take<uint8_t>(rt * 128 * (z.H / 32));
+    t.aq = c.take<uint8_t>(z.rpad_max * z.I);
+    t.as_sf = c.take<uint8_t>(rt * 128 * (z.I / 32));
+    t.dyq = c.take<uint8_t>(z.rpad_max * z.H);
+    t.dys = c.take<uint8_t>(rt * 128 * (z.H / 32));
+    t.dgq = c.take<uint8_t>(z.rpad_max * 2 * z.I);
+    t.dgs = c.take<uint8_t>(rt * 128 * (2 * z.I / 32));
+    t.sw_gu = c.take<uint8_t>(2 * EI * (z.H / 32));
+    t.sw_d = c.take<uint8_t>(EH * (z.I / 32));
+    t.swt_d = c.take<uint8_t>(EI * (z.H / 32));
+    t.swt_g = c.take<uint8_t>(EH * (z.I / 32));
+    t.swt_u = c.take<uint8_t>(EH * (z.I / 32));
   }
   if (s) {
     s->counts = d.counts;
@@ -187,6 +195,14 @@ bool make_tmap_bf16_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint6
 bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                    uint32_t box_outer) {
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, inner, outer, box_inner, box_outer);
+}
+
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                  uint32_t box_outer, int swizzle_bytes) {
+  const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                      : CU_TENSOR_MAP_SWIZZLE_32B;
+  return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, inner, outer, box_inner, box_outer, sw);
 }
 
 static mok_trace* g_trace = nullptr;
@@ -294,6 +310,12 @@ static bool all16(std::initializer_list<const void*> ps) {
   return true;
 }
 
+static bool all4(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p || (reinterpret_cast<uintptr_t>(p) & 3u) != 0) return false;
+  return true;
+}
+
 mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weights* w, void* out, void* fwd_ctx,
                        size_t fwd_ctx_bytes, void* stream) {
   Sizes z;
@@ -306,19 +328,18 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
   if (reinterpret_cast<uintptr_t>(fwd_ctx) % kAlign) return MOK_ERR_INVALID_ARG;
   if (z.T > 0 && (!x || !out || !aligned16(x) || !aligned16(out))) return MOK_ERR_INVALID_ARG;
   if (z.mx) {
-    if (!all16({w->q_gate, w->q_up, w->q_down}) || !w->s_gate || !w->s_up || !w->s_down) return MOK_ERR_INVALID_ARG;
+    if (!all16({w->q_gate, w->q_up, w->q_down}) || !all4({w->s_gate, w->s_up, w->s_down})) return MOK_ERR_INVALID_ARG;
   } else if (!all16({w->w_gate, w->w_up, w->w_down})) {
     return MOK_ERR_INVALID_ARG;
   }
   cudaStream_t s = as_stream(stream);
-  if (z.mx) {  // exact bf16 decodes of the pre-quantised forward copies
+  if (z.mx) {  // weight scales into atoms, then x quantised on the gather
     const int64_t EI = static_cast<int64_t>(z.E) * z.I, EH = static_cast<int64_t>(z.E) * z.H;
-    if (launch_mx_dequant(w->q_gate, w->s_gate, EI, z.H, st.wg_f, s) ||
-        launch_mx_dequant(w->q_up, w->s_up, EI, z.H, st.wu_f, s) ||
-        launch_mx_dequant(w->q_down, w->s_down, EH, z.I, st.wd_f, s))
-      return MOK_ERR_CUDA;
+    const ScaleJob jobs[2] = {{w->s_gate, w->s_up, st.sw_gu, EI / 64, z.H / 128, 1},
+                              {w->s_down, nullptr, st.sw_d, EH / 128, z.I / 128, 0}};
+    if (launch_mx_scale_atoms(jobs, 2, s)) return MOK_ERR_CUDA;
     if (launch_gather_rows_mx(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
-                              ctx.xg, K_GATHER_X, s))
+                              ctx.xg, st.xq, st.xs, K_GATHER_X, s))
       return MOK_ERR_CUDA;
   } else if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
                                 ctx.xg, K_GATHER_X, s)) {
@@ -343,7 +364,7 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   if (z.T > 0 && (!dy || !g->dx || !g->d_topk_weights || !aligned16(dy) || !aligned16(g->dx)))
     return MOK_ERR_INVALID_ARG;
   if (z.mx) {
-    if (!all16({w->qt_gate, w->qt_up, w->qt_down}) || !w->st_gate || !w->st_up || !w->st_down)
+    if (!all16({w->qt_gate, w->qt_up, w->qt_down}) || !all4({w->st_gate, w->st_up, w->st_down}))
       return MOK_ERR_INVALID_ARG;
   } else if (!all16({w->w_gate, w->w_up, w->w_down})) {
     return MOK_ERR_INVALID_ARG;
@@ -352,14 +373,14 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   carve_ctx(z, static_cast<char*>(const_cast<void*>(fwd_ctx)), &ctx);
   cudaStream_t s = as_stream(stream);
   const int grid = grid_of(sched);
-  if (z.mx) {  // exact bf16 decodes of the pre-quantised backward copies
+  if (z.mx) {  // weight scales into atoms, then dY quantised on the gather
     const int64_t EI = static_cast<int64_t>(z.E) * z.I, EH = static_cast<int64_t>(z.E) * z.H;
-    if (launch_mx_dequant(w->qt_gate, w->st_gate, EH, z.I, st.wg_b, s) ||
-        launch_mx_dequant(w->qt_up, w->st_up, EH, z.I, st.wu_b, s) ||
-        launch_mx_dequant(w->qt_down, w->st_down, EI, z.H, st.wd_b, s))
-      return MOK_ERR_CUDA;
+    const ScaleJob jobs[3] = {{w->st_down, nullptr, st.swt_d, EI / 128, z.H / 128, 0},
+                              {w->st_gate, nullptr, st.swt_g, EH / 128, z.I / 128, 0},
+                              {w->st_up, nullptr, st.swt_u, EH / 128, z.I / 128, 0}};
+    if (launch_mx_scale_atoms(jobs, 3, s)) return MOK_ERR_CUDA;
     if (launch_gather_rows_mx(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
-                              st.dyg, K_GATHER_DY, s))
+                              st.dyg, st.dyq, st.dys, K_GATHER_DY, s))
       return MOK_ERR_CUDA;
   } else if (launch_gather_rows(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
                                 st.dyg, K_GATHER_DY, s)) {
@@ -367,7 +388,7 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   }
   int e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 1, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
-  const int n_tiles1 = z.I / (z.I % 256 == 0 ? 256 : 128);
+  const int n_tiles1 = z.I / (z.I % 256 == 0 && !z.mx ? 256 : 128);
   if (launch_ds_reduce(st.dspart, sched->inv, z.R, n_tiles1, g->d_topk_weights, s)) return MOK_ERR_CUDA;
   e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 2, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
@@ -390,8 +411,25 @@ const char* mok_kernel_name(int32_t kind) {
       "sched_hist",      "sched_scan",    "sched_scatter", "gather_x",       "gemm_fwd_gateup",
       "gemm_fwd_down",   "combine",       "gather_dy",     "gemm_dgrad1",    "ds_reduce",
       "gemm_dgrad2",     "dx_reduce",     "gemm_wgrad_gu", "gemm_wgrad_d",   "mxfp8_quantize",
-      "mx_dequant"};
+      "mx_scale_atoms"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "?";
+}
+
+mok_status mok_mx_operands_of(const mok_schedule* sched, mok_mx_operands* out) {
+  Sizes z;
+  Staging st;
+  if (!out || check_sched(sched, &z, &st) != MOK_OK || !z.mx) return MOK_ERR_INVALID_ARG;
+  out->xq = st.xq;
+  out->xs = st.xs;
+  out->aq = st.aq;
+  out->as = st.as_sf;
+  out->dyq = st.dyq;
+  out->dys = st.dys;
+  out->dgq = st.dgq;
+  out->dgs = st.dgs;
+  out->dgdu = st.dgdu;
+  out->rows = z.rpad_max;
+  return MOK_OK;
 }
 
 mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream) {

@@ -12,7 +12,8 @@
 //
 // Roles: warp 0 lane 0 issues TMA tile loads into a ring of shared-memory stages; warp 1 owns the
 // tensor memory and its lane 0 issues tcgen05.mma (M = 128, N = BN, K = 16) into one of two TMEM
-// accumulators; four epilogue warps (one per TMEM lane quarter) drain the other accumulator
+// accumulators (MXFP8: the four K-major contractions run natively on E4M3 operands with
+// kind::mxf8f6f4.block_scale, K = 32, their E8M0 scale atoms copied shared -> TMEM per stage); four epilogue warps (one per TMEM lane quarter) drain the other accumulator
 // (tcgen05.ld), apply the epilogue math and write through swizzled shared tiles with TMA tile
 // stores.  Every output element is produced by
 // exactly one CTA with a fixed K order, so results are bitwise independent of the grid size and of
@@ -49,7 +50,7 @@ struct GemmArgs {
   int32_t n_tiles;         // N / BN
   int32_t m_tiles;         // weight-gradient variants: M / 128
   int32_t k_blocks;        // row-tiled variants: K / 64
-  int32_t kb_split;        // DGRAD2: K blocks read from Wg before switching to Wu (I / 64)
+  int32_t kb_split;        // DGRAD2: K blocks read from Wg before switching to Wu (I / 64; MX: I / 128)
   // epilogue operands
   void* out0;
   void* out1;
@@ -58,18 +59,34 @@ struct GemmArgs {
   const void* in1;
   const float* row_weight;
   uint32_t* status;
+  // MXFP8 variants: atom-tiled E8M0 scales (512-byte atoms of 128 rows x 4 k-groups, see
+  // sf_atom_offset) of A (k_blocks atoms per 128-row tile) and of B (sfb_kq atoms per tile; sfb2
+  // for DGRAD2's Wu half), and the scales the GATEUP / DGRAD1 epilogues write for the next GEMM.
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const uint8_t* sfb2;
+  int32_t sfb_kq;
+  int32_t out_kq;
+  uint8_t* out_sf;
 };
 
-template <int VAR, int BN>
+constexpr int kStageBufs = 2;  // staging tiles per epilogue warp
+
+// A stage holds one K block of A and B as rows of 128 bytes (64 bf16 or 128 e4m3 along K) and, with
+// MX, one 512-byte scale atom each for A and B.  MX tiles are 128 x 128 (the two accumulators
+// take TMEM columns [0, 256), the scale words of stage s columns 256 + 8 s .. + 7).
+template <int VAR, int BN, bool MX>
 struct GemmCfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
-  static constexpr int kStageBufs = 2;  // staging tiles per epilogue warp
+  static_assert(!MX || BN == 128, "block-scaled tiles are 128 x 128");
+  static constexpr int kStages = MX ? 5 : (BN == 256 ? 4 : 6);
   static constexpr int kEpiWarps = 4;   // one warp per TMEM lane quarter
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr uint32_t kABytes = kBM * kBK * 2;
-  static constexpr uint32_t kBBytes = BN * kBK * 2;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kTmemCols = 2 * BN;
+  static constexpr uint32_t kABytes = kBM * 128;
+  static constexpr uint32_t kBBytes = BN * 128;
+  static constexpr uint32_t kSfBytes = MX ? 1024 : 0;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfBytes;
+  static constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
+  static constexpr uint32_t kSfCol0 = 2 * BN;
   static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * 4096;  // per warp: tiles of 4 KB
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + kStagingBytes + 256;
 };
@@ -114,25 +131,40 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
   return w;
 }
 
-// Issue the TMA loads of one K block into stage (sa, sb), all completing on barrier `bar`.  With MX
-// the dgrad variants read B from K-major transposed weight copies ([E*I, H] for dgrad1, [E*H, I]
-// for dgrad2) instead of the MN-major forward layout.
+// Issue the loads of one K block into stage (sa, sb[, sf]), all completing on barrier `bar`.  MX
+// (E4M3, K-major A and B, 128 K values per block): A rows of the routed operand, B rows of the
+// caller's weight copy quantised along this GEMM's K ([E*I, H] Wg|Wu, [E*H, I] Wd, [E*I, H] Wd^T,
+// [E*H, I] Wg^T|Wu^T), plus the A and B scale atoms of the block by untiled bulk copies.  GATEUP's
+// B tile is 64 gate rows then the same 64 up rows, and its scale atoms are laid out in that pairing.
 template <int VAR, int BN, bool MX>
 __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
                                           uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
                                           const CUtensorMap* tB2) {
+  if constexpr (MX) {
+    const uint32_t sf = sb + BN * 128;  // A atom, then B atom
+    const int k0 = kb * 128;
+    tma_load_2d(sa, tA, bar, k0, w.row0);
+    bulk_load(sf, a.sfa + (static_cast<int64_t>(w.row0 >> 7) * a.k_blocks + kb) * 512, 512, bar);
+    if constexpr (VAR == V_FWD_GATEUP) {
+      const int n0 = w.e * a.I + w.nt * 64;
+      tma_load_2d(sb, tB, bar, k0, n0);
+      tma_load_2d(sb + 64 * 128, tB2, bar, k0, n0);
+      bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(n0 >> 6) * a.sfb_kq + kb) * 512, 512, bar);
+    } else if constexpr (VAR == V_DGRAD2) {
+      const bool first = kb < a.kb_split;
+      const int kq = first ? kb : kb - a.kb_split;
+      const int n0 = w.e * a.H + w.nt * 128;
+      tma_load_2d(sb, first ? tB : tB2, bar, kq * 128, n0);
+      bulk_load(sf + 512, (first ? a.sfb : a.sfb2) + (static_cast<int64_t>(n0 >> 7) * a.sfb_kq + kq) * 512, 512,
+                bar);
+    } else {  // FWD_DOWN: B rows e*H + n; DGRAD1: B rows e*I + n
+      const int n0 = w.e * (VAR == V_FWD_DOWN ? a.H : a.I) + w.nt * 128;
+      tma_load_2d(sb, tB, bar, k0, n0);
+      bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(n0 >> 7) * a.sfb_kq + kb) * 512, 512, bar);
+    }
+    return;
+  }
   const int k0 = kb * kBK;
-  if constexpr (MX && VAR == V_DGRAD1) {
-    tma_load_2d(sa, tA, bar, k0, w.row0);
-    tma_load_2d(sb, tB, bar, k0, w.e * a.I + w.nt * BN);
-    return;
-  }
-  if constexpr (MX && VAR == V_DGRAD2) {
-    tma_load_2d(sa, tA, bar, k0, w.row0);
-    const bool first = kb < a.kb_split;
-    tma_load_2d(sb, first ? tB : tB2, bar, first ? k0 : k0 - a.kb_split * kBK, w.e * a.H + w.nt * BN);
-    return;
-  }
   if constexpr (VAR == V_FWD_GATEUP) {
     tma_load_2d(sa, tA, bar, k0, w.row0);
     const int n0 = w.e * a.I + w.nt * (BN / 2);
@@ -170,12 +202,12 @@ __device__ __forceinline__ uint4 ldg_v4(const uint16_t* p) { return __ldg(reinte
 
 // Per-warp output stager: NBUF shared-memory tiles (4 KB apart) of 32 rows x ROW bytes in the TMA
 // swizzle layout of that row size -- 128-byte rows: 16-byte chunk j of row r sits at chunk
-// j ^ (r & 7); 64-byte rows: at j ^ ((r >> 1) & 3).  Both keep the 32 lanes' row writes free of
-// bank conflicts.  Each filled tile leaves as one asynchronous TMA tile store; a tile is refilled
-// only after its previous store has finished reading it, so up to NBUF stores are in flight.
-template <int ROW, int NBUF>
+// j ^ (r & 7); 64-byte rows: at j ^ ((r >> 1) & 3); 32-byte rows: at j ^ ((r >> 2) & 1).  All keep
+// the 32 lanes' row writes free of bank conflicts.  Each filled tile leaves as one asynchronous
+// TMA tile store; a tile is refilled only after its previous store has finished reading it, so up
+// to NBUF stores are in flight.
+template <int NBUF>
 struct Stager {
-  static constexpr int kChunks = ROW / 16;
   uint32_t buf0;
   int cur;
   int lane;
@@ -186,13 +218,15 @@ struct Stager {
     cur = cur + 1 == NBUF ? 0 : cur + 1;
     return b;
   }
-  // Lane r writes its row (kChunks chunks of 16 bytes) and the warp stores the tile at (c0, c1).
-  __device__ __forceinline__ void put_and_store(const uint4* ch, const CUtensorMap* tm, int c0, int c1) {
+  // Lane r writes its row (ROW / 16 chunks of 16 bytes) and the warp stores the tile at (c0, c1).
+  template <int ROW>
+  __device__ __forceinline__ void put(const uint4* ch, const CUtensorMap* tm, int c0, int c1) {
+    static_assert(ROW == 128 || ROW == 64 || ROW == 32, "row size with a TMA swizzle mode");
     const uint32_t b = acquire();
     const uint32_t row = b + static_cast<uint32_t>(lane) * ROW;
-    const int sw = ROW == 128 ? (lane & 7) : ((lane >> 1) & 3);
+    const int sw = ROW == 128 ? (lane & 7) : ROW == 64 ? ((lane >> 1) & 3) : ((lane >> 2) & 1);
 #pragma unroll
-    for (int j = 0; j < kChunks; ++j) st_shared_v4(row + (static_cast<uint32_t>(j ^ sw) << 4), ch[j]);
+    for (int j = 0; j < ROW / 16; ++j) st_shared_v4(row + (static_cast<uint32_t>(j ^ sw) << 4), ch[j]);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
@@ -254,17 +288,49 @@ __device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, i
   }
 }
 
-template <int VAR>
-constexpr int epi_row_bytes() { return VAR == V_DGRAD1 ? 64 : 128; }
-
 // Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab.
-// tO0 / tO1 are the output tensor maps of the variant; `tempty` is released as soon as the last
-// accumulator column has been read.  `pre` holds DGRAD1's first prefetched context chunk.
-template <int VAR, int BN, bool MX, class Stg>
+// tO0 / tO1 / tO2 are the output tensor maps of the variant; `tempty` is released as soon as the
+// last accumulator column has been read.  `pre` holds DGRAD1's first prefetched context chunk.
+template <int VAR, int BN, bool MX>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int lane, uint32_t taddr,
-                                              Stg& stg, const CUtensorMap* tO0, const CUtensorMap* tO1,
-                                              uint32_t tempty, Dg1Chunk& pre) {
-  if constexpr (VAR == V_FWD_GATEUP) {
+                                              Stager<kStageBufs>& stg, const CUtensorMap* tO0,
+                                              const CUtensorMap* tO1, const CUtensorMap* tO2, uint32_t tempty,
+                                              Dg1Chunk& pre) {
+  if constexpr (VAR == V_FWD_GATEUP && MX) {
+    // columns [0, 64) of the accumulator are gate, [64, 128) up, for I columns i0 ...  g and u
+    // leave in fp32 (the backward re-quantises dg, du from them); a = silu(g) u leaves MX-quantised
+    // along I: its dequantised values in bf16 for the backward, its E4M3 codes and scales for the
+    // down projection.
+    const int i0 = w.nt * 64;
+    const int rowc = w.row0 + q * 32;
+    const int64_t row = rowc + lane;
+#pragma unroll 1
+    for (int c = 0; c < 64; c += 32) {
+      uint32_t gr[32], ur[32];
+      tmem_ld_32x32b_x32(taddr + c, gr);
+      tmem_ld_32x32b_x32(taddr + 64 + c, ur);
+      tmem_ld_wait();
+      if (c + 32 >= 64) release_acc(tempty);
+      uint4 ch[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ch[j] = make_uint4(gr[4 * j], gr[4 * j + 1], gr[4 * j + 2], gr[4 * j + 3]);
+      stg.put<128>(ch, tO0, i0 + c, rowc);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ch[j] = make_uint4(ur[4 * j], ur[4 * j + 1], ur[4 * j + 2], ur[4 * j + 3]);
+      stg.put<128>(ch, tO0, a.I + i0 + c, rowc);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+      uint32_t codes[8];
+      const uint32_t sbyte = mx_quant32(v, codes);
+      pack_bf16<32>(v, ch);
+      stg.put<64>(ch, tO1, i0 + c, rowc);
+      ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      stg.put<32>(ch, tO2, i0 + c, rowc);
+      a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sbyte);
+    }
+  } else if constexpr (VAR == V_FWD_GATEUP) {
     // columns [0, BN/2) of the accumulator are gate, [BN/2, BN) up, for I columns i0 ...
     const int i0 = w.nt * (BN / 2);
     const int rowc = w.row0 + q * 32;
@@ -275,34 +341,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       tmem_ld64(taddr + BN / 2 + c, u);
       if (c + 64 >= BN / 2) release_acc(tempty);
       uint4 ch[8];
-      if constexpr (MX) {  // g, u kept in fp32 for the backward's re-quantisation of dg, du
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            ch[j] = make_uint4(__float_as_uint(g[32 * h + 4 * j]), __float_as_uint(g[32 * h + 4 * j + 1]),
-                               __float_as_uint(g[32 * h + 4 * j + 2]), __float_as_uint(g[32 * h + 4 * j + 3]));
-          stg.put_and_store(ch, tO0, i0 + c + 32 * h, rowc);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            ch[j] = make_uint4(__float_as_uint(u[32 * h + 4 * j]), __float_as_uint(u[32 * h + 4 * j + 1]),
-                               __float_as_uint(u[32 * h + 4 * j + 2]), __float_as_uint(u[32 * h + 4 * j + 3]));
-          stg.put_and_store(ch, tO0, a.I + i0 + c + 32 * h, rowc);
-        }
-      } else {
-        pack_bf16<64>(g, ch);
-        stg.put_and_store(ch, tO0, i0 + c, rowc);
-        pack_bf16<64>(u, ch);
-        stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
-      }
+      pack_bf16<64>(g, ch);
+      stg.put<128>(ch, tO0, i0 + c, rowc);
+      pack_bf16<64>(u, ch);
+      stg.put<128>(ch, tO0, a.I + i0 + c, rowc);
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
-      if constexpr (MX) {  // a leaves MX-quantised along I (two blocks of 32)
-        mx_fakequant32(g);
-        mx_fakequant32(g + 32);
-      }
       pack_bf16<64>(g, ch);
-      stg.put_and_store(ch, tO1, i0 + c, rowc);
+      stg.put<128>(ch, tO1, i0 + c, rowc);
     }
   } else if constexpr (VAR == V_FWD_DOWN || VAR == V_DGRAD2) {
     const int rowc = w.row0 + q * 32;
@@ -313,10 +359,12 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       if (c + 64 >= BN) release_acc(tempty);
       uint4 ch[8];
       pack_bf16<64>(v, ch);
-      stg.put_and_store(ch, tO0, w.nt * BN + c, rowc);
+      stg.put<128>(ch, tO0, w.nt * BN + c, rowc);
     }
   } else if constexpr (VAR == V_DGRAD1 && MX) {
-    // MXFP8: as below, with g, u read in fp32 and dg, du quantise-dequantised per block of 32.
+    // MXFP8: as below, with g, u read in fp32 and dg, du MX-quantised along I (blocks of 32): their
+    // dequantised values leave in bf16 for the weight gradients, their E4M3 codes and scales for
+    // the second data-gradient GEMM.
     const int64_t row = w.row0 + q * 32 + lane;
     const int64_t I = a.I;
     const int i0 = w.nt * BN;
@@ -349,13 +397,22 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
         dg[i] = da * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
         du[i] = da * g[i] * sg;
       }
-      mx_fakequant32(dg);
-      mx_fakequant32(du);
       uint4 ch[4];
+      uint32_t codes[8];
+      const uint32_t sg_byte = mx_quant32(dg, codes);
+      ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      stg.put<32>(ch, tO2, i0 + c, rowc);
       pack_bf16<32>(dg, ch);
-      stg.put_and_store(ch, tO0, i0 + c, rowc);
+      stg.put<64>(ch, tO0, i0 + c, rowc);
+      const uint32_t su_byte = mx_quant32(du, codes);
+      ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      stg.put<32>(ch, tO2, a.I + i0 + c, rowc);
       pack_bf16<32>(du, ch);
-      stg.put_and_store(ch, tO0, a.I + i0 + c, rowc);
+      stg.put<64>(ch, tO0, a.I + i0 + c, rowc);
+      a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sg_byte);
+      a.out_sf[sf_atom_offset(row, (a.I + i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(su_byte);
       float sa[32];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -368,7 +425,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
         }
       }
       pack_bf16<32>(sa, ch);
-      stg.put_and_store(ch, tO1, i0 + c, rowc);
+      stg.put<64>(ch, tO1, i0 + c, rowc);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else if constexpr (VAR == V_DGRAD1) {
@@ -410,9 +467,9 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
           pack_bf16<8>(sa, csa + j);
         }
       }
-      stg.put_and_store(cdg, tO0, i0 + c, rowc);
-      stg.put_and_store(cdu, tO0, a.I + i0 + c, rowc);
-      stg.put_and_store(csa, tO1, i0 + c, rowc);
+      stg.put<64>(cdg, tO0, i0 + c, rowc);
+      stg.put<64>(cdu, tO0, a.I + i0 + c, rowc);
+      stg.put<64>(csa, tO1, i0 + c, rowc);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else {  // weight gradients, fp32 out, 32-column tiles
@@ -442,7 +499,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       uint4 ch[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) ch[j] = make_uint4(rv[4 * j], rv[4 * j + 1], rv[4 * j + 2], rv[4 * j + 3]);
-      stg.put_and_store(ch, tm, w.nt * BN + c, r0);
+      stg.put<128>(ch, tm, w.nt * BN + c, r0);
     }
   }
 }
@@ -460,13 +517,15 @@ __device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity, u
 }
 
 template <int VAR, int BN, bool MX>
-__global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
-                const __grid_constant__ CUtensorMap tmO1, const GemmArgs args) {
-  using C = GemmCfg<VAR, BN>;
+                const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
+                const GemmArgs args) {
+  using C = GemmCfg<VAR, BN, MX>;
+  static_assert(!MX || VAR <= V_DGRAD2, "weight gradients run on the bf16 path");
   constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);
-  constexpr bool kBmn = (VAR >= V_DGRAD1) && !(MX && (VAR == V_DGRAD1 || VAR == V_DGRAD2));
+  constexpr bool kBmn = (VAR >= V_DGRAD1) && !MX;
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
   constexpr int S = C::kStages;
 
@@ -505,6 +564,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
     tma_prefetch_desc(&tmB2);
     tma_prefetch_desc(&tmO0);
     tma_prefetch_desc(&tmO1);
+    tma_prefetch_desc(&tmO2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -565,11 +625,26 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = base + stage * C::kStageBytes, sb = sa + C::kABytes;
+          if constexpr (MX) {
+            // this stage's scale atoms -> its own 8 TMEM columns (A words, then B words); the copies
+            // and the MMAs that read them execute in issue order
+            const uint32_t sf = sb + C::kBBytes;
+            const uint32_t tsf = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * 8);
+            tmem_cp_sf_atom(tsf, sdesc_plain(sf));
+            tmem_cp_sf_atom(tsf + 4, sdesc_plain(sf + 512));
 #pragma unroll
-          for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
-            const uint64_t ad = kAmn ? sdesc_sw128(sa + ks * 2048, 8192, 1024) : sdesc_sw128(sa + ks * 32, 16, 1024);
-            const uint64_t bd = kBmn ? sdesc_sw128(sb + ks * 2048, 8192, 1024) : sdesc_sw128(sb + ks * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)  // K = 32 e4m3 (32 bytes) per instruction; k-group ks
+              umma_mxf8(d_tmem, sdesc_sw128(sa + ks * 32, 16, 1024), sdesc_sw128(sb + ks * 32, 16, 1024),
+                        idesc_mx(kBM, BN, static_cast<uint32_t>(ks)), (kb | ks) != 0 ? 1u : 0u, tsf, tsf + 4);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
+              const uint64_t ad =
+                  kAmn ? sdesc_sw128(sa + ks * 2048, 8192, 1024) : sdesc_sw128(sa + ks * 32, 16, 1024);
+              const uint64_t bd =
+                  kBmn ? sdesc_sw128(sb + ks * 2048, 8192, 1024) : sdesc_sw128(sb + ks * 32, 16, 1024);
+              umma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(empty_bar(stage));
           if (++stage == S) {
@@ -592,8 +667,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    Stager<epi_row_bytes<VAR>(), C::kStageBufs> stg{
-        staging + static_cast<uint32_t>(warp - 2) * (C::kStageBufs * 4096u), 0, lane};
+    Stager<kStageBufs> stg{staging + static_cast<uint32_t>(warp - 2) * (kStageBufs * 4096u), 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
@@ -606,7 +680,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      gemm_epilogue<VAR, BN, MX>(args, w, q, lane, taddr, stg, &tmO0, &tmO1, tempty_bar(acc), pre);
+      gemm_epilogue<VAR, BN, MX>(args, w, q, lane, taddr, stg, &tmO0, &tmO1, &tmO2, tempty_bar(acc), pre);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -631,11 +705,14 @@ bool make_tmap_bf16_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint6
                          uint32_t box_outer);
 bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                    uint32_t box_outer);
+// bytes (E4M3 codes); swizzle_bytes 128, 64 or 32
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                  uint32_t box_outer, int swizzle_bytes);
 
 template <int VAR, int BN, bool MX = false>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o0,
-                const CUtensorMap& o1, const GemmArgs& args, int grid, cudaStream_t stream) {
-  using C = GemmCfg<VAR, BN>;
+                const CUtensorMap& o1, const CUtensorMap& o2, const GemmArgs& args, int grid, cudaStream_t stream) {
+  using C = GemmCfg<VAR, BN, MX>;
   static bool configured = false;  // per process; the attribute is per function, set once
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -651,7 +728,7 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
                         : VAR == V_WGRAD_GU  ? K_GEMM_WGRAD_GU
                                              : K_GEMM_WGRAD_D;
   trace_begin(stream, kKind);
-  gemm_kernel<VAR, BN, MX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, args);
+  gemm_kernel<VAR, BN, MX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, o2, args);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

@@ -25,18 +25,60 @@ static int clamp_grid(int num_ctas, int64_t units) {
   return static_cast<int>(units < num_ctas ? units : num_ctas);
 }
 
+// MXFP8: both GEMMs block-scaled on E4M3 operands (128 x 128 tiles).  B is the K-major transposed
+// weight copy quantised along this GEMM's K: Wd^T [E*I, H] for phase 1, Wg^T | Wu^T [E*H, I] for
+// phase 2.
+static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
+                                 const mok_weights& w, int num_ctas, int phase, cudaStream_t stream) {
+  CUtensorMap tA, tB, tB2, tO0, tO1, tO2;
+  GemmArgs a = common_args(z, s);
+  const uint64_t EI = static_cast<uint64_t>(z.E) * z.I, EH = static_cast<uint64_t>(z.E) * z.H;
+  if (phase == 1) {
+    if (!make_tmap_u8(&tA, st.dyq, z.H, z.rpad_max, 128, 128, 128)) return -1;
+    if (!make_tmap_u8(&tB, w.qt_down, z.H, EI, 128, 128, 128)) return -1;
+    a.n_tiles = z.I / 128;
+    a.k_blocks = z.H / 128;
+    a.sfa = st.dys;
+    a.sfb = st.swt_d;
+    a.sfb_kq = z.H / 128;
+    a.in0 = ctx.gu;
+    a.in1 = ctx.a;
+    a.out0 = st.dgdu;
+    a.out1 = st.as;
+    a.out2 = st.dspart;
+    a.out_sf = st.dgs;
+    a.out_kq = 2 * z.I / 128;
+    if (!make_tmap_bf16_sw64(&tO0, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
+    if (!make_tmap_bf16_sw64(&tO1, st.as, z.I, z.rpad_max, 32, 32)) return -1;
+    if (!make_tmap_u8(&tO2, st.dgq, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32, 32)) return -1;
+    return launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, tO2, a,
+                                            clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
+  }
+  if (!make_tmap_u8(&tA, st.dgq, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 128, 128, 128)) return -1;
+  if (!make_tmap_u8(&tB, w.qt_gate, z.I, EH, 128, 128, 128)) return -1;
+  if (!make_tmap_u8(&tB2, w.qt_up, z.I, EH, 128, 128, 128)) return -1;
+  a.n_tiles = z.H / 128;
+  a.k_blocks = 2 * z.I / 128;
+  a.kb_split = z.I / 128;
+  a.sfa = st.dgs;
+  a.sfb = st.swt_g;
+  a.sfb2 = st.swt_u;
+  a.sfb_kq = z.I / 128;
+  a.out0 = st.ybuf;
+  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
+  return launch_gemm<V_DGRAD2, 128, true>(tA, tB, tB2, tO0, tO0, tO0, a,
+                                          clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
+}
+
 int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                        const mok_weights& w, int num_ctas, int phase, cudaStream_t stream) {
+  if (z.mx) return launch_dgrad_gemms_mx(z, s, ctx, st, w, num_ctas, phase, stream);
   CUtensorMap tA, tB, tB2, tO0, tO1;
   GemmArgs a = common_args(z, s);
   if (phase == 1) {
     const int BN = z.I % 256 == 0 ? 256 : 128;
     if (!make_tmap_bf16(&tA, st.dyg, z.H, z.rpad_max, 64, 128)) return -1;
-    if (z.mx) {  // K-major B: Wd^T decoded from the copy quantised along H, [E*I, H]
-      if (!make_tmap_bf16(&tB, st.wd_b, z.H, static_cast<uint64_t>(z.E) * z.I, 64, BN)) return -1;
-    } else if (!make_tmap_bf16(&tB, w.w_down, z.I, static_cast<uint64_t>(z.E) * z.H, 64, 64)) {
-      return -1;
-    }
+    if (!make_tmap_bf16(&tB, w.w_down, z.I, static_cast<uint64_t>(z.E) * z.H, 64, 64)) return -1;
     a.n_tiles = z.I / BN;
     a.k_blocks = z.H / kBK;
     a.in0 = ctx.gu;
@@ -47,32 +89,21 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     if (!make_tmap_bf16_sw64(&tO0, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
     if (!make_tmap_bf16_sw64(&tO1, st.as, z.I, z.rpad_max, 32, 32)) return -1;
     const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
-    if (z.mx)
-      return BN == 256 ? launch_gemm<V_DGRAD1, 256, true>(tA, tB, tB, tO0, tO1, a, grid, stream)
-                       : launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, a, grid, stream);
-    return BN == 256 ? launch_gemm<V_DGRAD1, 256>(tA, tB, tB, tO0, tO1, a, grid, stream)
-                     : launch_gemm<V_DGRAD1, 128>(tA, tB, tB, tO0, tO1, a, grid, stream);
+    return BN == 256 ? launch_gemm<V_DGRAD1, 256>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
+                     : launch_gemm<V_DGRAD1, 128>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
   }
   const int BN = z.H % 256 == 0 ? 256 : 128;
   if (!make_tmap_bf16(&tA, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 128)) return -1;
-  if (z.mx) {  // K-major B: Wg^T, Wu^T decoded from the copies quantised along I, [E*H, I]
-    if (!make_tmap_bf16(&tB, st.wg_b, z.I, static_cast<uint64_t>(z.E) * z.H, 64, BN)) return -1;
-    if (!make_tmap_bf16(&tB2, st.wu_b, z.I, static_cast<uint64_t>(z.E) * z.H, 64, BN)) return -1;
-  } else {
-    if (!make_tmap_bf16(&tB, w.w_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
-    if (!make_tmap_bf16(&tB2, w.w_up, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
-  }
+  if (!make_tmap_bf16(&tB, w.w_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
+  if (!make_tmap_bf16(&tB2, w.w_up, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
   a.n_tiles = z.H / BN;
   a.k_blocks = 2 * z.I / kBK;
   a.kb_split = z.I / kBK;
   a.out0 = st.ybuf;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
-  if (z.mx)
-    return BN == 256 ? launch_gemm<V_DGRAD2, 256, true>(tA, tB, tB2, tO0, tO0, a, grid, stream)
-                     : launch_gemm<V_DGRAD2, 128, true>(tA, tB, tB2, tO0, tO0, a, grid, stream);
-  return BN == 256 ? launch_gemm<V_DGRAD2, 256>(tA, tB, tB2, tO0, tO0, a, grid, stream)
-                   : launch_gemm<V_DGRAD2, 128>(tA, tB, tB2, tO0, tO0, a, grid, stream);
+  return BN == 256 ? launch_gemm<V_DGRAD2, 256>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
+                   : launch_gemm<V_DGRAD2, 128>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream);
 }
 
 }  // namespace mok

@@ -27,8 +27,8 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     if (!make_tmap_f32(&tO1, g.dw_up, z.H, static_cast<uint64_t>(z.E) * z.I, 32, 32)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
     const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
-    const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256>(tA, tB, tB, tO0, tO1, a, grid, stream)
-                             : launch_gemm<V_WGRAD_GU, 128>(tA, tB, tB, tO0, tO1, a, grid, stream);
+    const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
+                             : launch_gemm<V_WGRAD_GU, 128>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
     if (rc) return rc;
   }
   // dWd_e = dYg_e^T (s a)_e   (M = H, N = I)
@@ -43,8 +43,8 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     if (!make_tmap_f32(&tO0, g.dw_down, z.I, static_cast<uint64_t>(z.E) * z.H, 32, 32)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
     const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
-    return BN == 256 ? launch_gemm<V_WGRAD_D, 256>(tA, tB, tB, tO0, tO0, a, grid, stream)
-                     : launch_gemm<V_WGRAD_D, 128>(tA, tB, tB, tO0, tO0, a, grid, stream);
+    return BN == 256 ? launch_gemm<V_WGRAD_D, 256>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
+                     : launch_gemm<V_WGRAD_D, 128>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
   }
 }
 

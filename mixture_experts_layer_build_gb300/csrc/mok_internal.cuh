@@ -28,13 +28,22 @@ struct Staging {
   uint16_t* as;      // [rpad_max, I] bf16: s * a
   float* dspart;     // [rpad_max, I/128] fp32: router-gradient partial sums per N tile
   int32_t* chunk_hist;  // [nchunks, E+1]
-  // MXFP8 mode only: exact bf16 decodes of the caller's pre-quantised weight copies
-  uint16_t* wg_f;    // [E*I, H]  Wg (quantised along H)
-  uint16_t* wu_f;    // [E*I, H]  Wu
-  uint16_t* wd_f;    // [E*H, I]  Wd (quantised along I)
-  uint16_t* wg_b;    // [E*H, I]  Wg^T (quantised along I)
-  uint16_t* wu_b;    // [E*H, I]  Wu^T
-  uint16_t* wd_b;    // [E*I, H]  Wd^T (quantised along H)
+  // MXFP8 mode only: E4M3 operands of the block-scaled GEMMs and their E8M0 scales, the scales
+  // atom-tiled (sf_atom_offset: 512 bytes per 128 rows x 4 k-groups)
+  uint8_t* xq;       // [rpad_max, H]  gathered x, quantised along H
+  uint8_t* xs;       //   scales: rtiles x H/128 atoms
+  uint8_t* aq;       // [rpad_max, I]  a, quantised along I
+  uint8_t* as_sf;    //   scales: rtiles x I/128 atoms
+  uint8_t* dyq;      // [rpad_max, H]  gathered dY, quantised along H
+  uint8_t* dys;      //   scales: rtiles x H/128 atoms
+  uint8_t* dgq;      // [rpad_max, 2I] [dg | du], quantised along I
+  uint8_t* dgs;      //   scales: rtiles x 2I/128 atoms
+  // the caller's weight scales re-tiled into atoms (per call)
+  uint8_t* sw_gu;    // s_gate | s_up paired per 64 rows: E*I/64 tiles x H/128 atoms
+  uint8_t* sw_d;     // s_down: E*H/128 tiles x I/128 atoms
+  uint8_t* swt_d;    // st_down: E*I/128 tiles x H/128 atoms
+  uint8_t* swt_g;    // st_gate: E*H/128 tiles x I/128 atoms
+  uint8_t* swt_u;    // st_up: E*H/128 tiles x I/128 atoms
 };
 struct Ctx {
   uint16_t* xg;      // [rpad_max, H] bf16: gathered x rows (zero on padding rows)
@@ -64,7 +73,7 @@ enum KernelKind : int {
   K_GEMM_WGRAD_GU,
   K_GEMM_WGRAD_D,
   K_MXFP8_QUANTIZE,
-  K_MX_DEQUANT,
+  K_MX_SCALE_ATOMS,
   K_NUM_KINDS
 };
 void trace_begin(cudaStream_t s, int kind);  // no-ops unless a trace is set
@@ -75,10 +84,21 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
                     cudaStream_t stream);
 int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                        int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
+// MX gather: dst = bf16 dequantised rows, dst_q = E4M3 codes, dst_sf = atom-tiled scales.
 int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                          int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
-int launch_mx_dequant(const uint8_t* q, const uint8_t* sc, int64_t rows, int64_t cols, uint16_t* dst,
-                      cudaStream_t stream);
+                          int32_t H, uint16_t* dst, uint8_t* dst_q, uint8_t* dst_sf, int kind,
+                          cudaStream_t stream);
+// Re-tile row-major E8M0 scales [rows, 4 kq] into 512-byte atoms (up to three jobs per launch).  A
+// paired job interleaves two sources per 128-row tile: 64 rows of src0, then the same 64 of src1.
+struct ScaleJob {
+  const uint8_t* src0;
+  const uint8_t* src1;  // paired jobs only
+  uint8_t* dst;
+  int64_t tiles;        // 128-row tiles of dst
+  int32_t kq;           // atoms per tile = k-groups / 4
+  int32_t paired;
+};
+int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream);
 int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
                    uint16_t* out, int kind, cudaStream_t stream);
 int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, float* ds,
@@ -88,9 +108,9 @@ int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_
 
 // GEMM phases
 int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st, const mok_weights& w,
-                     int num_ctas, cudaStream_t stream);  // MXFP8 mode (z.mx) reads st.w*_f
+                     int num_ctas, cudaStream_t stream);
 int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
-                       const mok_weights& w, int num_ctas, int phase, cudaStream_t stream);  // MXFP8: st.w*_b
+                       const mok_weights& w, int num_ctas, int phase, cudaStream_t stream);
 int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                        const mok_grads& g, int num_ctas, cudaStream_t stream);
 

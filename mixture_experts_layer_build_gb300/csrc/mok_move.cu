@@ -205,19 +205,17 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
   }
 }
 
-// Value of an unsigned E4M3 code (7 bits): subnormal m * 2^-9, else (8 + m) * 2^(E - 10).
-__device__ __forceinline__ float e4m3_mag(uint32_t c) {
-  const int E = static_cast<int>(c >> 3), m = static_cast<int>(c & 7u);
-  return E ? ldexpf(static_cast<float>(8 + m), E - 10) : ldexpf(static_cast<float>(m), -9);
-}
-
-// Gather with MX quantise-dequantise of each row (blocks of 32 along the row), bit-exact with
-// mxfp8_quantize_kernel's rounding: dst[row] = MX(src[row_token[row]]), zero padding rows.
+// Gather with MX quantisation of each row (blocks of 32 along the row), bit-exact with
+// mxfp8_quantize_kernel: dst_q[row] = E4M3 codes, dst_sf = E8M0 scales (atom-tiled, kq atoms per
+// 128-row tile), dst[row] = the dequantised values in bf16 (exact: E4M3 x 2^k fits bf16 down to
+// 2^-133).  Padding rows (row_token < 0) get zero codes, zero values and scale byte 0.
 // One warp per row; lane l handles the row's 32-element blocks l, l + 32, ...
 __global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint4* __restrict__ src,
                                                                      const int32_t* __restrict__ row_token,
                                                                      const int32_t* __restrict__ meta,
-                                                                     int64_t vecs, uint4* __restrict__ dst) {
+                                                                     int64_t vecs, uint4* __restrict__ dst,
+                                                                     uint4* __restrict__ dst_q,
+                                                                     uint8_t* __restrict__ dst_sf, int kq) {
   const int64_t rpad = meta[0];
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
@@ -226,38 +224,36 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint
        row += nwarps) {
     const int t = row_token[row];
     uint4* d = dst + row * vecs;
+    uint4* dq = dst_q + row * (vecs / 2);
     for (int64_t b = lane; b < nblk; b += 32) {
+      uint8_t* sf = dst_sf + sf_atom_offset(row, static_cast<int>(b), kq);
       if (t < 0) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d[b * 4 + i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 4; ++i) d[b * 4 + i] = z;
+        dq[b * 2] = z;
+        dq[b * 2 + 1] = z;
+        *sf = 0;
         continue;
       }
       const uint4* s = src + static_cast<int64_t>(t) * vecs + b * 4;
-      uint32_t w[16];
+      float o[32];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 v = __ldg(s + i);
-        w[4 * i] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
+        o[8 * i] = bf16_lo(v.x);
+        o[8 * i + 1] = bf16_hi(v.x);
+        o[8 * i + 2] = bf16_lo(v.y);
+        o[8 * i + 3] = bf16_hi(v.y);
+        o[8 * i + 4] = bf16_lo(v.z);
+        o[8 * i + 5] = bf16_hi(v.z);
+        o[8 * i + 6] = bf16_lo(v.w);
+        o[8 * i + 7] = bf16_hi(v.w);
       }
-      uint32_t amax = 0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t mag = (i & 1 ? (w[i >> 1] >> 16) : w[i >> 1]) & 0x7FFFu;
-        amax = mag > amax ? mag : amax;
-      }
-      int shared = amax == 0 ? -127 : bf16_floor_log2(amax) - 8;
-      shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
-      // bf16 * 2^-shared is exact in fp32, so the hardware E4M3 rounding matches e4m3_code's
-      float o[32];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        o[2 * i] = bf16_lo(w[i]);
-        o[2 * i + 1] = bf16_hi(w[i]);
-      }
-      mx_qdq_pairs(o, 32, shared);
+      uint32_t codes[8];
+      *sf = static_cast<uint8_t>(mx_quant32(o, codes));
+      dq[b * 2] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      dq[b * 2 + 1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         d[b * 4 + i] = make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
@@ -266,27 +262,30 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint
   }
 }
 
-// Exact decode of an MXFP8 matrix to bf16: dst = e4m3 * 2^(scale - 127); one thread per block of 32.
-__global__ void __launch_bounds__(kMoveThreads) mx_dequant_kernel(const uint4* __restrict__ q,
-                                                                 const uint8_t* __restrict__ sc, int64_t nblocks,
-                                                                 uint4* __restrict__ dst) {
+// Scale atoms: thread t writes line (t % 32) of atom t / 32 -- rows l, l+32, l+64, l+96 of the
+// atom's 128-row tile, four k-groups each.  blockIdx.y selects the job.
+struct ScaleJobs {
+  ScaleJob j[3];
+};
+__global__ void __launch_bounds__(kMoveThreads) mx_scale_atoms_kernel(const ScaleJobs jobs) {
+  const ScaleJob jb = jobs.j[blockIdx.y];
+  const int64_t lines = jb.tiles * jb.kq * 32;
+  const int64_t kg = 4 * static_cast<int64_t>(jb.kq);  // source row length in bytes
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
-  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; b < nblocks; b += stride) {
-    const uint4 q0 = __ldg(q + 2 * b), q1 = __ldg(q + 2 * b + 1);
-    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const int sbyte = __ldg(sc + b);
-    float o[32];
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; t < lines; t += stride) {
+    const int l = static_cast<int>(t & 31);
+    const int64_t atom = t >> 5;
+    const int64_t tile = atom / jb.kq;
+    const int64_t q = atom - tile * jb.kq;
+    uint32_t wv[4];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t c = (words[i >> 2] >> (8 * (i & 3))) & 0xFFu;
-      const float m = ((c & 0x7Fu) == 0x7Fu || sbyte == 0xFF) ? __int_as_float(0x7FC00000)
-                                                              : ldexpf(e4m3_mag(c & 0x7Fu), sbyte - 127);
-      o[i] = (c & 0x80u) ? -m : m;
+    for (int c = 0; c < 4; ++c) {
+      const int r = l + 32 * c;
+      const uint8_t* srcp = jb.paired ? (r < 64 ? jb.src0 : jb.src1) : jb.src0;
+      const int64_t srow = jb.paired ? tile * 64 + (r & 63) : tile * 128 + r;
+      wv[c] = __ldg(reinterpret_cast<const uint32_t*>(srcp + srow * kg + 4 * q));
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      dst[b * 4 + i] = make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
-                                  pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
+    reinterpret_cast<uint4*>(jb.dst)[t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
 }
 
@@ -310,24 +309,31 @@ int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int3
 }
 
 int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                          int32_t H, uint16_t* dst, int kind, cudaStream_t stream) {
+                          int32_t H, uint16_t* dst, uint8_t* dst_q, uint8_t* dst_sf, int kind,
+                          cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
   const int grid = grid_for(rpad_max, kMoveThreads / 32);
   trace_begin(stream, kind);
   gather_rows_mx_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), row_token, meta,
-                                                           H / 8, reinterpret_cast<uint4*>(dst));
+                                                           H / 8, reinterpret_cast<uint4*>(dst),
+                                                           reinterpret_cast<uint4*>(dst_q), dst_sf, H / 128);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
 
-int launch_mx_dequant(const uint8_t* q, const uint8_t* sc, int64_t rows, int64_t cols, uint16_t* dst,
-                      cudaStream_t stream) {
-  const int64_t nblocks = rows * (cols / 32);
-  if (nblocks <= 0) return 0;
-  const int grid = grid_for(nblocks, kMoveThreads);
-  trace_begin(stream, K_MX_DEQUANT);
-  mx_dequant_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(q), sc, nblocks,
-                                                       reinterpret_cast<uint4*>(dst));
+int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream) {
+  if (njobs <= 0 || njobs > 3) return static_cast<int>(cudaErrorInvalidValue);
+  ScaleJobs p{};
+  int64_t most = 0;
+  for (int i = 0; i < njobs; ++i) {
+    p.j[i] = jobs[i];
+    const int64_t lines = jobs[i].tiles * jobs[i].kq * 32;
+    most = lines > most ? lines : most;
+  }
+  if (most <= 0) return 0;
+  const dim3 grid(static_cast<unsigned>(grid_for(most, kMoveThreads)), static_cast<unsigned>(njobs));
+  trace_begin(stream, K_MX_SCALE_ATOMS);
+  mx_scale_atoms_kernel<<<grid, kMoveThreads, 0, stream>>>(p);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

@@ -106,6 +106,12 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src
                ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(c0), "r"(c1)
                : "memory");
 }
+// Untiled bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups still read their shared-memory sources.
 template <int N>
@@ -154,6 +160,27 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T with E4M3 A and B, one E8M0 scale per 32 K
+// values (OCP MX), fp32 accumulation; K = 32 per instruction.  sfa_tmem / sfb_tmem address the TMEM
+// columns holding the scale words of the A rows / B rows; the k-group byte used inside each 32-bit
+// word is selected by the instruction descriptor (idesc_mx).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate, uint32_t sfa_tmem, uint32_t sfb_tmem) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Copy one 512-byte scale atom (32 lines x 16 bytes) from shared memory to TMEM: line l lands in
+// lane l of four consecutive columns, replicated into all four 32-lane quarters.  `sdesc` is a
+// no-swizzle descriptor of the atom (sdesc_plain).
+__device__ __forceinline__ void tmem_cp_sf_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive once on the mbarrier when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -194,6 +221,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+
+// Shared-memory descriptor without swizzle (16-byte lines; SBO = 128 between 8-line groups).
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 A and B (format 0), K-major
+// both, fp32 D, UE8M0 scales (bit 23); bits 4-5 / 29-30 pick the byte (k-group) of the B / A scale
+// words that this K = 32 step uses.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t kgroup) {
+  return (kgroup << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (kgroup << 29);
 }
 
 // Instruction descriptor of tcgen05.mma.kind::f16: bf16 A and B, fp32 D, dense.
@@ -244,6 +288,50 @@ __device__ __forceinline__ void mx_fakequant32(float* v) {
   int shared = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
   shared = shared < -127 ? -127 : shared;
   mx_qdq_pairs(v, 32, shared);
+}
+
+// MX quantisation of 32 fp32 values (one block): returns the E8M0 scale byte, writes the E4M3 codes
+// (byte i of the 32 = element i) and replaces v by the dequantised values.  A block holding a NaN
+// or an infinity gets scale 0xFF and codes 0x7F (NaN), as the OCP MX format prescribes.
+__device__ __forceinline__ uint32_t mx_quant32(float* v, uint32_t (&codes)[8]) {
+  float amax = 0.0f;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float a = fabsf(v[i]);
+    bad |= !(a <= 3.402823466e38f);
+    amax = fmaxf(amax, a);
+  }
+  if (bad) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __int_as_float(0x7FC00000);
+    return 0xFFu;
+  }
+  int shared = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
+  shared = shared < -127 ? -127 : shared;
+  const float dn = pow2f(-shared), up = pow2f(shared);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint16_t q;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(v[2 * i + 1] * dn), "f"(v[2 * i] * dn));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q));
+    v[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))) * up;
+    v[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))) * up;
+    if (i & 1) codes[i >> 1] |= static_cast<uint32_t>(q) << 16;
+    else codes[i >> 1] = q;
+  }
+  return static_cast<uint32_t>(shared + 127);
+}
+
+// Byte offset of the scale of (row, k-group kg) in an atom-tiled MX scale array: 512-byte atoms of
+// 128 rows x 4 k-groups, kq atoms per 128-row tile along K; inside an atom, row r's four bytes sit
+// at (r % 32) * 16 + ((r / 32) % 4) * 4 -- the order in which tcgen05.cp's 32x128b.warpx4 shape
+// puts them into TMEM for the block-scaled MMA.
+__host__ __device__ __forceinline__ int64_t sf_atom_offset(int64_t row, int kg, int kq) {
+  return ((row >> 7) * kq + (kg >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kg & 3);
 }
 
 // bf16 helpers (round to nearest even, no special-value surprises for finite inputs)

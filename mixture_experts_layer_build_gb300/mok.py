@@ -108,9 +108,17 @@ _lib.mok_kernel_name.argtypes = [ctypes.c_int32]
 _lib.mok_read_device_status.restype = ctypes.c_int
 _lib.mok_read_device_status.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(ctypes.c_uint32), _P]
 
+class mok_mx_operands(ctypes.Structure):
+    _fields_ = [(k, _P) for k in ("xq", "xs", "aq", "as_", "dyq", "dys", "dgq", "dgs", "dgdu")] + \
+        [("rows", ctypes.c_int64)]
+
+
+_lib.mok_mx_operands_of.restype = ctypes.c_int
+_lib.mok_mx_operands_of.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(mok_mx_operands)]
+
 EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
             "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status", "mok_set_trace",
-            "mok_kernel_name", "mok_build_schedule_noalloc")
+            "mok_kernel_name", "mok_build_schedule_noalloc", "mok_mx_operands_of")
 _lib.mok_build_schedule_noalloc.restype = ctypes.c_int
 _lib.mok_build_schedule_noalloc.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape), _P, _P,
                                             ctypes.POINTER(mok_schedule), _P]
@@ -204,6 +212,25 @@ class Schedule:
                     mblocks=self._view("mblocks", 4 * self.c.mblocks_max).view(-1, 4),
                     meta=self._view("meta", 16), row_weight=self._view("row_weight", self.c.rpad_max, torch.float32),
                     row_token=self._view("row_token", self.c.rpad_max))
+
+
+    def mx_operands(self) -> dict:
+        """Device views of the MXFP8 operand copies in the workspace (mok_mx_operands_of): E4M3 codes
+        [rows, n] and their atom-tiled E8M0 scale arrays (flat uint8), plus the bf16 [dg | du]."""
+        m = mok_mx_operands()
+        _check(_lib.mok_mx_operands_of(ctypes.byref(self.c), ctypes.byref(m)), "mok_mx_operands_of")
+        H, I, rows = self.c.shape.H, self.c.shape.I, m.rows
+        rt = (rows + 127) // 128
+        wsb = self.ws.view(torch.uint8)
+        base = self.ws.data_ptr()
+
+        def v(ptr, n):
+            return wsb[ptr - base:ptr - base + n]
+        return dict(xq=v(m.xq, rows * H).view(rows, H), xs=v(m.xs, rt * 128 * (H // 32)),
+                    aq=v(m.aq, rows * I).view(rows, I), as_=v(m.as_, rt * 128 * (I // 32)),
+                    dyq=v(m.dyq, rows * H).view(rows, H), dys=v(m.dys, rt * 128 * (H // 32)),
+                    dgq=v(m.dgq, rows * 2 * I).view(rows, 2 * I), dgs=v(m.dgs, rt * 128 * (2 * I // 32)),
+                    dgdu=v(m.dgdu, rows * 2 * I * 2).view(torch.bfloat16).view(rows, 2 * I))
 
 
 def alloc_workspace(cfg: mok_config, shape: mok_shape, device="cuda") -> torch.Tensor:

@@ -107,8 +107,27 @@ def test_mxfp8_ep64_shard_sampled_parity_and_determinism(mok):
         assert torch.equal(v, r[k]), k
 
 
+def _untile_scales(atoms, rows, kg):
+    """Row-major [rows, kg] scale bytes from an atom-tiled array (the layout mok.h documents for
+    mok_mx_operands_of)."""
+    kq = kg // 4
+    r = np.arange(rows)[:, None]
+    g = np.arange(kg)[None, :]
+    off = ((r // 128) * kq + g // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + g % 4
+    return atoms[off]
+
+
+def _ctx_a(layer, w):
+    """bf16 view of the forward context's a = silu(g) u (MXFP8 context: xg bf16 | g,u fp32 | a)."""
+    up = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    rows = layer.sched.c.rpad_max
+    off = up(rows * w.H * 2) + up(rows * 2 * w.I * 4)
+    return layer.ctx.view(torch.uint8)[off:off + rows * w.I * 2].view(torch.bfloat16).view(rows, w.I)
+
+
 def test_mxfp8_gather_quantises_x_bit_exactly(mok):
-    """The quantise-on-gather of x equals the oracle's MX quantisation of x, bit for bit."""
+    """The quantise-on-gather of x equals the oracle's MX quantisation of x, bit for bit: the bf16
+    dequantised rows, the E4M3 codes and the atom-tiled E8M0 scales."""
     w = inputs.custom(T=200, H=512, I=128, E=4, K=2)
     d = inputs.make(w, seed=4)
     x = d["x"].clone()
@@ -127,6 +146,50 @@ def test_mxfp8_gather_quantises_x_bit_exactly(mok):
     got = to_f64(xg)[inv]
     ref = oracle.mx_fakequant(oracle.bf16_to_f64(inputs.bits(x)))[np.arange(w.R) // w.K]
     assert np.array_equal(got, ref)
+    q_ref, s_ref = oracle.mxfp8_quantize(inputs.bits(x))
+    ops = layer.sched.mx_operands()
+    xq = ops["xq"].cpu().numpy()
+    xs = _untile_scales(ops["xs"].cpu().numpy(), xq.shape[0], w.H // 32)
+    tok = np.arange(w.R) // w.K
+    assert np.array_equal(xq[inv], q_ref.reshape(w.T, w.H)[tok])
+    assert np.array_equal(xs[inv], s_ref.reshape(w.T, w.H // 32)[tok])
+    t = layer.sched.tables()
+    rpad = int(t["meta"][0])
+    pad = (t["row_token"][:rpad] < 0).cpu().numpy()
+    assert pad.any()
+    assert not xq[:rpad][pad].any() and not xs[:rpad][pad].any()
+
+
+@pytest.mark.parametrize("name,w", SMALL[1:], ids=[n for n, _ in SMALL[1:]])
+def test_mxfp8_operand_copies(mok, name, w):
+    """The E4M3 operands the block-scaled GEMMs read decode exactly to the bf16 copies the rest of
+    the path reads: a (written by the gate/up epilogue) and [dg | du] (dgrad1 epilogue); the
+    gathered dY's codes and scales equal the oracle's quantisation bit for bit."""
+    d = inputs.make(w, seed=7)
+    mx_gpu = _mx_inputs(mok, d)
+    cfg = mok.make_config(128, 256, precision=mok.MOK_MXFP8)
+    layer = mok.Layer(w.T, w.H, w.I, w.E, w.K, cfg)
+    weights = mok.weights_struct(mx=mx_gpu)
+    layer.schedule(d["topk_ids"].cuda(), d["topk_weights"].cuda())
+    layer.forward(d["x"].cuda(), weights)
+    layer.backward(d["dY"].cuda(), weights)
+    torch.cuda.synchronize()
+    t = layer.sched.tables()
+    rpad = int(t["meta"][0])
+    ops = {k: v.cpu().numpy() for k, v in layer.sched.mx_operands().items() if k != "dgdu"}
+    rows = ops["aq"].shape[0]
+    a_dec = oracle.mxfp8_dequantize(ops["aq"], _untile_scales(ops["as_"], rows, w.I // 32)).reshape(rows, w.I)
+    assert np.array_equal(a_dec[:rpad], to_f64(_ctx_a(layer, w)[:rpad]))
+    dg_dec = oracle.mxfp8_dequantize(ops["dgq"], _untile_scales(ops["dgs"], rows, 2 * w.I // 32))
+    dgdu = to_f64(layer.sched.mx_operands()["dgdu"][:rpad])
+    assert np.array_equal(dg_dec.reshape(rows, 2 * w.I)[:rpad], dgdu)
+    assert np.abs(dgdu).max() > 0
+    q_ref, s_ref = oracle.mxfp8_quantize(inputs.bits(d["dY"]))
+    inv = t["inv"].cpu().numpy().astype(np.int64)
+    tok = np.arange(w.R) // w.K
+    assert np.array_equal(ops["dyq"][inv], q_ref.reshape(w.T, w.H)[tok])
+    dys = _untile_scales(ops["dys"], rows, w.H // 32)
+    assert np.array_equal(dys[inv], s_ref.reshape(w.T, w.H // 32)[tok])
 
 
 @pytest.mark.parametrize("name", ["sweep_zipf0_mx", "sweep_zipf2_mx"])
