@@ -335,8 +335,9 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
   cudaStream_t s = as_stream(stream);
   if (z.mx) {  // weight scales into atoms, then x quantised on the gather
     const int64_t EI = static_cast<int64_t>(z.E) * z.I, EH = static_cast<int64_t>(z.E) * z.H;
-    const ScaleJob jobs[2] = {{w->s_gate, w->s_up, st.sw_gu, EI / 64, z.H / 128, 1},
-                              {w->s_down, nullptr, st.sw_d, EH / 128, z.I / 128, 0}};
+    const int ad = z.mx_bn_h() / 128;  // atoms per B tile of the down projection
+    const ScaleJob jobs[2] = {{w->s_gate, w->s_up, st.sw_gu, EI / 128, z.H / 128, 2, 1},
+                              {w->s_down, nullptr, st.sw_d, EH / (128 * ad), z.I / 128, ad, 0}};
     if (launch_mx_scale_atoms(jobs, 2, s)) return MOK_ERR_CUDA;
     if (launch_gather_rows_mx(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
                               ctx.xg, st.xq, st.xs, K_GATHER_X, s))
@@ -375,9 +376,10 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   const int grid = grid_of(sched);
   if (z.mx) {  // weight scales into atoms, then dY quantised on the gather
     const int64_t EI = static_cast<int64_t>(z.E) * z.I, EH = static_cast<int64_t>(z.E) * z.H;
-    const ScaleJob jobs[3] = {{w->st_down, nullptr, st.swt_d, EI / 128, z.H / 128, 0},
-                              {w->st_gate, nullptr, st.swt_g, EH / 128, z.I / 128, 0},
-                              {w->st_up, nullptr, st.swt_u, EH / 128, z.I / 128, 0}};
+    const int ag = z.mx_bn_h() / 128;  // atoms per B tile of the second data-gradient GEMM
+    const ScaleJob jobs[3] = {{w->st_down, nullptr, st.swt_d, EI / 128, z.H / 128, 1, 0},
+                              {w->st_gate, nullptr, st.swt_g, EH / (128 * ag), z.I / 128, ag, 0},
+                              {w->st_up, nullptr, st.swt_u, EH / (128 * ag), z.I / 128, ag, 0}};
     if (launch_mx_scale_atoms(jobs, 3, s)) return MOK_ERR_CUDA;
     if (launch_gather_rows_mx(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
                               st.dyg, st.dyq, st.dys, K_GATHER_DY, s))

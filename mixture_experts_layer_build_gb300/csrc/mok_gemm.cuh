@@ -73,20 +73,30 @@ struct GemmArgs {
 constexpr int kStageBufs = 2;  // staging tiles per epilogue warp
 
 // A stage holds one K block of A and B as rows of 128 bytes (64 bf16 or 128 e4m3 along K) and, with
-// MX, one 512-byte scale atom each for A and B.  MX tiles are 128 x 128 (the two accumulators
-// take TMEM columns [0, 256), the scale words of stage s columns 256 + 8 s .. + 7).
+// MX, the K block's scale atoms: one for A's 128 rows, BN / 128 for B's rows.
+//   bf16, and MX with BN = 128: two TMEM accumulators (the epilogue of one tile overlaps the
+//     main loop of the next), four epilogue warps.  MX puts stage s's scale words in TMEM columns
+//     256 + 8 s ...
+//   MX with BN = 256 ("wide"): two 256-column accumulators would fill TMEM and leave no room for
+//     the scale words, so there is one; eight epilogue warps (two per lane quarter, 128 columns
+//     each) copy it to registers and release it at once, then finish the tile's epilogue while
+//     the next tile's MMAs run.  Stage s's scale words sit in columns 256 + 12 s ...
 template <int VAR, int BN, bool MX>
 struct GemmCfg {
-  static_assert(!MX || BN == 128, "block-scaled tiles are 128 x 128");
-  static constexpr int kStages = MX ? 5 : (BN == 256 ? 4 : 6);
-  static constexpr int kEpiWarps = 4;   // one warp per TMEM lane quarter
+  static_assert(!MX || BN == 128 || BN == 256, "block-scaled tiles are 128 x 128 or 128 x 256");
+  static constexpr bool kWide = MX && BN == 256;
+  static constexpr int kAccBufs = kWide ? 1 : 2;
+  static constexpr int kStages = MX ? (kWide ? 3 : 5) : (BN == 256 ? 4 : 6);
+  static constexpr int kEpiWarps = kWide ? 8 : 4;  // warp w accesses TMEM lane quarter w % 4
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
-  static constexpr uint32_t kSfBytes = MX ? 1024 : 0;
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfBytes;
+  static constexpr uint32_t kSfBytes = MX ? 512 + BN * 4 : 0;
+  static constexpr uint32_t kTxBytes = kABytes + kBBytes + kSfBytes;         // bytes landing per stage
+  static constexpr uint32_t kStageBytes = (kTxBytes + 1023u) & ~1023u;         // stride: swizzle atoms
   static constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
-  static constexpr uint32_t kSfCol0 = 2 * BN;
+  static constexpr uint32_t kSfCol0 = kAccBufs * BN;
+  static constexpr uint32_t kSfCols = 4 + BN / 32;  // scale-word columns per stage (A, then B)
   static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * 4096;  // per warp: tiles of 4 KB
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + kStagingBytes + 256;
 };
@@ -134,33 +144,36 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
 // Issue the loads of one K block into stage (sa, sb[, sf]), all completing on barrier `bar`.  MX
 // (E4M3, K-major A and B, 128 K values per block): A rows of the routed operand, B rows of the
 // caller's weight copy quantised along this GEMM's K ([E*I, H] Wg|Wu, [E*H, I] Wd, [E*I, H] Wd^T,
-// [E*H, I] Wg^T|Wu^T), plus the A and B scale atoms of the block by untiled bulk copies.  GATEUP's
-// B tile is 64 gate rows then the same 64 up rows, and its scale atoms are laid out in that pairing.
+// [E*H, I] Wg^T|Wu^T), plus the block's scale atoms by untiled bulk copies: A's atom, and B's
+// BN / 128 atoms, which the per-call re-tiling stores next to each other.  GATEUP's B tile (BN =
+// 256) is 128 gate rows then the same 128 up rows; its atom pair is the gate atom, then the up.
 template <int VAR, int BN, bool MX>
 __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
                                           uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
                                           const CUtensorMap* tB2) {
   if constexpr (MX) {
-    const uint32_t sf = sb + BN * 128;  // A atom, then B atom
+    constexpr uint32_t kSfb = BN * 4;   // bytes of B scale atoms per K block
+    const uint32_t sf = sb + BN * 128;  // A atom, then B's atoms
     const int k0 = kb * 128;
     tma_load_2d(sa, tA, bar, k0, w.row0);
     bulk_load(sf, a.sfa + (static_cast<int64_t>(w.row0 >> 7) * a.k_blocks + kb) * 512, 512, bar);
     if constexpr (VAR == V_FWD_GATEUP) {
-      const int n0 = w.e * a.I + w.nt * 64;
+      static_assert(BN == 256, "MX gate/up tiles pair 128 gate and 128 up columns");
+      const int n0 = w.e * a.I + w.nt * 128;
       tma_load_2d(sb, tB, bar, k0, n0);
-      tma_load_2d(sb + 64 * 128, tB2, bar, k0, n0);
-      bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(n0 >> 6) * a.sfb_kq + kb) * 512, 512, bar);
+      tma_load_2d(sb + 128 * 128, tB2, bar, k0, n0);
+      bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(n0 >> 7) * a.sfb_kq + kb) * kSfb, kSfb, bar);
     } else if constexpr (VAR == V_DGRAD2) {
       const bool first = kb < a.kb_split;
       const int kq = first ? kb : kb - a.kb_split;
-      const int n0 = w.e * a.H + w.nt * 128;
+      const int n0 = w.e * a.H + w.nt * BN;
       tma_load_2d(sb, first ? tB : tB2, bar, kq * 128, n0);
-      bulk_load(sf + 512, (first ? a.sfb : a.sfb2) + (static_cast<int64_t>(n0 >> 7) * a.sfb_kq + kq) * 512, 512,
+      bulk_load(sf + 512, (first ? a.sfb : a.sfb2) + (static_cast<int64_t>(n0 / BN) * a.sfb_kq + kq) * kSfb, kSfb,
                 bar);
     } else {  // FWD_DOWN: B rows e*H + n; DGRAD1: B rows e*I + n
-      const int n0 = w.e * (VAR == V_FWD_DOWN ? a.H : a.I) + w.nt * 128;
+      const int n0 = w.e * (VAR == V_FWD_DOWN ? a.H : a.I) + w.nt * BN;
       tma_load_2d(sb, tB, bar, k0, n0);
-      bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(n0 >> 7) * a.sfb_kq + kb) * 512, 512, bar);
+      bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(n0 / BN) * a.sfb_kq + kb) * kSfb, kSfb, bar);
     }
     return;
   }
@@ -288,39 +301,44 @@ __device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, i
   }
 }
 
-// Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab.
-// tO0 / tO1 / tO2 are the output tensor maps of the variant; `tempty` is released as soon as the
-// last accumulator column has been read.  `pre` holds DGRAD1's first prefetched context chunk.
+// Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab; `h`
+// = the warp's column half in the wide (8-warp) configuration.  tO0 / tO1 / tO2 are the output
+// tensor maps of the variant; `tempty` is released as soon as the last accumulator column has been
+// read.  `pre` holds DGRAD1's first prefetched context chunk.
 template <int VAR, int BN, bool MX>
-__device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int lane, uint32_t taddr,
-                                              Stager<kStageBufs>& stg, const CUtensorMap* tO0,
+__device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int h, int lane,
+                                              uint32_t taddr, Stager<kStageBufs>& stg, const CUtensorMap* tO0,
                                               const CUtensorMap* tO1, const CUtensorMap* tO2, uint32_t tempty,
                                               Dg1Chunk& pre) {
   if constexpr (VAR == V_FWD_GATEUP && MX) {
-    // columns [0, 64) of the accumulator are gate, [64, 128) up, for I columns i0 ...  g and u
-    // leave in fp32 (the backward re-quantises dg, du from them); a = silu(g) u leaves MX-quantised
-    // along I: its dequantised values in bf16 for the backward, its E4M3 codes and scales for the
-    // down projection.
-    const int i0 = w.nt * 64;
+    // accumulator columns [0, 128) are gate, [128, 256) up, for I columns nt*128 ...; this warp
+    // takes 64 of them (half h).  g and u leave in fp32 (the backward re-quantises dg, du from
+    // them); a = silu(g) u leaves MX-quantised along I: its dequantised values in bf16 for the
+    // backward, its E4M3 codes and scales for the down projection.
+    const int i0 = w.nt * 128 + 64 * h;
     const int rowc = w.row0 + q * 32;
     const int64_t row = rowc + lane;
-#pragma unroll 1
+    uint32_t gr[64], ur[64];
+    tmem_ld_32x32b_x32(taddr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(gr));
+    tmem_ld_32x32b_x32(taddr + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(gr + 32));
+    tmem_ld_32x32b_x32(taddr + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(ur));
+    tmem_ld_32x32b_x32(taddr + 128 + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(ur + 32));
+    tmem_ld_wait();
+    release_acc(tempty);
+#pragma unroll
     for (int c = 0; c < 64; c += 32) {
-      uint32_t gr[32], ur[32];
-      tmem_ld_32x32b_x32(taddr + c, gr);
-      tmem_ld_32x32b_x32(taddr + 64 + c, ur);
-      tmem_ld_wait();
-      if (c + 32 >= 64) release_acc(tempty);
       uint4 ch[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ch[j] = make_uint4(gr[4 * j], gr[4 * j + 1], gr[4 * j + 2], gr[4 * j + 3]);
+      for (int j = 0; j < 8; ++j)
+        ch[j] = make_uint4(gr[c + 4 * j], gr[c + 4 * j + 1], gr[c + 4 * j + 2], gr[c + 4 * j + 3]);
       stg.put<128>(ch, tO0, i0 + c, rowc);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) ch[j] = make_uint4(ur[4 * j], ur[4 * j + 1], ur[4 * j + 2], ur[4 * j + 3]);
+      for (int j = 0; j < 8; ++j)
+        ch[j] = make_uint4(ur[c + 4 * j], ur[c + 4 * j + 1], ur[c + 4 * j + 2], ur[c + 4 * j + 3]);
       stg.put<128>(ch, tO0, a.I + i0 + c, rowc);
       float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = silu_f(__uint_as_float(gr[i])) * __uint_as_float(ur[i]);
+      for (int i = 0; i < 32; ++i) v[i] = silu_f(__uint_as_float(gr[c + i])) * __uint_as_float(ur[c + i]);
       uint32_t codes[8];
       const uint32_t sbyte = mx_quant32(v, codes);
       pack_bf16<32>(v, ch);
@@ -329,6 +347,27 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
       stg.put<32>(ch, tO2, i0 + c, rowc);
       a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sbyte);
+    }
+  } else if constexpr ((VAR == V_FWD_DOWN || VAR == V_DGRAD2) && MX && BN == 256) {
+    // wide tile: this warp's 128 columns go to registers, the accumulator is released, then the
+    // bf16 rows leave in two 64-column tiles
+    const int rowc = w.row0 + q * 32;
+    uint32_t r[128];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      tmem_ld_32x32b_x32(taddr + 128 * h + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * j));
+    tmem_ld_wait();
+    release_acc(tempty);
+#pragma unroll
+    for (int c = 0; c < 128; c += 64) {
+      uint4 ch[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        ch[j] = make_uint4(pack_bf16x2(__uint_as_float(r[c + 8 * j]), __uint_as_float(r[c + 8 * j + 1])),
+                           pack_bf16x2(__uint_as_float(r[c + 8 * j + 2]), __uint_as_float(r[c + 8 * j + 3])),
+                           pack_bf16x2(__uint_as_float(r[c + 8 * j + 4]), __uint_as_float(r[c + 8 * j + 5])),
+                           pack_bf16x2(__uint_as_float(r[c + 8 * j + 6]), __uint_as_float(r[c + 8 * j + 7])));
+      stg.put<128>(ch, tO0, w.nt * BN + 128 * h + c, rowc);
     }
   } else if constexpr (VAR == V_FWD_GATEUP) {
     // columns [0, BN/2) of the accumulator are gate, [BN/2, BN) up, for I columns i0 ...
@@ -591,7 +630,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+          mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
           const uint32_t sa = base + stage * C::kStageBytes;
           gemm_load<VAR, BN, MX>(args, w, kb, sa, sa + C::kABytes, full_bar(stage), &tmA, &tmB, &tmB2);
           last_parity[stage] = static_cast<int>(phase);
@@ -629,9 +668,11 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
             // this stage's scale atoms -> its own 8 TMEM columns (A words, then B words); the copies
             // and the MMAs that read them execute in issue order
             const uint32_t sf = sb + C::kBBytes;
-            const uint32_t tsf = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage * 8);
+            const uint32_t tsf = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage) * C::kSfCols;
             tmem_cp_sf_atom(tsf, sdesc_plain(sf));
-            tmem_cp_sf_atom(tsf + 4, sdesc_plain(sf + 512));
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)  // B row n's word lands in column n / 32
+              tmem_cp_sf_atom(tsf + 4 + 4 * j, sdesc_plain(sf + 512 + 512 * j));
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)  // K = 32 e4m3 (32 bytes) per instruction; k-group ks
               umma_mxf8(d_tmem, sdesc_sw128(sa + ks * 32, 16, 1024), sdesc_sw128(sb + ks * 32, 16, 1024),
@@ -654,7 +695,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
         }
         if (!ok) break;
         umma_commit(tfull_bar(acc));
-        if (++acc == 2) {
+        if (++acc == C::kAccBufs) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -666,7 +707,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue warps 2..5 ----------------
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;  // column half (wide configuration only)
     Stager<kStageBufs> stg{staging + static_cast<uint32_t>(warp - 2) * (kStageBufs * 4096u), 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -680,8 +722,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      gemm_epilogue<VAR, BN, MX>(args, w, q, lane, taddr, stg, &tmO0, &tmO1, &tmO2, tempty_bar(acc), pre);
-      if (++acc == 2) {
+      gemm_epilogue<VAR, BN, MX>(args, w, q, h, lane, taddr, stg, &tmO0, &tmO1, &tmO2, tempty_bar(acc), pre);
+      if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }

@@ -25,9 +25,9 @@ static int clamp_grid(int num_ctas, int64_t units) {
   return static_cast<int>(units < num_ctas ? units : num_ctas);
 }
 
-// MXFP8: both GEMMs block-scaled on E4M3 operands (128 x 128 tiles).  B is the K-major transposed
-// weight copy quantised along this GEMM's K: Wd^T [E*I, H] for phase 1, Wg^T | Wu^T [E*H, I] for
-// phase 2.
+// MXFP8: both GEMMs block-scaled on E4M3 operands.  B is the K-major transposed weight copy
+// quantised along this GEMM's K: Wd^T [E*I, H] for phase 1 (128 x 128 tiles: its epilogue keeps
+// two accumulators), Wg^T | Wu^T [E*H, I] for phase 2 (128 x 256 tiles when H allows).
 static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                                  const mok_weights& w, int num_ctas, int phase, cudaStream_t stream) {
   CUtensorMap tA, tB, tB2, tO0, tO1, tO2;
@@ -54,10 +54,11 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
     return launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, tO2, a,
                                             clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
   }
+  const int BN = z.mx_bn_h();
   if (!make_tmap_u8(&tA, st.dgq, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 128, 128, 128)) return -1;
-  if (!make_tmap_u8(&tB, w.qt_gate, z.I, EH, 128, 128, 128)) return -1;
-  if (!make_tmap_u8(&tB2, w.qt_up, z.I, EH, 128, 128, 128)) return -1;
-  a.n_tiles = z.H / 128;
+  if (!make_tmap_u8(&tB, w.qt_gate, z.I, EH, 128, BN, 128)) return -1;
+  if (!make_tmap_u8(&tB2, w.qt_up, z.I, EH, 128, BN, 128)) return -1;
+  a.n_tiles = z.H / BN;
   a.k_blocks = 2 * z.I / 128;
   a.kb_split = z.I / 128;
   a.sfa = st.dgs;
@@ -66,8 +67,9 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   a.sfb_kq = z.I / 128;
   a.out0 = st.ybuf;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
-  return launch_gemm<V_DGRAD2, 128, true>(tA, tB, tB2, tO0, tO0, tO0, a,
-                                          clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
+  const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+  return BN == 256 ? launch_gemm<V_DGRAD2, 256, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
+                   : launch_gemm<V_DGRAD2, 128, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream);
 }
 
 int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,

@@ -23,17 +23,18 @@ static int clamp_grid(int num_ctas, int64_t units) {
   return static_cast<int>(units < num_ctas ? units : num_ctas);
 }
 
-// MXFP8: both GEMMs block-scaled on E4M3 operands (128 x 128 tiles).
+// MXFP8: both GEMMs block-scaled on E4M3 operands, 128 x 256 tiles (128 x 128 for the down
+// projection when H is not a multiple of 256).
 static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                                const mok_weights& w, int num_ctas, cudaStream_t stream) {
   CUtensorMap tA, tB, tB2, tO0, tO1, tO2;
   GemmArgs a = common_args(z, s);
   const uint64_t EI = static_cast<uint64_t>(z.E) * z.I, EH = static_cast<uint64_t>(z.E) * z.H;
-  // [g | u] = Xq [Wg_e | Wu_e]^T: 64 gate columns and the same 64 up columns per tile
+  // [g | u] = Xq [Wg_e | Wu_e]^T: 128 gate columns and the same 128 up columns per tile
   if (!make_tmap_u8(&tA, st.xq, z.H, z.rpad_max, 128, 128, 128)) return -1;
-  if (!make_tmap_u8(&tB, w.q_gate, z.H, EI, 128, 64, 128)) return -1;
-  if (!make_tmap_u8(&tB2, w.q_up, z.H, EI, 128, 64, 128)) return -1;
-  a.n_tiles = z.I / 64;
+  if (!make_tmap_u8(&tB, w.q_gate, z.H, EI, 128, 128, 128)) return -1;
+  if (!make_tmap_u8(&tB2, w.q_up, z.H, EI, 128, 128, 128)) return -1;
+  a.n_tiles = z.I / 128;
   a.k_blocks = z.H / 128;
   a.sfa = st.xs;
   a.sfb = st.sw_gu;
@@ -45,13 +46,14 @@ static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx&
   if (!make_tmap_f32(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
   if (!make_tmap_bf16_sw64(&tO1, ctx.a, z.I, z.rpad_max, 32, 32)) return -1;
   if (!make_tmap_u8(&tO2, st.aq, z.I, z.rpad_max, 32, 32, 32)) return -1;
-  int rc = launch_gemm<V_FWD_GATEUP, 128, true>(tA, tB, tB2, tO0, tO1, tO2, a,
+  int rc = launch_gemm<V_FWD_GATEUP, 256, true>(tA, tB, tB2, tO0, tO1, tO2, a,
                                                 clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
   if (rc) return rc;
   // y = aq Wd_e^T
+  const int BN = z.mx_bn_h();
   if (!make_tmap_u8(&tA, st.aq, z.I, z.rpad_max, 128, 128, 128)) return -1;
-  if (!make_tmap_u8(&tB, w.q_down, z.I, EH, 128, 128, 128)) return -1;
-  a.n_tiles = z.H / 128;
+  if (!make_tmap_u8(&tB, w.q_down, z.I, EH, 128, BN, 128)) return -1;
+  a.n_tiles = z.H / BN;
   a.k_blocks = z.I / 128;
   a.sfa = st.as_sf;
   a.sfb = st.sw_d;
@@ -60,8 +62,9 @@ static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx&
   a.out1 = nullptr;
   a.out_sf = nullptr;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
-  return launch_gemm<V_FWD_DOWN, 128, true>(tA, tB, tB, tO0, tO0, tO0, a,
-                                            clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
+  const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+  return BN == 256 ? launch_gemm<V_FWD_DOWN, 256, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
+                   : launch_gemm<V_FWD_DOWN, 128, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
 }
 
 int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st, const mok_weights& w,

@@ -17,6 +17,8 @@ struct Sizes {
   int64_t T, R, rpad_max, tiles_max, mblocks_max, nchunks;
   int32_t H, I, E, K, mb, MB;
   bool mx;  // MXFP8 mode
+  // MXFP8 tile width (N) of the GEMMs whose N runs over H: 256 when H allows it
+  int32_t mx_bn_h() const { return H % 256 == 0 ? 256 : 128; }
 };
 bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s);
 
@@ -38,12 +40,12 @@ struct Staging {
   uint8_t* dys;      //   scales: rtiles x H/128 atoms
   uint8_t* dgq;      // [rpad_max, 2I] [dg | du], quantised along I
   uint8_t* dgs;      //   scales: rtiles x 2I/128 atoms
-  // the caller's weight scales re-tiled into atoms (per call)
-  uint8_t* sw_gu;    // s_gate | s_up paired per 64 rows: E*I/64 tiles x H/128 atoms
-  uint8_t* sw_d;     // s_down: E*H/128 tiles x I/128 atoms
-  uint8_t* swt_d;    // st_down: E*I/128 tiles x H/128 atoms
-  uint8_t* swt_g;    // st_gate: E*H/128 tiles x I/128 atoms
-  uint8_t* swt_u;    // st_up: E*H/128 tiles x I/128 atoms
+  // the caller's weight scales re-tiled into atom groups matching the B tiles (per call)
+  uint8_t* sw_gu;    // s_gate, s_up: per 128 rows of I, the gate atom then the up atom
+  uint8_t* sw_d;     // s_down: groups of BN_down / 128 atoms
+  uint8_t* swt_d;    // st_down: single atoms (128-row tiles)
+  uint8_t* swt_g;    // st_gate: groups of BN_dgrad2 / 128 atoms
+  uint8_t* swt_u;    // st_up: same
 };
 struct Ctx {
   uint16_t* xg;      // [rpad_max, H] bf16: gathered x rows (zero on padding rows)
@@ -88,15 +90,18 @@ int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int3
 int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                           int32_t H, uint16_t* dst, uint8_t* dst_q, uint8_t* dst_sf, int kind,
                           cudaStream_t stream);
-// Re-tile row-major E8M0 scales [rows, 4 kq] into 512-byte atoms (up to three jobs per launch).  A
-// paired job interleaves two sources per 128-row tile: 64 rows of src0, then the same 64 of src1.
+// Re-tile row-major E8M0 scales [rows, 4 kq] into groups of `atoms` 512-byte atoms (up to three
+// jobs per launch): group g, K atom q holds `atoms` consecutive atoms at ((g * kq + q) * atoms + j)
+// * 512.  One source: atom j covers rows (g * atoms + j) * 128 ...; two sources (atoms = 2): atom
+// j covers rows g * 128 ... of source j.
 struct ScaleJob {
   const uint8_t* src0;
-  const uint8_t* src1;  // paired jobs only
+  const uint8_t* src1;  // two-source jobs only
   uint8_t* dst;
-  int64_t tiles;        // 128-row tiles of dst
-  int32_t kq;           // atoms per tile = k-groups / 4
-  int32_t paired;
+  int64_t groups;
+  int32_t kq;           // K atoms = k-groups / 4
+  int32_t atoms;        // atoms per group: 1 or 2
+  int32_t two_src;
 };
 int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream);
 int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,

@@ -262,29 +262,29 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint
   }
 }
 
-// Scale atoms: thread t writes line (t % 32) of atom t / 32 -- rows l, l+32, l+64, l+96 of the
-// atom's 128-row tile, four k-groups each.  blockIdx.y selects the job.
+// Scale atoms: thread t writes line (t % 32) of atom t / 32 of the destination -- rows l, l+32,
+// l+64, l+96 of the atom's 128-row tile, four k-groups each.  blockIdx.y selects the job.
 struct ScaleJobs {
   ScaleJob j[3];
 };
 __global__ void __launch_bounds__(kMoveThreads) mx_scale_atoms_kernel(const ScaleJobs jobs) {
   const ScaleJob jb = jobs.j[blockIdx.y];
-  const int64_t lines = jb.tiles * jb.kq * 32;
+  const int64_t lines = jb.groups * jb.kq * jb.atoms * 32;
   const int64_t kg = 4 * static_cast<int64_t>(jb.kq);  // source row length in bytes
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; t < lines; t += stride) {
     const int l = static_cast<int>(t & 31);
-    const int64_t atom = t >> 5;
-    const int64_t tile = atom / jb.kq;
-    const int64_t q = atom - tile * jb.kq;
+    const int64_t atom = t >> 5;  // ((g * kq + q) * atoms + j)
+    const int j = static_cast<int>(atom % jb.atoms);
+    const int64_t gq = atom / jb.atoms;
+    const int64_t g = gq / jb.kq;
+    const int64_t q = gq - g * jb.kq;
+    const uint8_t* srcp = (jb.two_src && j) ? jb.src1 : jb.src0;
+    const int64_t row0 = jb.two_src ? g * 128 : (g * jb.atoms + j) * 128;
     uint32_t wv[4];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int r = l + 32 * c;
-      const uint8_t* srcp = jb.paired ? (r < 64 ? jb.src0 : jb.src1) : jb.src0;
-      const int64_t srow = jb.paired ? tile * 64 + (r & 63) : tile * 128 + r;
-      wv[c] = __ldg(reinterpret_cast<const uint32_t*>(srcp + srow * kg + 4 * q));
-    }
+    for (int c = 0; c < 4; ++c)
+      wv[c] = __ldg(reinterpret_cast<const uint32_t*>(srcp + (row0 + l + 32 * c) * kg + 4 * q));
     reinterpret_cast<uint4*>(jb.dst)[t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
 }
@@ -327,7 +327,7 @@ int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream) 
   int64_t most = 0;
   for (int i = 0; i < njobs; ++i) {
     p.j[i] = jobs[i];
-    const int64_t lines = jobs[i].tiles * jobs[i].kq * 32;
+    const int64_t lines = jobs[i].groups * jobs[i].kq * jobs[i].atoms * 32;
     most = lines > most ? lines : most;
   }
   if (most <= 0) return 0;
