@@ -70,7 +70,6 @@ struct GemmArgs {
   uint8_t* out_sf;
 };
 
-constexpr int kStageBufs = 2;  // staging tiles per epilogue warp
 
 // A stage holds one K block of A and B as rows of 128 bytes (64 bf16 or 128 e4m3 along K) and, with
 // MX, the K block's scale atoms: one for A's 128 rows, BN / 128 for B's rows.
@@ -80,25 +79,32 @@ constexpr int kStageBufs = 2;  // staging tiles per epilogue warp
 //   MX with BN = 256 ("wide"): two 256-column accumulators would fill TMEM and leave no room for
 //     the scale words, so there is one; eight epilogue warps (two per lane quarter, 128 columns
 //     each) copy it to registers and release it at once, then finish the tile's epilogue while
-//     the next tile's MMAs run.  Stage s's scale words sit in columns 256 + 12 s ...
+//     the next tile's MMAs run.  Stage s's scale words sit in columns 256 + 12 s ...  To fit four
+//     stages, each epilogue warp stages its stores through a single 2 KB tile.
+// The scale atoms of stage s live in a ring of their own after the A/B stages.
 template <int VAR, int BN, bool MX>
 struct GemmCfg {
   static_assert(!MX || BN == 128 || BN == 256, "block-scaled tiles are 128 x 128 or 128 x 256");
   static constexpr bool kWide = MX && BN == 256;
   static constexpr int kAccBufs = kWide ? 1 : 2;
-  static constexpr int kStages = MX ? (kWide ? 3 : 5) : (BN == 256 ? 4 : 6);
+  static constexpr int kStages = MX ? (kWide ? 4 : 5) : (BN == 256 ? 4 : 6);
   static constexpr int kEpiWarps = kWide ? 8 : 4;  // warp w accesses TMEM lane quarter w % 4
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
-  static constexpr uint32_t kSfBytes = MX ? 512 + BN * 4 : 0;
-  static constexpr uint32_t kTxBytes = kABytes + kBBytes + kSfBytes;         // bytes landing per stage
-  static constexpr uint32_t kStageBytes = (kTxBytes + 1023u) & ~1023u;         // stride: swizzle atoms
+  static constexpr uint32_t kSfBytes = MX ? 512 + BN * 4 : 0;  // A atom, then B's BN / 128 atoms
+  static constexpr uint32_t kTxBytes = kABytes + kBBytes + kSfBytes;  // bytes landing per stage
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;           // multiple of 1024: swizzle atoms
   static constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
   static constexpr uint32_t kSfCol0 = kAccBufs * BN;
   static constexpr uint32_t kSfCols = 4 + BN / 32;  // scale-word columns per stage (A, then B)
-  static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * 4096;  // per warp: tiles of 4 KB
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStages) * kStageBytes + kStagingBytes + 256;
+  static constexpr int kStageBufs = kWide ? 1 : 2;             // staging tiles per epilogue warp
+  static constexpr uint32_t kStageBufBytes = kWide ? 2048 : 4096;
+  static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
+  static constexpr uint32_t kSfRing = static_cast<uint32_t>(kStages) * kStageBytes;  // offset of the atom ring
+  static constexpr uint32_t kStagingOff = kSfRing + static_cast<uint32_t>(kStages) * kSfBytes;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStagingOff) + kStagingBytes + 256;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct Unit {
@@ -149,11 +155,10 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
 // 256) is 128 gate rows then the same 128 up rows; its atom pair is the gate atom, then the up.
 template <int VAR, int BN, bool MX>
 __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
-                                          uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
+                                          uint32_t sf, uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
                                           const CUtensorMap* tB2) {
   if constexpr (MX) {
-    constexpr uint32_t kSfb = BN * 4;   // bytes of B scale atoms per K block
-    const uint32_t sf = sb + BN * 128;  // A atom, then B's atoms
+    constexpr uint32_t kSfb = BN * 4;  // bytes of B scale atoms per K block; sf: A atom, then B's
     const int k0 = kb * 128;
     tma_load_2d(sa, tA, bar, k0, w.row0);
     bulk_load(sf, a.sfa + (static_cast<int64_t>(w.row0 >> 7) * a.k_blocks + kb) * 512, 512, bar);
@@ -219,7 +224,7 @@ __device__ __forceinline__ uint4 ldg_v4(const uint16_t* p) { return __ldg(reinte
 // the 32 lanes' row writes free of bank conflicts.  Each filled tile leaves as one asynchronous
 // TMA tile store; a tile is refilled only after its previous store has finished reading it, so up
 // to NBUF stores are in flight.
-template <int NBUF>
+template <int NBUF, uint32_t BUFBYTES>
 struct Stager {
   uint32_t buf0;
   int cur;
@@ -227,7 +232,7 @@ struct Stager {
   __device__ __forceinline__ uint32_t acquire() {
     if (lane == 0) bulk_wait_read<NBUF - 1>();
     __syncwarp();
-    const uint32_t b = buf0 + (static_cast<uint32_t>(cur) << 12);
+    const uint32_t b = buf0 + static_cast<uint32_t>(cur) * BUFBYTES;
     cur = cur + 1 == NBUF ? 0 : cur + 1;
     return b;
   }
@@ -235,6 +240,7 @@ struct Stager {
   template <int ROW>
   __device__ __forceinline__ void put(const uint4* ch, const CUtensorMap* tm, int c0, int c1) {
     static_assert(ROW == 128 || ROW == 64 || ROW == 32, "row size with a TMA swizzle mode");
+    static_assert(32 * ROW <= BUFBYTES, "tile fits the staging buffer");
     const uint32_t b = acquire();
     const uint32_t row = b + static_cast<uint32_t>(lane) * ROW;
     const int sw = ROW == 128 ? (lane & 7) : ROW == 64 ? ((lane >> 1) & 3) : ((lane >> 2) & 1);
@@ -305,9 +311,9 @@ __device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, i
 // = the warp's column half in the wide (8-warp) configuration.  tO0 / tO1 / tO2 are the output
 // tensor maps of the variant; `tempty` is released as soon as the last accumulator column has been
 // read.  `pre` holds DGRAD1's first prefetched context chunk.
-template <int VAR, int BN, bool MX>
+template <int VAR, int BN, bool MX, class Stg>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int h, int lane,
-                                              uint32_t taddr, Stager<kStageBufs>& stg, const CUtensorMap* tO0,
+                                              uint32_t taddr, Stg& stg, const CUtensorMap* tO0,
                                               const CUtensorMap* tO1, const CUtensorMap* tO2, uint32_t tempty,
                                               Dg1Chunk& pre) {
   if constexpr (VAR == V_FWD_GATEUP && MX) {
@@ -327,30 +333,35 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     release_acc(tempty);
 #pragma unroll
     for (int c = 0; c < 64; c += 32) {
-      uint4 ch[8];
+      uint4 ch[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        ch[j] = make_uint4(gr[c + 4 * j], gr[c + 4 * j + 1], gr[c + 4 * j + 2], gr[c + 4 * j + 3]);
-      stg.put<128>(ch, tO0, i0 + c, rowc);
+      for (int c16 = 0; c16 < 32; c16 += 16) {  // fp32 g, u in 16-column (64-byte) tiles
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        ch[j] = make_uint4(ur[c + 4 * j], ur[c + 4 * j + 1], ur[c + 4 * j + 2], ur[c + 4 * j + 3]);
-      stg.put<128>(ch, tO0, a.I + i0 + c, rowc);
+        for (int j = 0; j < 4; ++j)
+          ch[j] = make_uint4(gr[c + c16 + 4 * j], gr[c + c16 + 4 * j + 1], gr[c + c16 + 4 * j + 2],
+                             gr[c + c16 + 4 * j + 3]);
+        stg.template put<64>(ch, tO0, i0 + c + c16, rowc);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          ch[j] = make_uint4(ur[c + c16 + 4 * j], ur[c + c16 + 4 * j + 1], ur[c + c16 + 4 * j + 2],
+                             ur[c + c16 + 4 * j + 3]);
+        stg.template put<64>(ch, tO0, a.I + i0 + c + c16, rowc);
+      }
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = silu_f(__uint_as_float(gr[c + i])) * __uint_as_float(ur[c + i]);
       uint32_t codes[8];
       const uint32_t sbyte = mx_quant32(v, codes);
       pack_bf16<32>(v, ch);
-      stg.put<64>(ch, tO1, i0 + c, rowc);
+      stg.template put<64>(ch, tO1, i0 + c, rowc);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      stg.put<32>(ch, tO2, i0 + c, rowc);
+      stg.template put<32>(ch, tO2, i0 + c, rowc);
       a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sbyte);
     }
   } else if constexpr ((VAR == V_FWD_DOWN || VAR == V_DGRAD2) && MX && BN == 256) {
     // wide tile: this warp's 128 columns go to registers, the accumulator is released, then the
-    // bf16 rows leave in two 64-column tiles
+    // bf16 rows leave in four 32-column (64-byte) tiles
     const int rowc = w.row0 + q * 32;
     uint32_t r[128];
 #pragma unroll
@@ -359,15 +370,15 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     tmem_ld_wait();
     release_acc(tempty);
 #pragma unroll
-    for (int c = 0; c < 128; c += 64) {
-      uint4 ch[8];
+    for (int c = 0; c < 128; c += 32) {
+      uint4 ch[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 4; ++j)
         ch[j] = make_uint4(pack_bf16x2(__uint_as_float(r[c + 8 * j]), __uint_as_float(r[c + 8 * j + 1])),
                            pack_bf16x2(__uint_as_float(r[c + 8 * j + 2]), __uint_as_float(r[c + 8 * j + 3])),
                            pack_bf16x2(__uint_as_float(r[c + 8 * j + 4]), __uint_as_float(r[c + 8 * j + 5])),
                            pack_bf16x2(__uint_as_float(r[c + 8 * j + 6]), __uint_as_float(r[c + 8 * j + 7])));
-      stg.put<128>(ch, tO0, w.nt * BN + 128 * h + c, rowc);
+      stg.template put<64>(ch, tO0, w.nt * BN + 128 * h + c, rowc);
     }
   } else if constexpr (VAR == V_FWD_GATEUP) {
     // columns [0, BN/2) of the accumulator are gate, [BN/2, BN) up, for I columns i0 ...
@@ -381,13 +392,13 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       if (c + 64 >= BN / 2) release_acc(tempty);
       uint4 ch[8];
       pack_bf16<64>(g, ch);
-      stg.put<128>(ch, tO0, i0 + c, rowc);
+      stg.template put<128>(ch, tO0, i0 + c, rowc);
       pack_bf16<64>(u, ch);
-      stg.put<128>(ch, tO0, a.I + i0 + c, rowc);
+      stg.template put<128>(ch, tO0, a.I + i0 + c, rowc);
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
       pack_bf16<64>(g, ch);
-      stg.put<128>(ch, tO1, i0 + c, rowc);
+      stg.template put<128>(ch, tO1, i0 + c, rowc);
     }
   } else if constexpr (VAR == V_FWD_DOWN || VAR == V_DGRAD2) {
     const int rowc = w.row0 + q * 32;
@@ -398,7 +409,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       if (c + 64 >= BN) release_acc(tempty);
       uint4 ch[8];
       pack_bf16<64>(v, ch);
-      stg.put<128>(ch, tO0, w.nt * BN + c, rowc);
+      stg.template put<128>(ch, tO0, w.nt * BN + c, rowc);
     }
   } else if constexpr (VAR == V_DGRAD1 && MX) {
     // MXFP8: as below, with g, u read in fp32 and dg, du MX-quantised along I (blocks of 32): their
@@ -441,15 +452,15 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       const uint32_t sg_byte = mx_quant32(dg, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      stg.put<32>(ch, tO2, i0 + c, rowc);
+      stg.template put<32>(ch, tO2, i0 + c, rowc);
       pack_bf16<32>(dg, ch);
-      stg.put<64>(ch, tO0, i0 + c, rowc);
+      stg.template put<64>(ch, tO0, i0 + c, rowc);
       const uint32_t su_byte = mx_quant32(du, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      stg.put<32>(ch, tO2, a.I + i0 + c, rowc);
+      stg.template put<32>(ch, tO2, a.I + i0 + c, rowc);
       pack_bf16<32>(du, ch);
-      stg.put<64>(ch, tO0, a.I + i0 + c, rowc);
+      stg.template put<64>(ch, tO0, a.I + i0 + c, rowc);
       a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sg_byte);
       a.out_sf[sf_atom_offset(row, (a.I + i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(su_byte);
       float sa[32];
@@ -464,7 +475,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
         }
       }
       pack_bf16<32>(sa, ch);
-      stg.put<64>(ch, tO1, i0 + c, rowc);
+      stg.template put<64>(ch, tO1, i0 + c, rowc);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else if constexpr (VAR == V_DGRAD1) {
@@ -506,9 +517,9 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
           pack_bf16<8>(sa, csa + j);
         }
       }
-      stg.put<64>(cdg, tO0, i0 + c, rowc);
-      stg.put<64>(cdu, tO0, a.I + i0 + c, rowc);
-      stg.put<64>(csa, tO1, i0 + c, rowc);
+      stg.template put<64>(cdg, tO0, i0 + c, rowc);
+      stg.template put<64>(cdu, tO0, a.I + i0 + c, rowc);
+      stg.template put<64>(csa, tO1, i0 + c, rowc);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else {  // weight gradients, fp32 out, 32-column tiles
@@ -538,7 +549,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       uint4 ch[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) ch[j] = make_uint4(rv[4 * j], rv[4 * j + 1], rv[4 * j + 2], rv[4 * j + 3]);
-      stg.put<128>(ch, tm, w.nt * BN + c, r0);
+      stg.template put<128>(ch, tm, w.nt * BN + c, r0);
     }
   }
 }
@@ -572,8 +583,9 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t staging = base + S * C::kStageBytes;  // 1024-byte aligned
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + S * C::kStageBytes + C::kStagingBytes);
+  const uint32_t sf_ring = base + C::kSfRing;
+  const uint32_t staging = base + C::kStagingOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kStagingOff + C::kStagingBytes);
   // bars[0..S) full, [S..2S) empty, [2S, 2S+2) accumulator full, [2S+2, 2S+4) accumulator empty,
   // [2S+4] drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
@@ -632,7 +644,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
           }
           mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
           const uint32_t sa = base + stage * C::kStageBytes;
-          gemm_load<VAR, BN, MX>(args, w, kb, sa, sa + C::kABytes, full_bar(stage), &tmA, &tmB, &tmB2);
+          gemm_load<VAR, BN, MX>(args, w, kb, sa, sa + C::kABytes, sf_ring + stage * C::kSfBytes, full_bar(stage),
+                                 &tmA, &tmB, &tmB2);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == S) {
             stage = 0;
@@ -667,7 +680,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
           if constexpr (MX) {
             // this stage's scale atoms -> its own 8 TMEM columns (A words, then B words); the copies
             // and the MMAs that read them execute in issue order
-            const uint32_t sf = sb + C::kBBytes;
+            const uint32_t sf = sf_ring + stage * C::kSfBytes;
             const uint32_t tsf = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage) * C::kSfCols;
             tmem_cp_sf_atom(tsf, sdesc_plain(sf));
 #pragma unroll
@@ -709,7 +722,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
     // ---------------- epilogue warps 2..5 ----------------
     const int q = warp & 3;         // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;  // column half (wide configuration only)
-    Stager<kStageBufs> stg{staging + static_cast<uint32_t>(warp - 2) * (kStageBufs * 4096u), 0, lane};
+    Stager<C::kStageBufs, C::kStageBufBytes> stg{
+        staging + static_cast<uint32_t>(warp - 2) * (C::kStageBufs * C::kStageBufBytes), 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
@@ -747,6 +761,8 @@ bool make_tmap_bf16_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint6
                          uint32_t box_outer);
 bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                    uint32_t box_outer);
+bool make_tmap_f32_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                        uint32_t box_outer);
 // bytes (E4M3 codes); swizzle_bytes 128, 64 or 32
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                   uint32_t box_outer, int swizzle_bytes);

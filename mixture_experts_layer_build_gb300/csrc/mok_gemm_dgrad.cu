@@ -66,7 +66,9 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   a.sfb2 = st.swt_u;
   a.sfb_kq = z.I / 128;
   a.out0 = st.ybuf;
-  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
+  if (!(BN == 256 ? make_tmap_bf16_sw64(&tO0, st.ybuf, z.H, z.rpad_max, 32, 32)
+                  : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)))
+    return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
   return BN == 256 ? launch_gemm<V_DGRAD2, 256, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
                    : launch_gemm<V_DGRAD2, 128, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream);

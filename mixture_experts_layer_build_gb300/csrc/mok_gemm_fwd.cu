@@ -43,7 +43,8 @@ static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx&
   a.out1 = ctx.a;
   a.out_sf = st.as_sf;
   a.out_kq = z.I / 128;
-  if (!make_tmap_f32(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
+  // wide-tile epilogue stores: 2 KB tiles (16 fp32 / 32 bf16 / 32 e4m3 columns x 32 rows)
+  if (!make_tmap_f32_sw64(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 16, 32)) return -1;
   if (!make_tmap_bf16_sw64(&tO1, ctx.a, z.I, z.rpad_max, 32, 32)) return -1;
   if (!make_tmap_u8(&tO2, st.aq, z.I, z.rpad_max, 32, 32, 32)) return -1;
   int rc = launch_gemm<V_FWD_GATEUP, 256, true>(tA, tB, tB2, tO0, tO1, tO2, a,
@@ -61,7 +62,9 @@ static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx&
   a.out0 = st.ybuf;
   a.out1 = nullptr;
   a.out_sf = nullptr;
-  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
+  if (!(BN == 256 ? make_tmap_bf16_sw64(&tO0, st.ybuf, z.H, z.rpad_max, 32, 32)
+                  : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)))
+    return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
   return BN == 256 ? launch_gemm<V_FWD_DOWN, 256, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
                    : launch_gemm<V_FWD_DOWN, 128, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);

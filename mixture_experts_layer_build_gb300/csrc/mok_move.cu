@@ -45,46 +45,64 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* 
 }
 
 // out[t] = bf16( sum_{k = 0..K-1 ascending} w[t,k] * y[inv[t*K+k]] ), fp32 accumulation; w == nullptr
-// means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.  The K
-// row loads of a vector are issued together (8 at a time) before the fixed-order FMA chain.
+// means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.  Each
+// lane keeps eight 16-byte row loads in flight: U column vectors x (8 / U) of the K rows, issued
+// together before the fixed-order FMA chains (U = 8 for top-1 ... U = 1 for K >= 8).
+template <int U>
 __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __restrict__ y,
                                                               const int32_t* __restrict__ inv,
                                                               const float* __restrict__ w, int64_t T, int K,
                                                               int64_t vecs, uint4* __restrict__ out) {
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 8 / U;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); t < T;
        t += nwarps) {
-    for (int64_t c = lane; c < vecs; c += 32) {
-      float acc[8];
+    for (int64_t c0 = lane; c0 < vecs; c0 += 32 * U) {
+      float acc[U][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
       for (int k0 = 0; k0 < K; k0 += kBatch) {
-        uint4 v[kBatch];
+        uint4 v[U][kBatch];
         float wk[kBatch];
-        bool use[kBatch];
+        int row[kBatch];
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
           const int k = k0 + b;
-          const int row = k < K ? __ldg(inv + t * K + k) : -1;
-          use[b] = row >= 0;
-          wk[b] = (use[b] && w) ? __ldg(w + t * K + k) : 1.0f;
-          v[b] = use[b] ? __ldg(y + static_cast<int64_t>(row) * vecs + c) : make_uint4(0, 0, 0, 0);
+          row[b] = k < K ? __ldg(inv + t * K + k) : -1;
+          wk[b] = (row[b] >= 0 && w) ? __ldg(w + t * K + k) : 1.0f;
         }
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          if (!use[b]) continue;
-          const uint32_t p[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+        for (int u = 0; u < U; ++u)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(wk[b], bf16_lo(p[i]), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(wk[b], bf16_hi(p[i]), acc[2 * i + 1]);
+          for (int b = 0; b < kBatch; ++b) {
+            const int64_t c = c0 + 32 * u;
+            v[u][b] = (row[b] >= 0 && c < vecs) ? __ldg(y + static_cast<int64_t>(row[b]) * vecs + c)
+                                                : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          if (row[b] < 0) continue;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const uint32_t p[4] = {v[u][b].x, v[u][b].y, v[u][b].z, v[u][b].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[u][2 * i] = fmaf(wk[b], bf16_lo(p[i]), acc[u][2 * i]);
+              acc[u][2 * i + 1] = fmaf(wk[b], bf16_hi(p[i]), acc[u][2 * i + 1]);
+            }
           }
         }
       }
-      out[t * vecs + c] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = c0 + 32 * u;
+        if (c < vecs)
+          out[t * vecs + c] = make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
+                                         pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
+      }
     }
   }
 }
@@ -343,8 +361,16 @@ int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_
   if (T <= 0) return 0;
   const int grid = grid_for(T, kMoveThreads / 32);
   trace_begin(stream, kind);
-  combine_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(y), inv, s, T, K, H / 8,
-                                                    reinterpret_cast<uint4*>(out));
+  const uint4* yv = reinterpret_cast<const uint4*>(y);
+  uint4* ov = reinterpret_cast<uint4*>(out);
+  if (K == 1)
+    combine_kernel<8><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
+  else if (K == 2)
+    combine_kernel<4><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
+  else if (K <= 4)
+    combine_kernel<2><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
+  else
+    combine_kernel<1><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

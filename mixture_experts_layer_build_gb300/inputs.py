@@ -53,6 +53,9 @@ WORKLOADS = {
     # per-GPU shard of an EP64 layer: 2048 tokens x top-8 = 16384 routed rows onto 4 local experts
     "mxfp8_ep64_shard": Workload("mxfp8_ep64_shard", 16384, 7168, 2048, 4, 1, "gumbel_max", zipf=1.2,
                                  precision="mxfp8"),
+    # the same shard with a quarter of the rows: a case small enough for multi-pass ncu captures
+    "mxfp8_ep64_shard_4k": Workload("mxfp8_ep64_shard_4k", 4096, 7168, 2048, 4, 1, "gumbel_max", zipf=1.2,
+                                    precision="mxfp8"),
     # imbalance / granularity sweep
     "sweep_zipf0": Workload("sweep_zipf0", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=0.0),
     "sweep_zipf1": Workload("sweep_zipf1", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=1.0),
