@@ -14,7 +14,8 @@ namespace {
 constexpr int kMoveThreads = 256;
 
 // dst[row] = src[row_token[row]] for row < Rpad (= meta[0]); zero rows where row_token < 0.
-// One warp per row, 16-byte vectors, lanes striding along the row (coalesced).
+// One warp per row, 16-byte vectors, lanes striding along the row (coalesced).  The gathered rows
+// are written evict-first so that the source rows, read K times, stay in L2.
 __global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* __restrict__ src,
                                                                   const int32_t* __restrict__ row_token,
                                                                   const int32_t* __restrict__ meta, int64_t vecs,
@@ -31,15 +32,15 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* 
       int64_t c = lane;
       for (; c + 96 < vecs; c += 128) {
         const uint4 v0 = __ldg(s + c), v1 = __ldg(s + c + 32), v2 = __ldg(s + c + 64), v3 = __ldg(s + c + 96);
-        d[c] = v0;
-        d[c + 32] = v1;
-        d[c + 64] = v2;
-        d[c + 96] = v3;
+        __stcs(d + c, v0);
+        __stcs(d + c + 32, v1);
+        __stcs(d + c + 64, v2);
+        __stcs(d + c + 96, v3);
       }
-      for (; c < vecs; c += 32) d[c] = __ldg(s + c);
+      for (; c < vecs; c += 32) __stcs(d + c, __ldg(s + c));
     } else {
       const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int64_t c = lane; c < vecs; c += 32) d[c] = z;
+      for (int64_t c = lane; c < vecs; c += 32) __stcs(d + c, z);
     }
   }
 }
@@ -47,7 +48,8 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* 
 // out[t] = bf16( sum_{k = 0..K-1 ascending} w[t,k] * y[inv[t*K+k]] ), fp32 accumulation; w == nullptr
 // means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.  Each
 // lane keeps eight 16-byte row loads in flight: U column vectors x (8 / U) of the K rows, issued
-// together before the fixed-order FMA chains (U = 8 for top-1 ... U = 1 for K >= 8).
+// together before the fixed-order FMA chains (U = 8 for top-1 ... U = 1 for K >= 8).  Rows are
+// read once and written once: both streams are marked evict-first.
 template <int U>
 __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __restrict__ y,
                                                               const int32_t* __restrict__ inv,
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __re
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
             const int64_t c = c0 + 32 * u;
-            v[u][b] = (row[b] >= 0 && c < vecs) ? __ldg(y + static_cast<int64_t>(row[b]) * vecs + c)
+            v[u][b] = (row[b] >= 0 && c < vecs) ? __ldcs(y + static_cast<int64_t>(row[b]) * vecs + c)
                                                 : make_uint4(0, 0, 0, 0);
           }
 #pragma unroll
@@ -100,8 +102,9 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __re
       for (int u = 0; u < U; ++u) {
         const int64_t c = c0 + 32 * u;
         if (c < vecs)
-          out[t * vecs + c] = make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
-                                         pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7]));
+          __stcs(out + t * vecs + c,
+                 make_uint4(pack_bf16x2(acc[u][0], acc[u][1]), pack_bf16x2(acc[u][2], acc[u][3]),
+                            pack_bf16x2(acc[u][4], acc[u][5]), pack_bf16x2(acc[u][6], acc[u][7])));
       }
     }
   }
@@ -227,7 +230,31 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
 // mxfp8_quantize_kernel: dst_q[row] = E4M3 codes, dst_sf = E8M0 scales (atom-tiled, kq atoms per
 // 128-row tile), dst[row] = the dequantised values in bf16 (exact: E4M3 x 2^k fits bf16 down to
 // 2^-133).  Padding rows (row_token < 0) get zero codes, zero values and scale byte 0.
-// One warp per row; lane l handles the row's 32-element blocks l, l + 32, ...
+// One warp per row; lane l handles the row's 32-element blocks l, l + 32, ..., two at a time so
+// that eight 16-byte loads are in flight per lane; outputs are written evict-first.
+__device__ __forceinline__ void mx_block_out(const uint4 (&v)[4], uint4* d, uint4* dq, uint8_t* sf) {
+  float o[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[8 * i] = bf16_lo(v[i].x);
+    o[8 * i + 1] = bf16_hi(v[i].x);
+    o[8 * i + 2] = bf16_lo(v[i].y);
+    o[8 * i + 3] = bf16_hi(v[i].y);
+    o[8 * i + 4] = bf16_lo(v[i].z);
+    o[8 * i + 5] = bf16_hi(v[i].z);
+    o[8 * i + 6] = bf16_lo(v[i].w);
+    o[8 * i + 7] = bf16_hi(v[i].w);
+  }
+  uint32_t codes[8];
+  *sf = static_cast<uint8_t>(mx_quant32(o, codes));
+  __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+  __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    __stcs(d + i, make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
+                             pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7])));
+}
+
 __global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint4* __restrict__ src,
                                                                      const int32_t* __restrict__ row_token,
                                                                      const int32_t* __restrict__ meta,
@@ -243,39 +270,35 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint
     const int t = row_token[row];
     uint4* d = dst + row * vecs;
     uint4* dq = dst_q + row * (vecs / 2);
-    for (int64_t b = lane; b < nblk; b += 32) {
-      uint8_t* sf = dst_sf + sf_atom_offset(row, static_cast<int>(b), kq);
-      if (t < 0) {
-        const uint4 z = make_uint4(0, 0, 0, 0);
+    if (t < 0) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int64_t b = lane; b < nblk; b += 32) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) d[b * 4 + i] = z;
         dq[b * 2] = z;
         dq[b * 2 + 1] = z;
-        *sf = 0;
-        continue;
+        dst_sf[sf_atom_offset(row, static_cast<int>(b), kq)] = 0;
       }
-      const uint4* s = src + static_cast<int64_t>(t) * vecs + b * 4;
-      float o[32];
+      continue;
+    }
+    const uint4* s = src + static_cast<int64_t>(t) * vecs;
+    int64_t b = lane;
+    for (; b + 32 < nblk; b += 64) {
+      uint4 v0[4], v1[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint4 v = __ldg(s + i);
-        o[8 * i] = bf16_lo(v.x);
-        o[8 * i + 1] = bf16_hi(v.x);
-        o[8 * i + 2] = bf16_lo(v.y);
-        o[8 * i + 3] = bf16_hi(v.y);
-        o[8 * i + 4] = bf16_lo(v.z);
-        o[8 * i + 5] = bf16_hi(v.z);
-        o[8 * i + 6] = bf16_lo(v.w);
-        o[8 * i + 7] = bf16_hi(v.w);
+        v0[i] = __ldg(s + b * 4 + i);
+        v1[i] = __ldg(s + (b + 32) * 4 + i);
       }
-      uint32_t codes[8];
-      *sf = static_cast<uint8_t>(mx_quant32(o, codes));
-      dq[b * 2] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      dq[b * 2 + 1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      mx_block_out(v0, d + b * 4, dq + b * 2, dst_sf + sf_atom_offset(row, static_cast<int>(b), kq));
+      mx_block_out(v1, d + (b + 32) * 4, dq + (b + 32) * 2,
+                   dst_sf + sf_atom_offset(row, static_cast<int>(b + 32), kq));
+    }
+    if (b < nblk) {
+      uint4 v0[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        d[b * 4 + i] = make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
-                                  pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
+      for (int i = 0; i < 4; ++i) v0[i] = __ldg(s + b * 4 + i);
+      mx_block_out(v0, d + b * 4, dq + b * 2, dst_sf + sf_atom_offset(row, static_cast<int>(b), kq));
     }
   }
 }
