@@ -78,7 +78,7 @@ def _load():
             lib.orc_mx_fakequant.restype = None
             lib.orc_mx_fakequant.argtypes = [P, i64]
             lib.orc_layer_mx.restype = None
-            lib.orc_layer_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P]
+            lib.orc_layer_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
             lib.orc_tokens_mx.restype = None
             lib.orc_tokens_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i64, P, P, P, P]
             lib.orc_dw_block_mx.restype = None
@@ -314,8 +314,9 @@ def _mx_ptrs(mx: dict):
     return arrs, ptrs
 
 
-def layer_mx(ids, s, x, dY, mx: dict, E: int, I: int, with_aq: bool = False) -> dict:
-    """Full MXFP8-mode forward + backward (fp64 apart from the quantisation points)."""
+def layer_mx(ids, s, x, dY, mx: dict, E: int, I: int, with_aq: bool = False, with_dg: bool = False) -> dict:
+    """Full MXFP8-mode forward + backward (fp64 apart from the quantisation points).  with_aq adds
+    a_q [R, I]; with_dg adds the unquantised dg, du, a [R, I] (slot order)."""
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     s = np.ascontiguousarray(s, dtype=np.float32)
     x, dY = _u16(x), _u16(dY)
@@ -325,10 +326,16 @@ def layer_mx(ids, s, x, dY, mx: dict, E: int, I: int, with_aq: bool = False) -> 
     r = dict(out=np.empty((T, H)), dX=np.empty((T, H)), dWg=np.empty((E, I, H)), dWu=np.empty((E, I, H)),
              dWd=np.empty((E, H, I)), dS=np.empty((T, K)))
     aq = np.empty((T * K, I)) if with_aq else None
+    dg = np.empty((T * K, I)) if with_dg else None
+    du = np.empty((T * K, I)) if with_dg else None
+    a = np.empty((T * K, I)) if with_dg else None
     _load().orc_layer_mx(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(dY), ptrs, _p(r["out"]), _p(r["dX"]),
-                         _p(r["dWg"]), _p(r["dWu"]), _p(r["dWd"]), _p(r["dS"]), _p(aq) if with_aq else None)
+                         _p(r["dWg"]), _p(r["dWu"]), _p(r["dWd"]), _p(r["dS"]), _p(aq) if with_aq else None,
+                         _p(dg) if with_dg else None, _p(du) if with_dg else None, _p(a) if with_dg else None)
     if with_aq:
         r["aq"] = aq
+    if with_dg:
+        r["dg"], r["du"], r["a"] = dg, du, a
     return r
 
 

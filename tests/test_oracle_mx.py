@@ -8,6 +8,8 @@ H, a and dg/du along I, weights pre-quantised along each GEMM's K).  Pins:
     the BF16 oracle (pinned against torch autograd and finite differences);
   * with quantisation on, the saved a_q is exactly the quantised SwiGLU output of the BF16 oracle
     run on the quantised inputs;
+  * the weight gradients quantise their operands along the routed rows: rebuilt here from the
+    expert-grouped row order (numpy stable sort, zero padding to 128 rows, blocks of 32 rows);
   * the sampled entry points agree with the full one.
 """
 import numpy as np
@@ -128,3 +130,44 @@ def test_mx_mode_is_close_to_bf16():
     assert rel(r["out"], out) < 0.15
     for k in ("dX", "dWg", "dWd", "dS"):
         assert rel(r[k], ref[k]) < 0.2, k
+
+
+def _qr(m):
+    """MX quantise-dequantise along rows: every column of m [nrows, ncols] in blocks of 32 rows."""
+    out = np.empty_like(m)
+    for r0 in range(0, m.shape[0], 32):
+        out[r0:r0 + 32] = oracle.mx_fakequant(np.ascontiguousarray(m[r0:r0 + 32].T)).T
+    return out
+
+
+def test_wgrad_quantised_along_expert_rows():
+    rng = np.random.default_rng(4)
+    T, H, I, E, K = 100, 64, 64, 3, 2
+    ids = rng.integers(0, E - 1, size=(T, K)).astype(np.int32)  # expert E-1 gets no rows
+    s = rng.uniform(0.1, 0.9, size=(T, K)).astype(np.float32)
+    xf = rng.standard_normal((T, H)) * np.where(np.arange(T) < 30, 2.0 ** 8, 1.0)[:, None]
+    x, dY = _bits(xf), _bits(rng.standard_normal((T, H)))
+    Wg, Wu, Wd = (_bits(rng.standard_normal(sh) * 0.05) for sh in ((E, I, H), (E, I, H), (E, H, I)))
+    mx = oracle.mx_weights(Wg, Wu, Wd)
+    r = oracle.layer_mx(ids, s, x, dY, mx, E, I, with_dg=True)
+    xv, dyv = oracle.bf16_to_f64(x), oracle.bf16_to_f64(dY)
+    flat = ids.reshape(-1)
+    for e in range(E):
+        slots = np.flatnonzero(flat == e)  # ascending slot order inside the expert
+        npad = -(-slots.size // 128) * 128
+        def seg(rows):  # noqa: E306
+            m = np.zeros((npad, rows.shape[1]))
+            m[:slots.size] = rows
+            return m
+        qdg, qdu = _qr(seg(r["dg"][slots])), _qr(seg(r["du"][slots]))
+        qsa = _qr(seg(s.reshape(-1)[slots, None].astype(np.float64) * r["a"][slots]))
+        qx, qdy = _qr(seg(xv[slots // K])), _qr(seg(dyv[slots // K]))
+        np.testing.assert_allclose(r["dWg"][e], qdg.T @ qx, rtol=1e-11, atol=1e-12, err_msg=f"dWg {e}")
+        np.testing.assert_allclose(r["dWu"][e], qdu.T @ qx, rtol=1e-11, atol=1e-12, err_msg=f"dWu {e}")
+        np.testing.assert_allclose(r["dWd"][e], qdy.T @ qsa, rtol=1e-11, atol=1e-12, err_msg=f"dWd {e}")
+    assert not np.any(r["dWg"][E - 1]) and not np.any(r["dWd"][E - 1])
+    # the row blocks matter: quantising x along H instead would give a different dWg
+    qx_h = oracle.mx_fakequant(xv)
+    slots = np.flatnonzero(flat == 0)
+    alt = _qr(np.pad(r["dg"][slots], ((0, -slots.size % 128), (0, 0)))).T @ np.pad(qx_h[slots // K], ((0, -slots.size % 128), (0, 0)))
+    assert not np.allclose(alt, r["dWg"][0], rtol=1e-6)
