@@ -246,20 +246,28 @@ MOK_API mok_status mok_build_schedule_noalloc(const mok_config* cfg, const mok_s
                                               const int32_t* topk_ids, const float* topk_weights,
                                               mok_schedule* sched, void* stream);
 
-/* The MXFP8 operand copies that mok_forward / mok_backward write into the workspace, for
- * inspection (tests, debugging); the layer itself needs no call of this.  DEVICE pointers into
- * sched->ws, valid while the workspace is; rows = sched->rpad_max; row r of the expert-grouped
- * layout is routed slot perm[r] (padding rows hold zero codes and scale byte 0):
+/* The MXFP8 operand copies that mok_forward / mok_backward write, for inspection (tests,
+ * debugging); the layer itself needs no call of this.  DEVICE pointers into sched->ws or fwd_ctx
+ * (xr, xrs), valid while those are.  Row r of the expert-grouped layout is routed slot perm[r];
+ * padding rows hold zero codes and scale byte 0.  rows = sched->rpad_max; rcap = rows rounded up
+ * to a multiple of 128.
+ * Quantised along each GEMM's K, row-major (forward and data-gradient GEMMs):
  *   xq  [rows, H]  E4M3 of the gathered x (blocks of 32 along H)      xs  its E8M0 scales
  *   aq  [rows, I]  E4M3 of a = silu(g) u (blocks of 32 along I)         as  its scales
  *   dyq [rows, H]  E4M3 of the gathered dY                            dys its scales
  *   dgq [rows, 2I] E4M3 of [dg | du] (blocks of 32 along I)           dgs its scales
- *   dgdu [rows, 2I] bf16: the dequantised [dg | du] the weight-gradient GEMM reads.
- * Each scale array is atom-tiled for the block-scaled MMA: with kq = (row length) / 128, the scale
- * of row r, k-group g (elements 32g .. 32g+31) sits at byte
+ * Quantised along the routed rows (every column in blocks of 32 rows of the padded layout; the
+ * weight-gradient GEMMs' K), also row-major:
+ *   xr [rcap, H] x, dyr [rcap, H] dY, dgr [rcap, 2I] [dg | du], sar [rcap, I] s * a
+ * Scales are atom-tiled for the block-scaled MMA.  Row-major copies (kq = row length / 128): the
+ * scale of row r, k-group g (elements 32g .. 32g+31) sits at byte
  *   ((r / 128) * kq + g / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + g % 4.
+ * Copies quantised along the rows (column f, row block g = r / 32, kq = rcap / 128, G atoms per
+ * group: 1 for dyrs and dgrs, xr_groups for xrs, sar_groups for sars):
+ *   (((f / (128 G)) * kq + g / 4) * G + (f / 128) % G) * 512 + (f % 32) * 16 + ((f / 32) % 4) * 4
+ *   + g % 4.
  * Returns MOK_ERR_INVALID_ARG unless sched holds a workspace built with precision MOK_MXFP8.
- * The copies hold the values of the last mok_forward (xq, aq) / mok_backward (the rest). */
+ * The copies hold the values of the last mok_forward (xq, aq, xr) / mok_backward (the rest). */
 typedef struct {
   const uint8_t* xq;
   const uint8_t* xs;
@@ -269,11 +277,21 @@ typedef struct {
   const uint8_t* dys;
   const uint8_t* dgq;
   const uint8_t* dgs;
-  const void* dgdu;
+  const uint8_t* xr;
+  const uint8_t* xrs;
+  const uint8_t* dyr;
+  const uint8_t* dyrs;
+  const uint8_t* dgr;
+  const uint8_t* dgrs;
+  const uint8_t* sar;
+  const uint8_t* sars;
   int64_t rows;
+  int64_t rcap;
+  int32_t xr_groups;
+  int32_t sar_groups;
 } mok_mx_operands;
 
-MOK_API mok_status mok_mx_operands_of(const mok_schedule* sched, mok_mx_operands* out);
+MOK_API mok_status mok_mx_operands_of(const mok_schedule* sched, const void* fwd_ctx, mok_mx_operands* out);
 
 /* Copy the schedule's device status word to *out (host pointer) after synchronising the stream.
  * The only call that blocks. */

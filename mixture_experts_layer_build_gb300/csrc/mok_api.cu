@@ -83,9 +83,11 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
   Staging t{};
   t.chunk_hist = c.take<int32_t>(z.nchunks * (z.E + 1));
   t.ybuf = c.take<uint16_t>(z.rpad_max * z.H);
-  t.dyg = c.take<uint16_t>(z.rpad_max * z.H);
-  t.dgdu = c.take<uint16_t>(z.rpad_max * 2 * z.I);
-  t.as = c.take<uint16_t>(z.rpad_max * z.I);
+  if (!z.mx) {
+    t.dyg = c.take<uint16_t>(z.rpad_max * z.H);
+    t.dgdu = c.take<uint16_t>(z.rpad_max * 2 * z.I);
+    t.as = c.take<uint16_t>(z.rpad_max * z.I);
+  }
   t.dspart = c.take<float>(z.rpad_max * (z.I / 128));
   if (z.mx) {
     const int64_t rt = (z.rpad_max + kRowTile - 1) / kRowTile;  // 128-row tiles of the routed rows
@@ -98,6 +100,13 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
     t.dys = c.take<uint8_t>(rt * 128 * (z.H / 32));
     t.dgq = c.take<uint8_t>(z.rpad_max * 2 * z.I);
     t.dgs = c.take<uint8_t>(rt * 128 * (2 * z.I / 32));
+    const int64_t rcap = z.rcap();
+    t.dyr = c.take<uint8_t>(z.H * rcap);
+    t.dyrs = c.take<uint8_t>(z.H * rcap / 32);
+    t.dgr = c.take<uint8_t>(2 * z.I * rcap);
+    t.dgrs = c.take<uint8_t>(2 * z.I * rcap / 32);
+    t.sar = c.take<uint8_t>(z.I * rcap);
+    t.sars = c.take<uint8_t>(z.I * rcap / 32);
     t.sw_gu = c.take<uint8_t>(2 * EI * (z.H / 32));
     t.sw_d = c.take<uint8_t>(EH * (z.I / 32));
     t.swt_d = c.take<uint8_t>(EI * (z.H / 32));
@@ -124,7 +133,12 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
 size_t carve_ctx(const Sizes& z, char* base, Ctx* ctx) {
   Carver c{base};
   Ctx x{};
-  x.xg = c.take<uint16_t>(z.rpad_max * z.H);
+  if (z.mx) {
+    x.xr = c.take<uint8_t>(z.H * z.rcap());
+    x.xrs = c.take<uint8_t>(z.H * z.rcap() / 32);
+  } else {
+    x.xg = c.take<uint16_t>(z.rpad_max * z.H);
+  }
   x.gu = z.mx ? static_cast<void*>(c.take<float>(z.rpad_max * 2 * z.I))
               : static_cast<void*>(c.take<uint16_t>(z.rpad_max * 2 * z.I));
   x.a = c.take<uint16_t>(z.rpad_max * z.I);
@@ -346,7 +360,7 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
                               {w->s_down, nullptr, st.sw_d, EH / (128 * ad), z.I / 128, ad, 0}};
     if (launch_mx_scale_atoms(jobs, 2, s)) return MOK_ERR_CUDA;
     if (launch_gather_rows_mx(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
-                              ctx.xg, st.xq, st.xs, K_GATHER_X, s))
+                              st.xq, st.xs, ctx.xr, ctx.xrs, z.rcap(), z.mx_bn_h() / 128, K_GATHER_X, s))
       return MOK_ERR_CUDA;
   } else if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
                                 ctx.xg, K_GATHER_X, s)) {
@@ -388,7 +402,7 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
                               {w->st_up, nullptr, st.swt_u, EH / (128 * ag), z.I / 128, ag, 0}};
     if (launch_mx_scale_atoms(jobs, 3, s)) return MOK_ERR_CUDA;
     if (launch_gather_rows_mx(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
-                              st.dyg, st.dyq, st.dys, K_GATHER_DY, s))
+                              st.dyq, st.dys, st.dyr, st.dyrs, z.rcap(), 1, K_GATHER_DY, s))
       return MOK_ERR_CUDA;
   } else if (launch_gather_rows(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
                                 st.dyg, K_GATHER_DY, s)) {
@@ -423,10 +437,12 @@ const char* mok_kernel_name(int32_t kind) {
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "?";
 }
 
-mok_status mok_mx_operands_of(const mok_schedule* sched, mok_mx_operands* out) {
+mok_status mok_mx_operands_of(const mok_schedule* sched, const void* fwd_ctx, mok_mx_operands* out) {
   Sizes z;
   Staging st;
-  if (!out || check_sched(sched, &z, &st) != MOK_OK || !z.mx) return MOK_ERR_INVALID_ARG;
+  if (!out || !fwd_ctx || check_sched(sched, &z, &st) != MOK_OK || !z.mx) return MOK_ERR_INVALID_ARG;
+  Ctx ctx;
+  carve_ctx(z, static_cast<char*>(const_cast<void*>(fwd_ctx)), &ctx);
   out->xq = st.xq;
   out->xs = st.xs;
   out->aq = st.aq;
@@ -435,8 +451,18 @@ mok_status mok_mx_operands_of(const mok_schedule* sched, mok_mx_operands* out) {
   out->dys = st.dys;
   out->dgq = st.dgq;
   out->dgs = st.dgs;
-  out->dgdu = st.dgdu;
+  out->xr = ctx.xr;
+  out->xrs = ctx.xrs;
+  out->dyr = st.dyr;
+  out->dyrs = st.dyrs;
+  out->dgr = st.dgr;
+  out->dgrs = st.dgrs;
+  out->sar = st.sar;
+  out->sars = st.sars;
   out->rows = z.rpad_max;
+  out->rcap = z.rcap();
+  out->xr_groups = z.mx_bn_h() / 128;
+  out->sar_groups = z.mx_bn_i() / 128;
   return MOK_OK;
 }
 

@@ -68,6 +68,13 @@ struct GemmArgs {
   int32_t sfb_kq;
   int32_t out_kq;
   uint8_t* out_sf;
+  // MXFP8 weight gradients: operands quantised along the routed rows (row-major, MN-major for the
+  // MMA); sf_kq = 128-row K atoms of the routed-row capacity.  DGRAD1 writes their scales: out_sf2 ([dg | du],
+  // A operand), out_sf3 (s * a, B operand in groups of sa_groups atoms).
+  int32_t sf_kq;
+  int32_t sa_groups;
+  uint8_t* out_sf2;
+  uint8_t* out_sf3;
 };
 
 
@@ -119,7 +126,7 @@ __device__ __forceinline__ int gemm_num_units(const GemmArgs& a) {
 
 // Row-tiled variants: all units of one minibatch tile are consecutive, N tile outer and 128-row
 // block inner, so a weight tile is reused by the tile's blocks while it sits in L2.
-template <int VAR>
+template <int VAR, bool MX>
 __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
   Unit w;
   if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) {
@@ -130,7 +137,7 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
     w.nt = r - w.mt * a.n_tiles;
     const int p0 = __ldg(a.poff + w.e), p1 = __ldg(a.poff + w.e + 1);
     w.row0 = p0;
-    w.kblocks = (p1 - p0) / kBK;
+    w.kblocks = (p1 - p0) / (MX ? 128 : kBK);
   } else {
     const int bq = u / a.n_tiles;
     const int4 mbk = __ldg(reinterpret_cast<const int4*>(a.mblocks) + bq);
@@ -157,7 +164,19 @@ template <int VAR, int BN, bool MX>
 __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
                                           uint32_t sf, uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
                                           const CUtensorMap* tB2) {
-  if constexpr (MX) {
+  if constexpr (MX && (VAR == V_WGRAD_GU || VAR == V_WGRAD_D)) {
+    // weight gradients: A [rows, M features] and B [rows, N features] row-major, i.e. MN-major with
+    // K = the expert's routed rows (128 per block, one 128-byte swizzled row per K index, B in
+    // 128-feature chunks 16 KB apart); scale atoms indexed by the global 128-row block of the rows
+    constexpr uint32_t kSfb = BN * 4;
+    const int k0 = w.row0 + kb * 128;
+    tma_load_2d(sa, tA, bar, w.mt * kBM, k0);
+#pragma unroll
+    for (int j = 0; j < BN / 128; ++j) tma_load_2d(sb + j * 16384, tB, bar, w.nt * BN + j * 128, k0);
+    bulk_load(sf, a.sfa + (static_cast<int64_t>(w.mt) * a.sf_kq + (k0 >> 7)) * 512, 512, bar);
+    bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(w.nt) * a.sf_kq + (k0 >> 7)) * kSfb, kSfb, bar);
+    return;
+  } else if constexpr (MX) {
     constexpr uint32_t kSfb = BN * 4;  // bytes of B scale atoms per K block; sf: A atom, then B's
     const int k0 = kb * 128;
     tma_load_2d(sa, tA, bar, k0, w.row0);
@@ -307,6 +326,42 @@ __device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, i
   }
 }
 
+// MX quantisation of one 32 x 32 block along the rows: lane = row, v[j] = column j (feature f0 + j).
+// Column j's shared exponent comes from the amax over the warp's 32 rows; each lane's 32 codes
+// leave as its row of a 32 x 32 byte tile at (feature f0, row rowc), and lane j writes column j's
+// scale into the atom-tiled array (groups of g atoms, kq atoms along K).
+template <class Stg>
+__device__ __forceinline__ void quant_rows_store(const float (&v)[32], Stg& stg, const CUtensorMap* tm, uint8_t* sf,
+                                                 int rowc, int f0, int kq, int g, int lane) {
+  uint32_t codes[8];
+  uint32_t my_sb = 0;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    uint32_t sbj[2];
+    float sc[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j + k])));
+      int shared = static_cast<int>((m >> 23) & 0xFFu) - 127 - 8;
+      shared = shared < -127 ? -127 : shared;
+      const bool bad = m >= 0x7F800000u;
+      sbj[k] = bad ? 0xFFu : static_cast<uint32_t>(shared + 127);
+      sc[k] = bad ? 0.0f : pow2f(-shared);
+      if (lane == j + k) my_sb = sbj[k];
+    }
+    uint16_t q;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(v[j + 1] * sc[1]), "f"(v[j] * sc[0]));
+    if (sbj[0] == 0xFFu) q = static_cast<uint16_t>((q & 0xFF00u) | 0x7Fu);
+    if (sbj[1] == 0xFFu) q = static_cast<uint16_t>((q & 0x00FFu) | 0x7F00u);
+    if ((j & 2) == 0) codes[j >> 2] = q;
+    else codes[j >> 2] |= static_cast<uint32_t>(q) << 16;
+  }
+  const uint4 ch[2] = {make_uint4(codes[0], codes[1], codes[2], codes[3]),
+                       make_uint4(codes[4], codes[5], codes[6], codes[7])};
+  stg.template put<32>(ch, tm, f0, rowc);
+  sf[sf_atom_offset_g(f0 + lane, rowc >> 5, kq, g)] = static_cast<uint8_t>(my_sb);
+}
+
 // Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab; `h`
 // = the warp's column half in the wide (8-warp) configuration.  tO0 / tO1 / tO2 are the output
 // tensor maps of the variant; `tempty` is released as soon as the last accumulator column has been
@@ -412,9 +467,12 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       stg.template put<128>(ch, tO0, w.nt * BN + c, rowc);
     }
   } else if constexpr (VAR == V_DGRAD1 && MX) {
-    // MXFP8: as below, with g, u read in fp32 and dg, du MX-quantised along I (blocks of 32): their
-    // dequantised values leave in bf16 for the weight gradients, their E4M3 codes and scales for
-    // the second data-gradient GEMM.
+    // MXFP8: dA' = dYq Wd^T (block-scaled), the SwiGLU backward from the forward's fp32 g, u, and
+    // per 32-column chunk:
+    //   dS partial from a's quantisation along I (the context);
+    //   dg, du quantised along I (row-major codes + A atoms) for the second data-gradient GEMM;
+    //   dg, du and s * a (a recomputed in fp32 as the forward did) quantised along this warp's 32
+    //   routed rows, for the weight-gradient GEMMs.
     const int64_t row = w.row0 + q * 32 + lane;
     const int64_t I = a.I;
     const int i0 = w.nt * BN;
@@ -439,43 +497,38 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       if (c + 32 >= BN) release_acc(tempty);
       const float* g = reinterpret_cast<const float*>(g4);
       const float* u = reinterpret_cast<const float*>(u4);
-      float dg[32], du[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float da = s * __uint_as_float(rv[i]);
-        const float sg = sigmoid_f(g[i]);
-        dg[i] = da * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
-        du[i] = da * g[i] * sg;
-      }
-      uint4 ch[4];
-      uint32_t codes[8];
-      const uint32_t sg_byte = mx_quant32(dg, codes);
-      ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      stg.template put<32>(ch, tO2, i0 + c, rowc);
-      pack_bf16<32>(dg, ch);
-      stg.template put<64>(ch, tO0, i0 + c, rowc);
-      const uint32_t su_byte = mx_quant32(du, codes);
-      ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-      ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
-      stg.template put<32>(ch, tO2, a.I + i0 + c, rowc);
-      pack_bf16<32>(du, ch);
-      stg.template put<64>(ch, tO0, a.I + i0 + c, rowc);
-      a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sg_byte);
-      a.out_sf[sf_atom_offset(row, (a.I + i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(su_byte);
-      float sa[32];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         float a8[8];
         unpack8(ldg_v4(av + i0 + c + 8 * j), a8);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          part = fmaf(__uint_as_float(rv[8 * j + k]), a8[k], part);
-          sa[8 * j + k] = s * a8[k];
-        }
+        for (int k = 0; k < 8; ++k) part = fmaf(__uint_as_float(rv[8 * j + k]), a8[k], part);
       }
-      pack_bf16<32>(sa, ch);
-      stg.template put<64>(ch, tO1, i0 + c, rowc);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = s * (silu_f(g[i]) * u[i]);
+      quant_rows_store(v, stg, tO1, a.out_sf3, rowc, i0 + c, a.sf_kq, a.sa_groups, lane);
+      uint4 ch[2];
+      uint32_t codes[8];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float sg = sigmoid_f(g[i]);
+        v[i] = s * __uint_as_float(rv[i]) * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
+      }
+      quant_rows_store(v, stg, tO0, a.out_sf2, rowc, i0 + c, a.sf_kq, 1, lane);
+      uint32_t sb = mx_quant32(v, codes);
+      ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      stg.template put<32>(ch, tO2, i0 + c, rowc);
+      a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sb);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = s * __uint_as_float(rv[i]) * g[i] * sigmoid_f(g[i]);
+      quant_rows_store(v, stg, tO0, a.out_sf2, rowc, a.I + i0 + c, a.sf_kq, 1, lane);
+      sb = mx_quant32(v, codes);
+      ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+      ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+      stg.template put<32>(ch, tO2, a.I + i0 + c, rowc);
+      a.out_sf[sf_atom_offset(row, (a.I + i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sb);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else if constexpr (VAR == V_DGRAD1) {
@@ -522,6 +575,39 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       stg.template put<64>(csa, tO1, i0 + c, rowc);
     }
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
+  } else if constexpr ((VAR == V_WGRAD_GU || VAR == V_WGRAD_D) && MX && BN == 256) {
+    // wide MXFP8 weight-gradient tile: this warp's 128 fp32 columns go to registers, the accumulator
+    // is released, then the rows leave in 16-column (64-byte) tiles.  Experts without rows: zeros.
+    const bool empty = w.kblocks == 0;
+    const int m0 = w.mt * kBM + q * 32;
+    const CUtensorMap* tm;
+    int r0;
+    if constexpr (VAR == V_WGRAD_GU) {
+      tm = m0 < a.I ? tO0 : tO1;
+      r0 = w.e * a.I + (m0 < a.I ? m0 : m0 - a.I);
+    } else {
+      tm = tO0;
+      r0 = w.e * a.H + m0;
+    }
+    uint32_t r[128];
+    if (!empty) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tmem_ld_32x32b_x32(taddr + 128 * h + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * j));
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 128; ++i) r[i] = 0u;
+    }
+    release_acc(tempty);
+#pragma unroll
+    for (int c = 0; c < 128; c += 16) {
+      uint4 ch[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ch[j] = make_uint4(r[c + 4 * j], r[c + 4 * j + 1], r[c + 4 * j + 2], r[c + 4 * j + 3]);
+      stg.template put<64>(ch, tm, w.nt * BN + 128 * h + c, r0);
+    }
   } else {  // weight gradients, fp32 out, 32-column tiles
     const bool empty = w.kblocks == 0;
     const int m0 = w.mt * kBM + q * 32;  // first of this warp's 32 output rows
@@ -573,8 +659,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
                 const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
                 const GemmArgs args) {
   using C = GemmCfg<VAR, BN, MX>;
-  static_assert(!MX || VAR <= V_DGRAD2, "weight gradients run on the bf16 path");
-  constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);
+  constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) && !MX;
   constexpr bool kBmn = (VAR >= V_DGRAD1) && !MX;
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
   constexpr int S = C::kStages;
@@ -636,7 +721,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
       for (int s = 0; s < S; ++s) last_parity[s] = -1;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const Unit w = gemm_decode<VAR>(args, u);
+        const Unit w = gemm_decode<VAR, MX>(args, u);
         for (int kb = 0; kb < w.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
             ok = false;
@@ -666,7 +751,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const Unit w = gemm_decode<VAR>(args, u);
+        const Unit w = gemm_decode<VAR, MX>(args, u);
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -686,10 +771,14 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j)  // B row n's word lands in column n / 32
               tmem_cp_sf_atom(tsf + 4 + 4 * j, sdesc_plain(sf + 512 + 512 * j));
+            constexpr bool kMn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);  // both operands MN-major
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)  // K = 32 e4m3 (32 bytes) per instruction; k-group ks
-              umma_mxf8(d_tmem, sdesc_sw128(sa + ks * 32, 16, 1024), sdesc_sw128(sb + ks * 32, 16, 1024),
-                        idesc_mx(kBM, BN, static_cast<uint32_t>(ks)), (kb | ks) != 0 ? 1u : 0u, tsf, tsf + 4);
+            for (int ks = 0; ks < 4; ++ks) {  // K = 32 e4m3 per instruction; k-group ks
+              const uint64_t ad = kMn ? sdesc_sw128(sa + ks * 4096, 16384, 1024) : sdesc_sw128(sa + ks * 32, 16, 1024);
+              const uint64_t bd = kMn ? sdesc_sw128(sb + ks * 4096, 16384, 1024) : sdesc_sw128(sb + ks * 32, 16, 1024);
+              umma_mxf8(d_tmem, ad, bd, idesc_mx(kBM, BN, static_cast<uint32_t>(ks), kMn), (kb | ks) != 0 ? 1u : 0u,
+                        tsf, tsf + 4);
+            }
           } else {
 #pragma unroll
             for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
@@ -727,7 +816,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const Unit w = gemm_decode<VAR>(args, u);
+      const Unit w = gemm_decode<VAR, MX>(args, u);
       Dg1Chunk pre;
       if constexpr (VAR == V_DGRAD1 && !MX) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);  // before the wait
       int ok = 0;

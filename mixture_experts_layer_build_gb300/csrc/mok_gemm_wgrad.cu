@@ -1,12 +1,65 @@
-// mok_gemm_wgrad.cu -- weight-gradient expert GEMMs.  Each output tile of dW is reduced by one CTA
+// mok_gemm_wgrad.cu -- weight-gradient expert GEMMs (BF16, and block-scaled E4M3 in MXFP8 mode).  Each output tile of dW is reduced by one CTA
 // over its expert's rows in ascending row order (K = the expert's padded rows; padding rows are
 // zero), so the reduction order is fixed and no atomics are used.  Experts without rows get zeros.
 #include "mok_gemm.cuh"
 
 namespace mok {
 
+// MXFP8: block-scaled E4M3 on operands quantised along the routed rows (K), read MN-major from their
+// row-major copies: [dWg ; dWu]_e = [dg | du]_e^T x_e and dWd_e = dY_e^T (s a)_e over e's padded rows.
+static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
+                                 const mok_grads& g, int num_ctas, cudaStream_t stream) {
+  CUtensorMap tA, tB, tO0, tO1;
+  GemmArgs a{};
+  a.poff = s.poff;
+  a.E = z.E;
+  a.I = z.I;
+  a.H = z.H;
+  a.status = s.status;
+  a.sf_kq = static_cast<int32_t>(z.kq_rows());
+  const uint64_t rcap = static_cast<uint64_t>(z.rcap());
+  auto out_map = [&](CUtensorMap* m, float* p, uint64_t inner, uint64_t outer, int bn) {
+    return bn == 256 ? make_tmap_f32_sw64(m, p, inner, outer, 16, 32) : make_tmap_f32(m, p, inner, outer, 32, 32);
+  };
+  {  // [dWg ; dWu]_e: M = 2I (A = [dg | du]^T), N = H (B = x^T)
+    const int BN = z.mx_bn_h();
+    if (!make_tmap_u8(&tA, st.dgr, 2 * static_cast<uint64_t>(z.I), rcap, 128, 128, 128)) return -1;
+    if (!make_tmap_u8(&tB, ctx.xr, z.H, rcap, 128, 128, 128)) return -1;
+    a.m_tiles = 2 * z.I / kBM;
+    a.n_tiles = z.H / BN;
+    a.sfa = st.dgrs;
+    a.sfb = ctx.xrs;
+    a.out0 = g.dw_gate;
+    a.out1 = g.dw_up;
+    if (!out_map(&tO0, g.dw_gate, z.H, static_cast<uint64_t>(z.E) * z.I, BN)) return -1;
+    if (!out_map(&tO1, g.dw_up, z.H, static_cast<uint64_t>(z.E) * z.I, BN)) return -1;
+    const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
+    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
+                             : launch_gemm<V_WGRAD_GU, 128, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
+    if (rc) return rc;
+  }
+  {  // dWd_e: M = H (A = dY^T), N = I (B = (s a)^T)
+    const int BN = z.mx_bn_i();
+    if (!make_tmap_u8(&tA, st.dyr, z.H, rcap, 128, 128, 128)) return -1;
+    if (!make_tmap_u8(&tB, st.sar, z.I, rcap, 128, 128, 128)) return -1;
+    a.m_tiles = z.H / kBM;
+    a.n_tiles = z.I / BN;
+    a.sfa = st.dyrs;
+    a.sfb = st.sars;
+    a.out0 = g.dw_down;
+    a.out1 = nullptr;
+    if (!out_map(&tO0, g.dw_down, z.I, static_cast<uint64_t>(z.E) * z.H, BN)) return -1;
+    const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
+    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    return BN == 256 ? launch_gemm<V_WGRAD_D, 256, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
+                     : launch_gemm<V_WGRAD_D, 128, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
+  }
+}
+
 int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                        const mok_grads& g, int num_ctas, cudaStream_t stream) {
+  if (z.mx) return launch_wgrad_gemms_mx(z, s, ctx, st, g, num_ctas, stream);
   CUtensorMap tA, tB, tO0, tO1;
   GemmArgs a{};
   a.poff = s.poff;

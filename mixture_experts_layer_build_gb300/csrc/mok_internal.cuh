@@ -17,14 +17,19 @@ struct Sizes {
   int64_t T, R, rpad_max, tiles_max, mblocks_max, nchunks;
   int32_t H, I, E, K, mb, MB;
   bool mx;  // MXFP8 mode
-  // MXFP8 tile width (N) of the GEMMs whose N runs over H: 256 when H allows it
+  // MXFP8 tile width (N) of the GEMMs whose N runs over H (or I): 256 when the size allows it
   int32_t mx_bn_h() const { return H % 256 == 0 ? 256 : 128; }
+  int32_t mx_bn_i() const { return I % 256 == 0 ? 256 : 128; }
+  // MXFP8 weight gradients: routed-row capacity in 128-row K atoms, and in rows
+  int64_t kq_rows() const { return (rpad_max + kRowTile - 1) / kRowTile; }
+  int64_t rcap() const { return kq_rows() * kRowTile; }
 };
 bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s);
 
 // Staging buffers inside the workspace (after the schedule tables) and the forward context.
 struct Staging {
   uint16_t* ybuf;    // [rpad_max, H] bf16: expert outputs y (forward), then dX per row (backward)
+  // BF16 mode only
   uint16_t* dyg;     // [rpad_max, H] bf16: gathered upstream gradient rows
   uint16_t* dgdu;    // [rpad_max, 2I] bf16: [dg | du]
   uint16_t* as;      // [rpad_max, I] bf16: s * a
@@ -40,6 +45,15 @@ struct Staging {
   uint8_t* dys;      //   scales: rtiles x H/128 atoms
   uint8_t* dgq;      // [rpad_max, 2I] [dg | du], quantised along I
   uint8_t* dgs;      //   scales: rtiles x 2I/128 atoms
+  // weight-gradient operands, quantised along the routed rows (32-row blocks of the padded layout),
+  // row-major [rcap, features] (MN-major operands of the wgrad GEMMs); scales in sf_atom_offset_g
+  // layout (row f = feature, k-group = row / 32, kq_rows atoms along K)
+  uint8_t* dyr;      // [rcap, H]  dY          scales dyrs: A operand (G = 1)
+  uint8_t* dyrs;
+  uint8_t* dgr;      // [rcap, 2I] [dg | du]   scales dgrs: A operand (G = 1)
+  uint8_t* dgrs;
+  uint8_t* sar;      // [rcap, I]  s * a       scales sars: B operand (G = mx_bn_i / 128)
+  uint8_t* sars;
   // the caller's weight scales re-tiled into atom groups matching the B tiles (per call)
   uint8_t* sw_gu;    // s_gate, s_up: per 128 rows of I, the gate atom then the up atom
   uint8_t* sw_d;     // s_down: groups of BN_down / 128 atoms
@@ -48,10 +62,12 @@ struct Staging {
   uint8_t* swt_u;    // st_up: same
 };
 struct Ctx {
-  uint16_t* xg;      // [rpad_max, H] bf16: gathered x rows (zero on padding rows)
+  uint16_t* xg;      // BF16 mode: [rpad_max, H] bf16 gathered x rows (zero on padding rows)
+  uint8_t* xr;       // MXFP8 mode: [rcap, H] x quantised along the routed rows
+  uint8_t* xrs;      //   scales: B operand of the gate/up weight gradient (G = mx_bn_h / 128)
   void* gu;          // [rpad_max, 2I]: [g | u], bf16 (BF16 mode) or fp32 (MXFP8 mode, whose
-                     // backward re-quantises dg, du and needs g, u unrounded)
-  uint16_t* a;       // [rpad_max, I] bf16: silu(g) * u
+                     // backward re-quantises dg, du and s * a and needs g, u unrounded)
+  uint16_t* a;       // [rpad_max, I] bf16: silu(g) * u (MXFP8: its quantisation along I)
 };
 size_t carve_workspace(const Sizes& z, char* base, mok_schedule* sched, Staging* st);  // returns bytes
 size_t carve_ctx(const Sizes& z, char* base, Ctx* ctx);
@@ -86,10 +102,11 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
                     cudaStream_t stream);
 int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                        int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
-// MX gather: dst = bf16 dequantised rows, dst_q = E4M3 codes, dst_sf = atom-tiled scales.
+// MX gather of 32-row blocks: dst_q / dst_sf = rows quantised along H (A-operand atoms); dstR_q /
+// dstR_sf = the same rows quantised along the rows (atoms grouped gT at a time).  Both row-major.
 int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                          int32_t H, uint16_t* dst, uint8_t* dst_q, uint8_t* dst_sf, int kind,
-                          cudaStream_t stream);
+                          int32_t H, uint8_t* dst_q, uint8_t* dst_sf, uint8_t* dstR_q, uint8_t* dstR_sf,
+                          int64_t rcap, int gT, int kind, cudaStream_t stream);
 // Re-tile row-major E8M0 scales [rows, 4 kq] into groups of `atoms` 512-byte atoms (up to three
 // jobs per launch): group g, K atom q holds `atoms` consecutive atoms at ((g * kq + q) * atoms + j)
 // * 512.  One source: atom j covers rows (g * atoms + j) * 128 ...; two sources (atoms = 2): atom

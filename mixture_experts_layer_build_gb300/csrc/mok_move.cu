@@ -226,80 +226,78 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
   }
 }
 
-// Gather with MX quantisation of each row (blocks of 32 along the row), bit-exact with
-// mxfp8_quantize_kernel: dst_q[row] = E4M3 codes, dst_sf = E8M0 scales (atom-tiled, kq atoms per
-// 128-row tile), dst[row] = the dequantised values in bf16 (exact: E4M3 x 2^k fits bf16 down to
-// 2^-133).  Padding rows (row_token < 0) get zero codes, zero values and scale byte 0.
-// One warp per row; lane l handles the row's 32-element blocks l, l + 32, ..., two at a time so
-// that eight 16-byte loads are in flight per lane; outputs are written evict-first.
-__device__ __forceinline__ void mx_block_out(const uint4 (&v)[4], uint4* d, uint4* dq, uint8_t* sf) {
-  float o[32];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o[8 * i] = bf16_lo(v[i].x);
-    o[8 * i + 1] = bf16_hi(v[i].x);
-    o[8 * i + 2] = bf16_lo(v[i].y);
-    o[8 * i + 3] = bf16_hi(v[i].y);
-    o[8 * i + 4] = bf16_lo(v[i].z);
-    o[8 * i + 5] = bf16_hi(v[i].z);
-    o[8 * i + 6] = bf16_lo(v[i].w);
-    o[8 * i + 7] = bf16_hi(v[i].w);
-  }
-  uint32_t codes[8];
-  *sf = static_cast<uint8_t>(mx_quant32(o, codes));
-  __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-  __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    __stcs(d + i, make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
-                             pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7])));
-}
+// MX gather, one CTA per (32-row block of the expert-grouped layout, 128 columns).  The 32 gathered
+// rows are staged in shared memory as bf16 (zero for padding rows); each thread then quantises one
+// 32-column block of one row -- along H: E4M3 codes for the forward / data-gradient GEMMs,
+// A-operand atoms -- and one column over the 32 rows -- along the routed rows: codes for the
+// weight-gradient GEMM, atoms grouped gT at a time.  The column codes are collected in shared
+// memory and leave row-major like the others.  The rounding is bit-exact with
+// mxfp8_quantize_kernel (shared exponent from amax, E4M3 round-to-nearest-even, saturating).
+// Blocks of 32 rows never straddle two experts: segments start at multiples of 128.
+constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
+constexpr int kGmxCodeStride = 128 + 16;  // bytes per staged code row
 
-__global__ void __launch_bounds__(kMoveThreads) gather_rows_mx_kernel(const uint4* __restrict__ src,
-                                                                     const int32_t* __restrict__ row_token,
-                                                                     const int32_t* __restrict__ meta,
-                                                                     int64_t vecs, uint4* __restrict__ dst,
-                                                                     uint4* __restrict__ dst_q,
-                                                                     uint8_t* __restrict__ dst_sf, int kq) {
-  const int64_t rpad = meta[0];
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
-  const int64_t nblk = vecs / 4;  // 32-element blocks per row
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); row < rpad;
-       row += nwarps) {
-    const int t = row_token[row];
-    uint4* d = dst + row * vecs;
-    uint4* dq = dst_q + row * (vecs / 2);
-    if (t < 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int64_t b = lane; b < nblk; b += 32) {
+__global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint16_t* __restrict__ src,
+                                                            const int32_t* __restrict__ row_token,
+                                                            const int32_t* __restrict__ meta, int32_t H,
+                                                            uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf,
+                                                            uint8_t* __restrict__ dstR_q,
+                                                            uint8_t* __restrict__ dstR_sf, int64_t rcap, int gT) {
+  __shared__ __align__(16) uint8_t tile[32 * kGmxStride];
+  __shared__ __align__(16) uint8_t ctile[32 * kGmxCodeStride];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
+  if (r0 >= meta[0]) return;
+  const int c0 = static_cast<int>(blockIdx.y) * 128;
+  const int t = threadIdx.x;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d[b * 4 + i] = z;
-        dq[b * 2] = z;
-        dq[b * 2 + 1] = z;
-        dst_sf[sf_atom_offset(row, static_cast<int>(b), kq)] = 0;
-      }
-      continue;
-    }
-    const uint4* s = src + static_cast<int64_t>(t) * vecs;
-    int64_t b = lane;
-    for (; b + 32 < nblk; b += 64) {
-      uint4 v0[4], v1[4];
+  for (int i = 0; i < 4; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 8 i
+    const int r = t / 16 + 8 * i, v = t % 16;
+    const int tok = __ldg(row_token + r0 + r);
+    const uint4 val = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(tok) * H + c0) + v)
+                               : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(tile + r * kGmxStride + v * 16) = val;
+  }
+  __syncthreads();
+  {  // along H: row t / 4, columns c0 + 32 (t % 4) ... + 31
+    const int r = t / 4, b = t % 4;
+    float o[32];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v0[i] = __ldg(s + b * 4 + i);
-        v1[i] = __ldg(s + (b + 32) * 4 + i);
-      }
-      mx_block_out(v0, d + b * 4, dq + b * 2, dst_sf + sf_atom_offset(row, static_cast<int>(b), kq));
-      mx_block_out(v1, d + (b + 32) * 4, dq + (b + 32) * 2,
-                   dst_sf + sf_atom_offset(row, static_cast<int>(b + 32), kq));
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + r * kGmxStride + b * 64 + 16 * i);
+      o[8 * i] = bf16_lo(v.x);
+      o[8 * i + 1] = bf16_hi(v.x);
+      o[8 * i + 2] = bf16_lo(v.y);
+      o[8 * i + 3] = bf16_hi(v.y);
+      o[8 * i + 4] = bf16_lo(v.z);
+      o[8 * i + 5] = bf16_hi(v.z);
+      o[8 * i + 6] = bf16_lo(v.w);
+      o[8 * i + 7] = bf16_hi(v.w);
     }
-    if (b < nblk) {
-      uint4 v0[4];
+    uint32_t codes[8];
+    const uint32_t sb = mx_quant32(o, codes);
+    uint4* dq = reinterpret_cast<uint4*>(dst_q + (r0 + r) * H + c0 + 32 * b);
+    __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+    __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+    dst_sf[sf_atom_offset(r0 + r, (c0 >> 5) + b, H / 128)] = static_cast<uint8_t>(sb);
+  }
+  {  // along the rows: column c0 + t over the 32 rows; codes into the shared code tile
+    float o[32];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v0[i] = __ldg(s + b * 4 + i);
-      mx_block_out(v0, d + b * 4, dq + b * 2, dst_sf + sf_atom_offset(row, static_cast<int>(b), kq));
-    }
+    for (int r = 0; r < 32; ++r)
+      o[r] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + r * kGmxStride + 2 * t))
+                             << 16);
+    uint32_t codes[8];
+    const uint32_t sb = mx_quant32(o, codes);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) ctile[r * kGmxCodeStride + t] = static_cast<uint8_t>(codes[r >> 2] >> (8 * (r & 3)));
+    dstR_sf[sf_atom_offset_g(c0 + t, r0 >> 5, rcap / 128, gT)] = static_cast<uint8_t>(sb);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // 32 code rows of 128 bytes: thread t stores vector t % 8 of rows t / 8 + 16 i
+    const int r = t / 8 + 16 * i, v = t % 8;
+    __stcs(reinterpret_cast<uint4*>(dstR_q + (r0 + r) * H + c0) + v,
+           *reinterpret_cast<const uint4*>(ctile + r * kGmxCodeStride + v * 16));
   }
 }
 
@@ -350,14 +348,12 @@ int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int3
 }
 
 int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                          int32_t H, uint16_t* dst, uint8_t* dst_q, uint8_t* dst_sf, int kind,
-                          cudaStream_t stream) {
+                          int32_t H, uint8_t* dst_q, uint8_t* dst_sf, uint8_t* dstR_q, uint8_t* dstR_sf,
+                          int64_t rcap, int gT, int kind, cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
-  const int grid = grid_for(rpad_max, kMoveThreads / 32);
+  const dim3 grid(static_cast<unsigned>((rpad_max + 31) / 32), static_cast<unsigned>(H / 128));
   trace_begin(stream, kind);
-  gather_rows_mx_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), row_token, meta,
-                                                           H / 8, reinterpret_cast<uint4*>(dst),
-                                                           reinterpret_cast<uint4*>(dst_q), dst_sf, H / 128);
+  gather_rows_mx_kernel<<<grid, 128, 0, stream>>>(src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

@@ -124,6 +124,9 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+__device__ __forceinline__ void st_shared_u8(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -232,11 +235,11 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 A and B (format 0), K-major
-// both, fp32 D, UE8M0 scales (bit 23); bits 4-5 / 29-30 pick the byte (k-group) of the B / A scale
-// words that this K = 32 step uses.
-__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t kgroup) {
-  return (kgroup << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 A and B (format 0), fp32
+// D, UE8M0 scales (bit 23); bits 4-5 / 29-30 pick the byte (k-group) of the B / A scale words that
+// this K = 32 step uses; bits 15 / 16: A / B MN-major (mn = both).
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t kgroup, bool mn = false) {
+  return (kgroup << 4) | (mn ? (3u << 15) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>(M >> 4) << 24) | (kgroup << 29);
 }
 
@@ -332,6 +335,14 @@ __device__ __forceinline__ uint32_t mx_quant32(float* v, uint32_t (&codes)[8]) {
 // puts them into TMEM for the block-scaled MMA.
 __host__ __device__ __forceinline__ int64_t sf_atom_offset(int64_t row, int kg, int kq) {
   return ((row >> 7) * kq + (kg >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kg & 3);
+}
+
+// Scale offset in an atom-tiled array whose rows are grouped G atoms at a time (G = 1 for an A
+// operand, BN / 128 for a B operand read in BN-row tiles): row f (the operand's M or N index),
+// k-group kg (K / 32), kq atoms per 128-row tile along K.  G = 1 equals sf_atom_offset.
+__host__ __device__ __forceinline__ int64_t sf_atom_offset_g(int64_t f, int64_t kg, int64_t kq, int g) {
+  return (((f / (128 * g)) * kq + (kg >> 2)) * g + (f >> 7) % g) * 512 + (f & 31) * 16 + ((f >> 5) & 3) * 4 +
+         (kg & 3);
 }
 
 // bf16 helpers (round to nearest even, no special-value surprises for finite inputs)

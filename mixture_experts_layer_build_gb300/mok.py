@@ -109,12 +109,14 @@ _lib.mok_read_device_status.restype = ctypes.c_int
 _lib.mok_read_device_status.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(ctypes.c_uint32), _P]
 
 class mok_mx_operands(ctypes.Structure):
-    _fields_ = [(k, _P) for k in ("xq", "xs", "aq", "as_", "dyq", "dys", "dgq", "dgs", "dgdu")] + \
-        [("rows", ctypes.c_int64)]
+    _fields_ = [(k, _P) for k in ("xq", "xs", "aq", "as_", "dyq", "dys", "dgq", "dgs", "xr", "xrs", "dyr", "dyrs",
+                                  "dgr", "dgrs", "sar", "sars")] + \
+        [("rows", ctypes.c_int64), ("rcap", ctypes.c_int64), ("xr_groups", ctypes.c_int32),
+         ("sar_groups", ctypes.c_int32)]
 
 
 _lib.mok_mx_operands_of.restype = ctypes.c_int
-_lib.mok_mx_operands_of.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(mok_mx_operands)]
+_lib.mok_mx_operands_of.argtypes = [ctypes.POINTER(mok_schedule), _P, ctypes.POINTER(mok_mx_operands)]
 
 EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
             "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status", "mok_set_trace",
@@ -214,23 +216,31 @@ class Schedule:
                     row_token=self._view("row_token", self.c.rpad_max))
 
 
-    def mx_operands(self) -> dict:
-        """Device views of the MXFP8 operand copies in the workspace (mok_mx_operands_of): E4M3 codes
-        [rows, n] and their atom-tiled E8M0 scale arrays (flat uint8), plus the bf16 [dg | du]."""
+    def mx_operands(self, fwd_ctx: torch.Tensor) -> dict:
+        """Device views of the MXFP8 operand copies (mok_mx_operands_of): E4M3 codes ([rows, n]
+        quantised along each row, [rcap, n] quantised along the rows) and their atom-tiled E8M0
+        scale arrays (flat uint8), plus the layout numbers rows, rcap, xr_groups, sar_groups."""
         m = mok_mx_operands()
-        _check(_lib.mok_mx_operands_of(ctypes.byref(self.c), ctypes.byref(m)), "mok_mx_operands_of")
-        H, I, rows = self.c.shape.H, self.c.shape.I, m.rows
+        _check(_lib.mok_mx_operands_of(ctypes.byref(self.c), _ptr(fwd_ctx, None, "fwd_ctx"), ctypes.byref(m)),
+               "mok_mx_operands_of")
+        H, I, rows, rcap = self.c.shape.H, self.c.shape.I, m.rows, m.rcap
         rt = (rows + 127) // 128
-        wsb = self.ws.view(torch.uint8)
-        base = self.ws.data_ptr()
 
         def v(ptr, n):
-            return wsb[ptr - base:ptr - base + n]
+            for buf in (self.ws, fwd_ctx):
+                base = buf.data_ptr()
+                if base <= ptr < base + buf.numel() * buf.element_size():
+                    return buf.view(torch.uint8)[ptr - base:ptr - base + n]
+            raise ValueError("pointer outside the workspace and the context")
         return dict(xq=v(m.xq, rows * H).view(rows, H), xs=v(m.xs, rt * 128 * (H // 32)),
                     aq=v(m.aq, rows * I).view(rows, I), as_=v(m.as_, rt * 128 * (I // 32)),
                     dyq=v(m.dyq, rows * H).view(rows, H), dys=v(m.dys, rt * 128 * (H // 32)),
                     dgq=v(m.dgq, rows * 2 * I).view(rows, 2 * I), dgs=v(m.dgs, rt * 128 * (2 * I // 32)),
-                    dgdu=v(m.dgdu, rows * 2 * I * 2).view(torch.bfloat16).view(rows, 2 * I))
+                    xr=v(m.xr, H * rcap).view(rcap, H), xrs=v(m.xrs, H * rcap // 32),
+                    dyr=v(m.dyr, H * rcap).view(rcap, H), dyrs=v(m.dyrs, H * rcap // 32),
+                    dgr=v(m.dgr, 2 * I * rcap).view(rcap, 2 * I), dgrs=v(m.dgrs, 2 * I * rcap // 32),
+                    sar=v(m.sar, I * rcap).view(rcap, I), sars=v(m.sars, I * rcap // 32),
+                    rows=rows, rcap=rcap, xr_groups=m.xr_groups, sar_groups=m.sar_groups)
 
 
 def alloc_workspace(cfg: mok_config, shape: mok_shape, device="cuda") -> torch.Tensor:

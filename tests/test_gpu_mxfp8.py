@@ -3,7 +3,8 @@
 Tolerance (MXFP8): max|gpu - oracle| / max|oracle| <= 4e-2 per output tensor.  The pre-quantised
 weight bytes the GPU consumes come from mok_mxfp8_quantize and must equal the oracle's own
 quantisation bit for bit; activations are quantised inside the library (x, dY in the gather,
-a, dg, du in the GEMM epilogues) and the oracle mirrors those points in fp64.
+along H and along the routed rows; a, dg, du, s*a in the GEMM epilogues) and the oracle mirrors
+those points in fp64.
 """
 import numpy as np
 import pytest
@@ -110,7 +111,7 @@ def test_mxfp8_ep64_shard_sampled_parity_and_determinism(mok):
 
 def _untile_scales(atoms, rows, kg):
     """Row-major [rows, kg] scale bytes from an atom-tiled array (the layout mok.h documents for
-    mok_mx_operands_of)."""
+    mok_mx_operands_of's row-major copies)."""
     kq = kg // 4
     r = np.arange(rows)[:, None]
     g = np.arange(kg)[None, :]
@@ -118,17 +119,51 @@ def _untile_scales(atoms, rows, kg):
     return atoms[off]
 
 
+def _untile_scales_t(atoms, nf, rcap, groups):
+    """[nf, rcap / 32] scale bytes of a copy quantised along the rows (column f, row block g; atoms
+    grouped `groups` at a time), from the layout mok.h documents."""
+    kq = rcap // 128
+    f = np.arange(nf)[:, None]
+    g = np.arange(rcap // 32)[None, :]
+    off = (((f // (128 * groups)) * kq + g // 4) * groups + (f // 128) % groups) * 512 + (f % 32) * 16 \
+        + ((f // 32) % 4) * 4 + g % 4
+    return atoms[off]
+
+
+def _padded_rows(bits_tc, row_token, rpad):
+    """bf16 bit patterns of the expert-grouped padded layout (zero rows for padding)."""
+    rt = row_token[:rpad]
+    out = np.zeros((rpad, bits_tc.shape[1]), np.uint16)
+    out[rt >= 0] = bits_tc[rt[rt >= 0]]
+    return out
+
+
+def _rows_quantised(bits_pad):
+    """Oracle bytes of the quantisation along rows (32-row blocks), column-major: codes [n, rpad],
+    scales [n, rpad / 32]."""
+    rpad, n = bits_pad.shape
+    q = np.zeros((n, rpad), np.uint8)
+    sc = np.zeros((n, rpad // 32), np.uint8)
+    for b in range(rpad // 32):
+        qb, sb = oracle.mxfp8_quantize(np.ascontiguousarray(bits_pad[32 * b:32 * b + 32].T))
+        q[:, 32 * b:32 * b + 32] = qb
+        sc[:, b] = sb[:, 0]
+    return q, sc
+
+
 def _ctx_a(layer, w):
-    """bf16 view of the forward context's a = silu(g) u (MXFP8 context: xg bf16 | g,u fp32 | a)."""
+    """bf16 view of the forward context's a (MXFP8 context: xr | its scales | g,u fp32 | a)."""
     up = lambda n: (n + 255) // 256 * 256  # noqa: E731
     rows = layer.sched.c.rpad_max
-    off = up(rows * w.H * 2) + up(rows * 2 * w.I * 4)
+    rcap = (rows + 127) // 128 * 128
+    off = up(w.H * rcap) + up(w.H * rcap // 32) + up(rows * 2 * w.I * 4)
     return layer.ctx.view(torch.uint8)[off:off + rows * w.I * 2].view(torch.bfloat16).view(rows, w.I)
 
 
 def test_mxfp8_gather_quantises_x_bit_exactly(mok):
-    """The quantise-on-gather of x equals the oracle's MX quantisation of x, bit for bit: the bf16
-    dequantised rows, the E4M3 codes and the atom-tiled E8M0 scales."""
+    """The quantising gather of x equals the oracle's MX quantisation bit for bit, along H (the
+    row-major codes and scales) and along the 32-row blocks of the padded layout (the
+    codes and scales the weight gradient reads)."""
     w = inputs.custom(T=200, H=512, I=128, E=4, K=2)
     d = inputs.make(w, seed=4)
     x = d["x"].clone()
@@ -142,30 +177,35 @@ def test_mxfp8_gather_quantises_x_bit_exactly(mok):
     layer.schedule(d["topk_ids"].cuda(), d["topk_weights"].cuda())
     layer.forward(x.cuda(), mok.weights_struct(mx=mx_gpu))
     torch.cuda.synchronize()
-    inv = layer.sched.tables()["inv"].cpu().numpy().astype(np.int64)
-    xg = layer.ctx.view(torch.uint8)[: layer.sched.c.rpad_max * w.H * 2].view(torch.bfloat16).view(-1, w.H)
-    got = to_f64(xg)[inv]
-    ref = oracle.mx_fakequant(oracle.bf16_to_f64(inputs.bits(x)))[np.arange(w.R) // w.K]
-    assert np.array_equal(got, ref)
+    t = layer.sched.tables()
+    inv = t["inv"].cpu().numpy().astype(np.int64)
+    rpad = int(t["meta"][0])
+    row_token = t["row_token"].cpu().numpy()
     q_ref, s_ref = oracle.mxfp8_quantize(inputs.bits(x))
-    ops = layer.sched.mx_operands()
+    ops = layer.sched.mx_operands(layer.ctx)
     xq = ops["xq"].cpu().numpy()
     xs = _untile_scales(ops["xs"].cpu().numpy(), xq.shape[0], w.H // 32)
     tok = np.arange(w.R) // w.K
     assert np.array_equal(xq[inv], q_ref.reshape(w.T, w.H)[tok])
     assert np.array_equal(xs[inv], s_ref.reshape(w.T, w.H // 32)[tok])
-    t = layer.sched.tables()
-    rpad = int(t["meta"][0])
-    pad = (t["row_token"][:rpad] < 0).cpu().numpy()
+    pad = row_token[:rpad] < 0
     assert pad.any()
     assert not xq[:rpad][pad].any() and not xs[:rpad][pad].any()
+    qt_ref, st_ref = _rows_quantised(_padded_rows(inputs.bits(x), row_token, rpad))
+    xr = ops["xr"].cpu().numpy()
+    xrs = _untile_scales_t(ops["xrs"].cpu().numpy(), w.H, ops["rcap"], ops["xr_groups"])
+    assert np.array_equal(xr[:rpad].T, qt_ref)
+    assert np.array_equal(xrs[:, :rpad // 32], st_ref)
 
 
 @pytest.mark.parametrize("name,w", SMALL[1:], ids=[n for n, _ in SMALL[1:]])
 def test_mxfp8_operand_copies(mok, name, w):
-    """The E4M3 operands the block-scaled GEMMs read decode exactly to the bf16 copies the rest of
-    the path reads: a (written by the gate/up epilogue) and [dg | du] (dgrad1 epilogue); the
-    gathered dY's codes and scales equal the oracle's quantisation bit for bit."""
+    """The E4M3 copies the block-scaled GEMMs read:
+      * aq (gate/up epilogue) decodes exactly to the context's bf16 a;
+      * dY quantised along H and along the routed rows equals the oracle's quantisation bit for bit;
+      * dg, du and s*a quantised along the routed rows (dgrad1 epilogue, from fp32 values) match the
+        oracle's quantisation of its fp64 values to within one E4M3 step at the block's scale (fp32
+        and fp64 may round a value near a code boundary to neighbouring codes)."""
     d = inputs.make(w, seed=7)
     mx_gpu = _mx_inputs(mok, d)
     cfg = mok.make_config(128, 256, precision=mok.MOK_MXFP8)
@@ -177,22 +217,44 @@ def test_mxfp8_operand_copies(mok, name, w):
     torch.cuda.synchronize()
     t = layer.sched.tables()
     rpad = int(t["meta"][0])
-    ops = {k: v.cpu().numpy() for k, v in layer.sched.mx_operands().items() if k != "dgdu"}
-    rows = ops["aq"].shape[0]
+    row_token = t["row_token"].cpu().numpy()
+    perm = t["perm"].cpu().numpy()
+    ops = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in layer.sched.mx_operands(layer.ctx).items()}
+    rows, rcap = ops["rows"], ops["rcap"]
     a_dec = oracle.mxfp8_dequantize(ops["aq"], _untile_scales(ops["as_"], rows, w.I // 32)).reshape(rows, w.I)
     assert np.array_equal(a_dec[:rpad], to_f64(_ctx_a(layer, w)[:rpad]))
-    dg_dec = oracle.mxfp8_dequantize(ops["dgq"], _untile_scales(ops["dgs"], rows, 2 * w.I // 32))
-    dgdu = to_f64(layer.sched.mx_operands()["dgdu"][:rpad])
-    assert np.array_equal(dg_dec.reshape(rows, 2 * w.I)[:rpad], dgdu)
-    assert np.abs(dgdu).max() > 0
+    # dY, both axes, bit-exact
     q_ref, s_ref = oracle.mxfp8_quantize(inputs.bits(d["dY"]))
     inv = t["inv"].cpu().numpy().astype(np.int64)
     tok = np.arange(w.R) // w.K
     assert np.array_equal(ops["dyq"][inv], q_ref.reshape(w.T, w.H)[tok])
-    dys = _untile_scales(ops["dys"], rows, w.H // 32)
-    assert np.array_equal(dys[inv], s_ref.reshape(w.T, w.H // 32)[tok])
-
-
+    assert np.array_equal(_untile_scales(ops["dys"], rows, w.H // 32)[inv], s_ref.reshape(w.T, w.H // 32)[tok])
+    qt_ref, st_ref = _rows_quantised(_padded_rows(inputs.bits(d["dY"]), row_token, rpad))
+    assert np.array_equal(ops["dyr"][:rpad].T, qt_ref)
+    assert np.array_equal(_untile_scales_t(ops["dyrs"], w.H, rcap, 1)[:, :rpad // 32], st_ref)
+    # dg, du, s*a along the rows: within one E4M3 step of the oracle's values at the block scale
+    mx_ref = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
+    ref = oracle.layer_mx(d["topk_ids"].numpy(), d["topk_weights"].numpy(), inputs.bits(d["x"]),
+                          inputs.bits(d["dY"]), mx_ref, w.E, w.I, with_dg=True)
+    sflat = d["topk_weights"].numpy().reshape(-1).astype(np.float64)
+    valid = perm[:rpad] >= 0
+    slots = perm[:rpad][valid]
+    for name_, codes, scales, groups, src in (
+            ("dg", ops["dgr"][:, :w.I].T, _untile_scales_t(ops["dgrs"], 2 * w.I, rcap, 1)[:w.I], 1, ref["dg"]),
+            ("du", ops["dgr"][:, w.I:].T, _untile_scales_t(ops["dgrs"], 2 * w.I, rcap, 1)[w.I:], 1, ref["du"]),
+            ("sa", ops["sar"].T, _untile_scales_t(ops["sars"], w.I, rcap, ops["sar_groups"]), ops["sar_groups"],
+             sflat[:, None] * ref["a"])):
+        dec = oracle.mxfp8_dequantize(np.ascontiguousarray(codes[:, :rpad]),
+                                      np.ascontiguousarray(scales[:, :rpad // 32]))  # [features, rpad]
+        exact = np.zeros((rpad, src.shape[1]))
+        exact[valid] = src[slots]
+        refq = oracle.mx_fakequant(np.ascontiguousarray(exact.T))  # along the rows, blocks of 32
+        blk = np.abs(exact.T).reshape(src.shape[1], rpad // 32, 32).max(axis=2)
+        _, ex = np.frexp(np.where(blk > 0, blk, 1.0))
+        step = np.repeat(2.0 ** (ex - 1 - 3), 32, axis=1)  # one E4M3 step in the block's top binade
+        err = np.abs(dec - refq)
+        assert np.all(err <= step * (1 + 1e-6) + 1e-30), (name_, float((err / step).max()))
+        assert not dec[:, ~valid].any(), name_
 @pytest.mark.parametrize("name", ["sweep_zipf0_mx", "sweep_zipf2_mx"])
 def test_mxfp8_sweep_sampled_parity(mok, name):
     """T=8192, H=4096, I=1536, E=128, top-8, Zipf-skewed routing, MXFP8.  The oracle quantises only
