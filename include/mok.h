@@ -257,8 +257,8 @@ MOK_API mok_status mok_build_schedule_noalloc(const mok_config* cfg, const mok_s
  *   dyq [rows, H]  E4M3 of the gathered dY                            dys its scales
  *   dgq [rows, 2I] E4M3 of [dg | du] (blocks of 32 along I)           dgs its scales
  * Quantised along the routed rows (every column in blocks of 32 rows of the padded layout; the
- * weight-gradient GEMMs' K), also row-major:
- *   xr [rcap, H] x, dyr [rcap, H] dY, dgr [rcap, 2I] [dg | du], sar [rcap, I] s * a
+ * weight-gradient GEMMs' K), stored transposed [features, rcap]:
+ *   xr [H, rcap] x, dyr [H, rcap] dY, dgr [2I, rcap] [dg | du], sar [I, rcap] s * a
  * Scales are atom-tiled for the block-scaled MMA.  Row-major copies (kq = row length / 128): the
  * scale of row r, k-group g (elements 32g .. 32g+31) sits at byte
  *   ((r / 128) * kq + g / 4) * 512 + (r % 32) * 16 + ((r / 32) % 4) * 4 + g % 4.

@@ -68,8 +68,8 @@ struct GemmArgs {
   int32_t sfb_kq;
   int32_t out_kq;
   uint8_t* out_sf;
-  // MXFP8 weight gradients: operands quantised along the routed rows (row-major, MN-major for the
-  // MMA); sf_kq = 128-row K atoms of the routed-row capacity.  DGRAD1 writes their scales: out_sf2 ([dg | du],
+  // MXFP8 weight gradients: operands quantised along the routed rows, stored transposed [features,
+  // rcap] (K-major for the MMA); sf_kq = 128-row K atoms of the routed-row capacity.  DGRAD1 writes their scales: out_sf2 ([dg | du],
   // A operand), out_sf3 (s * a, B operand in groups of sa_groups atoms).
   int32_t sf_kq;
   int32_t sa_groups;
@@ -110,7 +110,10 @@ struct GemmCfg {
   static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
   static constexpr uint32_t kSfRing = static_cast<uint32_t>(kStages) * kStageBytes;  // offset of the atom ring
   static constexpr uint32_t kStagingOff = kSfRing + static_cast<uint32_t>(kStages) * kSfBytes;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kStagingOff) + kStagingBytes + 256;
+  // MXFP8 dgrad1: a 4 KB fp32 transpose scratch per epilogue warp (quantisation along the rows)
+  static constexpr uint32_t kScratchBytes = (MX && VAR == V_DGRAD1) ? kEpiWarps * 4096u : 0u;
+  static constexpr uint32_t kScratchOff = kStagingOff + kStagingBytes;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kScratchOff) + kScratchBytes + 256;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -165,14 +168,12 @@ __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int 
                                           uint32_t sf, uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
                                           const CUtensorMap* tB2) {
   if constexpr (MX && (VAR == V_WGRAD_GU || VAR == V_WGRAD_D)) {
-    // weight gradients: A [rows, M features] and B [rows, N features] row-major, i.e. MN-major with
-    // K = the expert's routed rows (128 per block, one 128-byte swizzled row per K index, B in
-    // 128-feature chunks 16 KB apart); scale atoms indexed by the global 128-row block of the rows
+    // weight gradients: A [M features, rows] and B [N features, rows], K-major with K = the
+    // expert's routed rows; scale atoms indexed by the global 128-row block of the rows
     constexpr uint32_t kSfb = BN * 4;
     const int k0 = w.row0 + kb * 128;
-    tma_load_2d(sa, tA, bar, w.mt * kBM, k0);
-#pragma unroll
-    for (int j = 0; j < BN / 128; ++j) tma_load_2d(sb + j * 16384, tB, bar, w.nt * BN + j * 128, k0);
+    tma_load_2d(sa, tA, bar, k0, w.mt * kBM);
+    tma_load_2d(sb, tB, bar, k0, w.nt * BN);
     bulk_load(sf, a.sfa + (static_cast<int64_t>(w.mt) * a.sf_kq + (k0 >> 7)) * 512, 512, bar);
     bulk_load(sf + 512, a.sfb + (static_cast<int64_t>(w.nt) * a.sf_kq + (k0 >> 7)) * kSfb, kSfb, bar);
     return;
@@ -327,39 +328,34 @@ __device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, i
 }
 
 // MX quantisation of one 32 x 32 block along the rows: lane = row, v[j] = column j (feature f0 + j).
-// Column j's shared exponent comes from the amax over the warp's 32 rows; each lane's 32 codes
-// leave as its row of a 32 x 32 byte tile at (feature f0, row rowc), and lane j writes column j's
-// scale into the atom-tiled array (groups of g atoms, kq atoms along K).
+// The block is transposed through the warp's fp32 scratch (element (r, c) at r * 32 + (c ^ r): both
+// the row writes and the column reads are free of bank conflicts), lane j then quantises column j
+// over the 32 rows as one MX block, and its 32 codes leave as row j of a byte tile stored at
+// (row rowc, feature f0) of the transposed [features, rows] copy; lane j writes column j's scale
+// into the atom-tiled array (groups of g atoms, kq atoms along K).
 template <class Stg>
-__device__ __forceinline__ void quant_rows_store(const float (&v)[32], Stg& stg, const CUtensorMap* tm, uint8_t* sf,
-                                                 int rowc, int f0, int kq, int g, int lane) {
+__device__ __forceinline__ void quant_rows_store(const float (&v)[32], uint32_t scratch, Stg& stg,
+                                                 const CUtensorMap* tm, uint8_t* sf, int rowc, int f0, int kq, int g,
+                                                 int lane) {
+  const uint32_t row = scratch + static_cast<uint32_t>(lane) * 128;
+#pragma unroll
+  for (int c = 0; c < 32; ++c)
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(row + (static_cast<uint32_t>(c ^ lane) << 2)), "f"(v[c]) : "memory");
+  __syncwarp();
+  float col[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r)
+    asm volatile("ld.shared.f32 %0, [%1];"
+                 : "=f"(col[r])
+                 : "r"(scratch + static_cast<uint32_t>(r) * 128 + (static_cast<uint32_t>(lane ^ r) << 2))
+                 : "memory");
+  __syncwarp();
   uint32_t codes[8];
-  uint32_t my_sb = 0;
-#pragma unroll
-  for (int j = 0; j < 32; j += 2) {
-    uint32_t sbj[2];
-    float sc[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v[j + k])));
-      int shared = static_cast<int>((m >> 23) & 0xFFu) - 127 - 8;
-      shared = shared < -127 ? -127 : shared;
-      const bool bad = m >= 0x7F800000u;
-      sbj[k] = bad ? 0xFFu : static_cast<uint32_t>(shared + 127);
-      sc[k] = bad ? 0.0f : pow2f(-shared);
-      if (lane == j + k) my_sb = sbj[k];
-    }
-    uint16_t q;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(v[j + 1] * sc[1]), "f"(v[j] * sc[0]));
-    if (sbj[0] == 0xFFu) q = static_cast<uint16_t>((q & 0xFF00u) | 0x7Fu);
-    if (sbj[1] == 0xFFu) q = static_cast<uint16_t>((q & 0x00FFu) | 0x7F00u);
-    if ((j & 2) == 0) codes[j >> 2] = q;
-    else codes[j >> 2] |= static_cast<uint32_t>(q) << 16;
-  }
+  const uint32_t sb = mx_quant32(col, codes);
   const uint4 ch[2] = {make_uint4(codes[0], codes[1], codes[2], codes[3]),
                        make_uint4(codes[4], codes[5], codes[6], codes[7])};
-  stg.template put<32>(ch, tm, f0, rowc);
-  sf[sf_atom_offset_g(f0 + lane, rowc >> 5, kq, g)] = static_cast<uint8_t>(my_sb);
+  stg.template put<32>(ch, tm, rowc, f0);
+  sf[sf_atom_offset_g(f0 + lane, rowc >> 5, kq, g)] = static_cast<uint8_t>(sb);
 }
 
 // Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab; `h`
@@ -368,7 +364,7 @@ __device__ __forceinline__ void quant_rows_store(const float (&v)[32], Stg& stg,
 // read.  `pre` holds DGRAD1's first prefetched context chunk.
 template <int VAR, int BN, bool MX, class Stg>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int h, int lane,
-                                              uint32_t taddr, Stg& stg, const CUtensorMap* tO0,
+                                              uint32_t taddr, Stg& stg, uint32_t scratch, const CUtensorMap* tO0,
                                               const CUtensorMap* tO1, const CUtensorMap* tO2, uint32_t tempty,
                                               Dg1Chunk& pre) {
   if constexpr (VAR == V_FWD_GATEUP && MX) {
@@ -471,8 +467,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     // per 32-column chunk:
     //   dS partial from a's quantisation along I (the context);
     //   dg, du quantised along I (row-major codes + A atoms) for the second data-gradient GEMM;
-    //   dg, du and s * a (a recomputed in fp32 as the forward did) quantised along this warp's 32
-    //   routed rows, for the weight-gradient GEMMs.
+    //   dg, du and s * a quantised along this warp's 32 routed rows, for the weight-gradient GEMMs.
     const int64_t row = w.row0 + q * 32 + lane;
     const int64_t I = a.I;
     const int i0 = w.nt * BN;
@@ -504,26 +499,27 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
 #pragma unroll
         for (int k = 0; k < 8; ++k) part = fmaf(__uint_as_float(rv[8 * j + k]), a8[k], part);
       }
-      float v[32];
+      float sg[32], v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = s * (silu_f(g[i]) * u[i]);
-      quant_rows_store(v, stg, tO1, a.out_sf3, rowc, i0 + c, a.sf_kq, a.sa_groups, lane);
+      for (int i = 0; i < 32; ++i) {
+        sg[i] = sigmoid_f(g[i]);
+        v[i] = s * (g[i] * sg[i] * u[i]);
+      }
+      quant_rows_store(v, scratch, stg, tO1, a.out_sf3, rowc, i0 + c, a.sf_kq, a.sa_groups, lane);
       uint4 ch[2];
       uint32_t codes[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float sg = sigmoid_f(g[i]);
-        v[i] = s * __uint_as_float(rv[i]) * u[i] * sg * (1.0f + g[i] * (1.0f - sg));
-      }
-      quant_rows_store(v, stg, tO0, a.out_sf2, rowc, i0 + c, a.sf_kq, 1, lane);
+      for (int i = 0; i < 32; ++i)
+        v[i] = s * __uint_as_float(rv[i]) * u[i] * sg[i] * (1.0f + g[i] * (1.0f - sg[i]));
+      quant_rows_store(v, scratch, stg, tO0, a.out_sf2, rowc, i0 + c, a.sf_kq, 1, lane);
       uint32_t sb = mx_quant32(v, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
       stg.template put<32>(ch, tO2, i0 + c, rowc);
       a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sb);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = s * __uint_as_float(rv[i]) * g[i] * sigmoid_f(g[i]);
-      quant_rows_store(v, stg, tO0, a.out_sf2, rowc, a.I + i0 + c, a.sf_kq, 1, lane);
+      for (int i = 0; i < 32; ++i) v[i] = s * __uint_as_float(rv[i]) * g[i] * sg[i];
+      quant_rows_store(v, scratch, stg, tO0, a.out_sf2, rowc, a.I + i0 + c, a.sf_kq, 1, lane);
       sb = mx_quant32(v, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
@@ -670,7 +666,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sf_ring = base + C::kSfRing;
   const uint32_t staging = base + C::kStagingOff;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kStagingOff + C::kStagingBytes);
+  const uint32_t scratch0 = base + C::kScratchOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kScratchOff + C::kScratchBytes);
   // bars[0..S) full, [S..2S) empty, [2S, 2S+2) accumulator full, [2S+2, 2S+4) accumulator empty,
   // [2S+4] drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
@@ -771,14 +768,10 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j)  // B row n's word lands in column n / 32
               tmem_cp_sf_atom(tsf + 4 + 4 * j, sdesc_plain(sf + 512 + 512 * j));
-            constexpr bool kMn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D);  // both operands MN-major
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {  // K = 32 e4m3 per instruction; k-group ks
-              const uint64_t ad = kMn ? sdesc_sw128(sa + ks * 4096, 16384, 1024) : sdesc_sw128(sa + ks * 32, 16, 1024);
-              const uint64_t bd = kMn ? sdesc_sw128(sb + ks * 4096, 16384, 1024) : sdesc_sw128(sb + ks * 32, 16, 1024);
-              umma_mxf8(d_tmem, ad, bd, idesc_mx(kBM, BN, static_cast<uint32_t>(ks), kMn), (kb | ks) != 0 ? 1u : 0u,
-                        tsf, tsf + 4);
-            }
+            for (int ks = 0; ks < 4; ++ks)  // K = 32 e4m3 (32 bytes) per instruction; k-group ks
+              umma_mxf8(d_tmem, sdesc_sw128(sa + ks * 32, 16, 1024), sdesc_sw128(sb + ks * 32, 16, 1024),
+                        idesc_mx(kBM, BN, static_cast<uint32_t>(ks)), (kb | ks) != 0 ? 1u : 0u, tsf, tsf + 4);
           } else {
 #pragma unroll
             for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
@@ -825,7 +818,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      gemm_epilogue<VAR, BN, MX>(args, w, q, h, lane, taddr, stg, &tmO0, &tmO1, &tmO2, tempty_bar(acc), pre);
+      gemm_epilogue<VAR, BN, MX>(args, w, q, h, lane, taddr, stg, scratch0 + static_cast<uint32_t>(warp - 2) * 4096u,
+                                 &tmO0, &tmO1, &tmO2, tempty_bar(acc), pre);
       if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;

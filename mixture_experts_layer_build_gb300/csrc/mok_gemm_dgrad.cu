@@ -50,10 +50,10 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
     a.sa_groups = z.mx_bn_i() / 128;
     a.out_sf2 = st.dgrs;
     a.out_sf3 = st.sars;
-    // 32 x 32 byte tiles of the row-quantised [dg | du] and s a, row-major [rcap, features]
+    // 32 x 32 byte tiles of the row-quantised [dg | du] and s a, transposed [features, rcap]
     const uint64_t rcap = static_cast<uint64_t>(z.rcap());
-    if (!make_tmap_u8(&tO0, st.dgr, 2 * static_cast<uint64_t>(z.I), rcap, 32, 32, 32)) return -1;
-    if (!make_tmap_u8(&tO1, st.sar, z.I, rcap, 32, 32, 32)) return -1;
+    if (!make_tmap_u8(&tO0, st.dgr, rcap, 2 * static_cast<uint64_t>(z.I), 32, 32, 32)) return -1;
+    if (!make_tmap_u8(&tO1, st.sar, rcap, z.I, 32, 32, 32)) return -1;
     if (!make_tmap_u8(&tO2, st.dgq, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32, 32)) return -1;
     return launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, tO2, a,
                                             clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);

@@ -5,8 +5,8 @@
 
 namespace mok {
 
-// MXFP8: block-scaled E4M3 on operands quantised along the routed rows (K), read MN-major from their
-// row-major copies: [dWg ; dWu]_e = [dg | du]_e^T x_e and dWd_e = dY_e^T (s a)_e over e's padded rows.
+// MXFP8: block-scaled E4M3 on operands quantised along the routed rows (K), read K-major from their
+// transposed copies: [dWg ; dWu]_e = [dg | du]_e^T x_e and dWd_e = dY_e^T (s a)_e over e's padded rows.
 static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
                                  const mok_grads& g, int num_ctas, cudaStream_t stream) {
   CUtensorMap tA, tB, tO0, tO1;
@@ -23,8 +23,8 @@ static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   };
   {  // [dWg ; dWu]_e: M = 2I (A = [dg | du]^T), N = H (B = x^T)
     const int BN = z.mx_bn_h();
-    if (!make_tmap_u8(&tA, st.dgr, 2 * static_cast<uint64_t>(z.I), rcap, 128, 128, 128)) return -1;
-    if (!make_tmap_u8(&tB, ctx.xr, z.H, rcap, 128, 128, 128)) return -1;
+    if (!make_tmap_u8(&tA, st.dgr, rcap, 2 * static_cast<uint64_t>(z.I), 128, 128, 128)) return -1;
+    if (!make_tmap_u8(&tB, ctx.xr, rcap, z.H, 128, BN, 128)) return -1;
     a.m_tiles = 2 * z.I / kBM;
     a.n_tiles = z.H / BN;
     a.sfa = st.dgrs;
@@ -41,8 +41,8 @@ static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   }
   {  // dWd_e: M = H (A = dY^T), N = I (B = (s a)^T)
     const int BN = z.mx_bn_i();
-    if (!make_tmap_u8(&tA, st.dyr, z.H, rcap, 128, 128, 128)) return -1;
-    if (!make_tmap_u8(&tB, st.sar, z.I, rcap, 128, 128, 128)) return -1;
+    if (!make_tmap_u8(&tA, st.dyr, rcap, z.H, 128, 128, 128)) return -1;
+    if (!make_tmap_u8(&tB, st.sar, rcap, z.I, 128, BN, 128)) return -1;
     a.m_tiles = z.H / kBM;
     a.n_tiles = z.I / BN;
     a.sfa = st.dyrs;

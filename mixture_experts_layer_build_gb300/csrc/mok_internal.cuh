@@ -46,13 +46,13 @@ struct Staging {
   uint8_t* dgq;      // [rpad_max, 2I] [dg | du], quantised along I
   uint8_t* dgs;      //   scales: rtiles x 2I/128 atoms
   // weight-gradient operands, quantised along the routed rows (32-row blocks of the padded layout),
-  // row-major [rcap, features] (MN-major operands of the wgrad GEMMs); scales in sf_atom_offset_g
+  // transposed [features, rcap] (K-major operands of the wgrad GEMMs); scales in sf_atom_offset_g
   // layout (row f = feature, k-group = row / 32, kq_rows atoms along K)
-  uint8_t* dyr;      // [rcap, H]  dY          scales dyrs: A operand (G = 1)
+  uint8_t* dyr;      // [H, rcap]  dY          scales dyrs: A operand (G = 1)
   uint8_t* dyrs;
-  uint8_t* dgr;      // [rcap, 2I] [dg | du]   scales dgrs: A operand (G = 1)
+  uint8_t* dgr;      // [2I, rcap] [dg | du]   scales dgrs: A operand (G = 1)
   uint8_t* dgrs;
-  uint8_t* sar;      // [rcap, I]  s * a       scales sars: B operand (G = mx_bn_i / 128)
+  uint8_t* sar;      // [I, rcap]  s * a       scales sars: B operand (G = mx_bn_i / 128)
   uint8_t* sars;
   // the caller's weight scales re-tiled into atom groups matching the B tiles (per call)
   uint8_t* sw_gu;    // s_gate, s_up: per 128 rows of I, the gate atom then the up atom
@@ -63,7 +63,7 @@ struct Staging {
 };
 struct Ctx {
   uint16_t* xg;      // BF16 mode: [rpad_max, H] bf16 gathered x rows (zero on padding rows)
-  uint8_t* xr;       // MXFP8 mode: [rcap, H] x quantised along the routed rows
+  uint8_t* xr;       // MXFP8 mode: [H, rcap] x quantised along the routed rows, transposed
   uint8_t* xrs;      //   scales: B operand of the gate/up weight gradient (G = mx_bn_h / 128)
   void* gu;          // [rpad_max, 2I]: [g | u], bf16 (BF16 mode) or fp32 (MXFP8 mode, whose
                      // backward re-quantises dg, du and s * a and needs g, u unrounded)
@@ -102,8 +102,9 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
                     cudaStream_t stream);
 int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                        int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
-// MX gather of 32-row blocks: dst_q / dst_sf = rows quantised along H (A-operand atoms); dstR_q /
-// dstR_sf = the same rows quantised along the rows (atoms grouped gT at a time).  Both row-major.
+// MX gather of 32-row blocks: dst_q / dst_sf = rows quantised along H (row-major, A-operand atoms);
+// dstR_q / dstR_sf = the same rows quantised along the rows, transposed [H, rcap] (atoms grouped gT
+// at a time).
 int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                           int32_t H, uint8_t* dst_q, uint8_t* dst_sf, uint8_t* dstR_q, uint8_t* dstR_sf,
                           int64_t rcap, int gT, int kind, cudaStream_t stream);

@@ -228,14 +228,13 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
 
 // MX gather, one CTA per (32-row block of the expert-grouped layout, 128 columns).  The 32 gathered
 // rows are staged in shared memory as bf16 (zero for padding rows); each thread then quantises one
-// 32-column block of one row -- along H: E4M3 codes for the forward / data-gradient GEMMs,
-// A-operand atoms -- and one column over the 32 rows -- along the routed rows: codes for the
-// weight-gradient GEMM, atoms grouped gT at a time.  The column codes are collected in shared
-// memory and leave row-major like the others.  The rounding is bit-exact with
+// 32-column block of one row -- along H: row-major E4M3 codes for the forward / data-gradient
+// GEMMs, A-operand atoms -- and one column over the 32 rows -- along the routed rows: its 32 codes
+// are 32 consecutive bytes of the transposed copy [H, rcap] the weight-gradient GEMM reads K-major,
+// atoms grouped gT at a time.  The rounding is bit-exact with
 // mxfp8_quantize_kernel (shared exponent from amax, E4M3 round-to-nearest-even, saturating).
 // Blocks of 32 rows never straddle two experts: segments start at multiples of 128.
 constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
-constexpr int kGmxCodeStride = 128 + 16;  // bytes per staged code row
 
 __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint16_t* __restrict__ src,
                                                             const int32_t* __restrict__ row_token,
@@ -244,7 +243,6 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint16_t* __r
                                                             uint8_t* __restrict__ dstR_q,
                                                             uint8_t* __restrict__ dstR_sf, int64_t rcap, int gT) {
   __shared__ __align__(16) uint8_t tile[32 * kGmxStride];
-  __shared__ __align__(16) uint8_t ctile[32 * kGmxCodeStride];
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
   if (r0 >= meta[0]) return;
   const int c0 = static_cast<int>(blockIdx.y) * 128;
@@ -280,7 +278,7 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint16_t* __r
     __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
     dst_sf[sf_atom_offset(r0 + r, (c0 >> 5) + b, H / 128)] = static_cast<uint8_t>(sb);
   }
-  {  // along the rows: column c0 + t over the 32 rows; codes into the shared code tile
+  {  // along the rows: column c0 + t over the 32 rows
     float o[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r)
@@ -288,16 +286,10 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint16_t* __r
                              << 16);
     uint32_t codes[8];
     const uint32_t sb = mx_quant32(o, codes);
-#pragma unroll
-    for (int r = 0; r < 32; ++r) ctile[r * kGmxCodeStride + t] = static_cast<uint8_t>(codes[r >> 2] >> (8 * (r & 3)));
+    uint4* dq = reinterpret_cast<uint4*>(dstR_q + static_cast<int64_t>(c0 + t) * rcap + r0);
+    __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+    __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
     dstR_sf[sf_atom_offset_g(c0 + t, r0 >> 5, rcap / 128, gT)] = static_cast<uint8_t>(sb);
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {  // 32 code rows of 128 bytes: thread t stores vector t % 8 of rows t / 8 + 16 i
-    const int r = t / 8 + 16 * i, v = t % 8;
-    __stcs(reinterpret_cast<uint4*>(dstR_q + (r0 + r) * H + c0) + v,
-           *reinterpret_cast<const uint4*>(ctile + r * kGmxCodeStride + v * 16));
   }
 }
 

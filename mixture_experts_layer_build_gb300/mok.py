@@ -218,8 +218,9 @@ class Schedule:
 
     def mx_operands(self, fwd_ctx: torch.Tensor) -> dict:
         """Device views of the MXFP8 operand copies (mok_mx_operands_of): E4M3 codes ([rows, n]
-        quantised along each row, [rcap, n] quantised along the rows) and their atom-tiled E8M0
-        scale arrays (flat uint8), plus the layout numbers rows, rcap, xr_groups, sar_groups."""
+        quantised along each row, transposed [n, rcap] quantised along the rows) and their
+        atom-tiled E8M0 scale arrays (flat uint8), plus the layout numbers rows, rcap, xr_groups,
+        sar_groups."""
         m = mok_mx_operands()
         _check(_lib.mok_mx_operands_of(ctypes.byref(self.c), _ptr(fwd_ctx, None, "fwd_ctx"), ctypes.byref(m)),
                "mok_mx_operands_of")
@@ -236,10 +237,10 @@ class Schedule:
                     aq=v(m.aq, rows * I).view(rows, I), as_=v(m.as_, rt * 128 * (I // 32)),
                     dyq=v(m.dyq, rows * H).view(rows, H), dys=v(m.dys, rt * 128 * (H // 32)),
                     dgq=v(m.dgq, rows * 2 * I).view(rows, 2 * I), dgs=v(m.dgs, rt * 128 * (2 * I // 32)),
-                    xr=v(m.xr, H * rcap).view(rcap, H), xrs=v(m.xrs, H * rcap // 32),
-                    dyr=v(m.dyr, H * rcap).view(rcap, H), dyrs=v(m.dyrs, H * rcap // 32),
-                    dgr=v(m.dgr, 2 * I * rcap).view(rcap, 2 * I), dgrs=v(m.dgrs, 2 * I * rcap // 32),
-                    sar=v(m.sar, I * rcap).view(rcap, I), sars=v(m.sars, I * rcap // 32),
+                    xr=v(m.xr, H * rcap).view(H, rcap), xrs=v(m.xrs, H * rcap // 32),
+                    dyr=v(m.dyr, H * rcap).view(H, rcap), dyrs=v(m.dyrs, H * rcap // 32),
+                    dgr=v(m.dgr, 2 * I * rcap).view(2 * I, rcap), dgrs=v(m.dgrs, 2 * I * rcap // 32),
+                    sar=v(m.sar, I * rcap).view(I, rcap), sars=v(m.sars, I * rcap // 32),
                     rows=rows, rcap=rcap, xr_groups=m.xr_groups, sar_groups=m.sar_groups)
 
 

@@ -194,7 +194,7 @@ def test_mxfp8_gather_quantises_x_bit_exactly(mok):
     qt_ref, st_ref = _rows_quantised(_padded_rows(inputs.bits(x), row_token, rpad))
     xr = ops["xr"].cpu().numpy()
     xrs = _untile_scales_t(ops["xrs"].cpu().numpy(), w.H, ops["rcap"], ops["xr_groups"])
-    assert np.array_equal(xr[:rpad].T, qt_ref)
+    assert np.array_equal(xr[:, :rpad], qt_ref)
     assert np.array_equal(xrs[:, :rpad // 32], st_ref)
 
 
@@ -230,7 +230,7 @@ def test_mxfp8_operand_copies(mok, name, w):
     assert np.array_equal(ops["dyq"][inv], q_ref.reshape(w.T, w.H)[tok])
     assert np.array_equal(_untile_scales(ops["dys"], rows, w.H // 32)[inv], s_ref.reshape(w.T, w.H // 32)[tok])
     qt_ref, st_ref = _rows_quantised(_padded_rows(inputs.bits(d["dY"]), row_token, rpad))
-    assert np.array_equal(ops["dyr"][:rpad].T, qt_ref)
+    assert np.array_equal(ops["dyr"][:, :rpad], qt_ref)
     assert np.array_equal(_untile_scales_t(ops["dyrs"], w.H, rcap, 1)[:, :rpad // 32], st_ref)
     # dg, du, s*a along the rows: within one E4M3 step of the oracle's values at the block scale
     mx_ref = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
@@ -240,9 +240,9 @@ def test_mxfp8_operand_copies(mok, name, w):
     valid = perm[:rpad] >= 0
     slots = perm[:rpad][valid]
     for name_, codes, scales, groups, src in (
-            ("dg", ops["dgr"][:, :w.I].T, _untile_scales_t(ops["dgrs"], 2 * w.I, rcap, 1)[:w.I], 1, ref["dg"]),
-            ("du", ops["dgr"][:, w.I:].T, _untile_scales_t(ops["dgrs"], 2 * w.I, rcap, 1)[w.I:], 1, ref["du"]),
-            ("sa", ops["sar"].T, _untile_scales_t(ops["sars"], w.I, rcap, ops["sar_groups"]), ops["sar_groups"],
+            ("dg", ops["dgr"][:w.I], _untile_scales_t(ops["dgrs"], 2 * w.I, rcap, 1)[:w.I], 1, ref["dg"]),
+            ("du", ops["dgr"][w.I:], _untile_scales_t(ops["dgrs"], 2 * w.I, rcap, 1)[w.I:], 1, ref["du"]),
+            ("sa", ops["sar"], _untile_scales_t(ops["sars"], w.I, rcap, ops["sar_groups"]), ops["sar_groups"],
              sflat[:, None] * ref["a"])):
         dec = oracle.mxfp8_dequantize(np.ascontiguousarray(codes[:, :rpad]),
                                       np.ascontiguousarray(scales[:, :rpad // 32]))  # [features, rpad]
