@@ -164,8 +164,6 @@ def kernel_work(w, e_active: int) -> dict:
     R, H, I, T, K, E = w.R, w.H, w.I, w.T, w.K, w.E
     b16 = 2
     work = {
-        "gemm_wgrad_gu": (4 * R * H * I, R * 2 * I * b16 + R * H * b16 + 2 * E * I * H * 4, "bf16"),
-        "gemm_wgrad_d": (2 * R * H * I, R * H * b16 + R * I * b16 + E * H * I * 4, "bf16"),
         # combine / dX reduce: routed rows read + weights/indices + token rows written
         "combine": (0, R * H * b16 + T * K * 8 + T * H * b16, None),
         "dx_reduce": (0, R * H * b16 + T * K * 4 + T * H * b16, None),
@@ -177,13 +175,17 @@ def kernel_work(w, e_active: int) -> dict:
             # reads Xq, Wg, Wu; writes g, u (fp32), a (bf16) and its MX copy
             "gemm_fwd_gateup": (4 * R * H * I, R * H * mx + 2 * wts + R * 2 * I * 4 + R * I * (b16 + mx), "e4m3"),
             "gemm_fwd_down": (2 * R * H * I, R * I * mx + wts + R * H * b16, "e4m3"),
-            # reads dYq, Wd^T, g, u (fp32), a; writes dg, du (bf16 and MX), s*a, dS partials
+            # reads dYq, Wd^T, g, u (fp32), a_q; writes [dg | du] quantised along I and along the rows,
+            # s*a quantised along the rows, dS partials
             "gemm_dgrad1": (2 * R * H * I, R * H * mx + wts + R * 2 * I * 4 + R * I * b16
-                            + R * 2 * I * (b16 + mx) + R * I * b16 + R * (I // 128) * 4, "e4m3"),
+                            + 2 * R * 2 * I * mx + R * I * mx + R * (I // 128) * 4, "e4m3"),
             "gemm_dgrad2": (4 * R * H * I, R * 2 * I * mx + 2 * wts + R * H * b16, "e4m3"),
-            # gather: unique token rows read once; routed rows written in bf16 and MX
-            "gather_x": (0, T * H * b16 + R * H * (b16 + mx), None),
-            "gather_dy": (0, T * H * b16 + R * H * (b16 + mx), None),
+            # block-scaled on the operands quantised along the routed rows; fp32 dW of every expert
+            "gemm_wgrad_gu": (4 * R * H * I, R * 2 * I * mx + R * H * mx + 2 * E * I * H * 4, "e4m3"),
+            "gemm_wgrad_d": (2 * R * H * I, R * H * mx + R * I * mx + E * H * I * 4, "e4m3"),
+            # gather: unique token rows read once; routed rows written quantised along H and along the rows
+            "gather_x": (0, T * H * b16 + 2 * R * H * mx, None),
+            "gather_dy": (0, T * H * b16 + 2 * R * H * mx, None),
             # three weight-scale matrices re-tiled into atoms per launch (read + write)
             "mx_scale_atoms": (0, 2 * 3 * E * H * I / 32, None),
         })
@@ -195,6 +197,8 @@ def kernel_work(w, e_active: int) -> dict:
             "gemm_dgrad1": (2 * R * H * I, R * H * b16 + wts + R * 2 * I * b16 + R * I * b16 + R * 3 * I * b16,
                             "bf16"),
             "gemm_dgrad2": (4 * R * H * I, R * 2 * I * b16 + 2 * wts + R * H * b16, "bf16"),
+            "gemm_wgrad_gu": (4 * R * H * I, R * 2 * I * b16 + R * H * b16 + 2 * E * I * H * 4, "bf16"),
+            "gemm_wgrad_d": (2 * R * H * I, R * H * b16 + R * I * b16 + E * H * I * 4, "bf16"),
             "gather_x": (0, T * H * b16 + R * H * b16, None),
             "gather_dy": (0, T * H * b16 + R * H * b16, None),
         })
