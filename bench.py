@@ -68,6 +68,12 @@ def dist_init():
     return 0, 1, 0
 
 
+def aggregate_tokens_per_s(tokens_per_rank: int, ws: int, ms_max: float) -> float:
+    """Whole-job throughput of the replicas: every rank processes its own shard of tokens_per_rank
+    (weak scaling); the job takes as long as the slowest rank."""
+    return tokens_per_rank * ws / (ms_max * 1e-3)
+
+
 def barrier(ws):
     if ws > 1:
         import torch.distributed as dist
@@ -497,7 +503,7 @@ def ours(args, rank, ws, local_rank):
 
     result = None
     if rank == 0:
-        tokens_per_s = w.T * ws / (ms_max * 1e-3)
+        tokens_per_s = aggregate_tokens_per_s(w.T, ws, ms_max)
         result = {
             "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
