@@ -433,8 +433,9 @@ def ours(args, rank, ws, local_rank):
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its own inputs host->device and its results device->host inside the timed
-    # region.  Inputs and outputs are double-buffered over a copy stream, so step i+1's uploads and
-    # step i-1's downloads overlap step i's compute (the usual prefetching input pipeline).
+    # region.  Inputs and outputs are double-buffered, uploads on one copy stream and downloads on
+    # another, so step i+1's uploads, step i-1's downloads and step i's compute all overlap (the
+    # usual prefetching input pipeline; the two directions of the host link run concurrently).
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     host_in = [pin(d["x"]), pin(d["topk_ids"]), pin(d["topk_weights"]), pin(d["dY"])]
     host_out = [[torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory(),
@@ -445,7 +446,8 @@ def ours(args, rank, ws, local_rank):
                     grads=mok.Grads.empty(w.T, w.H, w.I, w.E, w.K, device=dev)) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
-    copy_stream = torch.cuda.Stream(device=dev)
+    copy_stream = torch.cuda.Stream(device=dev)   # host -> device
+    down_stream = torch.cuda.Stream(device=dev)   # device -> host
     ev_in = [torch.cuda.Event() for _ in range(2)]      # uploads of buffer b landed
     ev_done = [torch.cuda.Event() for _ in range(2)]    # compute on buffer b finished
     ev_out = [torch.cuda.Event() for _ in range(2)]     # downloads of buffer b finished
@@ -473,12 +475,12 @@ def ours(args, rank, ws, local_rank):
 
     def download(i):
         b = i % 2
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(ev_done[b])
+        with torch.cuda.stream(down_stream):
+            down_stream.wait_event(ev_done[b])
             o, g = dev_out[b]["out"], dev_out[b]["grads"]
             for dst, src in zip(host_out[b], (o, g.dx, g.d_topk_weights)):
                 dst.copy_(src, non_blocking=True)
-            ev_out[b].record(copy_stream)
+            ev_out[b].record(down_stream)
 
     def e2e_run(n):
         # issue order keeps both streams busy: upload(i+1) before compute(i)'s results are fetched
@@ -494,8 +496,9 @@ def ours(args, rank, ws, local_rank):
     barrier(ws)
     e0.record(copy_stream)
     e2e_run(args.steps)
-    copy_stream.wait_stream(stream)
-    e1.record(copy_stream)
+    down_stream.wait_stream(stream)
+    down_stream.wait_stream(copy_stream)
+    e1.record(down_stream)
     torch.cuda.synchronize()
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
