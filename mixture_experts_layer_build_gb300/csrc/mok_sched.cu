@@ -103,10 +103,17 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
   const int W = E + 1;
   const int64_t L = (nchunks + 31) / 32;  // chunks per group; group g = warp g
   const int64_t c0 = warp * L, c1 = min(nchunks, c0 + L);
-  // level 1: per (group, expert) sums; lanes read consecutive experts of one chunk (coalesced)
+  // level 1: per (group, expert) sums; lanes read consecutive experts of one chunk (coalesced),
+  // eight chunks' loads in flight at a time
   for (int e = lane; e < W; e += 32) {
     int sum = 0;
-    for (int64_t c = c0; c < c1; ++c) sum += chunk_hist[c * W + e];
+    for (int64_t cb = c0; cb < c1; cb += 8) {
+      int v8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v8[k] = cb + k < c1 ? chunk_hist[(cb + k) * W + e] : 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum += v8[k];
+    }
     part[warp * W + e] = sum;
   }
   __syncthreads();
@@ -121,6 +128,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
     }
   }
   __shared__ int s_bad;
+  __shared__ int2 s_pad[1024];  // per expert: [first padding row, end of its padded segment)
   if (threadIdx.x == 0) {
     int bad = 0;
     for (int g = 0; g < 32; ++g) bad += part[g * W + E];
@@ -151,11 +159,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
       m[2] = min(kRowTile, cnt - b * kRowTile);
       m[3] = tst + (b * kRowTile) / mb;
     }
-    for (int r = pof + cnt; r < pof + padded; ++r) {
-      perm[r] = -1;
-      row_token[r] = -1;
-      row_weight[r] = 0.0f;
-    }
+    s_pad[e] = make_int2(pof + cnt, pof + padded);
     for (int g = 0; g < 32; ++g) part[g * W + e] += pof;  // first row of group g's slots of e
   }
   if (e == 0) {
@@ -171,13 +175,28 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
   }
   __syncthreads();
   if (overflow) return;
-  // every chunk's first row per expert, in place
+  // padding rows of every expert, spread over the whole block
+  for (int idx = threadIdx.x; idx < E * kRowTile; idx += blockDim.x) {
+    const int2 pr = s_pad[idx / kRowTile];
+    const int r = pr.x + idx % kRowTile;
+    if (r < pr.y) {
+      perm[r] = -1;
+      row_token[r] = -1;
+      row_weight[r] = 0.0f;
+    }
+  }
+  // every chunk's first row per expert, in place (eight chunks' loads in flight at a time)
   for (int ex = lane; ex < E; ex += 32) {
     int run = part[warp * W + ex];
-    for (int64_t c = c0; c < c1; ++c) {
-      const int vv = chunk_hist[c * W + ex];
-      chunk_hist[c * W + ex] = run;
-      run += vv;
+    for (int64_t cb = c0; cb < c1; cb += 8) {
+      int v8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v8[k] = cb + k < c1 ? chunk_hist[(cb + k) * W + ex] : 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (cb + k < c1) chunk_hist[(cb + k) * W + ex] = run;
+        run += v8[k];
+      }
     }
   }
 }
