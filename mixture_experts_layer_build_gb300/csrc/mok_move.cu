@@ -226,51 +226,63 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
   }
 }
 
-// MX gather, one CTA per (32-row block of the expert-grouped layout, 128 columns).  The 32 gathered
-// rows are staged in shared memory as bf16 (zero for padding rows); each thread then quantises one
-// 32-column block of one row -- along H: row-major E4M3 codes for the forward / data-gradient
-// GEMMs, A-operand atoms -- and one column over the 32 rows -- along the routed rows: its 32 codes
-// are 32 consecutive bytes of the transposed copy [H, rcap] the weight-gradient GEMM reads K-major,
-// atoms grouped gT at a time.  The rounding is bit-exact with
-// mxfp8_quantize_kernel (shared exponent from amax, E4M3 round-to-nearest-even, saturating).
-// Blocks of 32 rows never straddle two experts: segments start at multiples of 128.
+// MX gather, one CTA per (128-row block of the expert-grouped layout, 128 columns), 256 threads.
+// The 128 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
+//   along H: each thread quantises two 32-column blocks of rows -- row-major E4M3 codes for the
+//     forward / data-gradient GEMMs, A-operand atoms;
+//   along the routed rows: each thread quantises one column over two 32-row blocks -- 64
+//     consecutive bytes of the transposed copy [H, rcap] the weight-gradient GEMM reads K-major,
+//     atoms grouped gT at a time.
+// The rounding is bit-exact with mxfp8_quantize_kernel (shared exponent from amax, E4M3
+// round-to-nearest-even, saturating).  Row blocks never straddle two experts: segments start at
+// multiples of 128.
 constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
 
-__global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint16_t* __restrict__ src,
+__device__ __forceinline__ void gmx_row_block(const uint8_t* p, float (&o)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p + 16 * i);
+    o[8 * i] = bf16_lo(v.x);
+    o[8 * i + 1] = bf16_hi(v.x);
+    o[8 * i + 2] = bf16_lo(v.y);
+    o[8 * i + 3] = bf16_hi(v.y);
+    o[8 * i + 4] = bf16_lo(v.z);
+    o[8 * i + 5] = bf16_hi(v.z);
+    o[8 * i + 6] = bf16_lo(v.w);
+    o[8 * i + 7] = bf16_hi(v.w);
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint16_t* __restrict__ src,
                                                             const int32_t* __restrict__ row_token,
                                                             const int32_t* __restrict__ meta, int32_t H,
                                                             uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf,
                                                             uint8_t* __restrict__ dstR_q,
                                                             uint8_t* __restrict__ dstR_sf, int64_t rcap, int gT) {
-  __shared__ __align__(16) uint8_t tile[32 * kGmxStride];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
+  __shared__ __align__(16) uint8_t tile[128 * kGmxStride];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 128;
   if (r0 >= meta[0]) return;
   const int c0 = static_cast<int>(blockIdx.y) * 128;
   const int t = threadIdx.x;
+  {
+    uint4 val[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 8 i
-    const int r = t / 16 + 8 * i, v = t % 16;
-    const int tok = __ldg(row_token + r0 + r);
-    const uint4 val = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(tok) * H + c0) + v)
-                               : make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(tile + r * kGmxStride + v * 16) = val;
+    for (int i = 0; i < 8; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 16 i
+      const int r = t / 16 + 16 * i;
+      const int tok = __ldg(row_token + r0 + r);
+      val[i] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(tok) * H + c0) + t % 16)
+                        : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<uint4*>(tile + (t / 16 + 16 * i) * kGmxStride + (t % 16) * 16) = val[i];
   }
   __syncthreads();
-  {  // along H: row t / 4, columns c0 + 32 (t % 4) ... + 31
-    const int r = t / 4, b = t % 4;
-    float o[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + r * kGmxStride + b * 64 + 16 * i);
-      o[8 * i] = bf16_lo(v.x);
-      o[8 * i + 1] = bf16_hi(v.x);
-      o[8 * i + 2] = bf16_lo(v.y);
-      o[8 * i + 3] = bf16_hi(v.y);
-      o[8 * i + 4] = bf16_lo(v.z);
-      o[8 * i + 5] = bf16_hi(v.z);
-      o[8 * i + 6] = bf16_lo(v.w);
-      o[8 * i + 7] = bf16_hi(v.w);
-    }
+  for (int k = 0; k < 2; ++k) {  // along H: row it / 4, columns c0 + 32 (it % 4) ... + 31
+    const int it = t + 256 * k, r = it / 4, b = it % 4;
+    float o[32];
+    gmx_row_block(tile + r * kGmxStride + b * 64, o);
     uint32_t codes[8];
     const uint32_t sb = mx_quant32(o, codes);
     uint4* dq = reinterpret_cast<uint4*>(dst_q + (r0 + r) * H + c0 + 32 * b);
@@ -278,18 +290,23 @@ __global__ void __launch_bounds__(128) gather_rows_mx_kernel(const uint16_t* __r
     __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
     dst_sf[sf_atom_offset(r0 + r, (c0 >> 5) + b, H / 128)] = static_cast<uint8_t>(sb);
   }
-  {  // along the rows: column c0 + t over the 32 rows
-    float o[32];
+  {  // along the rows: column c0 + t % 128, row blocks 2 (t / 128) and 2 (t / 128) + 1
+    const int c = t % 128, rb0 = 2 * (t / 128);
+    uint4* dq = reinterpret_cast<uint4*>(dstR_q + static_cast<int64_t>(c0 + c) * rcap + r0 + 32 * rb0);
 #pragma unroll
-    for (int r = 0; r < 32; ++r)
-      o[r] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + r * kGmxStride + 2 * t))
-                             << 16);
-    uint32_t codes[8];
-    const uint32_t sb = mx_quant32(o, codes);
-    uint4* dq = reinterpret_cast<uint4*>(dstR_q + static_cast<int64_t>(c0 + t) * rcap + r0);
-    __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-    __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-    dstR_sf[sf_atom_offset_g(c0 + t, r0 >> 5, rcap / 128, gT)] = static_cast<uint8_t>(sb);
+    for (int k = 0; k < 2; ++k) {
+      float o[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        o[r] = __uint_as_float(
+            static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + (32 * (rb0 + k) + r) * kGmxStride + 2 * c))
+            << 16);
+      uint32_t codes[8];
+      const uint32_t sb = mx_quant32(o, codes);
+      __stcs(dq + 2 * k, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+      __stcs(dq + 2 * k + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+      dstR_sf[sf_atom_offset_g(c0 + c, (r0 >> 5) + rb0 + k, rcap / 128, gT)] = static_cast<uint8_t>(sb);
+    }
   }
 }
 
@@ -343,9 +360,9 @@ int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const i
                           int32_t H, uint8_t* dst_q, uint8_t* dst_sf, uint8_t* dstR_q, uint8_t* dstR_sf,
                           int64_t rcap, int gT, int kind, cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
-  const dim3 grid(static_cast<unsigned>((rpad_max + 31) / 32), static_cast<unsigned>(H / 128));
+  const dim3 grid(static_cast<unsigned>((rpad_max + 127) / 128), static_cast<unsigned>(H / 128));
   trace_begin(stream, kind);
-  gather_rows_mx_kernel<<<grid, 128, 0, stream>>>(src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
+  gather_rows_mx_kernel<<<grid, 256, 0, stream>>>(src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
