@@ -286,3 +286,39 @@ def test_mxfp8_sweep_sampled_parity(mok, name):
     assert not bad, errs
     del out, g
     torch.cuda.empty_cache()
+
+
+def test_mxfp8_unused_experts_and_single_row(mok):
+    """Experts without rows get exact zero weight gradients (their E4M3 GEMM tiles have no K), and a
+    layer with one routed row still matches the oracle (one 32-row block: 1 real row, 31 padding)."""
+    w = inputs.custom(T=50, H=256, I=128, E=7, K=2)
+    d = inputs.make(w, seed=2)
+    ids = d["topk_ids"]
+    ids[ids == 3] = 4
+    ids[ids == 6] = 0
+    d["topk_ids"] = ids
+    mx_gpu = _mx_inputs(mok, d)
+    out, g = _run_mx(mok, d, w, mok.make_config(128, 256, precision=mok.MOK_MXFP8), mx_gpu)
+    for e in (3, 6):
+        assert not g.dw_gate[e].any() and not g.dw_up[e].any() and not g.dw_down[e].any()
+    assert torch.isfinite(out).all() and torch.isfinite(g.dx).all()
+    w1 = inputs.custom(T=1, H=128, I=128, E=3, K=1)
+    d1 = inputs.make(w1, seed=3)
+    mx1 = _mx_inputs(mok, d1)
+    out1, g1 = _run_mx(mok, d1, w1, mok.make_config(128, 128, precision=mok.MOK_MXFP8), mx1)
+    mx_ref = oracle.mx_weights(inputs.bits(d1["Wg"]), inputs.bits(d1["Wu"]), inputs.bits(d1["Wd"]))
+    ref = oracle.layer_mx(d1["topk_ids"].numpy(), d1["topk_weights"].numpy(), inputs.bits(d1["x"]),
+                          inputs.bits(d1["dY"]), mx_ref, w1.E, w1.I)
+    errs = dict(out=rel_err(to_f64(out1), ref["out"]), dX=rel_err(to_f64(g1.dx), ref["dX"]),
+                dWg=rel_err(to_f64(g1.dw_gate), ref["dWg"]), dWd=rel_err(to_f64(g1.dw_down), ref["dWd"]),
+                dS=rel_err(to_f64(g1.d_topk_weights), ref["dS"]))
+    assert all(v <= TOL_MX for v in errs.values()), errs
+
+
+def test_mxfp8_empty_batch(mok):
+    w = inputs.custom(T=0, H=128, I=128, E=4, K=2)
+    d = inputs.make(w, seed=0)
+    mx_gpu = _mx_inputs(mok, d)
+    out, g = _run_mx(mok, d, w, mok.make_config(128, 128, precision=mok.MOK_MXFP8), mx_gpu)
+    assert out.numel() == 0
+    assert not g.dw_gate.any() and not g.dw_up.any() and not g.dw_down.any()
