@@ -91,7 +91,9 @@ typedef struct {
  *   inv[R]               row holding each slot
  *   tiles[tiles_max][4]  minibatch tiles {expert, first row, valid rows, first row / MB}
  *   mblocks[mblocks_max][4]  128-row blocks {expert, first row, valid rows, tile index}
- *   meta[16]             meta[0] = Rpad, meta[1] = number of tiles, meta[2] = number of blocks
+ *   meta[16]             meta[0] = Rpad, meta[1] = number of tiles, meta[2] = number of blocks,
+ *                        meta[3] = number of block pairs (two consecutive 128-row blocks of one
+ *                        tile, or a tile's last single block) used by the library's GEMMs
  *   row_weight[rpad_max] fp32 combine weight of each row (0 on padding rows)
  *   row_token[rpad_max]  token of each row (-1 on padding rows)
  *   status               device status word (bit (1 << mok_status code) per problem seen) */

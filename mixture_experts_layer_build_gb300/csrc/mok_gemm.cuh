@@ -10,6 +10,15 @@
 //   WGRAD_GU    [dWg;dWu]_e = [dg|du]_e^T Xg_e                                  (K = rows of e, A,B MN-major)
 //   WGRAD_D     dWd_e = dYg_e^T (s a)_e                                         (K = rows of e, A,B MN-major)
 //
+// Row-tiled BF16 tiles may run on CTA pairs (chosen by shape, use_pairs; a cluster of two CTAs,
+// tcgen05.mma.cta_group::2, M = 256): the
+// pair shares one B tile, each CTA loading half of it, so a CTA receives 32 KB per K block of a
+// 128 x 256 accumulator instead of 48 KB and keeps six K blocks in flight instead of four.  The
+// row-tiled variants pair two consecutive 128-row blocks of a minibatch tile (the second CTA of a
+// tile's last pair may have no rows: it loads its half of B, and skips its epilogue); the weight
+// gradients stay on single CTAs (bound by their fp32 dW writes, they lose to the pairing).  The
+// first CTA of the pair issues the MMAs; every CTA's epilogue drains its own TMEM rows.
+//
 // Roles: warp 0 lane 0 issues TMA tile loads into a ring of shared-memory stages; warp 1 owns the
 // tensor memory and its lane 0 issues tcgen05.mma (M = 128, N = BN, K = 16) into one of two TMEM
 // accumulators (MXFP8: the four K-major contractions run natively on E4M3 operands with
@@ -75,6 +84,8 @@ struct GemmArgs {
   int32_t sa_groups;
   uint8_t* out_sf2;
   uint8_t* out_sf3;
+  // CTA-pair row-tiled variants: pairs of 128-row blocks {expert, first row, tile, tile's first pair}
+  const int4* pairs;
 };
 
 
@@ -89,18 +100,20 @@ struct GemmArgs {
 //     the next tile's MMAs run.  Stage s's scale words sit in columns 256 + 12 s ...  To fit four
 //     stages, each epilogue warp stages its stores through a single 2 KB tile.
 // The scale atoms of stage s live in a ring of their own after the A/B stages.
-template <int VAR, int BN, bool MX>
+template <int VAR, int BN, bool MX, bool PAIR = false>
 struct GemmCfg {
   static_assert(!MX || BN == 128 || BN == 256, "block-scaled tiles are 128 x 128 or 128 x 256");
+  static_assert(!(MX && PAIR), "block-scaled tiles run on single CTAs");
   static constexpr bool kWide = MX && BN == 256;
   static constexpr int kAccBufs = kWide ? 1 : 2;
-  static constexpr int kStages = MX ? (kWide ? 4 : 5) : (BN == 256 ? 4 : 6);
+  static constexpr int kStages = MX ? (kWide ? 4 : 5) : PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : 6);
   static constexpr int kEpiWarps = kWide ? 8 : 4;  // warp w accesses TMEM lane quarter w % 4
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = kBM * 128;
-  static constexpr uint32_t kBBytes = BN * 128;
+  static constexpr uint32_t kBBytes = (PAIR ? BN / 2 : BN) * 128;  // the B rows this CTA holds
   static constexpr uint32_t kSfBytes = MX ? 512 + BN * 4 : 0;  // A atom, then B's BN / 128 atoms
-  static constexpr uint32_t kTxBytes = kABytes + kBBytes + kSfBytes;  // bytes landing per stage
+  // bytes landing per stage (a pair counts both CTAs' loads on the first CTA's barrier)
+  static constexpr uint32_t kTxBytes = (PAIR ? 2 : 1) * (kABytes + kBBytes) + kSfBytes;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;           // multiple of 1024: swizzle atoms
   static constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
   static constexpr uint32_t kSfCol0 = kAccBufs * BN;
@@ -119,20 +132,27 @@ struct GemmCfg {
 
 struct Unit {
   int e, row0, nt, mt, kblocks;
+  bool peer_rows;  // CTA pair: the other CTA of the pair has rows too
 };
 
-template <int VAR>
+// Units of work: one per CTA, or (PAIR) one per CTA pair.
+template <int VAR, bool PAIR>
 __device__ __forceinline__ int gemm_num_units(const GemmArgs& a) {
   if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) return a.E * a.m_tiles * a.n_tiles;
-  else return a.meta[2] * a.n_tiles;
+  else return (PAIR ? a.meta[3] : a.meta[2]) * a.n_tiles;
 }
 
 // Row-tiled variants: all units of one minibatch tile are consecutive, N tile outer and 128-row
 // block inner, so a weight tile is reused by the tile's blocks while it sits in L2.
-template <int VAR, bool MX>
-__device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
+// CTA pairs (row-tiled variants; rank = this CTA's place in the pair): the same enumeration over
+// pairs of row blocks (N tiles outer, pairs inner, within each minibatch tile).  A CTA without rows
+// gets row0 = -1.
+template <int VAR, bool MX, bool PAIR = false>
+__device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u, int rank = 0) {
   Unit w;
+  w.peer_rows = true;
   if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) {
+    static_assert(!PAIR, "weight gradients run on single CTAs");
     const int per_e = a.m_tiles * a.n_tiles;
     w.e = u / per_e;
     const int r = u - w.e * per_e;
@@ -141,6 +161,19 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u) {
     const int p0 = __ldg(a.poff + w.e), p1 = __ldg(a.poff + w.e + 1);
     w.row0 = p0;
     w.kblocks = (p1 - p0) / (MX ? 128 : kBK);
+  } else if constexpr (PAIR) {
+    const int4 pe = __ldg(a.pairs + u / a.n_tiles);
+    const int4 tl = __ldg(reinterpret_cast<const int4*>(a.tiles) + pe.z);
+    const int nmb = (tl.z + kBM - 1) / kBM;
+    const int npb = (nmb + 1) >> 1;
+    const int local = u - pe.w * a.n_tiles;
+    w.nt = local / npb;
+    const int blk = 2 * (local - w.nt * npb) + rank;
+    w.row0 = blk < nmb ? tl.y + blk * kBM : -1;
+    w.peer_rows = (blk ^ 1) < nmb;
+    w.e = pe.x;
+    w.mt = 0;
+    w.kblocks = a.k_blocks;
   } else {
     const int bq = u / a.n_tiles;
     const int4 mbk = __ldg(reinterpret_cast<const int4*>(a.mblocks) + bq);
@@ -231,6 +264,35 @@ __device__ __forceinline__ void gemm_load(const GemmArgs& a, const Unit& w, int 
   }
 }
 
+// CTA pair (BF16, row-tiled): the loads of this CTA's half of one K block, completing on the first
+// CTA's barrier `bar` (shared::cluster address).  A: this CTA's 128 rows (none when row0 < 0); B:
+// columns [rank * BN / 2, (rank + 1) * BN / 2) of the pair's N tile -- for GATEUP the first CTA
+// holds the 128 gate rows, the second the same 128 up rows.
+template <int VAR, int BN>
+__device__ __forceinline__ void gemm_load_pair(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
+                                               uint32_t bar, const CUtensorMap* tA, const CUtensorMap* tB,
+                                               const CUtensorMap* tB2, int rank) {
+  constexpr int HB = BN / 2;
+  const int k0 = kb * kBK;
+  if (w.row0 >= 0) tma_load_2d_pair(sa, tA, bar, k0, w.row0);
+  if constexpr (VAR == V_FWD_GATEUP) {
+    tma_load_2d_pair(sb, rank ? tB2 : tB, bar, k0, w.e * a.I + w.nt * HB);
+  } else if constexpr (VAR == V_FWD_DOWN) {
+    tma_load_2d_pair(sb, tB, bar, k0, w.e * a.H + w.nt * BN + rank * HB);
+  } else if constexpr (VAR == V_DGRAD1) {
+#pragma unroll
+    for (int j = 0; j < HB / 64; ++j)
+      tma_load_2d_pair(sb + j * 8192, tB, bar, w.nt * BN + rank * HB + j * 64, w.e * a.H + k0);
+  } else {
+    static_assert(VAR == V_DGRAD2, "row-tiled variants only");
+    const bool first = kb < a.kb_split;
+    const CUtensorMap* tm = first ? tB : tB2;
+    const int krow = w.e * a.I + (first ? k0 : k0 - a.kb_split * kBK);
+#pragma unroll
+    for (int j = 0; j < HB / 64; ++j) tma_load_2d_pair(sb + j * 8192, tm, bar, w.nt * BN + rank * HB + j * 64, krow);
+  }
+}
+
 // SwiGLU pieces in fp32 with the fast approximate division (about 2 ulp; the results are rounded to
 // bf16 next, 2^-9).
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
@@ -304,10 +366,13 @@ __device__ __forceinline__ void unpack8(uint4 x, float* v) {
   v[4] = bf16_lo(x.z); v[5] = bf16_hi(x.z); v[6] = bf16_lo(x.w); v[7] = bf16_hi(x.w);
 }
 
-// Hand the accumulator back to the MMA warp once this thread has read its last TMEM column.
+// Hand the accumulator back to the MMA warp once this thread has read its last TMEM column.  PAIR:
+// `tempty` is the shared::cluster address of the first CTA's barrier.
+template <bool PAIR = false>
 __device__ __forceinline__ void release_acc(uint32_t tempty) {
   tc_fence_before();
-  mbar_arrive(tempty);
+  if constexpr (PAIR) mbar_arrive_cluster(tempty);
+  else mbar_arrive(tempty);
 }
 
 // The forward context's g, u, a for one 32-column chunk of one row (DGRAD1 epilogue operand).
@@ -362,7 +427,7 @@ __device__ __forceinline__ void quant_rows_store(const float (&v)[32], uint32_t 
 // = the warp's column half in the wide (8-warp) configuration.  tO0 / tO1 / tO2 are the output
 // tensor maps of the variant; `tempty` is released as soon as the last accumulator column has been
 // read.  `pre` holds DGRAD1's first prefetched context chunk.
-template <int VAR, int BN, bool MX, class Stg>
+template <int VAR, int BN, bool MX, bool PAIR, class Stg>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int h, int lane,
                                               uint32_t taddr, Stg& stg, uint32_t scratch, const CUtensorMap* tO0,
                                               const CUtensorMap* tO1, const CUtensorMap* tO2, uint32_t tempty,
@@ -381,7 +446,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     tmem_ld_32x32b_x32(taddr + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(ur));
     tmem_ld_32x32b_x32(taddr + 128 + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(ur + 32));
     tmem_ld_wait();
-    release_acc(tempty);
+    release_acc<PAIR>(tempty);
 #pragma unroll
     for (int c = 0; c < 64; c += 32) {
       uint4 ch[4];
@@ -419,7 +484,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     for (int j = 0; j < 4; ++j)
       tmem_ld_32x32b_x32(taddr + 128 * h + 32 * j, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * j));
     tmem_ld_wait();
-    release_acc(tempty);
+    release_acc<PAIR>(tempty);
 #pragma unroll
     for (int c = 0; c < 128; c += 32) {
       uint4 ch[4];
@@ -440,7 +505,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       float g[64], u[64];
       tmem_ld64(taddr + c, g);
       tmem_ld64(taddr + BN / 2 + c, u);
-      if (c + 64 >= BN / 2) release_acc(tempty);
+      if (c + 64 >= BN / 2) release_acc<PAIR>(tempty);
       uint4 ch[8];
       pack_bf16<64>(g, ch);
       stg.template put<128>(ch, tO0, i0 + c, rowc);
@@ -457,7 +522,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     for (int c = 0; c < BN; c += 64) {
       float v[64];
       tmem_ld64(taddr + c, v);
-      if (c + 64 >= BN) release_acc(tempty);
+      if (c + 64 >= BN) release_acc<PAIR>(tempty);
       uint4 ch[8];
       pack_bf16<64>(v, ch);
       stg.template put<128>(ch, tO0, w.nt * BN + c, rowc);
@@ -489,7 +554,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       uint32_t rv[32];
       tmem_ld_32x32b_x32(taddr + c, rv);
       tmem_ld_wait();
-      if (c + 32 >= BN) release_acc(tempty);
+      if (c + 32 >= BN) release_acc<PAIR>(tempty);
       const float* g = reinterpret_cast<const float*>(g4);
       const float* u = reinterpret_cast<const float*>(u4);
 #pragma unroll
@@ -542,7 +607,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       uint32_t rv[32];
       tmem_ld_32x32b_x32(taddr + c, rv);
       tmem_ld_wait();
-      if (c + 32 >= BN) release_acc(tempty);
+      if (c + 32 >= BN) release_acc<PAIR>(tempty);
       uint4 cdg[4], cdu[4], csa[4];
       {
 #pragma unroll
@@ -595,7 +660,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
 #pragma unroll
       for (int i = 0; i < 128; ++i) r[i] = 0u;
     }
-    release_acc(tempty);
+    release_acc<PAIR>(tempty);
 #pragma unroll
     for (int c = 0; c < 128; c += 16) {
       uint4 ch[4];
@@ -616,14 +681,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       tm = tO0;
       r0 = w.e * a.H + m0;
     }
-    if (empty) release_acc(tempty);
+    if (empty) release_acc<PAIR>(tempty);
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
       uint32_t rv[32];
       if (!empty) {
         tmem_ld_32x32b_x32(taddr + c, rv);
         tmem_ld_wait();
-        if (c + 32 >= BN) release_acc(tempty);
+        if (c + 32 >= BN) release_acc<PAIR>(tempty);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) rv[i] = 0u;
@@ -648,16 +713,16 @@ __device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity, u
   return true;
 }
 
-template <int VAR, int BN, bool MX>
-__global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
+template <int VAR, int BN, bool MX, bool PAIR>
+__global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
                 const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
                 const GemmArgs args) {
-  using C = GemmCfg<VAR, BN, MX>;
+  using C = GemmCfg<VAR, BN, MX, PAIR>;
   constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) && !MX;
   constexpr bool kBmn = (VAR >= V_DGRAD1) && !MX;
-  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
+  constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * kBM : kBM, BN, kAmn, kBmn);
   constexpr int S = C::kStages;
 
   extern __shared__ uint8_t smem_raw[];
@@ -669,7 +734,9 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
   const uint32_t scratch0 = base + C::kScratchOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kScratchOff + C::kScratchBytes);
   // bars[0..S) full, [S..2S) empty, [2S, 2S+2) accumulator full, [2S+2, 2S+4) accumulator empty,
-  // [2S+4] drain
+  // [2S+4] drain.  A pair uses the first CTA's full and accumulator-empty barriers (both CTAs'
+  // loads and epilogues count there) and each CTA's own empty, accumulator-full and drain
+  // barriers (the first CTA's commits arrive on both).
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -680,6 +747,9 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * S + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
@@ -687,7 +757,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 32 * C::kEpiWarps);
+      mbar_init(tempty_bar(a), (PAIR ? 2 : 1) * 32 * C::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -700,14 +770,20 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
     tma_prefetch_desc(&tmO2);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int num_units = gemm_num_units<VAR>(args);
+  const int num_units = gemm_num_units<VAR, PAIR>(args);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -717,17 +793,24 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
       int last_parity[S];
       for (int s = 0; s < S; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const Unit w = gemm_decode<VAR, MX>(args, u);
+      for (int u = unit0; ok && u < num_units; u += unit_step) {
+        const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
         for (int kb = 0; kb < w.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
           const uint32_t sa = base + stage * C::kStageBytes;
-          gemm_load<VAR, BN, MX>(args, w, kb, sa, sa + C::kABytes, sf_ring + stage * C::kSfBytes, full_bar(stage),
-                                 &tmA, &tmB, &tmB2);
+          if constexpr (PAIR) {
+            if (rank == 0)
+              mbar_arrive_expect_tx(full_bar(stage), w.peer_rows ? C::kTxBytes : C::kTxBytes - C::kABytes);
+            gemm_load_pair<VAR, BN>(args, w, kb, sa, sa + C::kABytes, mapa_shared(full_bar(stage), 0), &tmA, &tmB,
+                                    &tmB2, rank);
+          } else {
+            mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
+            gemm_load<VAR, BN, MX>(args, w, kb, sa, sa + C::kABytes, sf_ring + stage * C::kSfBytes, full_bar(stage),
+                                   &tmA, &tmB, &tmB2);
+          }
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == S) {
             stage = 0;
@@ -735,21 +818,23 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
           }
         }
       }
-      if (!ok) {  // wind down: let the copies already issued land before the CTA exits
+      // wind down: let the copies already issued land before the CTA exits (a pair's second CTA
+      // counts its copies on the first CTA's barriers, which that CTA waits for)
+      if (!ok && rank == 0) {
         for (int s = 0; s < S; ++s)
           if (last_parity[s] >= 0) mbar_wait_final(full_bar(s), static_cast<uint32_t>(last_parity[s]), args.status);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (the first CTA of a pair) ----------------
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
-        const Unit w = gemm_decode<VAR, MX>(args, u);
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) break;
+      for (int u = unit0; ok && u < num_units; u += unit_step) {
+        const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
+        if (!mbar_wait<PAIR>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < w.kblocks; ++kb) {
@@ -779,25 +864,31 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
                   kAmn ? sdesc_sw128(sa + ks * 2048, 8192, 1024) : sdesc_sw128(sa + ks * 32, 16, 1024);
               const uint64_t bd =
                   kBmn ? sdesc_sw128(sb + ks * 2048, 8192, 1024) : sdesc_sw128(sb + ks * 32, 16, 1024);
-              umma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+              if constexpr (PAIR) umma_bf16_pair(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
+              else umma_bf16(d_tmem, ad, bd, kIdesc, (kb | ks) != 0 ? 1u : 0u);
             }
           }
-          umma_commit(empty_bar(stage));
+          if constexpr (PAIR) umma_commit_pair(empty_bar(stage));
+          else umma_commit(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        if constexpr (PAIR) umma_commit_pair(tfull_bar(acc));
+        else umma_commit(tfull_bar(acc));
         if (++acc == C::kAccBufs) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      // every MMA issued by this thread has completed before TMEM is released
-      umma_commit(drain_bar);
+      // every MMA issued by this thread has completed before TMEM is released (in both CTAs)
+      if constexpr (PAIR) umma_commit_pair(drain_bar);
+      else umma_commit(drain_bar);
       mbar_wait_final(drain_bar, 0, args.status);
+    } else if (PAIR && lane == 0) {
+      mbar_wait_final(drain_bar, 0, args.status);  // the first CTA's MMAs into this CTA's TMEM
     }
     __syncwarp();
   } else {
@@ -808,18 +899,27 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
         staging + static_cast<uint32_t>(warp - 2) * (C::kStageBufs * C::kStageBufBytes), 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const Unit w = gemm_decode<VAR, MX>(args, u);
+    for (int u = unit0; u < num_units; u += unit_step) {
+      const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
+      const uint32_t tempty = PAIR ? mapa_shared(tempty_bar(acc), 0) : tempty_bar(acc);
       Dg1Chunk pre;
-      if constexpr (VAR == V_DGRAD1 && !MX) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);  // before the wait
+      if constexpr (VAR == V_DGRAD1 && !MX) {  // before the wait
+        if (w.row0 >= 0) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);
+      }
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      gemm_epilogue<VAR, BN, MX>(args, w, q, h, lane, taddr, stg, scratch0 + static_cast<uint32_t>(warp - 2) * 4096u,
-                                 &tmO0, &tmO1, &tmO2, tempty_bar(acc), pre);
+      if (w.row0 >= 0) {
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+        gemm_epilogue<VAR, BN, MX, PAIR>(args, w, q, h, lane, taddr, stg,
+                                         scratch0 + static_cast<uint32_t>(warp - 2) * 4096u, &tmO0, &tmO1, &tmO2,
+                                         tempty, pre);
+      } else {
+        release_acc<PAIR>(tempty);  // a pair's CTA without rows: nothing to store
+      }
       if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
@@ -827,11 +927,21 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX>::kThreads, 1)
     }
     stg.drain();
   }
+  if constexpr (PAIR) {
+    if (*abort_flag) {  // failure path: copies or arrivals of the peer may still be in flight
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < kWaitLimitNs / 100) {
+      }
+    }
+    __syncwarp();
+  }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // neither CTA leaves while the other may still address it
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
@@ -850,18 +960,28 @@ bool make_tmap_f32_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint64
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                   uint32_t box_outer, int swizzle_bytes);
 
-template <int VAR, int BN, bool MX = false>
+// Row-tiled BF16 GEMMs run on CTA pairs when most pairs of 128-row blocks are full: minibatch
+// tiles of at least two blocks (pairs never cross a tile) and at least `rows` routed rows per
+// expert on average.  (Measured on GB300: gate/up, down and dgrad2 gain 2 to 8 % from two blocks
+// per expert on; dgrad1, whose epilogue dominates, only from four; with one block per expert every
+// pair is half empty and single CTAs are faster.)
+inline bool use_pairs(const Sizes& z, int rows) {
+  return z.mb >= 2 * kRowTile && z.R >= static_cast<int64_t>(rows) * z.E;
+}
+
+template <int VAR, int BN, bool MX = false, bool PAIR = false>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o0,
                 const CUtensorMap& o1, const CUtensorMap& o2, const GemmArgs& args, int grid, cudaStream_t stream) {
-  using C = GemmCfg<VAR, BN, MX>;
+  using C = GemmCfg<VAR, BN, MX, PAIR>;
   static bool configured = false;  // per process; the attribute is per function, set once
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(C::kSmemBytes));
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX, PAIR>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return static_cast<int>(e);
     configured = true;
   }
   if (grid <= 0) return 0;
+  if (PAIR) grid = grid < 2 ? 2 : grid & ~1;  // whole pairs
   constexpr int kKind = VAR == V_FWD_GATEUP  ? K_GEMM_FWD_GATEUP
                         : VAR == V_FWD_DOWN  ? K_GEMM_FWD_DOWN
                         : VAR == V_DGRAD1    ? K_GEMM_DGRAD1
@@ -869,9 +989,21 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
                         : VAR == V_WGRAD_GU  ? K_GEMM_WGRAD_GU
                                              : K_GEMM_WGRAD_D;
   trace_begin(stream, kKind);
-  gemm_kernel<VAR, BN, MX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(a, b, b2, o0, o1, o2, args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_kernel<VAR, BN, MX, PAIR>, a, b, b2, o0, o1, o2, args);
   trace_end(stream);
-  return static_cast<int>(cudaGetLastError());
+  return le != cudaSuccess ? static_cast<int>(le) : static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace mok

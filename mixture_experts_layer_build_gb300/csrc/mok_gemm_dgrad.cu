@@ -83,7 +83,9 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   if (z.mx) return launch_dgrad_gemms_mx(z, s, ctx, st, w, num_ctas, phase, stream);
   CUtensorMap tA, tB, tB2, tO0, tO1;
   GemmArgs a = common_args(z, s);
+  a.pairs = st.pairs;  // on a CTA pair each CTA loads BN / 2 columns of B
   if (phase == 1) {
+    const bool pair = use_pairs(z, 512);
     const int BN = z.I % 256 == 0 ? 256 : 128;
     if (!make_tmap_bf16(&tA, st.dyg, z.H, z.rpad_max, 64, 128)) return -1;
     if (!make_tmap_bf16(&tB, w.w_down, z.I, static_cast<uint64_t>(z.E) * z.H, 64, 64)) return -1;
@@ -96,10 +98,14 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.out2 = st.dspart;
     if (!make_tmap_bf16_sw64(&tO0, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
     if (!make_tmap_bf16_sw64(&tO1, st.as, z.I, z.rpad_max, 32, 32)) return -1;
-    const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+    const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+    if (pair)
+      return BN == 256 ? launch_gemm<V_DGRAD1, 256, false, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
+                       : launch_gemm<V_DGRAD1, 128, false, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
     return BN == 256 ? launch_gemm<V_DGRAD1, 256>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
                      : launch_gemm<V_DGRAD1, 128>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
   }
+  const bool pair = use_pairs(z, 256);
   const int BN = z.H % 256 == 0 ? 256 : 128;
   if (!make_tmap_bf16(&tA, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 128)) return -1;
   if (!make_tmap_bf16(&tB, w.w_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 64)) return -1;
@@ -109,7 +115,10 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   a.kb_split = z.I / kBK;
   a.out0 = st.ybuf;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
-  const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+  const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+  if (pair)
+    return BN == 256 ? launch_gemm<V_DGRAD2, 256, false, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
+                     : launch_gemm<V_DGRAD2, 128, false, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream);
   return BN == 256 ? launch_gemm<V_DGRAD2, 256>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
                    : launch_gemm<V_DGRAD2, 128>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream);
 }

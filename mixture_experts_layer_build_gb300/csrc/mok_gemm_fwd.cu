@@ -75,7 +75,10 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   if (z.mx) return launch_fwd_gemms_mx(z, s, ctx, st, w, num_ctas, stream);
   CUtensorMap tA, tB, tB2, tO0, tO1;
   GemmArgs a = common_args(z, s);
-  // [g | u] = Xg [Wg_e | Wu_e]^T : 128 gate columns and the same 128 up columns per tile
+  a.pairs = st.pairs;
+  const bool pair = use_pairs(z, 256);
+  // [g | u] = Xg [Wg_e | Wu_e]^T : 128 gate columns and the same 128 up columns per tile (on a CTA
+  // pair, the first CTA holds the gate rows of Wg, the second the up rows of Wu)
   if (!make_tmap_bf16(&tA, ctx.xg, z.H, z.rpad_max, 64, 128)) return -1;
   if (!make_tmap_bf16(&tB, w.w_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 128)) return -1;
   if (!make_tmap_bf16(&tB2, w.w_up, z.H, static_cast<uint64_t>(z.E) * z.I, 64, 128)) return -1;
@@ -85,19 +88,23 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   a.out1 = ctx.a;
   if (!make_tmap_bf16(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 32)) return -1;
   if (!make_tmap_bf16(&tO1, ctx.a, z.I, z.rpad_max, 64, 32)) return -1;
-  const int grid1 = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
-  int rc = launch_gemm<V_FWD_GATEUP, 256>(tA, tB, tB2, tO0, tO1, tO0, a, grid1, stream);
+  const int grid1 = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+  int rc = pair ? launch_gemm<V_FWD_GATEUP, 256, false, true>(tA, tB, tB2, tO0, tO1, tO0, a, grid1, stream)
+                : launch_gemm<V_FWD_GATEUP, 256>(tA, tB, tB2, tO0, tO1, tO0, a, grid1, stream);
   if (rc) return rc;
-  // y = a Wd_e^T
+  // y = a Wd_e^T (each CTA of a pair loads BN / 2 rows of Wd)
   const int BN = z.H % 256 == 0 ? 256 : 128;
   if (!make_tmap_bf16(&tA, ctx.a, z.I, z.rpad_max, 64, 128)) return -1;
-  if (!make_tmap_bf16(&tB, w.w_down, z.I, static_cast<uint64_t>(z.E) * z.H, 64, BN)) return -1;
+  if (!make_tmap_bf16(&tB, w.w_down, z.I, static_cast<uint64_t>(z.E) * z.H, 64, pair ? BN / 2 : BN)) return -1;
   a.n_tiles = z.H / BN;
   a.k_blocks = z.I / kBK;
   a.out0 = st.ybuf;
   a.out1 = nullptr;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
-  const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+  const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+  if (pair)
+    return BN == 256 ? launch_gemm<V_FWD_DOWN, 256, false, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
+                     : launch_gemm<V_FWD_DOWN, 128, false, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
   return BN == 256 ? launch_gemm<V_FWD_DOWN, 256>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
                    : launch_gemm<V_FWD_DOWN, 128>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
 }

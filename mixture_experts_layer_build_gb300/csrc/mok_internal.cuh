@@ -34,6 +34,9 @@ struct Staging {
   uint16_t* dgdu;    // [rpad_max, 2I] bf16: [dg | du]
   uint16_t* as;      // [rpad_max, I] bf16: s * a
   float* dspart;     // [rpad_max, I/128] fp32: router-gradient partial sums per N tile
+  // BF16 GEMMs run by CTA pairs: per pair of consecutive 128-row blocks of one minibatch tile
+  // {expert, first row, tile index, index of the tile's first pair}; meta[3] pairs
+  int4* pairs;       // [mblocks_max]
   int32_t* chunk_hist;  // [nchunks, E+1]
   // MXFP8 mode only: E4M3 operands of the block-scaled GEMMs and their E8M0 scales, the scales
   // atom-tiled (sf_atom_offset: 512 bytes per 128 rows x 4 k-groups)

@@ -67,23 +67,24 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 }
 
 // Exclusive block scan of three values (blockDim.x == 1024).  Returns totals through tot[3].
-__device__ void block_excl_scan3(int (&v)[3], int (&tot)[3]) {
-  __shared__ int wsum[3][32];
+template <int N>
+__device__ void block_excl_scan(int (&v)[N], int (&tot)[N]) {
+  __shared__ int wsum[N][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl[3];
+  int incl[N];
 #pragma unroll
-  for (int q = 0; q < 3; ++q) {
+  for (int q = 0; q < N; ++q) {
     incl[q] = warp_incl_scan(v[q], lane);
     if (lane == 31) wsum[q][warp] = incl[q];
   }
   __syncthreads();
   if (warp == 0) {
 #pragma unroll
-    for (int q = 0; q < 3; ++q) wsum[q][lane] = warp_incl_scan(wsum[q][lane], lane);
+    for (int q = 0; q < N; ++q) wsum[q][lane] = warp_incl_scan(wsum[q][lane], lane);
   }
   __syncthreads();
 #pragma unroll
-  for (int q = 0; q < 3; ++q) {
+  for (int q = 0; q < N; ++q) {
     const int before = warp > 0 ? wsum[q][warp - 1] : 0;
     const int ex = before + incl[q] - v[q];
     tot[q] = wsum[q][31];
@@ -97,7 +98,8 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ poff,
                                                          int32_t* __restrict__ perm, int32_t* __restrict__ row_token,
                                                          float* __restrict__ row_weight, int32_t* __restrict__ tiles,
-                                                         int32_t* __restrict__ mblocks, int32_t* __restrict__ meta) {
+                                                         int32_t* __restrict__ mblocks, int32_t* __restrict__ meta,
+                                                         int4* __restrict__ pairs) {
   extern __shared__ int32_t part[];  // [32 chunk groups][E + 1]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = E + 1;
@@ -136,9 +138,13 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
   }
   const int padded = (cnt + kRowTile - 1) / kRowTile * kRowTile;
   const int ntile = (cnt + mb - 1) / mb;
-  int v[3] = {cnt, padded, ntile}, tot[3];
-  block_excl_scan3(v, tot);
-  const int off = v[0], pof = v[1], tst = v[2];
+  // pairs of consecutive 128-row blocks within each minibatch tile (the last one may be single)
+  const int npair = ntile == 0 ? 0
+                               : (ntile - 1) * ((mb / kRowTile + 1) / 2) +
+                                     ((cnt - (ntile - 1) * mb + kRowTile - 1) / kRowTile + 1) / 2;
+  int v[4] = {cnt, padded, ntile, npair}, tot[4];
+  block_excl_scan<4>(v, tot);
+  const int off = v[0], pof = v[1], tst = v[2], ppo = v[3];
   const bool overflow = (tot[1] > rpad_max) || (tot[2] > tiles_max) || (tot[1] / kRowTile > mblocks_max);
   if (e < E && !overflow) {
     counts[e] = cnt;
@@ -159,6 +165,14 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
       m[2] = min(kRowTile, cnt - b * kRowTile);
       m[3] = tst + (b * kRowTile) / mb;
     }
+    if (pairs) {
+      int p = ppo;
+      for (int q = 0; q < ntile; ++q) {
+        const int np = ((min(mb, cnt - q * mb) + kRowTile - 1) / kRowTile + 1) / 2;
+        for (int j = 0; j < np; ++j) pairs[p + j] = make_int4(e, pof + q * mb + 2 * j * kRowTile, tst + q, p);
+        p += np;
+      }
+    }
     s_pad[e] = make_int2(pof + cnt, pof + padded);
     for (int g = 0; g < 32; ++g) part[g * W + e] += pof;  // first row of group g's slots of e
   }
@@ -168,6 +182,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
     meta[0] = overflow ? 0 : tot[1];
     meta[1] = overflow ? 0 : tot[2];
     meta[2] = overflow ? 0 : tot[1] / kRowTile;
+    meta[3] = overflow || !pairs ? 0 : tot[3];
     uint32_t st = 0;
     if (s_bad) st |= 1u << MOK_ERR_BAD_EXPERT_ID;
     if (overflow) st |= 1u << MOK_ERR_CAPACITY;
@@ -273,7 +288,7 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
   trace_begin(stream, K_SCHED_SCAN);
   sched_scan_kernel<<<1, 1024, sizeof(int32_t) * 32 * (z.E + 1), stream>>>(
       z.E, nchunks, st.chunk_hist, z.mb, z.MB, z.rpad_max, z.tiles_max, z.mblocks_max, s.counts, s.offsets, s.poff,
-      s.perm, s.row_token, s.row_weight, s.tiles, s.mblocks, s.meta);
+      s.perm, s.row_token, s.row_weight, s.tiles, s.mblocks, s.meta, st.pairs);
   trace_end(stream);
   if (blocks > 0) {
     const size_t sh = sizeof(int32_t) * kHistWarps * z.E;

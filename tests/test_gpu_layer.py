@@ -73,6 +73,32 @@ def test_forward_backward_full_parity(mok, name, w):
     assert errs["xg"] == 0.0  # the gather is a copy
 
 
+# CTA-pair GEMMs (minibatch tiles of 512 rows): full pairs, and tiles whose last pair has a single
+# 128-row block (about 600 rows per expert: 4 + 1 blocks; about 350: 2 + 1)
+PAIRED = [
+    ("pairs_h256", inputs.custom(T=900, H=256, I=256, E=3, K=2)),
+    ("pairs_h384", inputs.custom(T=700, H=384, I=128, E=2, K=1)),
+]
+
+
+@pytest.mark.parametrize("name,w", PAIRED, ids=[n for n, _ in PAIRED])
+def test_cta_pair_gemms_full_parity(mok, name, w):
+    d = inputs.make(w, seed=5)
+    _, out, g = _run(mok, d, w, mok.make_config(512, 2048))
+    args = _np_args(d)
+    ref_out = oracle.forward(*args)
+    ref = oracle.backward(*args, inputs.bits(d["dY"]))
+    errs = dict(out=rel_err(to_f64(out), ref_out), dX=rel_err(to_f64(g.dx), ref["dX"]),
+                dWg=rel_err(to_f64(g.dw_gate), ref["dWg"]), dWu=rel_err(to_f64(g.dw_up), ref["dWu"]),
+                dWd=rel_err(to_f64(g.dw_down), ref["dWd"]), dS=rel_err(to_f64(g.d_topk_weights), ref["dS"]))
+    bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
+    assert not bad, errs
+    # single-CTA tiles (minibatch 128) give the same bits
+    _, out1, g1 = _run(mok, d, w, mok.make_config(128, 256))
+    assert torch.equal(out1, out) and torch.equal(g1.dx, g.dx) and torch.equal(g1.d_topk_weights, g.d_topk_weights)
+    assert torch.equal(g1.dw_gate, g.dw_gate) and torch.equal(g1.dw_down, g.dw_down)
+
+
 def test_unused_experts_get_exact_zero_gradients(mok):
     w = inputs.custom(T=50, H=128, I=128, E=7, K=2)
     d = inputs.make(w, seed=2)

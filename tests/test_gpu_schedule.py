@@ -33,6 +33,9 @@ def _compare(ids, w, E, mb, MB, g):
     ref = oracle.schedule(ids, E, mb, MB)
     rp = ref["rpad"]
     assert g["meta"][0] == rp and g["meta"][1] == ref["tiles"].shape[0] and g["meta"][2] == rp // 128
+    # block pairs of the CTA-pair GEMMs: per tile, its 128-row blocks two at a time
+    blocks = (ref["tiles"][:, 2] + 127) // 128
+    assert g["meta"][3] == int(((blocks + 1) // 2).sum())
     assert np.array_equal(g["counts"], ref["counts"])
     assert np.array_equal(g["offsets"], ref["offsets"])
     assert np.array_equal(g["poff"], ref["poff"])
