@@ -18,8 +18,10 @@ static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   a.status = s.status;
   a.sf_kq = static_cast<int32_t>(z.kq_rows());
   const uint64_t rcap = static_cast<uint64_t>(z.rcap());
+  // fp32 dW leaves in 128-row tiles: 16 columns (wide tiles, one per group of four epilogue warps)
+  // or 32 columns
   auto out_map = [&](CUtensorMap* m, float* p, uint64_t inner, uint64_t outer, int bn) {
-    return bn == 256 ? make_tmap_f32_sw64(m, p, inner, outer, 16, 32) : make_tmap_f32(m, p, inner, outer, 32, 32);
+    return bn == 256 ? make_tmap_f32_sw64(m, p, inner, outer, 16, 128) : make_tmap_f32(m, p, inner, outer, 32, 128);
   };
   {  // [dWg ; dWu]_e: M = 2I (A = [dg | du]^T), N = H (B = x^T)
     const int BN = z.mx_bn_h();
@@ -67,6 +69,8 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   a.I = z.I;
   a.H = z.H;
   a.status = s.status;
+  // fp32 dW leaves in 128-row x 32-column tiles
+  constexpr uint32_t orows = 128;
   // [dWg ; dWu]_e = [dg | du]_e^T Xg_e   (M = 2I, N = H)
   {
     const int BN = z.H % 256 == 0 ? 256 : 128;
@@ -76,8 +80,8 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.n_tiles = z.H / BN;
     a.out0 = g.dw_gate;
     a.out1 = g.dw_up;
-    if (!make_tmap_f32(&tO0, g.dw_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 32, 32)) return -1;
-    if (!make_tmap_f32(&tO1, g.dw_up, z.H, static_cast<uint64_t>(z.E) * z.I, 32, 32)) return -1;
+    if (!make_tmap_f32(&tO0, g.dw_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 32, orows)) return -1;
+    if (!make_tmap_f32(&tO1, g.dw_up, z.H, static_cast<uint64_t>(z.E) * z.I, 32, orows)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
     const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
     const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
@@ -93,7 +97,7 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.n_tiles = z.I / BN;
     a.out0 = g.dw_down;
     a.out1 = nullptr;
-    if (!make_tmap_f32(&tO0, g.dw_down, z.I, static_cast<uint64_t>(z.E) * z.H, 32, 32)) return -1;
+    if (!make_tmap_f32(&tO0, g.dw_down, z.I, static_cast<uint64_t>(z.E) * z.H, 32, orows)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
     const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
     return BN == 256 ? launch_gemm<V_WGRAD_D, 256>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
