@@ -341,6 +341,42 @@ struct Stager {
   }
 };
 
+// Output stager shared by the four epilogue warps: two 16 KB tiles of 128 rows x 128 bytes (the
+// 128-byte swizzle) in the staging area.  Warp q writes rows q * 32 + lane; after a group barrier
+// (an mbarrier of 128 arrivals, bounded wait) one thread stores the tile with a single TMA store,
+// a quarter of the stores of per-warp 32-row tiles.  A tile is refilled only after its previous
+// store has read it.  Returns false after an abort.
+struct GroupStager {
+  uint32_t base;  // 32 KB: tile 0, then tile 1
+  uint32_t bar;
+  uint32_t phase;
+  int cur;
+  int row;        // this thread's row in the tile (q * 32 + lane)
+  bool leader;
+  __device__ __forceinline__ bool sync(volatile int* abort, uint32_t* status) {
+    mbar_arrive(bar);
+    if (!mbar_wait(bar, phase, abort, status)) return false;
+    phase ^= 1u;
+    return true;
+  }
+  __device__ __forceinline__ bool put(const uint4 (&ch)[8], const CUtensorMap* tm, int c0, int row0,
+                                      volatile int* abort, uint32_t* status) {
+    const uint32_t tile = base + static_cast<uint32_t>(cur) * 16384u;
+    const uint32_t r = tile + static_cast<uint32_t>(row) * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) st_shared_v4(r + (static_cast<uint32_t>(j ^ (row & 7)) << 4), ch[j]);
+    fence_proxy_async_smem();
+    if (!sync(abort, status)) return false;  // all 128 rows are in the tile
+    if (leader) {
+      tma_store_2d(tm, tile, c0, row0);
+      bulk_commit();
+      bulk_wait_read<1>();  // the other tile's store has read it
+    }
+    cur ^= 1;
+    return sync(abort, status);
+  }
+};
+
 template <int N>
 __device__ __forceinline__ void pack_bf16(const float* v, uint4* ch) {
 #pragma unroll
@@ -431,8 +467,8 @@ template <int VAR, int BN, bool MX, bool PAIR, class Stg>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int h, int lane,
                                               uint32_t taddr, Stg& stg, uint32_t scratch, const CUtensorMap* tO0,
                                               const CUtensorMap* tO1, const CUtensorMap* tO2, uint32_t tempty,
-                                              Dg1Chunk& pre, uint32_t epi_bar, uint32_t& epi_phase,
-                                              volatile int* abort_flag) {
+                                              Dg1Chunk& pre, GroupStager& gs, uint32_t epi_bar,
+                                              uint32_t& epi_phase, volatile int* abort_flag) {
   if constexpr (VAR == V_FWD_GATEUP && MX) {
     // accumulator columns [0, 128) are gate, [128, 256) up, for I columns nt*128 ...; this warp
     // takes 64 of them (half h).  g and u leave in fp32 (the backward re-quantises dg, du from
@@ -500,7 +536,6 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
   } else if constexpr (VAR == V_FWD_GATEUP) {
     // columns [0, BN/2) of the accumulator are gate, [BN/2, BN) up, for I columns i0 ...
     const int i0 = w.nt * (BN / 2);
-    const int rowc = w.row0 + q * 32;
 #pragma unroll 1
     for (int c = 0; c < BN / 2; c += 64) {
       float g[64], u[64];
@@ -509,16 +544,15 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       if (c + 64 >= BN / 2) release_acc<PAIR>(tempty);
       uint4 ch[8];
       pack_bf16<64>(g, ch);
-      stg.template put<128>(ch, tO0, i0 + c, rowc);
+      if (!gs.put(ch, tO0, i0 + c, w.row0, abort_flag, a.status)) return;
       pack_bf16<64>(u, ch);
-      stg.template put<128>(ch, tO0, a.I + i0 + c, rowc);
+      if (!gs.put(ch, tO0, a.I + i0 + c, w.row0, abort_flag, a.status)) return;
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
       pack_bf16<64>(g, ch);
-      stg.template put<128>(ch, tO1, i0 + c, rowc);
+      if (!gs.put(ch, tO1, i0 + c, w.row0, abort_flag, a.status)) return;
     }
   } else if constexpr (VAR == V_FWD_DOWN || VAR == V_DGRAD2) {
-    const int rowc = w.row0 + q * 32;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 64) {
       float v[64];
@@ -526,7 +560,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       if (c + 64 >= BN) release_acc<PAIR>(tempty);
       uint4 ch[8];
       pack_bf16<64>(v, ch);
-      stg.template put<128>(ch, tO0, w.nt * BN + c, rowc);
+      if (!gs.put(ch, tO0, w.nt * BN + c, w.row0, abort_flag, a.status)) return;
     }
   } else if constexpr (VAR == V_DGRAD1 && MX) {
     // MXFP8: dA' = dYq Wd^T (block-scaled), the SwiGLU backward from the forward's fp32 g, u, and
@@ -688,13 +722,10 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       epi_phase ^= 1u;
     }
   } else {
-    // weight gradients, fp32 out: the four epilogue warps fill one 128-row x 32-column tile (16 KB,
-    // two buffers in the staging area) and one thread stores it -- a quarter of the TMA stores of
-    // per-warp 32-row tiles, which measured 5 % (384 rows per expert) to 17 % (64 rows per expert)
-    // faster.  Experts without rows get zeros.
+    // weight gradients, fp32 out in 128-row x 32-column tiles of the group stager (a quarter of the
+    // TMA stores of per-warp 32-row tiles: 5 % (384 rows per expert) to 17 % (64 rows per expert)
+    // faster).  Experts without rows get zeros.
     const bool empty = w.kblocks == 0;
-    const uint32_t base = stg.buf0 - static_cast<uint32_t>((q + 2) & 3) * 8192u;  // warp 2's staging = tile 0
-    const bool leader = q == 2 && lane == 0;
     const int mt0 = w.mt * kBM;
     const CUtensorMap* tm;
     int rt;
@@ -717,25 +748,10 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
 #pragma unroll
         for (int i = 0; i < 32; ++i) rv[i] = 0u;
       }
-      // row q * 32 + lane of the tile, 16-byte chunk j at j ^ (row & 7) (the 128-byte swizzle)
-      const uint32_t tb = base + static_cast<uint32_t>((c >> 5) & 1) * 16384u;
-      const uint32_t row = tb + static_cast<uint32_t>(q * 32 + lane) * 128u;
+      uint4 ch[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        st_shared_v4(row + (static_cast<uint32_t>(j ^ (lane & 7)) << 4),
-                     make_uint4(rv[4 * j], rv[4 * j + 1], rv[4 * j + 2], rv[4 * j + 3]));
-      fence_proxy_async_smem();
-      mbar_arrive(epi_bar);  // all 128 rows are in the tile
-      if (!mbar_wait(epi_bar, epi_phase, abort_flag, a.status)) return;
-      epi_phase ^= 1u;
-      if (leader) {
-        tma_store_2d(tm, tb, w.nt * BN + c, rt);
-        bulk_commit();
-        bulk_wait_read<1>();  // the other buffer's store has read it
-      }
-      mbar_arrive(epi_bar);
-      if (!mbar_wait(epi_bar, epi_phase, abort_flag, a.status)) return;
-      epi_phase ^= 1u;
+      for (int j = 0; j < 8; ++j) ch[j] = make_uint4(rv[4 * j], rv[4 * j + 1], rv[4 * j + 2], rv[4 * j + 3]);
+      if (!gs.put(ch, tm, w.nt * BN + c, rt, abort_flag, a.status)) return;
     }
   }
 }
@@ -942,6 +958,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
         staging + static_cast<uint32_t>(warp - 2) * (C::kStageBufs * C::kStageBufBytes), 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0, epi_phase = 0;
+    // non-wide tiles: the four warps' staging (2 x 4 x 4 KB) serves as the group stager's two tiles
+    GroupStager gs{staging, epi_bar, 0u, 0, q * 32 + lane, q == 2 && lane == 0};
     for (int u = unit0; u < num_units; u += unit_step) {
       const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
       const uint32_t tempty = PAIR ? mapa_shared(tempty_bar(acc), 0) : tempty_bar(acc);
@@ -959,7 +977,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
         gemm_epilogue<VAR, BN, MX, PAIR>(args, w, q, h, lane, taddr, stg,
                                          scratch0 + static_cast<uint32_t>(warp - 2) * 4096u, &tmO0, &tmO1, &tmO2,
-                                         tempty, pre, epi_bar, epi_phase, abort_flag);
+                                         tempty, pre, gs, epi_bar, epi_phase, abort_flag);
       } else {
         release_acc<PAIR>(tempty);  // a pair's CTA without rows: nothing to store
       }

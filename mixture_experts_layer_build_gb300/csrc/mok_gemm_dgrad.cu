@@ -71,7 +71,7 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   a.sfb_kq = z.I / 128;
   a.out0 = st.ybuf;
   if (!(BN == 256 ? make_tmap_bf16_sw64(&tO0, st.ybuf, z.H, z.rpad_max, 32, 32)
-                  : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)))
+                  : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)))
     return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
   return BN == 256 ? launch_gemm<V_DGRAD2, 256, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
@@ -114,7 +114,7 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   a.k_blocks = 2 * z.I / kBK;
   a.kb_split = z.I / kBK;
   a.out0 = st.ybuf;
-  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
+  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)) return -1;
   const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
   if (pair)
     return BN == 256 ? launch_gemm<V_DGRAD2, 256, false, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)

@@ -63,7 +63,7 @@ static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx&
   a.out1 = nullptr;
   a.out_sf = nullptr;
   if (!(BN == 256 ? make_tmap_bf16_sw64(&tO0, st.ybuf, z.H, z.rpad_max, 32, 32)
-                  : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)))
+                  : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)))
     return -1;
   const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
   return BN == 256 ? launch_gemm<V_FWD_DOWN, 256, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
@@ -86,8 +86,8 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   a.k_blocks = z.H / kBK;
   a.out0 = ctx.gu;
   a.out1 = ctx.a;
-  if (!make_tmap_bf16(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 32)) return -1;
-  if (!make_tmap_bf16(&tO1, ctx.a, z.I, z.rpad_max, 64, 32)) return -1;
+  if (!make_tmap_bf16(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 128)) return -1;
+  if (!make_tmap_bf16(&tO1, ctx.a, z.I, z.rpad_max, 64, 128)) return -1;
   const int grid1 = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
   int rc = pair ? launch_gemm<V_FWD_GATEUP, 256, false, true>(tA, tB, tB2, tO0, tO1, tO0, a, grid1, stream)
                 : launch_gemm<V_FWD_GATEUP, 256>(tA, tB, tB2, tO0, tO1, tO0, a, grid1, stream);
@@ -100,7 +100,7 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   a.k_blocks = z.I / kBK;
   a.out0 = st.ybuf;
   a.out1 = nullptr;
-  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 32)) return -1;
+  if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)) return -1;
   const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
   if (pair)
     return BN == 256 ? launch_gemm<V_FWD_DOWN, 256, false, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
