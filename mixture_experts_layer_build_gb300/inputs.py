@@ -122,6 +122,9 @@ def make(w: Workload, seed: int = 0, weight_device: str = "cpu", with_dy: bool =
     Wu = _normal(gw, (E, I, H), 0.02, weight_device)
     Wd = _normal(gw, (E, H, I), 0.02, weight_device)
     out = dict(x=x, topk_ids=ids.to(torch.int32).contiguous(), topk_weights=wts.contiguous(), Wg=Wg, Wu=Wu, Wd=Wd)
+    if w.router in ("softmax", "softmax_bias"):  # the router's own draws, for the router step
+        out["Wr"] = Wr
+        out["router_bias"] = bias if w.router == "softmax_bias" else None
     if with_dy:
         out["dY"] = _normal(g, (T, H), 1.0, "cpu")
     return out

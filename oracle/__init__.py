@@ -3,7 +3,8 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference arm may
 import this package.  The CUDA library never does, and the two share no code.
 
-This module is argument marshalling over ``mok_oracle.c`` (plain C, fp64 loops); every function
+This module is argument marshalling over ``mok_oracle.c`` (plain C, fp64 loops), ``mok_oracle_mx.c``
+(the MXFP8 mode) and ``mok_oracle_router.c`` (the router step before the layer); every function
 cites, in the C source, the page passage it follows.  Arrays cross as numpy arrays:
 bf16 tensors as ``uint16`` bit patterns, E4M3 / E8M0 as ``uint8``.
 
@@ -22,6 +23,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mok_oracle.c")
 _SRC_MX = os.path.join(_HERE, "mok_oracle_mx.c")
+_SRC_ROUTER = os.path.join(_HERE, "mok_oracle_router.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -31,11 +33,12 @@ MT = 128  # GEMM row tile used for the padded expert-grouped layout
 
 def build(force: bool = False) -> str:
     """Compile ``mok_oracle.c`` into ``liboracle.so`` with gcc (OpenMP, no fast-math)."""
-    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_MX))
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_MX), os.path.getmtime(_SRC_ROUTER))
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, _SRC_MX, "-lm"])
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, _SRC_MX, _SRC_ROUTER,
+             "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -83,6 +86,12 @@ def _load():
             lib.orc_tokens_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i64, P, P, P, P]
             lib.orc_dw_block_mx.restype = None
             lib.orc_dw_block_mx.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, i32, i32, i64, P, P, P, P]
+            lib.orc_router_logits.restype = None
+            lib.orc_router_logits.argtypes = [P, P, P, i64, i32, i32, P]
+            lib.orc_router_topk.restype = None
+            lib.orc_router_topk.argtypes = [P, i64, i32, i32, P, P]
+            lib.orc_router_backward.restype = None
+            lib.orc_router_backward.argtypes = [P, P, i64, i32, i32, i32, P, P, P, P, P, P]
             lib.orc_num_threads.restype = ctypes.c_int
             lib.orc_num_threads.argtypes = []
             _lib = lib
@@ -366,3 +375,47 @@ def dw_block_mx(ids, s, x, dY, mx: dict, E: int, I: int, e: int, i0: int, hs):
     _load().orc_dw_block_mx(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(dY), ptrs, int(e), int(i0), hs.size, _p(hs),
                             _p(dwg), _p(dwu), _p(dwd))
     return dwg, dwu, dwd
+
+
+# ---------------------------------------------------------------------------------------------
+# router step (mok_oracle_router.c): logits in fp32 as the kernel takes its top-k decision, the
+# rest in fp64
+# ---------------------------------------------------------------------------------------------
+def router_logits(x, w, bias=None) -> np.ndarray:
+    """fp32 logits [T,E] of x [T,H] (bf16 bits) and W [H,E] (bf16 bits), + bias [E] fp32."""
+    x, w = _u16(x), _u16(w)
+    T, H = x.shape
+    E = w.shape[1]
+    assert w.shape[0] == H
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    out = np.empty((T, E), dtype=np.float32)
+    _load().orc_router_logits(_p(x), _p(w), None if b is None else _p(b), T, H, E, _p(out))
+    return out
+
+
+def router_topk(logits, K: int):
+    """Top-K ids [T,K] int32 (descending logit, equal logits in ascending id) and the renormalised
+    weights [T,K] fp64."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    ids = np.empty((T, K), dtype=np.int32)
+    wts = np.empty((T, K))
+    _load().orc_router_topk(_p(lg), T, E, K, _p(ids), _p(wts))
+    return ids, wts
+
+
+def router_backward(x, w, ids, weights, d_topk, with_bias: bool = False):
+    """dW [H,E], dbias [E] (or None) and dx [T,H], fp64, from the forward's ids / fp32 weights and
+    the fp32 top-k weight gradient."""
+    x, w = _u16(x), _u16(w)
+    T, H = x.shape
+    E = w.shape[1]
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    K = ids.shape[1]
+    wt = np.ascontiguousarray(weights, dtype=np.float32)
+    dt = np.ascontiguousarray(d_topk, dtype=np.float32)
+    dw, dx = np.empty((H, E)), np.empty((T, H))
+    db = np.empty(E) if with_bias else None
+    _load().orc_router_backward(_p(x), _p(w), T, H, E, K, _p(ids), _p(wt), _p(dt), _p(dw),
+                                None if db is None else _p(db), _p(dx))
+    return dw, db, dx
