@@ -348,6 +348,85 @@ def config_of(w, args, n):
             "l2": f"inputs larger than L2: {wbytes / 1e6:.0f} MB of expert weights streamed every step, no flush"}
 
 
+# fp32 fused multiply-add peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def time_router(args, mok, w, d, cfg, dev, stream, peaks) -> dict:
+    """Router forward (logits, top-k) and backward (W transposed, g and dx, dW and d_bias) on the
+    workload's own router draws, with the schedule built from the router's ids; CUDA events
+    around K steps after W warm-ups, then the per-kernel event trace."""
+    x = d["x"].to(dev)
+    Wr = d["Wr"].to(dev)
+    b = None if d["router_bias"] is None else d["router_bias"].to(dev)
+    T, H, E, K = w.T, w.H, w.E, w.K
+    shape = mok.make_shape(T, H, w.I, E, K)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, K), dtype=torch.float32, device=dev)
+    dtopk = torch.randn((T, K), generator=torch.Generator().manual_seed(5)).to(dev)
+    dw = torch.empty((H, E), dtype=torch.float32, device=dev)
+    db = torch.empty((E,), dtype=torch.float32, device=dev) if b is not None else None
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    rws = torch.empty(mok.mok_router_workspace_bytes(shape), dtype=torch.uint8, device=dev)
+    sws = mok.alloc_workspace(cfg, shape, device=dev)
+    with torch.cuda.stream(stream):
+        mok.mok_router_forward(shape, x, Wr, b, logits, ids, wts, stream)
+        sched = mok.mok_build_schedule(cfg, shape, ids, wts, sws, stream)
+
+    def fwd():
+        mok.mok_router_forward(shape, x, Wr, b, logits, ids, wts, stream)
+
+    def bwd():
+        mok.mok_router_backward(sched, x, Wr, ids, wts, dtopk, dw, db, dx, False, rws, stream)
+
+    res = {"note": "router step before the layer (logits x W_r + b, softmax top-k, renormalised weights; "
+                   "backward to W_r, b and x); timed on its own, not part of the layer step"}
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            fwd()
+            bwd()
+    torch.cuda.synchronize()
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    e[0].record(stream)
+    for _ in range(args.steps):
+        fwd()
+    e[1].record(stream)
+    for _ in range(args.steps):
+        bwd()
+    e[2].record(stream)
+    torch.cuda.synchronize()
+    res["fwd_ms"] = e[0].elapsed_time(e[1]) / args.steps
+    res["bwd_ms"] = e[1].elapsed_time(e[2]) / args.steps
+    res["ms_per_step"] = res["fwd_ms"] + res["bwd_ms"]
+    tr = mok.Tracer(capacity=8 * args.steps + 16)
+    with tr:
+        for _ in range(args.steps):
+            fwd()
+            bwd()
+    per = {}
+    for name, t in tr.records():
+        p = per.setdefault(name, [0.0, 0])
+        p[0] += t
+        p[1] += 1
+    kern = {k: {"avg_ms": v[0] / v[1], "launches": v[1]} for k, v in per.items()}
+    if "router_logits" in kern:  # fp32 fused multiply-adds on the CUDA cores: ALU-bound
+        ms = kern["router_logits"]["avg_ms"]
+        tf = 2.0 * T * H * E / (ms * 1e-3) / 1e12
+        kern["router_logits"].update({"tflops": tf, "bound": "alu", "peak_tflops": FP32_ALU_TFLOPS,
+                                      "frac": tf / FP32_ALU_TFLOPS})
+    hbm = peaks["hbm_gbs"]
+    # unique bytes: W^T read once by dx (its K rows per token are L2 hits), x read once by dW
+    byts = {"router_topk": T * E * 4 + T * K * 8, "router_transpose": 2 * H * E * 2,
+            "router_dx": T * K * 12 + E * H * 2 + T * H * 2, "router_dw": T * K * 8 + T * H * 2 + H * E * 4}
+    for k, nb in byts.items():
+        if k in kern:
+            g = nb / (kern[k]["avg_ms"] * 1e-3) / 1e9
+            kern[k].update({"gbs": g, "bound": "hbm", "frac": g / hbm})
+    res["kernels"] = kern
+    return res
+
+
 def ours(args, rank, ws, local_rank):
     from mixture_experts_layer_build_gb300 import inputs, mok
 
@@ -430,6 +509,9 @@ def ours(args, rank, ws, local_rank):
                  "peak_source": (f"{peak_src} (burst bf16 GEMM / STREAM copy)" if peak_src == "measured"
                                  else "fallback") + (" x2 nominal e4m3/bf16" if kd == "e4m3" else ""),
                  "traffic_note": tnote, "algorithmic_flops_per_launch": fl, "algorithmic_bytes_per_launch": nb})
+
+    # ---- the router step before the layer (timed on its own; not part of the layer step) ----
+    router = time_router(args, mok, w, d, cfg, dev, stream, peaks) if "Wr" in d else None
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its own inputs host->device and its results device->host inside the timed
@@ -523,6 +605,8 @@ def ours(args, rank, ws, local_rank):
             "clocks": clk,
             "device_status": status,
         }
+        if router is not None:
+            result["router"] = router
     return result, d, w
 
 

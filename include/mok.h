@@ -295,6 +295,42 @@ typedef struct {
 
 MOK_API mok_status mok_mx_operands_of(const mok_schedule* sched, const void* fwd_ctx, mok_mx_operands* out);
 
+/* ---------------------------------------------------------------------------------------------
+ * Router step (before the layer; its outputs are mok_build_schedule's inputs).  "Mixture-of-
+ * Kittens (MoK)" project card, "Functional API": the schedule takes the router's top-k expert ids
+ * and weights; "Cursor Open-Sources ...", English summary: the router-weight gradient is part of
+ * the backward.  A linear router: logits = x W + b, W [H,E] bf16 row-major, b [E] fp32 optional.
+ * Shapes: H a multiple of 128, 1 <= K <= 32, K <= E <= 1024.
+ * ------------------------------------------------------------------------------------------- */
+
+/* Bytes of device workspace mok_router_backward needs (256-byte aligned): W transposed (E*H bf16)
+ * and the gradient of the chosen logits (T*K fp32).  0 for an unsupported shape. */
+MOK_API size_t mok_router_workspace_bytes(const mok_shape* shape);
+
+/* logits [T,E] fp32: logits[t,e] = (sum over h = 0 .. H-1 in ascending order of x[t,h] W[h,e],
+ * one fused multiply-add per step in fp32) + b[e] (one fp32 add; bias may be NULL).  topk_ids
+ * [T,K] int32: the K largest logits of each token in descending order, equal logits in ascending
+ * expert id (NaN logits are never chosen; a token with fewer than K non-NaN logits gets id -1).
+ * topk_weights [T,K] fp32: the softmax over the K chosen logits, which is the softmax over all E
+ * renormalised to the chosen K.  x [T,H] bf16 and W device pointers; all outputs device, written
+ * in full. */
+MOK_API mok_status mok_router_forward(const mok_shape* shape, const void* x, const void* w_router, const float* bias,
+                                      float* logits, int32_t* topk_ids, float* topk_weights, void* stream);
+
+/* Router backward from d_topk_weights [T,K] fp32 (mok_backward's router-weight gradient).  With
+ * the forward's ids and weights: g[t,k] = w[t,k] (d[t,k] - sum_j w[t,j] d[t,j]) is the gradient of
+ * the chosen logit (the others get 0).  Writes dw_router [H,E] fp32, dw[h,e] = sum over the rows
+ * of expert e in the schedule's ascending order of x[token,h] g; d_bias [E] fp32 (may be NULL)
+ * likewise of g; dx [T,H] bf16: dx[t,h] = (accumulate_dx ? dx[t,h] : 0) + sum over k ascending of
+ * g[t,k] W[h, ids[t,k]], fp32, rounded once (accumulate_dx adds the router's share to the layer's
+ * dX in place).  sched: the schedule mok_build_schedule built from these ids (its shape gives T,
+ * H, E, K).  ws: device workspace of mok_router_workspace_bytes bytes, 256-byte aligned.  x 4-byte
+ * and dx 16-byte aligned. */
+MOK_API mok_status mok_router_backward(const mok_schedule* sched, const void* x, const void* w_router,
+                                       const int32_t* topk_ids, const float* topk_weights,
+                                       const float* d_topk_weights, float* dw_router, float* d_bias, void* dx,
+                                       int32_t accumulate_dx, void* ws, size_t ws_bytes, void* stream);
+
 /* Copy the schedule's device status word to *out (host pointer) after synchronising the stream.
  * The only call that blocks. */
 MOK_API mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream);

@@ -17,6 +17,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["mok_api.cu", "mok_sched.cu", "mok_move.cu", "mok_gemm_fwd.cu", "mok_gemm_dgrad.cu", "mok_gemm_wgrad.cu",
+           "mok_router.cu",
            "mok_noalloc.cu"]
 
 

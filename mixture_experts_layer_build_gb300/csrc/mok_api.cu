@@ -434,7 +434,8 @@ const char* mok_kernel_name(int32_t kind) {
       "sched_hist",      "sched_scan",    "sched_scatter", "gather_x",       "gemm_fwd_gateup",
       "gemm_fwd_down",   "combine",       "gather_dy",     "gemm_dgrad1",    "ds_reduce",
       "gemm_dgrad2",     "dx_reduce",     "gemm_wgrad_gu", "gemm_wgrad_d",   "mxfp8_quantize",
-      "mx_scale_atoms"};
+      "mx_scale_atoms",  "router_logits", "router_topk",   "router_transpose", "router_dx",
+      "router_dw"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "?";
 }
 

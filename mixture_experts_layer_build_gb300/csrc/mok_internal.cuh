@@ -95,6 +95,11 @@ enum KernelKind : int {
   K_GEMM_WGRAD_D,
   K_MXFP8_QUANTIZE,
   K_MX_SCALE_ATOMS,
+  K_ROUTER_LOGITS,
+  K_ROUTER_TOPK,
+  K_ROUTER_TRANSPOSE,
+  K_ROUTER_DX,
+  K_ROUTER_DW,
   K_NUM_KINDS
 };
 void trace_begin(cudaStream_t s, int kind);  // no-ops unless a trace is set

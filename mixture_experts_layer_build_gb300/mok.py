@@ -120,7 +120,15 @@ _lib.mok_mx_operands_of.argtypes = [ctypes.POINTER(mok_schedule), _P, ctypes.POI
 
 EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
             "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status", "mok_set_trace",
-            "mok_kernel_name", "mok_build_schedule_noalloc", "mok_mx_operands_of")
+            "mok_kernel_name", "mok_build_schedule_noalloc", "mok_mx_operands_of", "mok_router_workspace_bytes",
+            "mok_router_forward", "mok_router_backward")
+_lib.mok_router_workspace_bytes.restype = ctypes.c_size_t
+_lib.mok_router_workspace_bytes.argtypes = [ctypes.POINTER(mok_shape)]
+_lib.mok_router_forward.restype = ctypes.c_int
+_lib.mok_router_forward.argtypes = [ctypes.POINTER(mok_shape), _P, _P, _P, _P, _P, _P, _P]
+_lib.mok_router_backward.restype = ctypes.c_int
+_lib.mok_router_backward.argtypes = [ctypes.POINTER(mok_schedule), _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int32,
+                                     _P, ctypes.c_size_t, _P]
 _lib.mok_build_schedule_noalloc.restype = ctypes.c_int
 _lib.mok_build_schedule_noalloc.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape), _P, _P,
                                             ctypes.POINTER(mok_schedule), _P]
@@ -336,6 +344,66 @@ def mok_read_device_status(sched: Schedule, stream=None) -> int:
     _check(_lib.mok_read_device_status(ctypes.byref(sched.c), ctypes.byref(v), _stream(stream)),
            "mok_read_device_status")
     return v.value
+
+
+# ---------------------------------------------------------------------------------------------
+# router step (before the layer)
+# ---------------------------------------------------------------------------------------------
+def mok_router_workspace_bytes(shape: mok_shape) -> int:
+    n = _lib.mok_router_workspace_bytes(ctypes.byref(shape))
+    if n == 0:
+        raise MokError(MOK_ERR_INVALID_ARG, "mok_router_workspace_bytes")
+    return n
+
+
+def mok_router_forward(shape: mok_shape, x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor | None,
+                       logits: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, stream=None):
+    _check(_lib.mok_router_forward(ctypes.byref(shape), _ptr(x, torch.bfloat16, "x"),
+                                   _ptr(w_router, torch.bfloat16, "w_router"), _ptr(bias, torch.float32, "bias"),
+                                   _ptr(logits, torch.float32, "logits"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                   _ptr(topk_weights, torch.float32, "topk_weights"), _stream(stream)),
+           "mok_router_forward")
+
+
+def mok_router_backward(sched: Schedule, x: torch.Tensor, w_router: torch.Tensor, topk_ids: torch.Tensor,
+                        topk_weights: torch.Tensor, d_topk_weights: torch.Tensor, dw_router: torch.Tensor,
+                        d_bias: torch.Tensor | None, dx: torch.Tensor, accumulate_dx: bool, ws: torch.Tensor,
+                        stream=None):
+    _check(_lib.mok_router_backward(ctypes.byref(sched.c), _ptr(x, torch.bfloat16, "x"),
+                                    _ptr(w_router, torch.bfloat16, "w_router"), _ptr(topk_ids, torch.int32, "ids"),
+                                    _ptr(topk_weights, torch.float32, "topk_weights"),
+                                    _ptr(d_topk_weights, torch.float32, "d_topk_weights"),
+                                    _ptr(dw_router, torch.float32, "dw_router"), _ptr(d_bias, torch.float32, "d_bias"),
+                                    _ptr(dx, torch.bfloat16, "dx"), 1 if accumulate_dx else 0, _ptr(ws, None, "ws"),
+                                    ws.numel() * ws.element_size(), _stream(stream)), "mok_router_backward")
+
+
+def router_forward(x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor | None, K: int, stream=None):
+    """Allocating form: returns (logits [T,E] fp32, topk_ids [T,K] int32, topk_weights [T,K] fp32)."""
+    T, H = x.shape
+    E = w_router.shape[1]
+    shape = make_shape(T, H, 128, E, K)
+    logits = torch.empty((T, E), dtype=torch.float32, device=x.device)
+    ids = torch.empty((T, K), dtype=torch.int32, device=x.device)
+    wts = torch.empty((T, K), dtype=torch.float32, device=x.device)
+    mok_router_forward(shape, x, w_router, bias, logits, ids, wts, stream)
+    return logits, ids, wts
+
+
+def router_backward(sched: Schedule, x: torch.Tensor, w_router: torch.Tensor, topk_ids: torch.Tensor,
+                    topk_weights: torch.Tensor, d_topk_weights: torch.Tensor, with_bias: bool = False,
+                    dx: torch.Tensor | None = None, stream=None):
+    """Allocating form: returns (dw_router [H,E] fp32, d_bias [E] fp32 or None, dx [T,H] bf16).  A
+    given dx receives the router's share added in place."""
+    H, E = w_router.shape
+    dw = torch.empty((H, E), dtype=torch.float32, device=x.device)
+    db = torch.empty((E,), dtype=torch.float32, device=x.device) if with_bias else None
+    acc = dx is not None
+    if dx is None:
+        dx = torch.empty_like(x)
+    ws = torch.empty(mok_router_workspace_bytes(sched.c.shape), dtype=torch.uint8, device=x.device)
+    mok_router_backward(sched, x, w_router, topk_ids, topk_weights, d_topk_weights, dw, db, dx, acc, ws, stream)
+    return dw, db, dx
 
 
 class Layer:
