@@ -312,8 +312,8 @@ MOK_API size_t mok_router_workspace_bytes(const mok_shape* shape);
  * [T,K] int32: the K largest logits of each token in descending order, equal logits in ascending
  * expert id (NaN logits are never chosen; a token with fewer than K non-NaN logits gets id -1).
  * topk_weights [T,K] fp32: the softmax over the K chosen logits, which is the softmax over all E
- * renormalised to the chosen K.  x [T,H] bf16 and W device pointers; all outputs device, written
- * in full. */
+ * renormalised to the chosen K.  x [T,H] bf16 (16-byte aligned) and W device pointers; all
+ * outputs device, written in full. */
 MOK_API mok_status mok_router_forward(const mok_shape* shape, const void* x, const void* w_router, const float* bias,
                                       float* logits, int32_t* topk_ids, float* topk_weights, void* stream);
 

@@ -22,53 +22,82 @@ namespace {
 // ---------------------------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------------------------
-constexpr int kLgExperts = 64;  // experts per block (one per lane pair of warps)
-constexpr int kLgTokens = 16;   // tokens per block, four per thread
-constexpr int kLgChunk = 64;    // h values staged per step
+constexpr int kLgExperts = 64;  // experts per block
+constexpr int kLgTokens = 32;   // tokens per block
+constexpr int kLgChunk = 32;    // h values staged per step
 
-// logits[t,e] = (sum over h ascending of x[t,h] W[h,e], fused multiply-add) + bias[e].  Block:
-// 64 experts x 16 tokens; thread (el, tg) owns expert e0 + el and tokens t0 + 4 tg ... + 3.
-// x and W chunks of 64 h are staged in shared memory as fp32; every thread reads W[h][el] and the
-// four x values (broadcasts).
-__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ x,
+// logits[t,e] = (sum over h ascending of x[t,h] W[h,e], fused multiply-add) + bias[e].  Block of
+// 128 threads: 32 tokens x 64 experts; thread (te, tt) owns experts e0 + 4 te .. + 3 and tokens
+// t0 + 4 tt .. + 3 (16 independent accumulation chains).  x and W chunks of 32 h are staged in
+// shared memory as fp32: per h a thread reads its four W values as one 16-byte load and its four
+// x values (shared by the warp's two token groups).
+__global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __restrict__ x,
                                                             const uint16_t* __restrict__ w,
                                                             const float* __restrict__ bias, int64_t T, int H, int E,
                                                             float* __restrict__ logits) {
-  __shared__ float xs[kLgTokens][kLgChunk];
-  __shared__ float ws[kLgChunk][kLgExperts + 1];
+  __shared__ __align__(16) float xs[kLgTokens][kLgChunk + 4];
+  __shared__ __align__(16) float ws[kLgChunk][kLgExperts];
   const int tid = threadIdx.x;
-  const int el = tid & (kLgExperts - 1), tg = tid >> 6;
+  const int te = tid & 15, tt = tid >> 4;
   const int e0 = blockIdx.x * kLgExperts;
   const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kLgTokens;
-  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+  // chunk c + 1 is loaded into registers while chunk c is computed: x as one 16-byte load per
+  // thread (token tid / 4, 8 h), W as 16 coalesced loads (h row q / 64, expert q % 64)
+  const int xr = tid >> 2, xc = (tid & 3) * 8;
+  const int64_t xt = t0 + xr;
+  uint4 xv4 = make_uint4(0, 0, 0, 0);
+  uint16_t wv16[16];
+  auto fetch = [&](int h0) {
+    if (xt < T) xv4 = __ldg(reinterpret_cast<const uint4*>(x + xt * H + h0 + xc));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int q = tid + 128 * j, r = q >> 6, c = q & 63;
+      wv16[j] = e0 + c < E ? __ldg(w + static_cast<int64_t>(h0 + r) * E + e0 + c) : static_cast<uint16_t>(0);
+    }
+  };
+  fetch(0);
   for (int h0 = 0; h0 < H; h0 += kLgChunk) {
-    __syncthreads();
-    for (int i = tid; i < kLgTokens * kLgChunk; i += 256) {
-      const int r = i / kLgChunk, c = i % kLgChunk;
-      const int64_t t = t0 + r;
-      xs[r][c] = t < T ? __uint_as_float(static_cast<uint32_t>(x[t * H + h0 + c]) << 16) : 0.0f;
+    __syncthreads();  // the previous chunk's reads of xs / ws are done
+    {
+      const uint32_t p[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
+      float4* d = reinterpret_cast<float4*>(&xs[xr][xc]);
+      d[0] = make_float4(bf16_lo(p[0]), bf16_hi(p[0]), bf16_lo(p[1]), bf16_hi(p[1]));
+      d[1] = make_float4(bf16_lo(p[2]), bf16_hi(p[2]), bf16_lo(p[3]), bf16_hi(p[3]));
     }
-    for (int i = tid; i < kLgChunk * kLgExperts; i += 256) {
-      const int r = i / kLgExperts, c = i % kLgExperts;
-      ws[r][c] = e0 + c < E ? __uint_as_float(static_cast<uint32_t>(w[static_cast<int64_t>(h0 + r) * E + e0 + c])
-                                              << 16)
-                            : 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int q = tid + 128 * j;
+      ws[q >> 6][q & 63] = __uint_as_float(static_cast<uint32_t>(wv16[j]) << 16);
     }
     __syncthreads();
+    if (h0 + kLgChunk < H) fetch(h0 + kLgChunk);
 #pragma unroll 8
     for (int h = 0; h < kLgChunk; ++h) {
-      const float wv = ws[h][el];
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[h][4 * te]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = __fmaf_rn(xs[4 * tg + i][h], wv, acc[i]);
+      for (int i = 0; i < 4; ++i) {
+        const float xv = xs[4 * tt + i][h];
+        acc[i][0] = __fmaf_rn(xv, wv.x, acc[i][0]);
+        acc[i][1] = __fmaf_rn(xv, wv.y, acc[i][1]);
+        acc[i][2] = __fmaf_rn(xv, wv.z, acc[i][2]);
+        acc[i][3] = __fmaf_rn(xv, wv.w, acc[i][3]);
+      }
     }
   }
-  const int e = e0 + el;
-  if (e >= E) return;
-  const float b = bias ? bias[e] : 0.0f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int64_t t = t0 + 4 * tg + i;
-    if (t < T) logits[t * E + e] = bias ? __fadd_rn(acc[i], b) : acc[i];
+    const int64_t t = t0 + 4 * tt + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + 4 * te + j;
+      if (e < E) logits[t * E + e] = bias ? __fadd_rn(acc[i][j], bias[e]) : acc[i][j];
+    }
   }
 }
 
@@ -201,29 +230,44 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t* __restric
 }
 
 // dW[h, e] = sum over expert e's routed rows in ascending order (the schedule's expert-grouped
-// layout) of x[token, h] g[slot]; db[e] likewise of g[slot].  Block (expert e, 256 h): thread
-// h0 + 2 tid .. + 1.
-__global__ void __launch_bounds__(128) router_dw_kernel(const uint16_t* __restrict__ x,
+// layout) of x[token, h] g[slot]; db[e] likewise of g[slot].  Block (expert e, 512 h), thread
+// h0 + 2 tid .. + 1.  The rows' (token, g) come through shared memory 64 at a time, so the x loads
+// of several rows are in flight while the fused multiply-adds keep the row order.
+constexpr int kDwRows = 64;
+__global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ gbuf,
                                                         const int32_t* __restrict__ counts,
                                                         const int32_t* __restrict__ poff,
                                                         const int32_t* __restrict__ perm, int H, int E, int K,
                                                         float* __restrict__ dw, float* __restrict__ db) {
+  __shared__ int64_t s_tok[kDwRows];
+  __shared__ float s_g[kDwRows];
   const int e = blockIdx.x;
-  const int h = blockIdx.y * 256 + 2 * threadIdx.x;
+  const int h = blockIdx.y * 512 + 2 * threadIdx.x;
   const int r0 = __ldg(poff + e), n = __ldg(counts + e);
   float a0 = 0.0f, a1 = 0.0f, ab = 0.0f;
-  for (int r = r0; r < r0 + n; ++r) {
-    const int j = __ldg(perm + r);
-    if (j < 0) continue;
-    const float g = __ldg(gbuf + j);
-    const int64_t t = j / K;
-    if (h < H) {
-      const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + t * H + h));
-      a0 = __fmaf_rn(bf16_lo(v), g, a0);
-      a1 = __fmaf_rn(bf16_hi(v), g, a1);
+  for (int c0 = 0; c0 < n; c0 += kDwRows) {
+    const int m = min(kDwRows, n - c0);
+    __syncthreads();
+    if (threadIdx.x < m) {
+      const int j = __ldg(perm + r0 + c0 + threadIdx.x);
+      s_tok[threadIdx.x] = j < 0 ? -1 : j / K;
+      s_g[threadIdx.x] = j < 0 ? 0.0f : __ldg(gbuf + j);
     }
-    ab += g;
+    __syncthreads();
+    if (h < H) {
+#pragma unroll 8
+      for (int i = 0; i < m; ++i) {
+        const int64_t t = s_tok[i];
+        if (t < 0) continue;
+        const float g = s_g[i];
+        const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + t * H + h));
+        a0 = __fmaf_rn(bf16_lo(v), g, a0);
+        a1 = __fmaf_rn(bf16_hi(v), g, a1);
+      }
+    }
+    if (threadIdx.x == 0)
+      for (int i = 0; i < m; ++i) ab += s_g[i];
   }
   if (h < H) {
     dw[static_cast<int64_t>(h) * E + e] = a0;
@@ -253,11 +297,12 @@ extern "C" MOK_API mok_status mok_router_forward(const mok_shape* s, const void*
                                                  float* topk_weights, void* stream) {
   if (!s || !router_shape_ok(s->T, s->H, s->E, s->K)) return MOK_ERR_INVALID_ARG;
   if (s->T == 0) return MOK_OK;
-  if (!x || !w_router || !logits || !topk_ids || !topk_weights) return MOK_ERR_INVALID_ARG;
+  if (!x || !w_router || !logits || !topk_ids || !topk_weights || (reinterpret_cast<uintptr_t>(x) & 15))
+    return MOK_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dim3 g1((s->E + kLgExperts - 1) / kLgExperts, static_cast<unsigned>((s->T + kLgTokens - 1) / kLgTokens));
   trace_begin(st, K_ROUTER_LOGITS);
-  router_logits_kernel<<<g1, 256, 0, st>>>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w_router),
+  router_logits_kernel<<<g1, 128, 0, st>>>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w_router),
                                            bias, s->T, s->H, s->E, logits);
   trace_end(st);
   trace_begin(st, K_ROUTER_TOPK);
@@ -295,9 +340,9 @@ extern "C" MOK_API mok_status mok_router_backward(const mok_schedule* sched, con
         accumulate_dx);
     trace_end(st);
   }
-  const dim3 gw(s.E, (s.H + 255) / 256);
+  const dim3 gw(s.E, (s.H + 511) / 512);
   trace_begin(st, K_ROUTER_DW);
-  router_dw_kernel<<<gw, 128, 0, st>>>(static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
+  router_dw_kernel<<<gw, 256, 0, st>>>(static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
                                        sched->perm, s.H, s.E, s.K, dw_router, d_bias);
   trace_end(st);
   return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
