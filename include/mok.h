@@ -60,9 +60,14 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  * communication-SM count has no meaning on one GPU).
  *  minibatch_rows  rows of one minibatch tile of the schedule; a multiple of 128, >= 128.  Tiles
  *                  never cross experts.  It sets the order in which GEMM tiles are visited (all
- *                  tiles of one minibatch are visited together, weights then stay in L2); it
- *                  never changes a result.
+ *                  tiles of one minibatch are visited together, weights then stay in L2) and
+ *                  whether row tiles pair up on CTA pairs (tiles of 256 rows and more); it never
+ *                  changes a result.  0 = automatic: the average routed rows per expert,
+ *                  ceil(T*K/E), rounded up to a power of two times 128 in [256, 2048].
  *  macrobatch_rows a multiple of minibatch_rows; each tile records first_row / macrobatch_rows.
+ *                  0 = automatic: the smallest multiple of minibatch_rows that is at least
+ *                  4 * minibatch_rows and 2048.
+ *  The schedule built with a config holds the resolved sizes in its copy of the config.
  *  num_ctas        persistent grid size of the GEMM kernels; 0 = one CTA per SM.
  *  precision       mok_precision.
  *  debug_flags     must be 0. */

@@ -45,8 +45,22 @@ bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s) {
   if (p.H % 128 != 0 || p.I % 128 != 0) return false;
   if (p.K > p.E || p.E > 1024) return false;
   if (p.T * static_cast<int64_t>(p.K) >= (int64_t(1) << 31)) return false;
-  if (cfg->minibatch_rows < kRowTile || cfg->minibatch_rows % kRowTile != 0) return false;
-  if (cfg->macrobatch_rows < cfg->minibatch_rows || cfg->macrobatch_rows % cfg->minibatch_rows != 0) return false;
+  // 0 = automatic granularity: a minibatch tile of about one expert's share of the routed rows (the
+  // average rows per expert rounded up to 256 .. 2048 in powers of two; measured on GB300, every
+  // size from 256 rows up ran within noise of the best, 128 rows 2 to 3 % slower), and a
+  // macrobatch of at least four minibatches and 2048 rows
+  int32_t mb = cfg->minibatch_rows, MB = cfg->macrobatch_rows;
+  if (mb == 0) {
+    const int64_t avg = (p.T * p.K + p.E - 1) / p.E;
+    mb = 2 * kRowTile;
+    while (mb < avg && mb < 2048) mb *= 2;
+  }
+  if (mb < kRowTile || mb % kRowTile != 0) return false;
+  if (MB == 0) {
+    const int32_t want = 4 * mb > 2048 ? 4 * mb : 2048;
+    MB = (want + mb - 1) / mb * mb;
+  }
+  if (MB < mb || MB % mb != 0) return false;
   if (cfg->num_ctas < 0 || cfg->debug_flags != 0) return false;
   if (cfg->precision != MOK_BF16 && cfg->precision != MOK_MXFP8) return false;
   s->T = p.T;
@@ -54,8 +68,8 @@ bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s) {
   s->I = p.I;
   s->E = p.E;
   s->K = p.K;
-  s->mb = cfg->minibatch_rows;
-  s->MB = cfg->macrobatch_rows;
+  s->mb = mb;
+  s->MB = MB;
   s->R = p.T * p.K;
   s->rpad_max = s->R + static_cast<int64_t>(p.E) * (kRowTile - 1);
   s->tiles_max = (s->R + s->mb - 1) / s->mb + p.E;
@@ -299,6 +313,8 @@ mok_status mok_build_schedule(const mok_config* cfg, const mok_shape* shape, con
   if (ws_bytes < need) return MOK_ERR_WORKSPACE_TOO_SMALL;
   s.shape = *shape;
   s.config = *cfg;
+  s.config.minibatch_rows = z.mb;  // automatic sizes resolved
+  s.config.macrobatch_rows = z.MB;
   s.rpad_max = z.rpad_max;
   s.tiles_max = z.tiles_max;
   s.mblocks_max = z.mblocks_max;

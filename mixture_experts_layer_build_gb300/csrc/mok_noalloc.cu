@@ -59,6 +59,8 @@ extern "C" MOK_API mok_status mok_build_schedule_noalloc(const mok_config* cfg, 
   if (!scratch) return MOK_ERR_CUDA;
   sched->shape = *shape;
   sched->config = *cfg;
+  sched->config.minibatch_rows = z.mb;  // automatic sizes resolved
+  sched->config.macrobatch_rows = z.MB;
   sched->rpad_max = z.rpad_max;
   sched->tiles_max = z.tiles_max;
   sched->mblocks_max = z.mblocks_max;

@@ -67,6 +67,23 @@ def test_workspace_sizes_and_validation(mok):
             mok.mok_workspace_bytes(c, shp)
 
 
+def test_automatic_granularity_resolves_like_the_documented_rule(mok):
+    # minibatch = ceil(T*K/E) rounded up to 128 * 2^k in [256, 2048]; macrobatch = the smallest
+    # multiple of it that is >= 4 * minibatch and >= 2048
+    for (T, H, I, E, K), mb, MB in [((4096, 2048, 1024, 64, 6), 512, 2048), ((2048, 7168, 2048, 256, 8), 256, 2048),
+                                     ((16384, 7168, 2048, 4, 1), 2048, 8192), ((0, 128, 128, 4, 2), 256, 2048),
+                                     ((8192, 4096, 1536, 128, 8), 512, 2048)]:
+        shp = mok.make_shape(T, H, I, E, K)
+        auto = mok.mok_workspace_bytes(mok.make_config(0, 0), shp)
+        assert auto == mok.mok_workspace_bytes(mok.make_config(mb, MB), shp), (T, E, K)
+        if 0 < T and mb < 2048:  # another minibatch size changes the tile table's bound
+            assert auto != mok.mok_workspace_bytes(mok.make_config(2 * mb, max(2 * mb, MB)), shp)
+    # an explicit minibatch with an automatic macrobatch
+    shp = mok.make_shape(64, 128, 128, 4, 2)
+    assert mok.mok_workspace_bytes(mok.make_config(384, 0), shp) == mok.mok_workspace_bytes(
+        mok.make_config(384, 2304), shp)
+
+
 def test_host_rejects_bad_calls_without_touching_the_device(mok):
     cfg = mok.make_config()
     shp = mok.make_shape(16, 128, 128, 4, 2)

@@ -167,9 +167,11 @@ def test_full_size_properties(full_size):
 def test_determinism_repeats_grids_and_minibatches(mok, full_size):
     w, d, r = full_size
     cfgs = [mok.make_config(512, 2048)] * 9 + [mok.make_config(128, 256, 37), mok.make_config(2048, 4096, 1),
-                                                 mok.make_config(256, 256, 300)]
+                                                 mok.make_config(256, 256, 300), mok.make_config(0, 0)]
     for i, cfg in enumerate(cfgs):
-        _, out, g = _run(mok, d, w, cfg)
+        layer, out, g = _run(mok, d, w, cfg)
+        if cfg.minibatch_rows == 0:  # automatic granularity: 384 rows per expert -> 512, 2048
+            assert (layer.sched.c.config.minibatch_rows, layer.sched.c.config.macrobatch_rows) == (512, 2048)
         for k, v in dict(out=out, dx=g.dx, dwg=g.dw_gate, dwu=g.dw_up, dwd=g.dw_down, ds=g.d_topk_weights).items():
             assert torch.equal(v, r[k]), (i, k)
 
