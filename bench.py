@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--minibatch", type=int, default=512)
     p.add_argument("--macrobatch", type=int, default=2048)
     p.add_argument("--num-ctas", type=int, default=0, help="persistent GEMM grid (0: one CTA per SM)")
+    p.add_argument("--static-tiles", action="store_true",
+                   help="static round-robin GEMM tiles instead of cluster launch control")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU seconds of the oracle sample")
     return p.parse_args()
@@ -438,7 +440,8 @@ def ours(args, rank, ws, local_rank):
     Wg, Wu, Wd = d["Wg"], d["Wu"], d["Wd"]
     mxfp8 = w.precision == "mxfp8"
     cfg = mok.make_config(args.minibatch, max(args.macrobatch, args.minibatch), args.num_ctas,
-                          precision=mok.MOK_MXFP8 if mxfp8 else mok.MOK_BF16)
+                          precision=mok.MOK_MXFP8 if mxfp8 else mok.MOK_BF16,
+                          flags=mok.MOK_FLAG_STATIC_TILES if args.static_tiles else 0)
     layer = mok.Layer(w.T, w.H, w.I, w.E, w.K, cfg, device=dev)
     if mxfp8:  # weights are pre-quantised once, outside the step (the caller's optimiser step)
         mx = mok.quantize_weights(Wg.to(dev), Wu.to(dev), Wd.to(dev))

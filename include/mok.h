@@ -66,11 +66,18 @@ typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_precision;
  *                  ceil(T*K/E), rounded up to a power of two times 128 in [256, 2048].
  *  macrobatch_rows a multiple of minibatch_rows; each tile records first_row / macrobatch_rows.
  *                  0 = automatic: the smallest multiple of minibatch_rows that is at least
- *                  4 * minibatch_rows and 2048.
- *  The schedule built with a config holds the resolved sizes in its copy of the config.
- *  num_ctas        persistent grid size of the GEMM kernels; 0 = one CTA per SM.
+ *                  4 * minibatch_rows and 2048.  A schedule holds the resolved sizes in its copy
+ *                  of the config.
+ *  num_ctas        persistent grid size of the statically scheduled GEMM kernels (CTA pairs, and
+ *                  every kernel under MOK_FLAG_STATIC_TILES); 0 = one CTA per SM.
  *  precision       mok_precision.
- *  debug_flags     must be 0. */
+ *  debug_flags     0, or MOK_FLAG_STATIC_TILES.  By default the single-CTA GEMM kernels launch one
+ *                  CTA per tile and the running CTAs take over the tiles of CTAs that have not
+ *                  started (cluster launch control, "Cursor Open-Sources Mixture-of-Kittens (MoK)
+ *                  ...", English summary: Cluster Launch Control scheduling); with the flag every
+ *                  GEMM walks its tiles in a static round robin over a persistent grid.  Either
+ *                  way each tile is computed by one CTA in a fixed K order: the same bits. */
+#define MOK_FLAG_STATIC_TILES 1u
 typedef struct {
   int32_t minibatch_rows;
   int32_t macrobatch_rows;

@@ -61,7 +61,7 @@ bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s) {
     MB = (want + mb - 1) / mb * mb;
   }
   if (MB < mb || MB % mb != 0) return false;
-  if (cfg->num_ctas < 0 || cfg->debug_flags != 0) return false;
+  if (cfg->num_ctas < 0 || (cfg->debug_flags & ~MOK_FLAG_STATIC_TILES) != 0) return false;
   if (cfg->precision != MOK_BF16 && cfg->precision != MOK_MXFP8) return false;
   s->T = p.T;
   s->H = p.H;
@@ -76,6 +76,7 @@ bool make_sizes(const mok_config* cfg, const mok_shape* shape, Sizes* s) {
   s->mblocks_max = s->rpad_max / kRowTile;
   s->nchunks = (s->R + kSchedChunk - 1) / kSchedChunk;
   s->mx = cfg->precision == MOK_MXFP8;
+  s->clc = (cfg->debug_flags & MOK_FLAG_STATIC_TILES) == 0;
   if (s->rpad_max >= (int64_t(1) << 31)) return false;
   return true;
 }

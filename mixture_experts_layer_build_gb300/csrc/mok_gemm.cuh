@@ -86,7 +86,14 @@ struct GemmArgs {
   uint8_t* out_sf3;
   // CTA-pair row-tiled variants: pairs of 128-row blocks {expert, first row, tile, tile's first pair}
   const int4* pairs;
+  // single-CTA tiles: 1 = the grid holds one CTA per unit and running CTAs take over the units of
+  // CTAs that have not started (cluster launch control); 0 = static persistent round robin
+  int32_t clc;
 };
+
+// Units of a CTA under cluster launch control travel from the producer thread, which asks for
+// them, to the MMA thread and the epilogue warps through a ring in shared memory.
+constexpr int kUnitRing = 8;
 
 
 // A stage holds one K block of A and B as rows of 128 bytes (64 bf16 or 128 e4m3 along K) and, with
@@ -126,7 +133,7 @@ struct GemmCfg {
   // MXFP8 dgrad1: a 4 KB fp32 transpose scratch per epilogue warp (quantisation along the rows)
   static constexpr uint32_t kScratchBytes = (MX && VAR == V_DGRAD1) ? kEpiWarps * 4096u : 0u;
   static constexpr uint32_t kScratchOff = kStagingOff + kStagingBytes;
-  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kScratchOff) + kScratchBytes + 256;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kScratchOff) + kScratchBytes + 512;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
@@ -792,7 +799,13 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
   // [2S+4] drain, [2S+5, 2S+7) epilogue group barriers.  A pair uses the first CTA's full and accumulator-empty barriers (both CTAs'
   // loads and epilogues count there) and each CTA's own empty, accumulator-full and drain
   // barriers (the first CTA's commits arrive on both).
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 7);
+  // [2S+7, +8) unit ring full, [2S+15, +8) unit ring empty, [2S+23] cluster-launch-control answer;
+  // then the 16-byte answer, the ring's units, the TMEM address and the abort flag
+  const uint32_t uq_full0 = smem_u32(bars + 2 * S + 7), uq_empty0 = smem_u32(bars + 2 * S + 15);
+  const uint32_t clc_bar = smem_u32(bars + 2 * S + 23);
+  const uint32_t clc_resp = smem_u32(bars + 2 * S + 24);
+  volatile int* unit_q = reinterpret_cast<volatile int*>(bars + 2 * S + 26);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 30);
   // group barriers of four epilogue warps (the wide MX tiles' column half h uses epi_bar + 8 h)
   const uint32_t epi_bar = smem_u32(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -819,6 +832,11 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
     mbar_init(drain_bar, 1);
     mbar_init(epi_bar, 128);
     mbar_init(epi_bar + 8, 128);
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(uq_full0 + 8u * i, 1);
+      mbar_init(uq_empty0 + 8u * i, 1 + C::kEpiWarps);
+    }
+    mbar_init(clc_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
@@ -843,6 +861,21 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_units = gemm_num_units<VAR, PAIR>(args);
+  const bool clc = !PAIR && args.clc != 0;
+  // consumers' side of the unit ring: the next unit, -1 at the end (or after an abort)
+  auto unit_pop = [&](int& qi, uint32_t& qph, bool one_per_warp) -> int {
+    int v = -1;
+    if (!one_per_warp || lane == 0) {
+      if (mbar_wait(uq_full0 + 8u * qi, qph, abort_flag, args.status)) v = unit_q[qi];
+      mbar_arrive(uq_empty0 + 8u * qi);
+    }
+    if (one_per_warp) v = __shfl_sync(0xffffffffu, v, 0);
+    if (++qi == kUnitRing) {
+      qi = 0;
+      qph ^= 1u;
+    }
+    return v;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -852,7 +885,26 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
       int last_parity[S];
       for (int s = 0; s < S; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int u = unit0; ok && u < num_units; u += unit_step) {
+      int qi = 0;
+      uint32_t qph = 0, clc_phase = 0;
+      bool clc_pending = false;
+      for (int u = unit0; ok;) {
+        if (clc) {  // hand the unit to the other roles, ask for the next one while it runs
+          const int uu = u < num_units ? u : -1;
+          if (!mbar_wait(uq_empty0 + 8u * qi, qph ^ 1u, abort_flag, args.status)) break;
+          unit_q[qi] = uu;
+          mbar_arrive(uq_full0 + 8u * qi);
+          if (++qi == kUnitRing) {
+            qi = 0;
+            qph ^= 1u;
+          }
+          if (uu < 0) break;
+          mbar_arrive_expect_tx(clc_bar, 16);
+          clc_try_cancel(clc_resp, clc_bar);
+          clc_pending = true;
+        } else if (u >= num_units) {
+          break;
+        }
         const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
         for (int kb = 0; kb < w.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
@@ -876,7 +928,31 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
             phase ^= 1u;
           }
         }
+        if (clc) {
+          // the next unit: the CTA the answer cancelled; CTAs past the last unit (row-tiled grids
+          // are sized for the most units a schedule can have) are cancelled and dropped here, so
+          // they never start; nothing cancelled: the next round ends the ring
+          int nx = num_units;
+          while (ok) {
+            if (!mbar_wait(clc_bar, clc_phase, abort_flag, args.status)) {
+              ok = false;
+              break;
+            }
+            clc_phase ^= 1u;
+            clc_pending = false;
+            nx = clc_cancelled_x(clc_resp);
+            if (nx < num_units) break;
+            mbar_arrive_expect_tx(clc_bar, 16);
+            clc_try_cancel(clc_resp, clc_bar);
+            clc_pending = true;
+          }
+          if (!ok) break;
+          u = nx < 0 ? num_units : nx;
+        } else {
+          u += unit_step;
+        }
       }
+      if (clc_pending) mbar_wait_final(clc_bar, clc_phase, args.status);  // the answer lands before exit
       // wind down: let the copies already issued land before the CTA exits (a pair's second CTA
       // counts its copies on the first CTA's barriers, which that CTA waits for)
       if (!ok && rank == 0) {
@@ -891,7 +967,15 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int u = unit0; ok && u < num_units; u += unit_step) {
+      int qi = 0;
+      uint32_t qph = 0;
+      for (int u = unit0; ok; u += unit_step) {
+        if (clc) {
+          u = unit_pop(qi, qph, false);
+          if (u < 0) break;
+        } else if (u >= num_units) {
+          break;
+        }
         const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
         if (!mbar_wait<PAIR>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
@@ -960,7 +1044,15 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
     uint32_t acc_phase = 0, epi_phase = 0;
     // non-wide tiles: the four warps' staging (2 x 4 x 4 KB) serves as the group stager's two tiles
     GroupStager gs{staging, epi_bar, 0u, 0, q * 32 + lane, q == 2 && lane == 0};
-    for (int u = unit0; u < num_units; u += unit_step) {
+    int qi = 0;
+    uint32_t qph = 0;
+    for (int u = unit0;; u += unit_step) {
+      if (clc) {
+        u = unit_pop(qi, qph, true);
+        if (u < 0) break;
+      } else if (u >= num_units) {
+        break;
+      }
       const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
       const uint32_t tempty = PAIR ? mapa_shared(tempty_bar(acc), 0) : tempty_bar(acc);
       Dg1Chunk pre;
@@ -1020,6 +1112,16 @@ bool make_tmap_f32_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint64
 // bytes (E4M3 codes); swizzle_bytes 128, 64 or 32
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                   uint32_t box_outer, int swizzle_bytes);
+
+// CTAs to launch: one per unit under cluster launch control (single-CTA tiles; the running CTAs
+// take over the units of those that have not started), else the persistent grid of num_ctas
+// (CTA pairs: two CTAs per unit), never more CTAs than units.  Sets args.clc to match.
+inline int gemm_grid(const Sizes& z, int num_ctas, int64_t units, bool pair, GemmArgs& a) {
+  a.clc = (!pair && z.clc) ? 1 : 0;
+  if (a.clc) return static_cast<int>(units < 0x7fffffff ? units : 0x7fffffff);
+  const int64_t cap = pair ? 2 * units : units;
+  return static_cast<int>(cap < num_ctas ? cap : num_ctas);
+}
 
 // Row-tiled BF16 GEMMs run on CTA pairs when most pairs of 128-row blocks are full: minibatch
 // tiles of at least two blocks (pairs never cross a tile) and at least `rows` routed rows per

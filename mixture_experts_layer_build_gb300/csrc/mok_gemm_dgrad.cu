@@ -21,10 +21,6 @@ static GemmArgs common_args(const Sizes& z, const mok_schedule& s) {
   return a;
 }
 
-static int clamp_grid(int num_ctas, int64_t units) {
-  return static_cast<int>(units < num_ctas ? units : num_ctas);
-}
-
 // MXFP8: both GEMMs block-scaled on E4M3 operands.  B is the K-major transposed weight copy
 // quantised along this GEMM's K: Wd^T [E*I, H] for phase 1 (128 x 128 tiles: its epilogue keeps
 // two accumulators), Wg^T | Wu^T [E*H, I] for phase 2 (128 x 256 tiles when H allows).
@@ -55,8 +51,8 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
     if (!make_tmap_u8(&tO0, st.dgr, rcap, 2 * static_cast<uint64_t>(z.I), 32, 32, 32)) return -1;
     if (!make_tmap_u8(&tO1, st.sar, rcap, z.I, 32, 32, 32)) return -1;
     if (!make_tmap_u8(&tO2, st.dgq, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32, 32)) return -1;
-    return launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, tO2, a,
-                                            clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
+    const int grid = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, false, a);
+    return launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, tO2, a, grid, stream);
   }
   const int BN = z.mx_bn_h();
   if (!make_tmap_u8(&tA, st.dgq, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 128, 128, 128)) return -1;
@@ -73,7 +69,7 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   if (!(BN == 256 ? make_tmap_bf16_sw64(&tO0, st.ybuf, z.H, z.rpad_max, 32, 32)
                   : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)))
     return -1;
-  const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+  const int grid = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, false, a);
   return BN == 256 ? launch_gemm<V_DGRAD2, 256, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
                    : launch_gemm<V_DGRAD2, 128, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream);
 }
@@ -98,7 +94,7 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.out2 = st.dspart;
     if (!make_tmap_bf16_sw64(&tO0, st.dgdu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32)) return -1;
     if (!make_tmap_bf16_sw64(&tO1, st.as, z.I, z.rpad_max, 32, 32)) return -1;
-    const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+    const int grid = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, pair, a);
     if (pair)
       return BN == 256 ? launch_gemm<V_DGRAD1, 256, false, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
                        : launch_gemm<V_DGRAD1, 128, false, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
@@ -115,7 +111,7 @@ int launch_dgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   a.kb_split = z.I / kBK;
   a.out0 = st.ybuf;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)) return -1;
-  const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+  const int grid = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, pair, a);
   if (pair)
     return BN == 256 ? launch_gemm<V_DGRAD2, 256, false, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream)
                      : launch_gemm<V_DGRAD2, 128, false, true>(tA, tB, tB2, tO0, tO0, tO0, a, grid, stream);

@@ -19,10 +19,6 @@ static GemmArgs common_args(const Sizes& z, const mok_schedule& s) {
   return a;
 }
 
-static int clamp_grid(int num_ctas, int64_t units) {
-  return static_cast<int>(units < num_ctas ? units : num_ctas);
-}
-
 // MXFP8: both GEMMs block-scaled on E4M3 operands, 128 x 256 tiles (128 x 128 for the down
 // projection when H is not a multiple of 256).
 static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx& ctx, const Staging& st,
@@ -47,8 +43,8 @@ static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx&
   if (!make_tmap_f32_sw64(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 16, 32)) return -1;
   if (!make_tmap_bf16_sw64(&tO1, ctx.a, z.I, z.rpad_max, 32, 32)) return -1;
   if (!make_tmap_u8(&tO2, st.aq, z.I, z.rpad_max, 32, 32, 32)) return -1;
-  int rc = launch_gemm<V_FWD_GATEUP, 256, true>(tA, tB, tB2, tO0, tO1, tO2, a,
-                                                clamp_grid(num_ctas, z.mblocks_max * a.n_tiles), stream);
+  const int grid1 = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, false, a);
+  int rc = launch_gemm<V_FWD_GATEUP, 256, true>(tA, tB, tB2, tO0, tO1, tO2, a, grid1, stream);
   if (rc) return rc;
   // y = aq Wd_e^T
   const int BN = z.mx_bn_h();
@@ -65,7 +61,7 @@ static int launch_fwd_gemms_mx(const Sizes& z, const mok_schedule& s, const Ctx&
   if (!(BN == 256 ? make_tmap_bf16_sw64(&tO0, st.ybuf, z.H, z.rpad_max, 32, 32)
                   : make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)))
     return -1;
-  const int grid = clamp_grid(num_ctas, z.mblocks_max * a.n_tiles);
+  const int grid = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, false, a);
   return BN == 256 ? launch_gemm<V_FWD_DOWN, 256, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
                    : launch_gemm<V_FWD_DOWN, 128, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
 }
@@ -88,7 +84,7 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   a.out1 = ctx.a;
   if (!make_tmap_bf16(&tO0, ctx.gu, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 64, 128)) return -1;
   if (!make_tmap_bf16(&tO1, ctx.a, z.I, z.rpad_max, 64, 128)) return -1;
-  const int grid1 = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+  const int grid1 = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, pair, a);
   int rc = pair ? launch_gemm<V_FWD_GATEUP, 256, false, true>(tA, tB, tB2, tO0, tO1, tO0, a, grid1, stream)
                 : launch_gemm<V_FWD_GATEUP, 256>(tA, tB, tB2, tO0, tO1, tO0, a, grid1, stream);
   if (rc) return rc;
@@ -101,7 +97,7 @@ int launch_fwd_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, cons
   a.out0 = st.ybuf;
   a.out1 = nullptr;
   if (!make_tmap_bf16(&tO0, st.ybuf, z.H, z.rpad_max, 64, 128)) return -1;
-  const int grid = clamp_grid(num_ctas, 2 * z.mblocks_max * a.n_tiles);
+  const int grid = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, pair, a);
   if (pair)
     return BN == 256 ? launch_gemm<V_FWD_DOWN, 256, false, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
                      : launch_gemm<V_FWD_DOWN, 128, false, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);

@@ -36,7 +36,7 @@ static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
     if (!out_map(&tO0, g.dw_gate, z.H, static_cast<uint64_t>(z.E) * z.I, BN)) return -1;
     if (!out_map(&tO1, g.dw_up, z.H, static_cast<uint64_t>(z.E) * z.I, BN)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
-    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    const int grid = gemm_grid(z, num_ctas, units, false, a);
     const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
                              : launch_gemm<V_WGRAD_GU, 128, true>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
     if (rc) return rc;
@@ -53,7 +53,7 @@ static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
     a.out1 = nullptr;
     if (!out_map(&tO0, g.dw_down, z.I, static_cast<uint64_t>(z.E) * z.H, BN)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
-    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    const int grid = gemm_grid(z, num_ctas, units, false, a);
     return BN == 256 ? launch_gemm<V_WGRAD_D, 256, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
                      : launch_gemm<V_WGRAD_D, 128, true>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
   }
@@ -83,7 +83,7 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     if (!make_tmap_f32(&tO0, g.dw_gate, z.H, static_cast<uint64_t>(z.E) * z.I, 32, orows)) return -1;
     if (!make_tmap_f32(&tO1, g.dw_up, z.H, static_cast<uint64_t>(z.E) * z.I, 32, orows)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
-    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    const int grid = gemm_grid(z, num_ctas, units, false, a);
     const int rc = BN == 256 ? launch_gemm<V_WGRAD_GU, 256>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream)
                              : launch_gemm<V_WGRAD_GU, 128>(tA, tB, tB, tO0, tO1, tO0, a, grid, stream);
     if (rc) return rc;
@@ -99,7 +99,7 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
     a.out1 = nullptr;
     if (!make_tmap_f32(&tO0, g.dw_down, z.I, static_cast<uint64_t>(z.E) * z.H, 32, orows)) return -1;
     const int64_t units = static_cast<int64_t>(z.E) * a.m_tiles * a.n_tiles;
-    const int grid = static_cast<int>(units < num_ctas ? units : num_ctas);
+    const int grid = gemm_grid(z, num_ctas, units, false, a);
     return BN == 256 ? launch_gemm<V_WGRAD_D, 256>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream)
                      : launch_gemm<V_WGRAD_D, 128>(tA, tB, tB, tO0, tO0, tO0, a, grid, stream);
   }

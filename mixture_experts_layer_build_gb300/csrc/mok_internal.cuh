@@ -17,6 +17,7 @@ struct Sizes {
   int64_t T, R, rpad_max, tiles_max, mblocks_max, nchunks;
   int32_t H, I, E, K, mb, MB;
   bool mx;  // MXFP8 mode
+  bool clc;  // single-CTA GEMM tiles scheduled by cluster launch control (else static round robin)
   // MXFP8 tile width (N) of the GEMMs whose N runs over H (or I): 256 when the size allows it
   int32_t mx_bn_h() const { return H % 256 == 0 ? 256 : 128; }
   int32_t mx_bn_i() const { return I % 256 == 0 ? 256 : 128; }

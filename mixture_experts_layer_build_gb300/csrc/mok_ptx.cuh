@@ -122,6 +122,33 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 
 // ------------------------------------------------------------------------------------------------
+// cluster launch control: a running CTA takes over the work of a CTA that has not started yet
+// ------------------------------------------------------------------------------------------------
+// Ask to cancel a not-yet-running CTA of this grid; the 16-byte answer lands at `resp` (16-byte
+// aligned) and completes 16 bytes on mbarrier `bar`.  One thread; no new request after an answer
+// that cancelled nothing.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               ::"r"(resp), "r"(bar)
+               : "memory");
+}
+// The x index of the CTA the answer at `resp` cancelled, or -1 when it cancelled none.
+__device__ __forceinline__ int clc_cancelled_x(uint32_t resp) {
+  uint32_t x, ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+      "mov.u32 %0, 0;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %1, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x), "=r"(ok)
+      : "r"(resp)
+      : "memory");
+  return ok ? static_cast<int>(x) : -1;
+}
+
+// ------------------------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) tile loads, completion counted on an mbarrier
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {

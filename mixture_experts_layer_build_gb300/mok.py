@@ -161,8 +161,11 @@ def mok_version() -> str:
     return _lib.mok_version().decode()
 
 
-def make_config(minibatch_rows=512, macrobatch_rows=2048, num_ctas=0, precision=MOK_BF16) -> mok_config:
-    return mok_config(minibatch_rows, macrobatch_rows, num_ctas, precision, 0)
+MOK_FLAG_STATIC_TILES = 1  # static round-robin GEMM tile scheduling instead of cluster launch control
+
+
+def make_config(minibatch_rows=512, macrobatch_rows=2048, num_ctas=0, precision=MOK_BF16, flags=0) -> mok_config:
+    return mok_config(minibatch_rows, macrobatch_rows, num_ctas, precision, flags)
 
 
 def make_shape(T, H, I, E, K) -> mok_shape:

@@ -166,8 +166,12 @@ def test_full_size_properties(full_size):
 
 def test_determinism_repeats_grids_and_minibatches(mok, full_size):
     w, d, r = full_size
+    static = mok.MOK_FLAG_STATIC_TILES  # round-robin tiles instead of cluster launch control: same bits
     cfgs = [mok.make_config(512, 2048)] * 9 + [mok.make_config(128, 256, 37), mok.make_config(2048, 4096, 1),
-                                                 mok.make_config(256, 256, 300), mok.make_config(0, 0)]
+                                                 mok.make_config(256, 256, 300), mok.make_config(0, 0),
+                                                 mok.make_config(512, 2048, 0, flags=static),
+                                                 mok.make_config(128, 256, 37, flags=static),
+                                                 mok.make_config(256, 512, 1, flags=static)]
     for i, cfg in enumerate(cfgs):
         layer, out, g = _run(mok, d, w, cfg)
         if cfg.minibatch_rows == 0:  # automatic granularity: 384 rows per expert -> 512, 2048
@@ -215,7 +219,7 @@ def test_workload_sampled_parity_and_grid_determinism(mok, name):
     assert not bad, errs
     # other grids and every minibatch size of the granularity sweep (128 .. 2048 rows) must give
     # the same bits
-    cfgs = [mok.make_config(128, 1024, 61)]
+    cfgs = [mok.make_config(128, 1024, 61), mok.make_config(512, 2048, 61, flags=mok.MOK_FLAG_STATIC_TILES)]
     if name.startswith("sweep"):
         cfgs += [mok.make_config(mb, 2 * mb) for mb in (256, 1024, 2048)]
     for cfg in cfgs:

@@ -103,10 +103,13 @@ def test_mxfp8_ep64_shard_sampled_parity_and_determinism(mok):
     assert not bad, errs
     for k, v in r.items():
         assert torch.isfinite(v).all(), k
-    # bitwise identical on another grid and minibatch size
-    out2, g2 = _run_mx(mok, d, w, mok.make_config(256, 512, 37, precision=mok.MOK_MXFP8), mx_gpu)
-    for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down, ds=g2.d_topk_weights).items():
-        assert torch.equal(v, r[k]), k
+    # bitwise identical on another grid and minibatch size, and with static tile scheduling
+    for cfg in (mok.make_config(256, 512, 37, precision=mok.MOK_MXFP8),
+                mok.make_config(512, 2048, 37, precision=mok.MOK_MXFP8, flags=mok.MOK_FLAG_STATIC_TILES)):
+        out2, g2 = _run_mx(mok, d, w, cfg, mx_gpu)
+        for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down,
+                         ds=g2.d_topk_weights).items():
+            assert torch.equal(v, r[k]), k
 
 
 def _untile_scales(atoms, rows, kg):
