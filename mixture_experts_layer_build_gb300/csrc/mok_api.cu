@@ -104,7 +104,6 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
     t.as = c.take<uint16_t>(z.rpad_max * z.I);
   }
   t.dspart = c.take<float>(z.rpad_max * (z.I / 128));
-  t.pairs = reinterpret_cast<int4*>(c.take<int32_t>(4 * z.mblocks_max));
   if (z.mx) {
     const int64_t rt = (z.rpad_max + kRowTile - 1) / kRowTile;  // 128-row tiles of the routed rows
     const int64_t EH = static_cast<int64_t>(z.E) * z.H, EI = static_cast<int64_t>(z.E) * z.I;
@@ -129,6 +128,7 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
     t.swt_g = c.take<uint8_t>(EH * (z.I / 32));
     t.swt_u = c.take<uint8_t>(EH * (z.I / 32));
   }
+  t.pairs = reinterpret_cast<int4*>(c.take<int32_t>(4 * z.mblocks_max));
   if (s) {
     s->counts = d.counts;
     s->offsets = d.offsets;

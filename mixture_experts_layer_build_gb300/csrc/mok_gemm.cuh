@@ -680,22 +680,20 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else if constexpr ((VAR == V_WGRAD_GU || VAR == V_WGRAD_D) && MX && BN == 256) {
     // wide MXFP8 weight-gradient tile: this warp's 128 fp32 columns go to registers, the accumulator
-    // is released, then the four warps of column half h fill 128-row x 16-column (64-byte rows)
-    // tiles together in their 8 KB of staging, one thread storing each.  Experts without rows: zeros.
+    // is released, then the rows leave in 16-column (64-byte) tiles of the warp's own 32 rows
+    // (measured: 128-row tiles shared by four warps, single-buffered in the wide configuration's
+    // staging, were up to 15 % slower here).  Experts without rows: zeros.
     const bool empty = w.kblocks == 0;
-    const int mt0 = w.mt * kBM;
+    const int m0 = w.mt * kBM + q * 32;
     const CUtensorMap* tm;
-    int rt;
+    int r0;
     if constexpr (VAR == V_WGRAD_GU) {
-      tm = mt0 < a.I ? tO0 : tO1;
-      rt = w.e * a.I + (mt0 < a.I ? mt0 : mt0 - a.I);
+      tm = m0 < a.I ? tO0 : tO1;
+      r0 = w.e * a.I + (m0 < a.I ? m0 : m0 - a.I);
     } else {
       tm = tO0;
-      rt = w.e * a.H + mt0;
+      r0 = w.e * a.H + m0;
     }
-    const uint32_t gbuf = stg.buf0 - static_cast<uint32_t>((q + 2) & 3) * 2048u;  // this half's 8 KB
-    const uint32_t gbar = epi_bar + 8u * static_cast<uint32_t>(h);
-    const bool leader = q == 2 && lane == 0;
     uint32_t r[128];
     if (!empty) {
 #pragma unroll
@@ -707,26 +705,13 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       for (int i = 0; i < 128; ++i) r[i] = 0u;
     }
     release_acc<PAIR>(tempty);
-    // row q * 32 + lane, 16-byte chunk j at j ^ ((row >> 1) & 3) (the 64-byte swizzle)
-    const uint32_t row = gbuf + static_cast<uint32_t>(q * 32 + lane) * 64u;
 #pragma unroll
     for (int c = 0; c < 128; c += 16) {
+      uint4 ch[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        st_shared_v4(row + (static_cast<uint32_t>(j ^ ((lane >> 1) & 3)) << 4),
-                     make_uint4(r[c + 4 * j], r[c + 4 * j + 1], r[c + 4 * j + 2], r[c + 4 * j + 3]));
-      fence_proxy_async_smem();
-      mbar_arrive(gbar);  // the half's 128 rows are in the tile
-      if (!mbar_wait(gbar, epi_phase, abort_flag, a.status)) return;
-      epi_phase ^= 1u;
-      if (leader) {
-        tma_store_2d(tm, gbuf, w.nt * BN + 128 * h + c, rt);
-        bulk_commit();
-        bulk_wait_read<0>();  // the tile is free again
-      }
-      mbar_arrive(gbar);
-      if (!mbar_wait(gbar, epi_phase, abort_flag, a.status)) return;
-      epi_phase ^= 1u;
+        ch[j] = make_uint4(r[c + 4 * j], r[c + 4 * j + 1], r[c + 4 * j + 2], r[c + 4 * j + 3]);
+      stg.template put<64>(ch, tm, w.nt * BN + 128 * h + c, r0);
     }
   } else {
     // weight gradients, fp32 out in 128-row x 32-column tiles of the group stager (a quarter of the
@@ -1057,14 +1042,14 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
       const uint32_t tempty = PAIR ? mapa_shared(tempty_bar(acc), 0) : tempty_bar(acc);
       Dg1Chunk pre;
       if constexpr (VAR == V_DGRAD1 && !MX) {  // before the wait
-        if (w.row0 >= 0) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);
+        if (!PAIR || w.row0 >= 0) dgrad1_fetch(args, w, q, lane, w.nt * BN, pre);
       }
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, args.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      if (w.row0 >= 0) {
+      if (!PAIR || w.row0 >= 0) {
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
         gemm_epilogue<VAR, BN, MX, PAIR>(args, w, q, h, lane, taddr, stg,
@@ -1117,7 +1102,7 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
 // take over the units of those that have not started), else the persistent grid of num_ctas
 // (CTA pairs: two CTAs per unit), never more CTAs than units.  Sets args.clc to match.
 inline int gemm_grid(const Sizes& z, int num_ctas, int64_t units, bool pair, GemmArgs& a) {
-  a.clc = (!pair && z.clc) ? 1 : 0;
+  a.clc = (!pair && !z.mx && z.clc) ? 1 : 0;
   if (a.clc) return static_cast<int>(units < 0x7fffffff ? units : 0x7fffffff);
   const int64_t cap = pair ? 2 * units : units;
   return static_cast<int>(cap < num_ctas ? cap : num_ctas);

@@ -18,10 +18,10 @@ static int launch_wgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
   a.status = s.status;
   a.sf_kq = static_cast<int32_t>(z.kq_rows());
   const uint64_t rcap = static_cast<uint64_t>(z.rcap());
-  // fp32 dW leaves in 128-row tiles: 16 columns (wide tiles, one per group of four epilogue warps)
-  // or 32 columns
+  // fp32 dW tiles: 32 rows x 16 columns per warp (wide tiles) or 128 rows x 32 columns per group
+  // of four epilogue warps
   auto out_map = [&](CUtensorMap* m, float* p, uint64_t inner, uint64_t outer, int bn) {
-    return bn == 256 ? make_tmap_f32_sw64(m, p, inner, outer, 16, 128) : make_tmap_f32(m, p, inner, outer, 32, 128);
+    return bn == 256 ? make_tmap_f32_sw64(m, p, inner, outer, 16, 32) : make_tmap_f32(m, p, inner, outer, 32, 128);
   };
   {  // [dWg ; dWu]_e: M = 2I (A = [dg | du]^T), N = H (B = x^T)
     const int BN = z.mx_bn_h();
