@@ -103,7 +103,7 @@ size_t carve_workspace(const Sizes& z, char* base, mok_schedule* s, Staging* st)
     t.dgdu = c.take<uint16_t>(z.rpad_max * 2 * z.I);
     t.as = c.take<uint16_t>(z.rpad_max * z.I);
   }
-  t.dspart = c.take<float>(z.rpad_max * (z.I / 128));
+  t.dspart = c.take<float>(z.rpad_max * (z.I / 64));  // dS partials: at most two per 128 columns
   if (z.mx) {
     const int64_t rt = (z.rpad_max + kRowTile - 1) / kRowTile;  // 128-row tiles of the routed rows
     const int64_t EH = static_cast<int64_t>(z.E) * z.H, EI = static_cast<int64_t>(z.E) * z.I;
@@ -428,7 +428,9 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   }
   int e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 1, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
-  const int n_tiles1 = z.I / (z.I % 256 == 0 && !z.mx ? 256 : 128);
+  // dS partials per row: one per N tile of the first data-gradient GEMM (two per 128-column tile
+  // when the block-scaled one splits its columns between two warps)
+  const int n_tiles1 = z.mx ? z.I / (z.mx_dg1_split() ? 64 : 128) : z.I / (z.I % 256 == 0 ? 256 : 128);
   if (launch_ds_reduce(st.dspart, sched->inv, z.R, n_tiles1, g->d_topk_weights, s)) return MOK_ERR_CUDA;
   e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 2, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;

@@ -107,14 +107,18 @@ constexpr int kUnitRing = 8;
 //     the next tile's MMAs run.  Stage s's scale words sit in columns 256 + 12 s ...  To fit four
 //     stages, each epilogue warp stages its stores through a single 2 KB tile.
 // The scale atoms of stage s live in a ring of their own after the A/B stages.
-template <int VAR, int BN, bool MX, bool PAIR = false>
+template <int VAR, int BN, bool MX, bool PAIR = false, bool SPLIT = false>
 struct GemmCfg {
   static_assert(!MX || BN == 128 || BN == 256, "block-scaled tiles are 128 x 128 or 128 x 256");
   static_assert(!(MX && PAIR), "block-scaled tiles run on single CTAs");
   static constexpr bool kWide = MX && BN == 256;
+  // SPLIT (block-scaled DGRAD1 only): eight epilogue warps, two per lane quarter, 64 columns each
+  static_assert(!SPLIT || (MX && VAR == V_DGRAD1 && BN == 128), "split epilogue: block-scaled DGRAD1");
+  static constexpr bool kSplitEpi = SPLIT;
+  static constexpr bool kDg1Mx = MX && VAR == V_DGRAD1;
   static constexpr int kAccBufs = kWide ? 1 : 2;
   static constexpr int kStages = MX ? (kWide ? 4 : 5) : PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : 6);
-  static constexpr int kEpiWarps = kWide ? 8 : 4;  // warp w accesses TMEM lane quarter w % 4
+  static constexpr int kEpiWarps = kWide || kSplitEpi ? 8 : 4;  // warp w accesses TMEM lane quarter w % 4
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = (PAIR ? BN / 2 : BN) * 128;  // the B rows this CTA holds
@@ -125,13 +129,15 @@ struct GemmCfg {
   static constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
   static constexpr uint32_t kSfCol0 = kAccBufs * BN;
   static constexpr uint32_t kSfCols = 4 + BN / 32;  // scale-word columns per stage (A, then B)
-  static constexpr int kStageBufs = kWide ? 1 : 2;             // staging tiles per epilogue warp
-  static constexpr uint32_t kStageBufBytes = kWide ? 2048 : 4096;
+  static constexpr int kStageBufs = kWide ? 1 : 2;  // staging tiles per epilogue warp
+  // (block-scaled DGRAD1 stores 1 KB tiles only: 32 rows x 32 E4M3 codes)
+  static constexpr uint32_t kStageBufBytes = kWide ? 2048 : kDg1Mx ? 1024 : 4096;
   static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
   static constexpr uint32_t kSfRing = static_cast<uint32_t>(kStages) * kStageBytes;  // offset of the atom ring
   static constexpr uint32_t kStagingOff = kSfRing + static_cast<uint32_t>(kStages) * kSfBytes;
-  // MXFP8 dgrad1: a 4 KB fp32 transpose scratch per epilogue warp (quantisation along the rows)
-  static constexpr uint32_t kScratchBytes = (MX && VAR == V_DGRAD1) ? kEpiWarps * 4096u : 0u;
+  // MXFP8 dgrad1: a 32 x 33 fp32 transpose scratch per epilogue warp (quantisation along the rows)
+  static constexpr uint32_t kScratchWarp = 32u * 33u * 4u;
+  static constexpr uint32_t kScratchBytes = kDg1Mx ? kEpiWarps * kScratchWarp : 0u;
   static constexpr uint32_t kScratchOff = kStagingOff + kStagingBytes;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kScratchOff) + kScratchBytes + 512;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -436,41 +442,38 @@ __device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, i
 }
 
 // MX quantisation of one 32 x 32 block along the rows: lane = row, v[j] = column j (feature f0 + j).
-// The block is transposed through the warp's fp32 scratch (element (r, c) at r * 32 + (c ^ r): both
-// the row writes and the column reads are free of bank conflicts), lane j then quantises column j
+// The block is transposed through the warp's fp32 scratch (element (r, c) at r * 33 + c: both the
+// row writes and the column reads are free of bank conflicts, and every address is a per-lane base
+// plus a constant, so no table of addresses stays live), lane j then quantises column j
 // over the 32 rows as one MX block, and its 32 codes leave as row j of a byte tile stored at
 // (row rowc, feature f0) of the transposed [features, rows] copy; lane j writes column j's scale
-// into the atom-tiled array (groups of g atoms, kq atoms along K).
+// into the atom-tiled array (groups of 2^gl atoms, kq atoms along K).
 template <class Stg>
 __device__ __forceinline__ void quant_rows_store(const float (&v)[32], uint32_t scratch, Stg& stg,
-                                                 const CUtensorMap* tm, uint8_t* sf, int rowc, int f0, int kq, int g,
+                                                 const CUtensorMap* tm, uint8_t* sf, int rowc, int f0, int kq, int gl,
                                                  int lane) {
-  const uint32_t row = scratch + static_cast<uint32_t>(lane) * 128;
+  const uint32_t row = scratch + static_cast<uint32_t>(lane) * 132;
 #pragma unroll
-  for (int c = 0; c < 32; ++c)
-    asm volatile("st.shared.f32 [%0], %1;" ::"r"(row + (static_cast<uint32_t>(c ^ lane) << 2)), "f"(v[c]) : "memory");
+  for (int c = 0; c < 32; ++c) asm volatile("st.shared.f32 [%0], %1;" ::"r"(row + 4u * c), "f"(v[c]) : "memory");
   __syncwarp();
   float col[32];
+  const uint32_t colp = scratch + static_cast<uint32_t>(lane) * 4;
 #pragma unroll
-  for (int r = 0; r < 32; ++r)
-    asm volatile("ld.shared.f32 %0, [%1];"
-                 : "=f"(col[r])
-                 : "r"(scratch + static_cast<uint32_t>(r) * 128 + (static_cast<uint32_t>(lane ^ r) << 2))
-                 : "memory");
+  for (int r = 0; r < 32; ++r) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(col[r]) : "r"(colp + 132u * r) : "memory");
   __syncwarp();
   uint32_t codes[8];
   const uint32_t sb = mx_quant32(col, codes);
   const uint4 ch[2] = {make_uint4(codes[0], codes[1], codes[2], codes[3]),
                        make_uint4(codes[4], codes[5], codes[6], codes[7])};
   stg.template put<32>(ch, tm, rowc, f0);
-  sf[sf_atom_offset_g(f0 + lane, rowc >> 5, kq, g)] = static_cast<uint8_t>(sb);
+  sf[sf_atom_offset_p2(f0 + lane, rowc >> 5, kq, gl)] = static_cast<uint8_t>(sb);
 }
 
 // Epilogue of one unit for the warp's 32 accumulator rows (slab `q`); lane = row in the slab; `h`
 // = the warp's column half in the wide (8-warp) configuration.  tO0 / tO1 / tO2 are the output
 // tensor maps of the variant; `tempty` is released as soon as the last accumulator column has been
 // read.  `pre` holds DGRAD1's first prefetched context chunk.
-template <int VAR, int BN, bool MX, bool PAIR, class Stg>
+template <int VAR, int BN, bool MX, bool PAIR, bool SPLIT, class Stg>
 __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, int q, int h, int lane,
                                               uint32_t taddr, Stg& stg, uint32_t scratch, const CUtensorMap* tO0,
                                               const CUtensorMap* tO1, const CUtensorMap* tO2, uint32_t tempty,
@@ -575,6 +578,8 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     //   dS partial from a's quantisation along I (the context);
     //   dg, du quantised along I (row-major codes + A atoms) for the second data-gradient GEMM;
     //   dg, du and s * a quantised along this warp's 32 routed rows, for the weight-gradient GEMMs.
+    // SPLIT (eight warps): this one takes columns [64 h, 64 h + 64) of the tile, and its dS
+    // partial has a slot of its own (two per N tile and row).
     const int64_t row = w.row0 + q * 32 + lane;
     const int64_t I = a.I;
     const int i0 = w.nt * BN;
@@ -583,57 +588,70 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
     const float s = __ldg(a.row_weight + row);
     const int rowc = w.row0 + q * 32;
     float part = 0.0f;
+    const int c_beg = SPLIT ? 64 * h : 0, c_end = SPLIT ? 64 * h + 64 : BN;
+    const int sa_gl = a.sa_groups == 2 ? 1 : 0;  // s * a's scales: groups of 1 or 2 atoms
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      float4 g4[8], u4[8];
-      const float4* gp = reinterpret_cast<const float4*>(gu + i0 + c);
-      const float4* up = reinterpret_cast<const float4*>(gu + I + i0 + c);
+    for (int c = c_beg; c < c_end; c += 32) {
+      // g and u of 32 columns; s * a first (it needs no accumulator), then dA' from TMEM, and dg,
+      // du computed in place of u, g: at most four 32-value arrays are live at once
+      float g[32], u[32];
+      {
+        const float4* gp = reinterpret_cast<const float4*>(gu + i0 + c);
+        const float4* up = reinterpret_cast<const float4*>(gu + I + i0 + c);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        g4[j] = __ldg(gp + j);
-        u4[j] = __ldg(up + j);
+        for (int j = 0; j < 8; ++j) {
+          const float4 x = __ldg(gp + j), y = __ldg(up + j);
+          g[4 * j] = x.x, g[4 * j + 1] = x.y, g[4 * j + 2] = x.z, g[4 * j + 3] = x.w;
+          u[4 * j] = y.x, u[4 * j + 1] = y.y, u[4 * j + 2] = y.z, u[4 * j + 3] = y.w;
+        }
       }
-      uint32_t rv[32];
-      tmem_ld_32x32b_x32(taddr + c, rv);
-      tmem_ld_wait();
-      if (c + 32 >= BN) release_acc<PAIR>(tempty);
-      const float* g = reinterpret_cast<const float*>(g4);
-      const float* u = reinterpret_cast<const float*>(u4);
+      float sg[32];
+      {
+        float v[32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float a8[8];
-        unpack8(ldg_v4(av + i0 + c + 8 * j), a8);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) part = fmaf(__uint_as_float(rv[8 * j + k]), a8[k], part);
+        for (int i = 0; i < 32; ++i) {
+          sg[i] = sigmoid_f(g[i]);
+          v[i] = s * (g[i] * sg[i] * u[i]);
+        }
+        quant_rows_store(v, scratch, stg, tO1, a.out_sf3, rowc, i0 + c, a.sf_kq, sa_gl, lane);
       }
-      float sg[32], v[32];
+      {
+        uint32_t rv[32];
+        tmem_ld_32x32b_x32(taddr + c, rv);
+        tmem_ld_wait();
+        if (c + 32 >= c_end) release_acc<PAIR>(tempty);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sg[i] = sigmoid_f(g[i]);
-        v[i] = s * (g[i] * sg[i] * u[i]);
+        for (int j = 0; j < 4; ++j) {
+          float a8[8];
+          unpack8(ldg_v4(av + i0 + c + 8 * j), a8);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) part = fmaf(__uint_as_float(rv[8 * j + k]), a8[k], part);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float da = s * __uint_as_float(rv[i]);
+          const float dg = da * u[i] * sg[i] * (1.0f + g[i] * (1.0f - sg[i]));
+          g[i] = da * g[i] * sg[i];  // du
+          u[i] = dg;
+        }
       }
-      quant_rows_store(v, scratch, stg, tO1, a.out_sf3, rowc, i0 + c, a.sf_kq, a.sa_groups, lane);
       uint4 ch[2];
       uint32_t codes[8];
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        v[i] = s * __uint_as_float(rv[i]) * u[i] * sg[i] * (1.0f + g[i] * (1.0f - sg[i]));
-      quant_rows_store(v, scratch, stg, tO0, a.out_sf2, rowc, i0 + c, a.sf_kq, 1, lane);
-      uint32_t sb = mx_quant32(v, codes);
+      quant_rows_store(u, scratch, stg, tO0, a.out_sf2, rowc, i0 + c, a.sf_kq, 0, lane);
+      uint32_t sb = mx_quant32(u, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
       stg.template put<32>(ch, tO2, i0 + c, rowc);
       a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sb);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = s * __uint_as_float(rv[i]) * g[i] * sg[i];
-      quant_rows_store(v, scratch, stg, tO0, a.out_sf2, rowc, a.I + i0 + c, a.sf_kq, 1, lane);
-      sb = mx_quant32(v, codes);
+      quant_rows_store(g, scratch, stg, tO0, a.out_sf2, rowc, a.I + i0 + c, a.sf_kq, 0, lane);
+      sb = mx_quant32(g, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
       stg.template put<32>(ch, tO2, a.I + i0 + c, rowc);
       a.out_sf[sf_atom_offset(row, (a.I + i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sb);
     }
-    static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
+    if constexpr (SPLIT) static_cast<float*>(a.out2)[(row * a.n_tiles + w.nt) * 2 + h] = part;
+    else static_cast<float*>(a.out2)[row * a.n_tiles + w.nt] = part;
   } else if constexpr (VAR == V_DGRAD1) {
     // dA' = dY Wd (this tile's BN columns of I); the forward's g, u, a come from the context,
     // fetched one 32-column chunk ahead.  dg, du and s*a leave as 32 x 64-byte tiles.
@@ -760,13 +778,13 @@ __device__ __forceinline__ bool mbar_wait_final(uint32_t bar, uint32_t parity, u
   return true;
 }
 
-template <int VAR, int BN, bool MX, bool PAIR>
-__global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
+template <int VAR, int BN, bool MX, bool PAIR, bool SPLIT>
+__global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR, SPLIT>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
                 const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
                 const GemmArgs args) {
-  using C = GemmCfg<VAR, BN, MX, PAIR>;
+  using C = GemmCfg<VAR, BN, MX, PAIR, SPLIT>;
   constexpr bool kAmn = (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) && !MX;
   constexpr bool kBmn = (VAR >= V_DGRAD1) && !MX;
   constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * kBM : kBM, BN, kAmn, kBmn);
@@ -1052,8 +1070,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR>::kThreads, 1)
       if (!PAIR || w.row0 >= 0) {
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-        gemm_epilogue<VAR, BN, MX, PAIR>(args, w, q, h, lane, taddr, stg,
-                                         scratch0 + static_cast<uint32_t>(warp - 2) * 4096u, &tmO0, &tmO1, &tmO2,
+        gemm_epilogue<VAR, BN, MX, PAIR, SPLIT>(args, w, q, h, lane, taddr, stg,
+                                         scratch0 + static_cast<uint32_t>(warp - 2) * C::kScratchWarp, &tmO0, &tmO1, &tmO2,
                                          tempty, pre, gs, epi_bar, epi_phase, abort_flag);
       } else {
         release_acc<PAIR>(tempty);  // a pair's CTA without rows: nothing to store
@@ -1117,13 +1135,13 @@ inline bool use_pairs(const Sizes& z, int rows) {
   return z.mb >= 2 * kRowTile && z.R >= static_cast<int64_t>(rows) * z.E;
 }
 
-template <int VAR, int BN, bool MX = false, bool PAIR = false>
+template <int VAR, int BN, bool MX = false, bool PAIR = false, bool SPLIT = false>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o0,
                 const CUtensorMap& o1, const CUtensorMap& o2, const GemmArgs& args, int grid, cudaStream_t stream) {
-  using C = GemmCfg<VAR, BN, MX, PAIR>;
+  using C = GemmCfg<VAR, BN, MX, PAIR, SPLIT>;
   static bool configured = false;  // per process; the attribute is per function, set once
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX, PAIR>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX, PAIR, SPLIT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
     if (e != cudaSuccess) return static_cast<int>(e);
     configured = true;
@@ -1149,7 +1167,7 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = PAIR ? 1 : 0;
-  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_kernel<VAR, BN, MX, PAIR>, a, b, b2, o0, o1, o2, args);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_kernel<VAR, BN, MX, PAIR, SPLIT>, a, b, b2, o0, o1, o2, args);
   trace_end(stream);
   return le != cudaSuccess ? static_cast<int>(le) : static_cast<int>(cudaGetLastError());
 }

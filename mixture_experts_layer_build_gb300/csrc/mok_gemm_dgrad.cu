@@ -52,6 +52,10 @@ static int launch_dgrad_gemms_mx(const Sizes& z, const mok_schedule& s, const Ct
     if (!make_tmap_u8(&tO1, st.sar, rcap, z.I, 32, 32, 32)) return -1;
     if (!make_tmap_u8(&tO2, st.dgq, 2 * static_cast<uint64_t>(z.I), z.rpad_max, 32, 32, 32)) return -1;
     const int grid = gemm_grid(z, num_ctas, z.mblocks_max * a.n_tiles, false, a);
+    // The tile's epilogue (dg, du and s a, each quantised along both axes) is about as long as
+    // its MMAs over K = H = 4096: up to there eight epilogue warps pay; beyond, the operand feed
+    // bounds the tile and four warps are as fast.
+    if (z.mx_dg1_split()) return launch_gemm<V_DGRAD1, 128, true, false, true>(tA, tB, tB, tO0, tO1, tO2, a, grid, stream);
     return launch_gemm<V_DGRAD1, 128, true>(tA, tB, tB, tO0, tO1, tO2, a, grid, stream);
   }
   const int BN = z.mx_bn_h();

@@ -21,6 +21,9 @@ struct Sizes {
   // MXFP8 tile width (N) of the GEMMs whose N runs over H (or I): 256 when the size allows it
   int32_t mx_bn_h() const { return H % 256 == 0 ? 256 : 128; }
   int32_t mx_bn_i() const { return I % 256 == 0 ? 256 : 128; }
+  // block-scaled first data-gradient GEMM: eight epilogue warps (two column halves, two dS
+  // partials per 128-column tile) while K = H is short enough that the epilogue bounds the tile
+  bool mx_dg1_split() const { return mx && H <= 4096; }
   // MXFP8 weight gradients: routed-row capacity in 128-row K atoms, and in rows
   int64_t kq_rows() const { return (rpad_max + kRowTile - 1) / kRowTile; }
   int64_t rcap() const { return kq_rows() * kRowTile; }

@@ -453,6 +453,14 @@ __host__ __device__ __forceinline__ int64_t sf_atom_offset_g(int64_t f, int64_t 
          (kg & 3);
 }
 
+// sf_atom_offset_g for a power-of-two group count G = 1 << gl: shifts and masks instead of the
+// 64-bit division and remainder (a called routine on the device).
+__device__ __forceinline__ int64_t sf_atom_offset_p2(int64_t f, int64_t kg, int64_t kq, int gl) {
+  const int64_t g = int64_t{1} << gl;
+  return (((f >> (7 + gl)) * kq + (kg >> 2)) * g + ((f >> 7) & (g - 1))) * 512 + (f & 31) * 16 +
+         ((f >> 5) & 3) * 4 + (kg & 3);
+}
+
 // bf16 helpers (round to nearest even, no special-value surprises for finite inputs)
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
