@@ -4,10 +4,13 @@
 Default workload: T=4096 tokens, H=2048, I=1024, E=64 experts, top-6, BF16 (near-uniform softmax
 routing), synthetic seeded inputs.  Prints ONE JSON line (rank 0):
   value     tokens/s of the whole job (all ranks), inputs resident in HBM, CUDA events on the
-            launching stream, max over ranks;
+            launching stream, max over ranks.  The step runs as in training: captured once as a
+            CUDA graph (every launch through the C ABI) and replayed; "step" also reports the same
+            K steps launched eagerly from the host (--no-graph times those instead);
   e2e       the same metric through the C ABI with host (pinned) inputs: H2D of x, ids, weights,
             dY and D2H of out, dX, d_topk_weights for every timed step, double-buffered over a
-            copy stream so transfers overlap the neighbouring steps' compute;
+            copy stream so transfers overlap the neighbouring steps' compute (one graph per buffer
+            set);
   roofline  the dominant kernel's algorithmic flops (or bytes) per launch over its average launch
             time, measured live with per-launch CUDA events (the library's trace hook), against
             the measured peak;
@@ -53,6 +56,7 @@ def parse():
     p.add_argument("--static-tiles", action="store_true",
                    help="static round-robin GEMM tiles instead of cluster launch control")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU seconds of the oracle sample")
     return p.parse_args()
 
@@ -354,6 +358,16 @@ def config_of(w, args, n):
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
+def capture_step(fn, stream):
+    """One CUDA graph of the layer step fn (schedule, forward, backward: every launch through the C
+    ABI).  The step allocates nothing and reads nothing back, so it captures as is; each replay
+    rebuilds the schedule on the device from whatever the captured input buffers hold."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
 def time_router(args, mok, w, d, cfg, dev, stream, peaks) -> dict:
     """Router forward (logits, top-k) and backward (W transposed, g and dx, dW and d_bias) on the
     workload's own router draws, with the schedule built from the router's ids; CUDA events
@@ -459,25 +473,47 @@ def ours(args, rank, ws, local_rank):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
+    # the step as it runs in training: one CUDA graph, replayed (eager launches if capture fails)
+    graph, graph_error = None, None
+    if not args.no_graph:
+        try:
+            graph = capture_step(step, stream)
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    graph.replay()
+            torch.cuda.synchronize()
+        except Exception as ex:  # reported in the JSON line; the eager step is timed instead
+            graph, graph_error = None, f"{type(ex).__name__}: {str(ex)[:200]}"
+    run = graph.replay if graph is not None else step
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
 
-    # ---- timed region: inputs resident in HBM ----
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        return max_over_ranks(a.elapsed_time(b) / args.steps, ws, dev)
+
+    # ---- timed region: inputs resident in HBM, K replays of the step ----
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
     clocks.mark("t0")
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms_max = timed(run)
     clocks.mark("t1")
-    barrier(ws)
-    ms = e0.elapsed_time(e1) / args.steps
-    ms_max = max_over_ranks(ms, ws, dev)
     status = mok.mok_read_device_status(layer.sched, stream)
+    # the same K steps launched one kernel at a time from the host, for comparison
+    eager_ms = timed(step) if graph is not None else ms_max
+    step_mode = {"mode": "cuda_graph" if graph is not None else "eager",
+                 "eager_ms_per_step": eager_ms, "eager_value": aggregate_tokens_per_s(w.T, ws, eager_ms)}
+    if graph_error:
+        step_mode["graph_error"] = graph_error
 
     # ---- per-kernel times: the same K steps with the library's event trace ----
     tr = mok.Tracer(capacity=20 * args.steps + 64)
@@ -546,16 +582,24 @@ def ours(args, rank, ws, local_rank):
                 dst.copy_(src, non_blocking=True)
             ev_in[b].record(copy_stream)
 
+    def abi_step(b):  # the step on buffer set b, through the C ABI entry points
+        def fn():
+            xx, ii, ss, dd = dev_in[b]
+            sch = mok.mok_build_schedule(layer.cfg, layer.shape, ii, ss, layer.ws, stream)
+            mok.mok_forward(sch, xx, weights, dev_out[b]["out"], layer.ctx, stream)
+            mok.mok_backward(sch, layer.ctx, dd, weights, dev_out[b]["grads"], stream)
+        return fn
+
+    # one CUDA graph per buffer set when the resident-input step ran from a graph
+    steps_b = [capture_step(abi_step(b), stream).replay if graph is not None else abi_step(b) for b in range(2)]
+
     def compute(i):
         b = i % 2
-        xx, ii, ss, dd = dev_in[b]
         with torch.cuda.stream(stream):
             stream.wait_event(ev_in[b])
             if i >= 2:
                 stream.wait_event(ev_out[b])  # buffer b's previous results have been downloaded
-            sch = mok.mok_build_schedule(layer.cfg, layer.shape, ii, ss, layer.ws, stream)
-            mok.mok_forward(sch, xx, weights, dev_out[b]["out"], layer.ctx, stream)
-            mok.mok_backward(sch, layer.ctx, dd, weights, dev_out[b]["grads"], stream)
+            steps_b[b]()
             ev_done[b].record(stream)
 
     def download(i):
@@ -607,6 +651,7 @@ def ours(args, rank, ws, local_rank):
             "launches_per_step": launches_per_step,
             "clocks": clk,
             "device_status": status,
+            "step": step_mode,
         }
         if router is not None:
             result["router"] = router

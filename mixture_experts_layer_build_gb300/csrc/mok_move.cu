@@ -230,39 +230,71 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
 // The 128 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
 //   along H: each thread quantises two 32-column blocks of rows -- row-major E4M3 codes for the
 //     forward / data-gradient GEMMs, A-operand atoms;
-//   along the routed rows: each thread quantises one column over two 32-row blocks -- 64
-//     consecutive bytes of the transposed copy [H, rcap] the weight-gradient GEMM reads K-major,
-//     atoms grouped gT at a time.
+//   along the routed rows: each thread quantises two adjacent columns over one 32-row block
+//     (reading both as one 32-bit word per row) -- 32 consecutive bytes per column of the
+//     transposed copy [H, rcap] the weight-gradient GEMM reads K-major, atoms grouped gT at a time.
+// The scale bytes are collected in shared memory and leave as one 32-bit word per row (its four
+// 32-column blocks) and per column (its four 32-row blocks): in both atom layouts these four
+// bytes are adjacent.
 // The rounding is bit-exact with mxfp8_quantize_kernel (shared exponent from amax, E4M3
 // round-to-nearest-even, saturating).  Row blocks never straddle two experts: segments start at
 // multiples of 128.
 constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
 
-__device__ __forceinline__ void gmx_row_block(const uint8_t* p, float (&o)[32]) {
+// E4M3 codes and scale byte of one 32-value MX block of bf16 values held as packed words, without
+// 32 fp32 registers: MODE 0 / 1 = value i is the low / high half of w[i] (32 words, one column
+// of a staged pair of columns), MODE 2 = values 2i, 2i + 1 are the low, high halves of w[i] (16
+// words along a row).  The same codes and scale as mx_quant32 on the fp32 values: a bf16
+// magnitude's bits order like the value, and its exponent field is the fp32 one.
+template <int MODE, int N>
+__device__ __forceinline__ uint32_t gmx_quant(const uint32_t (&w)[N], uint32_t (&codes)[8]) {
+  static_assert((MODE < 2 && N == 32) || (MODE == 2 && N == 16), "32 values");
+  uint32_t amax = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p + 16 * i);
-    o[8 * i] = bf16_lo(v.x);
-    o[8 * i + 1] = bf16_hi(v.x);
-    o[8 * i + 2] = bf16_lo(v.y);
-    o[8 * i + 3] = bf16_hi(v.y);
-    o[8 * i + 4] = bf16_lo(v.z);
-    o[8 * i + 5] = bf16_hi(v.z);
-    o[8 * i + 6] = bf16_lo(v.w);
-    o[8 * i + 7] = bf16_hi(v.w);
+  for (int i = 0; i < N; ++i) {
+    const uint32_t m = MODE == 0 ? w[i] & 0x7FFFu : MODE == 1 ? (w[i] >> 16) & 0x7FFFu
+                                                              : max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu);
+    amax = max(amax, m);
   }
+  if (amax >= 0x7F80u) {  // an Inf or NaN in the block
+#pragma unroll
+    for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
+    return 0xFFu;
+  }
+  int shared = static_cast<int>(amax >> 7) - 127 - 8;
+  shared = shared < -127 ? -127 : shared;
+  const float dn = pow2f(-shared);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {  // values 2i, 2i + 1
+    float v0, v1;
+    if constexpr (MODE == 2) {
+      v0 = __uint_as_float(w[i] << 16);
+      v1 = __uint_as_float(w[i] & 0xFFFF0000u);
+    } else {
+      v0 = MODE ? __uint_as_float(w[2 * i] & 0xFFFF0000u) : __uint_as_float(w[2 * i] << 16);
+      v1 = MODE ? __uint_as_float(w[2 * i + 1] & 0xFFFF0000u) : __uint_as_float(w[2 * i + 1] << 16);
+    }
+    uint16_t q;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(v1 * dn), "f"(v0 * dn));
+    if (i & 1) codes[i >> 1] |= static_cast<uint32_t>(q) << 16;
+    else codes[i >> 1] = q;
+  }
+  return static_cast<uint32_t>(shared + 127);
 }
 
-__global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint16_t* __restrict__ src,
+// Five CTAs per SM (48 registers; the packed-word quantisation keeps that free of spills).
+__global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const uint16_t* __restrict__ src,
                                                             const int32_t* __restrict__ row_token,
                                                             const int32_t* __restrict__ meta, int32_t H,
                                                             uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf,
                                                             uint8_t* __restrict__ dstR_q,
                                                             uint8_t* __restrict__ dstR_sf, int64_t rcap, int gT) {
   __shared__ __align__(16) uint8_t tile[128 * kGmxStride];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 128;
+  __shared__ __align__(4) uint8_t sc_row[128 * 4];  // [row][32-column block]
+  __shared__ __align__(4) uint8_t sc_col[128 * 4];  // [column][32-row block]
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
   if (r0 >= meta[0]) return;
-  const int c0 = static_cast<int>(blockIdx.y) * 128;
+  const int c0 = static_cast<int>(blockIdx.x) * 128;
   const int t = threadIdx.x;
   {
     uint4 val[8];
@@ -281,32 +313,44 @@ __global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint16_t* __r
 #pragma unroll
   for (int k = 0; k < 2; ++k) {  // along H: row it / 4, columns c0 + 32 (it % 4) ... + 31
     const int it = t + 256 * k, r = it / 4, b = it % 4;
-    float o[32];
-    gmx_row_block(tile + r * kGmxStride + b * 64, o);
+    uint32_t wr[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + r * kGmxStride + b * 64 + 16 * i);
+      wr[4 * i] = v.x, wr[4 * i + 1] = v.y, wr[4 * i + 2] = v.z, wr[4 * i + 3] = v.w;
+    }
     uint32_t codes[8];
-    const uint32_t sb = mx_quant32(o, codes);
+    sc_row[4 * r + b] = static_cast<uint8_t>(gmx_quant<2>(wr, codes));
     uint4* dq = reinterpret_cast<uint4*>(dst_q + (r0 + r) * H + c0 + 32 * b);
     __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
     __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-    dst_sf[sf_atom_offset(r0 + r, (c0 >> 5) + b, H / 128)] = static_cast<uint8_t>(sb);
   }
-  {  // along the rows: column c0 + t % 128, row blocks 2 (t / 128) and 2 (t / 128) + 1
-    const int c = t % 128, rb0 = 2 * (t / 128);
-    uint4* dq = reinterpret_cast<uint4*>(dstR_q + static_cast<int64_t>(c0 + c) * rcap + r0 + 32 * rb0);
+  {  // along the rows: columns c0 + 2 (t % 64) and the next one, row block t / 64
+    const int cp = t % 64, rb = t / 64;
+    uint32_t w2[32];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      float o[32];
+    for (int r = 0; r < 32; ++r)
+      w2[r] = *reinterpret_cast<const uint32_t*>(tile + (32 * rb + r) * kGmxStride + 4 * cp);
 #pragma unroll
-      for (int r = 0; r < 32; ++r)
-        o[r] = __uint_as_float(
-            static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(tile + (32 * (rb0 + k) + r) * kGmxStride + 2 * c))
-            << 16);
+    for (int j = 0; j < 2; ++j) {
       uint32_t codes[8];
-      const uint32_t sb = mx_quant32(o, codes);
-      __stcs(dq + 2 * k, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-      __stcs(dq + 2 * k + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
-      dstR_sf[sf_atom_offset_g(c0 + c, (r0 >> 5) + rb0 + k, rcap / 128, gT)] = static_cast<uint8_t>(sb);
+      const uint32_t sb = j ? gmx_quant<1>(w2, codes) : gmx_quant<0>(w2, codes);
+      sc_col[4 * (2 * cp + j) + rb] = static_cast<uint8_t>(sb);
+      uint4* dq = reinterpret_cast<uint4*>(dstR_q + static_cast<int64_t>(c0 + 2 * cp + j) * rcap + r0 + 32 * rb);
+      __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+      __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
     }
+  }
+  __syncthreads();
+  // k-groups c0 / 32 ... + 3 of row r0 + t, and row groups r0 / 32 ... + 3 of column c0 + t - 128:
+  // both start at a multiple of 4 (c0 and r0 are multiples of 128), so each word is aligned
+  if (t < 128) {
+    *reinterpret_cast<uint32_t*>(dst_sf + sf_atom_offset(r0 + t, c0 >> 5, H / 128)) =
+        *reinterpret_cast<const uint32_t*>(sc_row + 4 * t);
+  } else {
+    const int c = t - 128;
+    *reinterpret_cast<uint32_t*>(dstR_sf + sf_atom_offset_g(c0 + c, r0 >> 5, rcap / 128, gT)) =
+        *reinterpret_cast<const uint32_t*>(sc_col + 4 * c);
   }
 }
 
@@ -360,7 +404,10 @@ int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const i
                           int32_t H, uint8_t* dst_q, uint8_t* dst_sf, uint8_t* dstR_q, uint8_t* dstR_sf,
                           int64_t rcap, int gT, int kind, cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
-  const dim3 grid(static_cast<unsigned>((rpad_max + 127) / 128), static_cast<unsigned>(H / 128));
+  // column tiles fastest: blocks running together read whole source rows, not 256-byte pieces of
+  // 128 scattered rows
+  if ((rpad_max + 127) / 128 > 65535) return static_cast<int>(cudaErrorInvalidValue);
+  const dim3 grid(static_cast<unsigned>(H / 128), static_cast<unsigned>((rpad_max + 127) / 128));
   trace_begin(stream, kind);
   gather_rows_mx_kernel<<<grid, 256, 0, stream>>>(src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
   trace_end(stream);

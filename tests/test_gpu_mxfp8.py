@@ -49,7 +49,7 @@ SMALL = [
     ("ragged", inputs.custom(T=100, H=256, I=256, E=5, K=3)),
     ("multi_tile", inputs.custom(T=700, H=512, I=384, E=3, K=2)),
     ("h384", inputs.custom(T=300, H=384, I=256, E=3, K=2)),  # H not a multiple of 256: 128-wide tiles
-    # H above 4096: the first data-gradient GEMM runs its other epilogue (four warps, six stages)
+    # H above 4096: the first data-gradient GEMM runs its other epilogue (four warps)
     ("long_h", inputs.custom(T=160, H=4224, I=256, E=3, K=2)),
 ]
 
