@@ -24,13 +24,15 @@ namespace {
 // ---------------------------------------------------------------------------------------------
 constexpr int kLgExperts = 64;  // experts per block
 constexpr int kLgTokens = 32;   // tokens per block
-constexpr int kLgChunk = 32;    // h values staged per step
+constexpr int kLgChunk = 64;    // h values staged per step
 
 // logits[t,e] = (sum over h ascending of x[t,h] W[h,e], fused multiply-add) + bias[e].  Block of
 // 128 threads: 32 tokens x 64 experts; thread (te, tt) owns experts e0 + 4 te .. + 3 and tokens
-// t0 + 4 tt .. + 3 (16 independent accumulation chains).  x and W chunks of 32 h are staged in
+// t0 + 4 tt .. + 3 (16 independent accumulation chains).  x and W chunks of 64 h are staged in
 // shared memory as fp32: per h a thread reads its four W values as one 16-byte load and its four
-// x values (shared by the warp's two token groups).
+// x values (shared by the warp's two token groups).  Chunk c + 1 is loaded into registers while
+// chunk c is computed, in 16-byte loads: 64 h of compute is what covers a global load's latency
+// (32 h did not).
 __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __restrict__ x,
                                                             const uint16_t* __restrict__ w,
                                                             const float* __restrict__ bias, int64_t T, int H, int E,
@@ -41,51 +43,86 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
   const int te = tid & 15, tt = tid >> 4;
   const int e0 = blockIdx.x * kLgExperts;
   const int64_t t0 = static_cast<int64_t>(blockIdx.y) * kLgTokens;
+  const bool wvec = (E & 7) == 0;  // W rows of 8 experts are 16-byte aligned
   float acc[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-  // chunk c + 1 is loaded into registers while chunk c is computed: x as one 16-byte load per
-  // thread (token tid / 4, 8 h), W as 16 coalesced loads (h row q / 64, expert q % 64)
-  const int xr = tid >> 2, xc = (tid & 3) * 8;
+  // x: token tid / 4, h (tid % 4) * 16 .. + 15 (two 16-byte loads).  W, 8-expert rows: row q / 8,
+  // experts (q % 8) * 8 .. + 7 for q = tid + 128 j (four 16-byte loads); otherwise element q % 64 of
+  // row q / 64 for q = tid + 128 j, j < 32, packed two per word.
+  const int xr = tid >> 2, xc = (tid & 3) * 16;
   const int64_t xt = t0 + xr;
-  uint4 xv4 = make_uint4(0, 0, 0, 0);
-  uint16_t wv16[16];
+  uint4 xv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  uint4 wv[4];
   auto fetch = [&](int h0) {
-    if (xt < T) xv4 = __ldg(reinterpret_cast<const uint4*>(x + xt * H + h0 + xc));
+    if (xt < T) {
+      const uint4* p = reinterpret_cast<const uint4*>(x + xt * H + h0 + xc);
+      xv[0] = __ldg(p);
+      xv[1] = __ldg(p + 1);
+    }
+    if (wvec) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int q = tid + 128 * j, r = q >> 6, c = q & 63;
-      wv16[j] = e0 + c < E ? __ldg(w + static_cast<int64_t>(h0 + r) * E + e0 + c) : static_cast<uint16_t>(0);
+      for (int j = 0; j < 4; ++j) {
+        const int q = tid + 128 * j, r = q >> 3, c = (q & 7) * 8;
+        wv[j] = e0 + c < E ? __ldg(reinterpret_cast<const uint4*>(w + static_cast<int64_t>(h0 + r) * E + e0 + c))
+                           : make_uint4(0, 0, 0, 0);
+      }
+    } else {
+      uint32_t* pw = reinterpret_cast<uint32_t*>(wv);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        uint32_t v2 = 0;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int q = tid + 128 * (j + k), r = q >> 6, c = q & 63;
+          const uint32_t b = e0 + c < E ? __ldg(w + static_cast<int64_t>(h0 + r) * E + e0 + c) : 0u;
+          v2 |= b << (16 * k);
+        }
+        pw[j >> 1] = v2;
+      }
     }
   };
   fetch(0);
   for (int h0 = 0; h0 < H; h0 += kLgChunk) {
     __syncthreads();  // the previous chunk's reads of xs / ws are done
     {
-      const uint32_t p[4] = {xv4.x, xv4.y, xv4.z, xv4.w};
       float4* d = reinterpret_cast<float4*>(&xs[xr][xc]);
-      d[0] = make_float4(bf16_lo(p[0]), bf16_hi(p[0]), bf16_lo(p[1]), bf16_hi(p[1]));
-      d[1] = make_float4(bf16_lo(p[2]), bf16_hi(p[2]), bf16_lo(p[3]), bf16_hi(p[3]));
-    }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int q = tid + 128 * j;
-      ws[q >> 6][q & 63] = __uint_as_float(static_cast<uint32_t>(wv16[j]) << 16);
+      for (int i = 0; i < 2; ++i) {
+        d[2 * i] = make_float4(bf16_lo(xv[i].x), bf16_hi(xv[i].x), bf16_lo(xv[i].y), bf16_hi(xv[i].y));
+        d[2 * i + 1] = make_float4(bf16_lo(xv[i].z), bf16_hi(xv[i].z), bf16_lo(xv[i].w), bf16_hi(xv[i].w));
+      }
+    }
+    if (wvec) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = tid + 128 * j, r = q >> 3, c = (q & 7) * 8;
+        float4* d = reinterpret_cast<float4*>(&ws[r][c]);
+        d[0] = make_float4(bf16_lo(wv[j].x), bf16_hi(wv[j].x), bf16_lo(wv[j].y), bf16_hi(wv[j].y));
+        d[1] = make_float4(bf16_lo(wv[j].z), bf16_hi(wv[j].z), bf16_lo(wv[j].w), bf16_hi(wv[j].w));
+      }
+    } else {
+      const uint32_t* pw = reinterpret_cast<const uint32_t*>(wv);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int q = tid + 128 * j;
+        ws[q >> 6][q & 63] = (j & 1) ? bf16_hi(pw[j >> 1]) : bf16_lo(pw[j >> 1]);
+      }
     }
     __syncthreads();
     if (h0 + kLgChunk < H) fetch(h0 + kLgChunk);
 #pragma unroll 8
     for (int h = 0; h < kLgChunk; ++h) {
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[h][4 * te]);
+      const float4 wq = *reinterpret_cast<const float4*>(&ws[h][4 * te]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float xv = xs[4 * tt + i][h];
-        acc[i][0] = __fmaf_rn(xv, wv.x, acc[i][0]);
-        acc[i][1] = __fmaf_rn(xv, wv.y, acc[i][1]);
-        acc[i][2] = __fmaf_rn(xv, wv.z, acc[i][2]);
-        acc[i][3] = __fmaf_rn(xv, wv.w, acc[i][3]);
+        const float xq = xs[4 * tt + i][h];
+        acc[i][0] = __fmaf_rn(xq, wq.x, acc[i][0]);
+        acc[i][1] = __fmaf_rn(xq, wq.y, acc[i][1]);
+        acc[i][2] = __fmaf_rn(xq, wq.z, acc[i][2]);
+        acc[i][3] = __fmaf_rn(xq, wq.w, acc[i][3]);
       }
     }
   }
