@@ -17,6 +17,12 @@
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Every
  *    call only enqueues work on it and returns; none synchronises, except
  *    mok_read_device_status.  Inputs must stay valid until the enqueued work has run.
+ *  - CUDA graphs: mok_build_schedule, mok_forward and mok_backward allocate nothing and read
+ *    nothing back, and their grids and tensor maps depend only on the shape and the buffer
+ *    addresses.  A step made of them may be captured once (stream capture) and replayed; each
+ *    replay rebuilds the schedule on the device from the routing the captured buffers then hold.
+ *    Call each entry point once outside capture first, so that its one-time kernel attribute
+ *    setup is done.
  *  - Errors: argument, shape, alignment and size problems are detected on the host and returned
  *    before anything is enqueued.  Data-dependent problems found on the device (an expert id
  *    outside [0, E), a bounded wait that timed out) set bits (1 << code) in the schedule's device
