@@ -26,6 +26,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -234,13 +235,20 @@ def roofline_of(flops, nbytes, ms, peaks, kind="bf16"):
     return dict(bound="hbm", achieved=nbytes / sec / 1e9, peak=peaks["hbm_gbs"], unit="GB/s", frac=t_hbm / sec)
 
 
+def _code_only(text: str) -> bytes:
+    """Source text without comments, trailing blanks and empty lines: what the compiler sees."""
+    text = re.sub(r"/\*.*?\*/|//[^\n]*", "", text, flags=re.S)
+    return "\n".join(l.rstrip() for l in text.splitlines() if l.strip()).encode()
+
+
 def src_hash() -> str:
+    """Hash of the CUDA sources and the ABI header (code only), keying the stored ncu counters."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mixture_experts_layer_build_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "mok.h"), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, f)).read()))
+    h.update(_code_only(open(os.path.join(ROOT, "include", "mok.h")).read()))
     return h.hexdigest()[:16]
 
 
