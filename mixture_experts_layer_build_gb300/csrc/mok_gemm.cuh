@@ -99,8 +99,9 @@ constexpr int kUnitRing = 8;
 // A stage holds one K block of A and B as rows of 128 bytes (64 bf16 or 128 e4m3 along K) and, with
 // MX, the K block's scale atoms: one for A's 128 rows, BN / 128 for B's rows.
 //   bf16, and MX with BN = 128: two TMEM accumulators (the epilogue of one tile overlaps the
-//     main loop of the next), four epilogue warps.  MX puts stage s's scale words in TMEM columns
-//     256 + 8 s ...
+//     main loop of the next), four epilogue warps (eight, two per lane quarter with 64 columns
+//     each, for the block-scaled DGRAD1 with SPLIT).  MX puts stage s's scale words in TMEM
+//     columns 256 + 8 s ...
 //   MX with BN = 256 ("wide"): two 256-column accumulators would fill TMEM and leave no room for
 //     the scale words, so there is one; eight epilogue warps (two per lane quarter, 128 columns
 //     each) copy it to registers and release it at once, then finish the tile's epilogue while
