@@ -353,6 +353,13 @@ MOK_API mok_status mok_router_backward(const mok_schedule* sched, const void* x,
  * The only call that blocks. */
 MOK_API mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream);
 
+/* Failure-path self test.  Enqueues one single-thread kernel that waits, through the library's
+ * bounded mbarrier wait (the one every GEMM role uses), on a barrier that nothing completes.  The
+ * wait gives up at the library's deadline (2 s), ORs (1 << MOK_ERR_TIMEOUT) into *status (a device
+ * word the caller owns) and the kernel returns normally, leaving the context usable.  No GPU
+ * fault, trap or unbounded wait is involved. */
+MOK_API mok_status mok_selftest_wait_timeout(uint32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -241,6 +241,18 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, inner, outer, box_inner, box_outer, sw);
 }
 
+// One thread waits on an mbarrier that nothing completes, through the bounded wait every GEMM role
+// uses: it must give up at the deadline, record MOK_ERR_TIMEOUT in *status and return.
+__global__ void selftest_wait_kernel(uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  fence_barrier_init();
+  mbar_wait(smem_u32(&bar), 0u, reinterpret_cast<volatile int*>(&abort_flag), status);
+}
+
 static mok_trace* g_trace = nullptr;
 
 void trace_begin(cudaStream_t s, int kind) {
@@ -454,7 +466,7 @@ const char* mok_kernel_name(int32_t kind) {
       "gemm_fwd_down",   "combine",       "gather_dy",     "gemm_dgrad1",    "ds_reduce",
       "gemm_dgrad2",     "dx_reduce",     "gemm_wgrad_gu", "gemm_wgrad_d",   "mxfp8_quantize",
       "mx_scale_atoms",  "router_logits", "router_topk",   "router_transpose", "router_dx",
-      "router_dw"};
+      "router_dw",       "selftest_wait"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "?";
 }
 
@@ -485,6 +497,14 @@ mok_status mok_mx_operands_of(const mok_schedule* sched, const void* fwd_ctx, mo
   out->xr_groups = z.mx_bn_h() / 128;
   out->sar_groups = z.mx_bn_i() / 128;
   return MOK_OK;
+}
+
+mok_status mok_selftest_wait_timeout(uint32_t* status, void* stream) {
+  if (!status) return MOK_ERR_INVALID_ARG;
+  trace_begin(as_stream(stream), K_SELFTEST_WAIT);
+  selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(status);
+  trace_end(as_stream(stream));
+  return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
 }
 
 mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream) {

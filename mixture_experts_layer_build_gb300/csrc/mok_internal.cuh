@@ -104,6 +104,7 @@ enum KernelKind : int {
   K_ROUTER_TRANSPOSE,
   K_ROUTER_DX,
   K_ROUTER_DW,
+  K_SELFTEST_WAIT,
   K_NUM_KINDS
 };
 void trace_begin(cudaStream_t s, int kind);  // no-ops unless a trace is set

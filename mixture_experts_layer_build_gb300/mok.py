@@ -107,6 +107,8 @@ _lib.mok_kernel_name.restype = ctypes.c_char_p
 _lib.mok_kernel_name.argtypes = [ctypes.c_int32]
 _lib.mok_read_device_status.restype = ctypes.c_int
 _lib.mok_read_device_status.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(ctypes.c_uint32), _P]
+_lib.mok_selftest_wait_timeout.restype = ctypes.c_int
+_lib.mok_selftest_wait_timeout.argtypes = [_P, _P]
 
 class mok_mx_operands(ctypes.Structure):
     _fields_ = [(k, _P) for k in ("xq", "xs", "aq", "as_", "dyq", "dys", "dgq", "dgs", "xr", "xrs", "dyr", "dyrs",
@@ -121,7 +123,7 @@ _lib.mok_mx_operands_of.argtypes = [ctypes.POINTER(mok_schedule), _P, ctypes.POI
 EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
             "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status", "mok_set_trace",
             "mok_kernel_name", "mok_build_schedule_noalloc", "mok_mx_operands_of", "mok_router_workspace_bytes",
-            "mok_router_forward", "mok_router_backward")
+            "mok_router_forward", "mok_router_backward", "mok_selftest_wait_timeout")
 _lib.mok_router_workspace_bytes.restype = ctypes.c_size_t
 _lib.mok_router_workspace_bytes.argtypes = [ctypes.POINTER(mok_shape)]
 _lib.mok_router_forward.restype = ctypes.c_int
@@ -347,6 +349,14 @@ def mok_read_device_status(sched: Schedule, stream=None) -> int:
     _check(_lib.mok_read_device_status(ctypes.byref(sched.c), ctypes.byref(v), _stream(stream)),
            "mok_read_device_status")
     return v.value
+
+
+def mok_selftest_wait_timeout(status: torch.Tensor, stream=None) -> None:
+    """status: one int32 (bit pattern of a uint32) on the device; the timeout bit is OR-ed in."""
+    if status.dtype != torch.int32 or status.numel() != 1 or not status.is_cuda:
+        raise ValueError("status must be one int32 on the GPU")
+    _check(_lib.mok_selftest_wait_timeout(ctypes.c_void_p(status.data_ptr()), _stream(stream)),
+           "mok_selftest_wait_timeout")
 
 
 # ---------------------------------------------------------------------------------------------
