@@ -266,51 +266,71 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t* __restric
   }
 }
 
-// dW[h, e] = sum over expert e's routed rows in ascending order (the schedule's expert-grouped
-// layout) of x[token, h] g[slot]; db[e] likewise of g[slot].  Block (expert e, 512 h), thread
-// h0 + 2 tid .. + 1.  The rows' (token, g) come through shared memory 64 at a time, so the x loads
-// of several rows are in flight while the fused multiply-adds keep the row order.
+// dW[h, e] = sum over expert e's routed rows (the schedule's expert-grouped layout) of
+// x[token, h] g[slot]; db[e] likewise of g[slot].  Block (expert e, 512 h) of 256 P threads: the
+// expert's rows are split into P parts; thread part p (tid / 256) sums part p in ascending row
+// order for h0 + 2 (tid % 256) .. + 1, and the result is part 0 + part 1 (a fixed order).  The
+// loop is bound by load latency, so P = 2 halves the time when the grid is too small to fill the
+// GPU (fewer than two blocks per SM); otherwise P = 1 (every row in one ascending chain).  Each
+// part's rows (token, g) come through shared memory 64 at a time.
 constexpr int kDwRows = 64;
-__global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restrict__ x,
+template <int P>
+__global__ void __launch_bounds__(256 * P) router_dw_kernel(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ gbuf,
                                                         const int32_t* __restrict__ counts,
                                                         const int32_t* __restrict__ poff,
                                                         const int32_t* __restrict__ perm, int H, int E, int K,
                                                         float* __restrict__ dw, float* __restrict__ db) {
-  __shared__ int64_t s_tok[kDwRows];
-  __shared__ float s_g[kDwRows];
+  static_assert(P == 1 || P == 2, "one or two row parts");
+  __shared__ int64_t s_tok[P][kDwRows];
+  __shared__ float s_g[P][kDwRows];
+  __shared__ float2 s_part[256];
+  __shared__ float s_db;
   const int e = blockIdx.x;
-  const int h = blockIdx.y * 512 + 2 * threadIdx.x;
-  const int r0 = __ldg(poff + e), n = __ldg(counts + e);
+  const int p = P == 2 ? static_cast<int>(threadIdx.x >> 8) : 0, tl = threadIdx.x & 255;
+  const int h = blockIdx.y * 512 + 2 * tl;
+  const int n = __ldg(counts + e), nh = (n + P - 1) / P;
+  const int r0 = __ldg(poff + e) + (p ? nh : 0), np = p ? n - nh : nh;  // this part's rows
   float a0 = 0.0f, a1 = 0.0f, ab = 0.0f;
-  for (int c0 = 0; c0 < n; c0 += kDwRows) {
-    const int m = min(kDwRows, n - c0);
+  for (int c0 = 0; c0 < nh; c0 += kDwRows) {  // both parts take the same number of steps
+    const int m = max(0, min(kDwRows, np - c0));
     __syncthreads();
-    if (threadIdx.x < m) {
-      const int j = __ldg(perm + r0 + c0 + threadIdx.x);
-      s_tok[threadIdx.x] = j < 0 ? -1 : j / K;
-      s_g[threadIdx.x] = j < 0 ? 0.0f : __ldg(gbuf + j);
+    if (tl < m) {
+      const int j = __ldg(perm + r0 + c0 + tl);
+      s_tok[p][tl] = j < 0 ? -1 : j / K;
+      s_g[p][tl] = j < 0 ? 0.0f : __ldg(gbuf + j);
     }
     __syncthreads();
     if (h < H) {
 #pragma unroll 8
       for (int i = 0; i < m; ++i) {
-        const int64_t t = s_tok[i];
+        const int64_t t = s_tok[p][i];
         if (t < 0) continue;
-        const float g = s_g[i];
+        const float g = s_g[p][i];
         const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(x + t * H + h));
         a0 = __fmaf_rn(bf16_lo(v), g, a0);
         a1 = __fmaf_rn(bf16_hi(v), g, a1);
       }
     }
-    if (threadIdx.x == 0)
-      for (int i = 0; i < m; ++i) ab += s_g[i];
+    if (tl == 0)
+      for (int i = 0; i < m; ++i) ab += s_g[p][i];
+  }
+  if constexpr (P == 2) {
+    if (p == 1) {
+      s_part[tl] = make_float2(a0, a1);
+      if (tl == 0) s_db = ab;
+    }
+    __syncthreads();
+    if (p == 1) return;
+    a0 = __fadd_rn(a0, s_part[tl].x);
+    a1 = __fadd_rn(a1, s_part[tl].y);
+    ab = __fadd_rn(ab, s_db);
   }
   if (h < H) {
     dw[static_cast<int64_t>(h) * E + e] = a0;
     dw[static_cast<int64_t>(h + 1) * E + e] = a1;
   }
-  if (db && blockIdx.y == 0 && threadIdx.x == 0) db[e] = ab;
+  if (db && blockIdx.y == 0 && tl == 0) db[e] = ab;
 }
 
 bool router_shape_ok(int64_t T, int H, int E, int K) {
@@ -379,8 +399,12 @@ extern "C" MOK_API mok_status mok_router_backward(const mok_schedule* sched, con
   }
   const dim3 gw(s.E, (s.H + 511) / 512);
   trace_begin(st, K_ROUTER_DW);
-  router_dw_kernel<<<gw, 256, 0, st>>>(static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
-                                       sched->perm, s.H, s.E, s.K, dw_router, d_bias);
+  if (static_cast<int64_t>(gw.x) * gw.y < 2 * static_cast<int64_t>(sm_count()))  // small grid: two row parts
+    router_dw_kernel<2><<<gw, 512, 0, st>>>(static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
+                                            sched->perm, s.H, s.E, s.K, dw_router, d_bias);
+  else
+    router_dw_kernel<1><<<gw, 256, 0, st>>>(static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
+                                            sched->perm, s.H, s.E, s.K, dw_router, d_bias);
   trace_end(st);
   return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
 }

@@ -66,7 +66,8 @@ def _check(x, w, b, K, d, got):
 
 @pytest.mark.parametrize("T,H,E,K,bias", [(200, 256, 12, 3, False), (333, 384, 40, 8, True), (64, 128, 1, 1, False),
                                           (50, 256, 32, 32, True), (0, 128, 8, 2, False),
-                                          (100, 512, 160, 8, True)])  # three expert blocks, the last partial
+                                          (100, 512, 160, 8, True),  # three expert blocks, the last partial
+                                          (64, 1024, 320, 4, False)])  # dW grid of 640 blocks: one row part
 def test_router_parity(mok, T, H, E, K, bias):
     x, w, b, d = _router_case(T, H, E, K, bias, seed=T + E)
     got = _run(mok, x, w, b, K, d)
