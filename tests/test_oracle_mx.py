@@ -10,6 +10,12 @@ H, a and dg/du along I, weights pre-quantised along each GEMM's K).  Pins:
     run on the quantised inputs;
   * the weight gradients quantise their operands along the routed rows: rebuilt here from the
     expert-grouped row order (numpy stable sort, zero padding to 128 rows, blocks of 32 rows);
+  * the forward and data-gradient quantisation points (x and dY along H, a along I, dA' from the
+    copy of Wd^T, dS on a_q, dg and du along I into the copies of Wg^T and Wu^T) are rebuilt from
+    independent parts: a numpy / torch-float8 quantiser, weights decoded by torch, numpy matmuls
+    and torch autograd for the SwiGLU backward; plausible slips (dY left unquantised, a in place
+    of a_q, the forward copy of Wd in place of Wd^T's, dg left unquantised) are shown to move the
+    result far beyond the tolerance;
   * the sampled entry points agree with the full one.
 """
 import numpy as np
@@ -136,7 +142,7 @@ def _qr(m):
     """MX quantise-dequantise along rows: every column of m [nrows, ncols] in blocks of 32 rows."""
     out = np.empty_like(m)
     for r0 in range(0, m.shape[0], 32):
-        out[r0:r0 + 32] = oracle.mx_fakequant(np.ascontiguousarray(m[r0:r0 + 32].T)).T
+        out[r0:r0 + 32] = _q32(np.ascontiguousarray(m[r0:r0 + 32].T)).T
     return out
 
 
@@ -171,3 +177,132 @@ def test_wgrad_quantised_along_expert_rows():
     slots = np.flatnonzero(flat == 0)
     alt = _qr(np.pad(r["dg"][slots], ((0, -slots.size % 128), (0, 0)))).T @ np.pad(qx_h[slots // K], ((0, -slots.size % 128), (0, 0)))
     assert not np.allclose(alt, r["dWg"][0], rtol=1e-6)
+
+
+# ------------------------------------------------------------------------------------------------
+# Independent rebuild of the forward and data-gradient quantisation points
+# ------------------------------------------------------------------------------------------------
+def _e4m3_grid():
+    """Non-negative finite E4M3 values in code order (codes 0x00 .. 0x7E), decoded by torch."""
+    codes = torch.arange(0x7F, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+_GRID = _e4m3_grid()
+
+
+def _q32(v):
+    """MX quantise-dequantise along the last axis in blocks of 32, built without the oracle: the
+    shared exponent floor(log2 amax) - 8 from numpy's frexp (clamped to [-127, 127], -127 for an
+    all-zero block), then the nearest value of torch's decoded E4M3 grid with ties to the even
+    code, saturating at 448."""
+    v = np.asarray(v, np.float64)
+    blocks = v.reshape(-1, 32)
+    amax = np.abs(blocks).max(axis=1)
+    _, ex = np.frexp(amax)
+    shared = np.where(amax > 0, np.clip(ex - 1 - 8, -127, 127), -127).astype(np.float64)
+    scale = 2.0 ** shared[:, None]
+    mag = np.minimum(np.abs(blocks) / scale, _GRID[-1])
+    hi = np.clip(np.searchsorted(_GRID, mag), 0, _GRID.size - 1)
+    lo = np.clip(hi - 1, 0, _GRID.size - 1)
+    dlo, dhi = mag - _GRID[lo], _GRID[hi] - mag
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return (np.sign(blocks) * _GRID[pick] * scale).reshape(v.shape)
+
+
+def _decode(q, sc):
+    """Value of an MXFP8 matrix from its bytes: torch's float8 decode times 2^(scale - 127)."""
+    codes = torch.from_numpy(np.ascontiguousarray(q)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return codes * np.repeat(2.0 ** (sc.astype(np.float64) - 127.0), 32, axis=1)
+
+
+def _rebuild(ids, s, x, dY, mx, E, I, *, quant_dy=True, ds_on_aq=True, dap_from_wdt=True, quant_dg=True):
+    """Forward and data gradients of the MXFP8 mode from the reading of the quantisation points,
+    with switches that plant the slips the test must catch."""
+    T, K = ids.shape
+    H = x.shape[1]
+    R = T * K
+    e = ids.reshape(-1).astype(np.int64)
+    t = np.arange(R) // K
+    sv = s.reshape(-1).astype(np.float64)
+    Wg = _decode(mx["q_gate"], mx["s_gate"]).reshape(E, I, H)    # along H
+    Wu = _decode(mx["q_up"], mx["s_up"]).reshape(E, I, H)
+    Wd = _decode(mx["q_down"], mx["s_down"]).reshape(E, H, I)    # along I
+    Wgt = _decode(mx["qt_gate"], mx["st_gate"]).reshape(E, H, I)  # Wg^T along I
+    Wut = _decode(mx["qt_up"], mx["st_up"]).reshape(E, H, I)
+    Wdt = _decode(mx["qt_down"], mx["st_down"]).reshape(E, I, H)  # Wd^T along H
+    xq = _q32(oracle.bf16_to_f64(x))
+    dy = oracle.bf16_to_f64(dY)
+    dyq = _q32(dy) if quant_dy else dy
+    g = torch.from_numpy(np.einsum("jih,jh->ji", Wg[e], xq[t])).requires_grad_(True)
+    u = torch.from_numpy(np.einsum("jih,jh->ji", Wu[e], xq[t])).requires_grad_(True)
+    a_t = torch.nn.functional.silu(g) * u
+    a = a_t.detach().numpy()
+    aq = _q32(a)
+    y = np.einsum("jhi,ji->jh", Wd[e], aq)
+    out = np.zeros((T, H))
+    np.add.at(out, t, sv[:, None] * y)
+    if dap_from_wdt:
+        dap = np.einsum("jih,jh->ji", Wdt[e], dyq[t])
+    else:  # the forward copy of Wd (quantised along I) read transposed
+        dap = np.einsum("jhi,jh->ji", Wd[e], dyq[t])
+    dS = np.einsum("ji,ji->j", dap, aq if ds_on_aq else a).reshape(T, K)
+    a_t.backward(torch.from_numpy(sv[:, None] * dap))  # SwiGLU backward by autograd
+    dg, du = g.grad.numpy(), u.grad.numpy()
+    dgq, duq = (_q32(dg), _q32(du)) if quant_dg else (dg, du)
+    dX = np.zeros((T, H))
+    np.add.at(dX, t, np.einsum("jhi,ji->jh", Wgt[e], dgq) + np.einsum("jhi,ji->jh", Wut[e], duq))
+    return dict(out=out, a=a, aq=aq, dS=dS, dg=dg, du=du, dX=dX)
+
+
+def _mx_case(seed=11):
+    rng = np.random.default_rng(seed)
+    T, H, I, E, K = 40, 128, 96, 3, 2
+    ids = rng.integers(0, E, size=(T, K)).astype(np.int32)
+    s = rng.uniform(0.1, 0.9, size=(T, K)).astype(np.float32)
+    row_scale = 2.0 ** rng.integers(-6, 7, size=(T, 1))  # spread the block exponents
+    x = _bits(rng.standard_normal((T, H)) * row_scale)
+    dY = _bits(rng.standard_normal((T, H)) * row_scale[::-1])
+    Wg, Wu, Wd = (_bits(rng.standard_normal(sh) * 0.05) for sh in ((E, I, H), (E, I, H), (E, H, I)))
+    return ids, s, x, dY, oracle.mx_weights(Wg, Wu, Wd), E, I
+
+
+def test_quantiser_rebuild_agrees_with_oracle_quantiser():
+    """The test's own quantiser (numpy + torch float8 grid) equals the oracle's on fp64 values off
+    the bf16 grid, including ties and saturation -- so the rebuild below shares nothing with the
+    oracle but agrees with it where they must."""
+    rng = np.random.default_rng(12)
+    v = rng.standard_normal((64, 96)) * 2.0 ** rng.integers(-30, 30, size=(64, 1))
+    v[0, :32] = 0.0
+    v[1, :32] = np.linspace(-1, 1, 32) * 448.0 * 1.9  # block whose top values saturate
+    # a block with shared = 0 (amax 256) holding exact ties between neighbouring codes
+    v[2, :32] = 0.0
+    v[2, :6] = [256.0, 1.0625, 1.1875, -1.0625, 3 * 2.0 ** -10, 2.0 ** -10]
+    v[3, :32] = 2.0 ** -140 * np.arange(32)  # clamped exponent (-127), subnormal codes
+    assert np.array_equal(_q32(v), oracle.mx_fakequant(v))
+
+
+def test_data_gradient_quantisation_points_rebuilt():
+    ids, s, x, dY, mx, E, I = _mx_case()
+    r = oracle.layer_mx(ids, s, x, dY, mx, E, I, with_aq=True, with_dg=True)
+    ref = _rebuild(ids, s, x, dY, mx, E, I)
+    rel = lambda a, b: np.abs(a - b).max() / np.abs(b).max()  # noqa: E731
+    for k_or, k_rb in (("out", "out"), ("a", "a"), ("aq", "aq"), ("dS", "dS"), ("dg", "dg"), ("du", "du"),
+                       ("dX", "dX")):
+        assert rel(r[k_or], ref[k_rb]) <= 1e-11, (k_or, rel(r[k_or], ref[k_rb]))
+
+
+@pytest.mark.parametrize("slip,keys", [
+    (dict(quant_dy=False), ("dS", "dg", "dX")),     # dY not quantised along H
+    (dict(ds_on_aq=False), ("dS",)),                # dS formed with a instead of a_q
+    (dict(dap_from_wdt=False), ("dS", "dg", "dX")),  # the forward copy of Wd instead of Wd^T's
+    (dict(quant_dg=False), ("dX",)),                # dg, du not quantised along I before dgrad2
+])
+def test_planted_quantisation_slips_are_caught(slip, keys):
+    """Each plausible slip moves the affected outputs by far more than the rebuild's 1e-11, so the
+    pin above would fail on it."""
+    ids, s, x, dY, mx, E, I = _mx_case()
+    r = oracle.layer_mx(ids, s, x, dY, mx, E, I, with_aq=True, with_dg=True)
+    bad = _rebuild(ids, s, x, dY, mx, E, I, **slip)
+    for k in keys:
+        assert np.abs(r[k] - bad[k]).max() / np.abs(r[k]).max() > 1e-4, k
