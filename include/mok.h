@@ -13,7 +13,8 @@
  *    arrays of 16-bit patterns; fp32 is IEEE binary32; E4M3 / E8M0 are bytes.
  *  - Ownership: the caller allocates and frees every buffer (inputs, outputs, the workspace and
  *    the forward context).  The library never allocates device memory and keeps no state
- *    between calls beyond a per-device cache of the SM count and one driver entry point.
+ *    between calls beyond per-device caches (the SM count, which kernels have had their
+ *    shared-memory limit raised on that device) and one driver entry point.
  *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Every
  *    call only enqueues work on it and returns; none synchronises, except
  *    mok_read_device_status.  Inputs must stay valid until the enqueued work has run.
@@ -21,8 +22,8 @@
  *    nothing back, and their grids and tensor maps depend only on the shape and the buffer
  *    addresses.  A step made of them may be captured once (stream capture) and replayed; each
  *    replay rebuilds the schedule on the device from the routing the captured buffers then hold.
- *    Call each entry point once outside capture first, so that its one-time kernel attribute
- *    setup is done.
+ *    Call each entry point once outside capture first on each device, so that its one-time
+ *    kernel attribute setup for that device is done.
  *  - Errors: argument, shape, alignment and size problems are detected on the host and returned
  *    before anything is enqueued.  Data-dependent problems found on the device (an expert id
  *    outside [0, E), a bounded wait that timed out) set bits (1 << code) in the schedule's device
@@ -246,16 +247,21 @@ MOK_API const char* mok_kernel_name(int32_t kind);
 /* Schedule build for callers that cannot allocate device memory.  The pages have no counterpart
  * to this call: it exists for code that may not call cudaMalloc (or any allocating routine) while
  * it runs, e.g. a runtime that only hands out fixed, pre-sized buffers.  It computes exactly the
- * tables of mok_build_schedule, but its scratch (the per-chunk expert histogram) lives in a
- * fixed array inside the library: 2 MiB of device memory per GPU that loads the library, held
- * until the process exits.
+ * tables of mok_build_schedule (for either precision: the tables do not depend on it), but its
+ * scratch (the per-chunk expert histogram) lives in a fixed array inside the library: 2 MiB of
+ * device memory per GPU that loads the library, held until the process exits.
  *   sched   HOST struct.  On entry the caller sets these DEVICE pointers to its own buffers:
  *           counts [E], offsets [E+1], poff [E+1], perm [rpad_max], inv [T*K], tiles
  *           [tiles_max*4], mblocks [mblocks_max*4], meta [16], row_weight [rpad_max] (fp32),
- *           row_token [rpad_max], with rpad_max = T*K + 127*E, tiles_max = ceil(T*K / mb) + E,
- *           mblocks_max = floor(rpad_max / 128).  The call fills the remaining fields (status
- *           points at meta[15]; ws is NULL).  Such a schedule holds no workspace, so it serves
- *           inspection and the caller's own kernels, not mok_forward / mok_backward.
+ *           row_token [rpad_max]; and rpad_max, tiles_max, mblocks_max to the capacities of those
+ *           buffers.  The shape needs rpad_max >= T*K + 127*E, tiles_max >= ceil(T*K / mb) + E and
+ *           mblocks_max >= floor((T*K + 127*E) / 128), mb the minibatch rows; with minibatch_rows
+ *           = 0 (automatic) mb is at least 256, so tiles_max = ceil(T*K / 256) + E always
+ *           suffices.  A smaller capacity gives MOK_ERR_WORKSPACE_TOO_SMALL before any work is
+ *           enqueued.  The call sets the capacity fields to the sizes the shape needs and fills the
+ *           remaining fields (config holds the resolved minibatch and macrobatch; status points at
+ *           meta[15]; ws is NULL).  Such a schedule holds no workspace, so it serves inspection and
+ *           the caller's own kernels, not mok_forward / mok_backward.
  * Limit: ceil(T*K / 512) * (E + 1) <= 524288, else MOK_ERR_UNSUPPORTED is returned before any
  * work is enqueued.  The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture.  All calls share the one

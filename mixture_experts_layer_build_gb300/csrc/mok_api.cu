@@ -162,15 +162,17 @@ size_t carve_ctx(const Sizes& z, char* base, Ctx* ctx) {
   return align_up(c.off);
 }
 
+// SM count of the current device, cached per device; 0 when it cannot be read (the caller's launch
+// then fails and reports MOK_ERR_CUDA rather than running on a guessed grid).
 int sm_count() {
   static std::mutex mu;
   static int cached[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lk(mu);
   if (!cached[dev]) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
     cached[dev] = n;
   }
   return cached[dev];
@@ -397,6 +399,7 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
     return MOK_ERR_CUDA;
   }
   const int g = grid_of(sched);
+  if (g <= 0) return MOK_ERR_CUDA;
   int e = launch_fwd_gemms(z, *sched, ctx, st, *w, g, s);
   if (e < 0) return MOK_ERR_INVALID_ARG;
   if (e) return MOK_ERR_CUDA;
@@ -424,6 +427,7 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   carve_ctx(z, static_cast<char*>(const_cast<void*>(fwd_ctx)), &ctx);
   cudaStream_t s = as_stream(stream);
   const int grid = grid_of(sched);
+  if (grid <= 0) return MOK_ERR_CUDA;
   if (z.mx) {  // weight scales into atoms, then dY quantised on the gather
     const int64_t EI = static_cast<int64_t>(z.E) * z.I, EH = static_cast<int64_t>(z.E) * z.H;
     const int ag = z.mx_bn_h() / 128;  // atoms per B tile of the second data-gradient GEMM

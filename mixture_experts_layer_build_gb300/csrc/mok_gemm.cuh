@@ -32,6 +32,7 @@
 #include <cuda.h>
 
 #include "mok_internal.cuh"
+#include "mok_once.h"
 #include "mok_ptx.cuh"
 
 namespace mok {
@@ -1140,13 +1141,15 @@ template <int VAR, int BN, bool MX = false, bool PAIR = false, bool SPLIT = fals
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& o0,
                 const CUtensorMap& o1, const CUtensorMap& o2, const GemmArgs& args, int grid, cudaStream_t stream) {
   using C = GemmCfg<VAR, BN, MX, PAIR, SPLIT>;
-  static bool configured = false;  // per process; the attribute is per function, set once
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX, PAIR, SPLIT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmemBytes));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    configured = true;
-  }
+  static DeviceOnce once;  // the shared-memory limit is set on each device that launches the kernel
+  const int se = once.run([](int* d) { return static_cast<int>(cudaGetDevice(d)); },
+                          [] {
+                            return static_cast<int>(cudaFuncSetAttribute(gemm_kernel<VAR, BN, MX, PAIR, SPLIT>,
+                                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                         static_cast<int>(C::kSmemBytes)));
+                          },
+                          static_cast<int>(cudaErrorInvalidDevice));
+  if (se) return se;
   if (grid <= 0) return 0;
   if (PAIR) grid = grid < 2 ? 2 : grid & ~1;  // whole pairs
   constexpr int kKind = VAR == V_FWD_GATEUP  ? K_GEMM_FWD_GATEUP

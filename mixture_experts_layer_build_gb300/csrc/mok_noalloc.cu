@@ -47,8 +47,11 @@ extern "C" MOK_API mok_status mok_build_schedule_noalloc(const mok_config* cfg, 
                                                          mok_schedule* sched, void* stream) {
   Sizes z;
   if (!sched || !make_sizes(cfg, shape, &z)) return MOK_ERR_INVALID_ARG;
-  if (cfg->precision != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (z.nchunks * (z.E + 1) > kNoallocHistEntries) return MOK_ERR_UNSUPPORTED;  // beyond the static scratch
+  // the caller states the capacities of its tables; the kernels write up to the sizes this shape
+  // and the resolved minibatch need, so a smaller buffer is refused before anything is enqueued
+  if (sched->rpad_max < z.rpad_max || sched->tiles_max < z.tiles_max || sched->mblocks_max < z.mblocks_max)
+    return MOK_ERR_WORKSPACE_TOO_SMALL;
   if (z.R > 0 && (!topk_ids || !topk_weights)) return MOK_ERR_INVALID_ARG;
   if (!sched->counts || !sched->offsets || !sched->poff || !sched->perm || !sched->inv || !sched->tiles ||
       !sched->mblocks || !sched->meta || !sched->row_weight || !sched->row_token)

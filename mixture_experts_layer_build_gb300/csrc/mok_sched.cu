@@ -18,6 +18,7 @@
 #include <climits>
 
 #include "mok_internal.cuh"
+#include "mok_once.h"
 #include "mok_ptx.cuh"
 
 namespace mok {
@@ -270,13 +271,15 @@ __global__ void __launch_bounds__(kHistWarps * 32) sched_scatter_kernel(
 
 int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mok_schedule& s, const Staging& st,
                     cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {  // the scan's group sums need up to 32 x 1025 int32 of shared memory
-    const cudaError_t e = cudaFuncSetAttribute(sched_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(sizeof(int32_t) * 32 * 1025));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    configured = true;
-  }
+  static DeviceOnce once;  // the scan's group sums need up to 32 x 1025 int32 of shared memory, on each device
+  const int se = once.run([](int* d) { return static_cast<int>(cudaGetDevice(d)); },
+                          [] {
+                            return static_cast<int>(cudaFuncSetAttribute(
+                                sched_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(sizeof(int32_t) * 32 * 1025)));
+                          },
+                          static_cast<int>(cudaErrorInvalidDevice));
+  if (se) return se;
   const int64_t nchunks = z.nchunks;
   const int blocks = static_cast<int>((nchunks + kHistWarps - 1) / kHistWarps);
   if (blocks > 0) {
