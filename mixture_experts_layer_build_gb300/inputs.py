@@ -60,6 +60,11 @@ WORKLOADS = {
     "sweep_zipf0": Workload("sweep_zipf0", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=0.0),
     "sweep_zipf1": Workload("sweep_zipf1", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=1.0),
     "sweep_zipf2": Workload("sweep_zipf2", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=2.0),
+    # the sweep's layer shape and rows per expert (512 on average) with 2048 tokens, 16 experts and
+    # top-4: a case small enough for multi-pass ncu captures (about 2 GB on the device)
+    "sweep_zipf1_2k": Workload("sweep_zipf1_2k", 2048, 4096, 1536, 16, 4, "gumbel_topk", zipf=1.0),
+    "sweep_zipf1_2k_mx": Workload("sweep_zipf1_2k_mx", 2048, 4096, 1536, 16, 4, "gumbel_topk", zipf=1.0,
+                                  precision="mxfp8"),
     "sweep_zipf0_mx": Workload("sweep_zipf0_mx", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=0.0,
                                precision="mxfp8"),
     "sweep_zipf1_mx": Workload("sweep_zipf1_mx", 8192, 4096, 1536, 128, 8, "gumbel_topk", zipf=1.0,
