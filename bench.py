@@ -1,8 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of the routed SwiGLU expert layer: one step = schedule + forward + backward.
 
-Default workload: T=4096 tokens, H=2048, I=1024, E=64 experts, top-6, BF16 (near-uniform softmax
-routing), synthetic seeded inputs.  Prints ONE JSON line (rank 0):
+Default workload: the imbalance / granularity sweep at Zipf s = 1 in BF16 -- T=8192 tokens,
+H=4096, I=1536, E=128 experts, top-8, expert loads skewed by Gumbel-top-k sampling on
+-ln(e+1) logits -- with synthetic seeded inputs.  The same line carries two further objects timed
+the same way: "mxfp8" (the same sweep in MXFP8) and "ep64_shard" (the per-GPU shard of an EP64
+layer in MXFP8: 16,384 routed rows onto 4 experts, H=7168, I=2048, Zipf 1.2).  Prints ONE JSON line
+(rank 0):
   value     tokens/s of the whole job (all ranks), inputs resident in HBM, CUDA events on the
             launching stream, max over ranks.  The step runs as in training: captured once as a
             CUDA graph (every launch through the C ABI) and replayed; "step" also reports the same
@@ -14,7 +18,8 @@ routing), synthetic seeded inputs.  Prints ONE JSON line (rank 0):
   roofline  the dominant kernel's algorithmic flops (or bytes) per launch over its average launch
             time, measured live with per-launch CUDA events (the library's trace hook), against
             the measured peak;
-  cpu_baseline  the fp64 CPU oracle as it stands, timed on a bounded token sample.
+  cpu_baseline  the CPU oracle's layer loops built in fp32 at -O3 (OpenMP over all host cores),
+            timed on a bounded token sample; the fp64 build stays the parity reference.
 ``--impl reference`` times the oracle alone (the reference arm; rank 0 only).
 
 Multi-GPU (torchrun): every rank runs an independent data-parallel shard of the same shape (its
@@ -50,7 +55,9 @@ def parse():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="bf16_e64")
+    p.add_argument("--workload", default="sweep_zipf1")
+    p.add_argument("--extra", default="mxfp8=sweep_zipf1_mx,ep64_shard=mxfp8_ep64_shard",
+                   help="further workloads timed into objects of the same line (key=workload,...; '' for none)")
     p.add_argument("--minibatch", type=int, default=512)
     p.add_argument("--macrobatch", type=int, default=2048)
     p.add_argument("--num-ctas", type=int, default=0, help="persistent GEMM grid (0: one CTA per SM)")
@@ -287,7 +294,8 @@ def oracle_sample_args(d, tokens: int):
 
 def time_oracle_step(d, wbits, tokens: int) -> float:
     """One oracle fwd + bwd of the first `tokens` tokens.  wbits = (Wg, Wu, Wd) bf16 bit patterns
-    for the BF16 oracle, or a dict of pre-quantised copies for the MXFP8 oracle."""
+    for the BF16 layer loops (their fp32 -O3 build), or a dict of pre-quantised copies for the
+    MXFP8 oracle (fp64; it has no fp32 build)."""
     import oracle
     ids, s, x, dY = oracle_sample_args(d, tokens)
     t0 = time.perf_counter()
@@ -296,9 +304,13 @@ def time_oracle_step(d, wbits, tokens: int) -> float:
         oracle.layer_mx(ids, s, x, dY, wbits, E, I)
     else:
         Wg, Wu, Wd = wbits
-        oracle.forward(ids, s, x, Wg, Wu, Wd)
-        oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
+        oracle.step_f32(ids, s, x, Wg, Wu, Wd, dY)
     return time.perf_counter() - t0
+
+
+def oracle_kind(wbits) -> str:
+    return ("fp64 MXFP8 oracle (C loops, OpenMP)" if isinstance(wbits, dict)
+            else "the oracle's layer loops in fp32, gcc -O3 -fopenmp")
 
 
 def calibrate_oracle_tokens(d, wbits, target_s: float, T: int) -> tuple[int, float]:
@@ -344,27 +356,46 @@ def reference_arm(args, rank, ws):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, args, args.gpus),
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64" if isinstance(wbits, dict) else "f32",
+        "data": "synthetic", "config": config_of(w, args, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"fwd+bwd of the first {tokens} of {w.T} tokens per step (all their routed "
-                                   f"rows, full dW), fp64 C loops with OpenMP"},
+                                   f"rows, full dW), {oracle_kind(wbits)}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
+WORKLOAD_TITLES = {
+    "tiny": "tiny layer",
+    "bf16_e64": "near-uniform softmax routing",
+    "dsv3_e256": "DeepSeek-V3-style layer, all 256 experts resident, per-expert router bias",
+    "mxfp8_ep64_shard": "per-GPU shard of an EP64 layer (2048 tokens x top-8 onto 4 local experts, Zipf 1.2)",
+    "sweep_zipf0": "imbalance / granularity sweep at Zipf s=0",
+    "sweep_zipf1": "imbalance / granularity sweep at Zipf s=1",
+    "sweep_zipf2": "imbalance / granularity sweep at Zipf s=2",
+    "sweep_zipf0_mx": "imbalance / granularity sweep at Zipf s=0",
+    "sweep_zipf1_mx": "imbalance / granularity sweep at Zipf s=1",
+    "sweep_zipf2_mx": "imbalance / granularity sweep at Zipf s=2",
+}
+
+
 def config_of(w, args, n):
     wbytes = 3 * w.E * w.H * w.I * 2
-    return {"workload": f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} top-{w.K} {w.precision.upper()}, router "
-                        f"{w.router}, seeded synthetic", "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
+    title = WORKLOAD_TITLES.get(w.name, w.name)
+    return {"workload": f"{title}, {w.precision.upper()}: T={w.T} H={w.H} I={w.I} E={w.E} top-{w.K}, router "
+                        f"{w.router}, seeded synthetic ({w.name})", "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K,
             "global_batch": w.T * n, "minibatch_rows": args.minibatch, "macrobatch_rows": args.macrobatch,
             "parallelism": f"replicas x{n} (independent data-parallel shards; the layer has no collective)",
             "l2": f"inputs larger than L2: {wbytes / 1e6:.0f} MB of expert weights streamed every step, no flush"}
 
 
-# fp32 fused multiply-add peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
-FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+def fp32_alu_tflops(dev, peaks) -> float:
+    """fp32 fused multiply-add peak of the CUDA cores: SMs x 128 fp32 lanes x 2 flops x the maximum
+    SM clock (the device's SM count; the clock from the measured peaks, else 2070 MHz)."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = float(peaks.get("sm_max_mhz") or 2070.0)
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
 
 
 def capture_step(fn, stream):
@@ -438,8 +469,8 @@ def time_router(args, mok, w, d, cfg, dev, stream, peaks) -> dict:
     if "router_logits" in kern:  # fp32 fused multiply-adds on the CUDA cores: ALU-bound
         ms = kern["router_logits"]["avg_ms"]
         tf = 2.0 * T * H * E / (ms * 1e-3) / 1e12
-        kern["router_logits"].update({"tflops": tf, "bound": "alu", "peak_tflops": FP32_ALU_TFLOPS,
-                                      "frac": tf / FP32_ALU_TFLOPS})
+        alu = fp32_alu_tflops(dev, peaks)
+        kern["router_logits"].update({"tflops": tf, "bound": "alu", "peak_tflops": alu, "frac": tf / alu})
     hbm = peaks["hbm_gbs"]
     # unique bytes: W^T read once by dx (its K rows per token are L2 hits), x read once by dW
     byts = {"router_topk": T * E * 4 + T * K * 8, "router_transpose": 2 * H * E * 2,
@@ -452,12 +483,15 @@ def time_router(args, mok, w, d, cfg, dev, stream, peaks) -> dict:
     return res
 
 
-def ours(args, rank, ws, local_rank):
+def ours(args, rank, ws, local_rank, name, with_router=True):
+    """Every measurement of one workload: the step from a CUDA graph and eagerly, the per-kernel
+    event trace and roofline, the router step (workloads with a softmax router), and e2e through
+    the C ABI with host buffers."""
     from mixture_experts_layer_build_gb300 import inputs, mok
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = inputs.WORKLOADS[args.workload]
+    w = inputs.WORKLOADS[name]
     d = inputs.make(w, seed=rank, weight_device=str(dev))
     x, ids, s, dY = (d[k].to(dev) for k in ("x", "topk_ids", "topk_weights", "dY"))
     Wg, Wu, Wd = d["Wg"], d["Wu"], d["Wd"]
@@ -551,7 +585,7 @@ def ours(args, rank, ws, local_rank):
             v["bound"], v["frac"] = rf["bound"], rf["frac"]
     dom = max((k for k in kernels if k in work), key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
     fl, nb, kd = work[dom]
-    traffic, tnote = traffic_for(dom, args.workload)
+    traffic, tnote = traffic_for(dom, name)
     roof = roofline_of(fl, nb, kernels[dom]["avg_ms"], peaks, kd)
     roof.update({"traffic": traffic, "kernel": dom,
                  "peak_source": (f"{peak_src} (burst bf16 GEMM / STREAM copy)" if peak_src == "measured"
@@ -559,7 +593,7 @@ def ours(args, rank, ws, local_rank):
                  "traffic_note": tnote, "algorithmic_flops_per_launch": fl, "algorithmic_bytes_per_launch": nb})
 
     # ---- the router step before the layer (timed on its own; not part of the layer step) ----
-    router = time_router(args, mok, w, d, cfg, dev, stream, peaks) if "Wr" in d else None
+    router = time_router(args, mok, w, d, cfg, dev, stream, peaks) if with_router and "Wr" in d else None
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its own inputs host->device and its results device->host inside the timed
@@ -667,14 +701,40 @@ def ours(args, rank, ws, local_rank):
     return result, d, w
 
 
+def parse_extra(spec: str):
+    out = []
+    for item in (spec or "").split(","):
+        item = item.strip()
+        if item:
+            key, _, wl = item.partition("=")
+            out.append((key.strip(), wl.strip()))
+    return out
+
+
+# keys of a further workload's object (its full kernel table stays on the headline only)
+EXTRA_KEYS = ("metric", "value", "unit", "ms_per_step", "dtype", "config", "tflops", "roofline", "e2e",
+              "gpu_launches", "launches_per_step", "clocks", "device_status", "step")
+
+
 def main():
     args = parse()
     rank, ws, local_rank = dist_init()
     if args.impl == "reference":
         reference_arm(args, rank, ws)
         return
-    res, d, w = ours(args, rank, ws, local_rank)
+    res, d, w = ours(args, rank, ws, local_rank, args.workload)
+    extras = {}
+    for key, wl in parse_extra(args.extra):
+        if wl == args.workload:
+            continue
+        r2, _, _ = ours(args, rank, ws, local_rank, wl, with_router=False)
+        torch.cuda.empty_cache()
+        if rank == 0:
+            extras[key] = {k: r2[k] for k in EXTRA_KEYS if k in r2}
+            extras[key]["kernels"] = {k: {kk: v[kk] for kk in ("avg_ms", "bound", "frac", "tflops", "gbs") if kk in v}
+                                      for k, v in r2["kernels"].items()}
     if rank == 0:
+        res.update(extras)
         if ws == 1 and not args.no_cpu_baseline:
             from mixture_experts_layer_build_gb300 import inputs
             wbits = (inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
@@ -684,8 +744,8 @@ def main():
             tokens, _ = calibrate_oracle_tokens(d, wbits, args.cpu_seconds, w.T)
             t = time_oracle_step(d, wbits, tokens)
             res["cpu_baseline"] = {"value": tokens / t, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
-                                   "sample": f"fp64 oracle fwd+bwd of the first {tokens} of {w.T} tokens (all their "
-                                             f"routed rows, full dW), {t:.1f} s"}
+                                   "sample": f"fwd+bwd of the first {tokens} of {w.T} tokens (all their routed rows, "
+                                             f"full dW), {oracle_kind(wbits)}, {t:.1f} s"}
         print(json.dumps(res), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -25,21 +25,28 @@ _SRC = os.path.join(_HERE, "mok_oracle.c")
 _SRC_MX = os.path.join(_HERE, "mok_oracle_mx.c")
 _SRC_ROUTER = os.path.join(_HERE, "mok_oracle_router.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_LIB32_PATH = os.path.join(_HERE, "liboracle_f32.so")
 _lock = threading.Lock()
 _lib = None
+_lib32 = None
 
 MT = 128  # GEMM row tile used for the padded expert-grouped layout
 
 
 def build(force: bool = False) -> str:
-    """Compile ``mok_oracle.c`` into ``liboracle.so`` with gcc (OpenMP, no fast-math)."""
-    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_MX), os.path.getmtime(_SRC_ROUTER))
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, _SRC_MX, _SRC_ROUTER,
-             "-lm"])
-        os.replace(tmp, _LIB_PATH)
+    """Compile the oracle with gcc (OpenMP, no fast-math): ``liboracle.so``, the fp64 reference of
+    every parity check, and ``liboracle_f32.so``, the same layer loops in fp32 at -O3 -- the timed
+    CPU baseline, never a reference."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_MX), os.path.getmtime(_SRC_ROUTER),
+                 os.path.getmtime(os.path.abspath(__file__)))
+    common = ["-std=c11", "-fopenmp", "-fPIC", "-fno-semantic-interposition", "-shared"]
+    jobs = [(_LIB_PATH, ["gcc", "-O2", *common, _SRC, _SRC_MX, _SRC_ROUTER, "-lm"]),
+            (_LIB32_PATH, ["gcc", "-O3", *common, "-DORC_REAL=float", "-DORC_TIMING_ONLY", _SRC, "-lm"])]
+    for path, cmd in jobs:
+        if force or not os.path.exists(path) or os.path.getmtime(path) < newest:
+            tmp = path + f".tmp{os.getpid()}"
+            subprocess.check_call([*cmd, "-o", tmp])
+            os.replace(tmp, path)
     return _LIB_PATH
 
 
@@ -76,6 +83,8 @@ def _load():
             lib.orc_backward_tokens.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i64, P, P, P]
             lib.orc_dw_entries.restype = None
             lib.orc_dw_entries.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i64, P, P, P, P, P]
+            lib.orc_dw_block.restype = None
+            lib.orc_dw_block.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32, i64, P, P, P, P]
             lib.orc_mx_set_quant.restype = None
             lib.orc_mx_set_quant.argtypes = [ctypes.c_int]
             lib.orc_mx_fakequant.restype = None
@@ -241,6 +250,37 @@ def backward(ids, s, x, Wg, Wu, Wd, dY, check: bool = False):
     return r
 
 
+def _load32():
+    global _lib32
+    if _lib32 is None:
+        _load()  # builds both libraries
+        with _lock:
+            lib = ctypes.CDLL(_LIB32_PATH)
+            P = ctypes.c_void_p
+            i64, i32 = ctypes.c_int64, ctypes.c_int32
+            lib.orc_forward.restype = None
+            lib.orc_forward.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P]
+            lib.orc_backward.restype = None
+            lib.orc_backward.argtypes = [i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P, P, P, P]
+            _lib32 = lib
+    return _lib32
+
+
+def step_f32(ids, s, x, Wg, Wu, Wd, dY):
+    """Forward + backward of the layer loops in fp32 (-O3): the timed CPU baseline.  Returns out,
+    dX [T,H], dWg, dWu [E,I,H], dWd [E,H,I], dS [T,K] as float32 arrays."""
+    ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
+    dY = _u16(dY)
+    f = np.float32
+    out, dX, dS = np.empty((T, H), f), np.empty((T, H), f), np.empty((T, K), f)
+    dWg, dWu, dWd = np.empty((E, I, H), f), np.empty((E, I, H), f), np.empty((E, H, I), f)
+    lib = _load32()
+    lib.orc_forward(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(out), None, None, None, None)
+    lib.orc_backward(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), _p(dX), _p(dWg), _p(dWu),
+                     _p(dWd), _p(dS), None)
+    return dict(out=out, dX=dX, dWg=dWg, dWu=dWu, dWd=dWd, dS=dS)
+
+
 def forward_tokens(ids, s, x, Wg, Wu, Wd, tokens):
     ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
     tok = np.ascontiguousarray(tokens, dtype=np.int64)
@@ -273,6 +313,17 @@ def dw_entries(ids, s, x, Wg, Wu, Wd, dY, which, e, m, c):
     _load().orc_dw_entries(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), which.size,
                            _p(which), _p(e), _p(m), _p(c), _p(val))
     return val
+
+
+def dw_block(ids, s, x, Wg, Wu, Wd, dY, e: int, i0: int, hs):
+    """dWg, dWu [32, nh] and dWd [nh, 32] of expert e on I columns [i0, i0+32) and hidden columns hs."""
+    ids, s, x, Wg, Wu, Wd, T, H, I, E, K = _layer_args(ids, s, x, Wg, Wu, Wd)
+    dY = _u16(dY)
+    hs = np.ascontiguousarray(hs, dtype=np.int32)
+    dwg, dwu, dwd = np.empty((32, hs.size)), np.empty((32, hs.size)), np.empty((hs.size, 32))
+    _load().orc_dw_block(T, H, I, E, K, _p(ids), _p(s), _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), int(e), int(i0),
+                         hs.size, _p(hs), _p(dwg), _p(dwu), _p(dwd))
+    return dwg, dwu, dwd
 
 
 # ----------------------------------------------------------------------------------------------

@@ -29,7 +29,9 @@
  *     ascending id, each expert's segment padded to a multiple of the GEMM row tile Mt.
  *   - MXFP8: OCP MX E4M3 elements with one E8M0 scale per 32 consecutive values.
  *
- * All arithmetic is fp64; bf16 and E4M3 inputs enter as their exact values.
+ * All arithmetic is fp64; bf16 and E4M3 inputs enter as their exact values.  The layer loops
+ * (expert_up .. orc_backward) take their arithmetic type from ORC_REAL (default double): a second
+ * build with ORC_REAL=float serves only as the timed fp32 CPU baseline, never as a reference.
  */
 #include <math.h>
 #include <stdint.h>
@@ -38,6 +40,13 @@
 #ifdef _OPENMP
 #include <omp.h>
 #endif
+
+#ifndef ORC_REAL
+#define ORC_REAL double
+#endif
+typedef ORC_REAL real;
+/* exp in the arithmetic type of the layer loops */
+static inline real real_exp(real z) { return sizeof(real) == sizeof(float) ? (real)expf((float)z) : (real)exp((double)z); }
 
 /* ------------------------------------------------------------------------------------------ */
 /* number formats                                                                              */
@@ -235,6 +244,9 @@ int orc_schedule(int64_t T, int32_t K, int32_t E, const int32_t *ids, int32_t Mt
 /* the SwiGLU expert, one routed slot at a time ([MTP] English summary: SwiGLU experts)        */
 /* ------------------------------------------------------------------------------------------ */
 
+static real sigmoid_r(real z) { return (real)1 / ((real)1 + real_exp(-z)); }
+/* a bf16 value in the arithmetic type (exact in either) */
+static inline real bf16r(uint16_t b) { return (real)orc_bf16_value(b); }
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 
 typedef struct {
@@ -250,55 +262,55 @@ typedef struct {
 } layer_t;
 
 /* g = Wg[e] x[t], u = Wu[e] x[t] (length I), a = silu(g) * u. */
-static void expert_up(const layer_t *L, int32_t e, int64_t t, double *g, double *u, double *a) {
+static void expert_up(const layer_t *L, int32_t e, int64_t t, real *g, real *u, real *a) {
     const int64_t H = L->H, I = L->I;
     const uint16_t *xt = L->x + t * H;
     for (int64_t i = 0; i < I; ++i) {
         const uint16_t *wg = L->Wg + ((int64_t)e * I + i) * H;
         const uint16_t *wu = L->Wu + ((int64_t)e * I + i) * H;
-        double sg = 0.0, su = 0.0;
+        real sg = (real)0, su = (real)0;
         for (int64_t h = 0; h < H; ++h) {
-            double xv = orc_bf16_value(xt[h]);
-            sg += orc_bf16_value(wg[h]) * xv;
-            su += orc_bf16_value(wu[h]) * xv;
+            real xv = bf16r(xt[h]);
+            sg += bf16r(wg[h]) * xv;
+            su += bf16r(wu[h]) * xv;
         }
         g[i] = sg;
         u[i] = su;
-        a[i] = sg * sigmoid(sg) * su;
+        a[i] = sg * sigmoid_r(sg) * su;
     }
 }
 
 /* y = Wd[e] a (length H). */
-static void expert_down(const layer_t *L, int32_t e, const double *a, double *y) {
+static void expert_down(const layer_t *L, int32_t e, const real *a, real *y) {
     const int64_t H = L->H, I = L->I;
     for (int64_t h = 0; h < H; ++h) {
         const uint16_t *wd = L->Wd + ((int64_t)e * H + h) * I;
-        double acc = 0.0;
-        for (int64_t i = 0; i < I; ++i) acc += orc_bf16_value(wd[i]) * a[i];
+        real acc = (real)0;
+        for (int64_t i = 0; i < I; ++i) acc += bf16r(wd[i]) * a[i];
         y[h] = acc;
     }
 }
 
 /* dA' = Wd[e]^T dY[t] (length I). */
-static void expert_down_t(const layer_t *L, int32_t e, int64_t t, double *dap) {
+static void expert_down_t(const layer_t *L, int32_t e, int64_t t, real *dap) {
     const int64_t H = L->H, I = L->I;
     const uint16_t *dy = L->dY + t * H;
-    for (int64_t i = 0; i < I; ++i) dap[i] = 0.0;
+    for (int64_t i = 0; i < I; ++i) dap[i] = (real)0;
     for (int64_t h = 0; h < H; ++h) {
-        double d = orc_bf16_value(dy[h]);
+        real d = bf16r(dy[h]);
         const uint16_t *wd = L->Wd + ((int64_t)e * H + h) * I;
-        for (int64_t i = 0; i < I; ++i) dap[i] += orc_bf16_value(wd[i]) * d;
+        for (int64_t i = 0; i < I; ++i) dap[i] += bf16r(wd[i]) * d;
     }
 }
 
 /* SwiGLU backward for one slot with combine weight sv:
  *   dA = sv * dA';  dg = dA * u * sig(g) * (1 + g (1 - sig(g)));  du = dA * g * sig(g). */
-static void swiglu_bwd(int64_t I, double sv, const double *g, const double *u, const double *dap, double *dg,
-                       double *du) {
+static void swiglu_bwd(int64_t I, real sv, const real *g, const real *u, const real *dap, real *dg,
+                       real *du) {
     for (int64_t i = 0; i < I; ++i) {
-        double sg = sigmoid(g[i]);
-        double da = sv * dap[i];
-        dg[i] = da * u[i] * sg * (1.0 + g[i] * (1.0 - sg));
+        real sg = sigmoid_r(g[i]);
+        real da = sv * dap[i];
+        dg[i] = da * u[i] * sg * ((real)1 + g[i] * ((real)1 - sg));
         du[i] = da * g[i] * sg;
     }
 }
@@ -315,28 +327,28 @@ static layer_t make_layer(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K,
  * Optional per-slot intermediates (slot order j = t*K + k): g, u, a [R, I]; y [R, H]; pass NULL
  * to skip.  [MTP] English summary (SwiGLU experts, forward); [ATT] section 4 (1) (combine). */
 void orc_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const int32_t *ids, const float *s,
-                 const uint16_t *x, const uint16_t *Wg, const uint16_t *Wu, const uint16_t *Wd, double *out, double *g,
-                 double *u, double *a, double *y) {
+                 const uint16_t *x, const uint16_t *Wg, const uint16_t *Wu, const uint16_t *Wd, real *out, real *g,
+                 real *u, real *a, real *y) {
     layer_t L = make_layer(T, H, I, E, K, ids, s, x, Wg, Wu, Wd, NULL);
 #pragma omp parallel
     {
-        double *gb = malloc(sizeof(double) * I), *ub = malloc(sizeof(double) * I), *ab = malloc(sizeof(double) * I);
-        double *yb = malloc(sizeof(double) * H);
+        real *gb = malloc(sizeof(real) * I), *ub = malloc(sizeof(real) * I), *ab = malloc(sizeof(real) * I);
+        real *yb = malloc(sizeof(real) * H);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t t = 0; t < T; ++t) {
-            double *o = out + t * H;
-            for (int64_t h = 0; h < H; ++h) o[h] = 0.0;
+            real *o = out + t * H;
+            for (int64_t h = 0; h < H; ++h) o[h] = (real)0;
             for (int32_t k = 0; k < K; ++k) {
                 int64_t j = t * K + k;
                 int32_t e = ids[j];
                 expert_up(&L, e, t, gb, ub, ab);
                 expert_down(&L, e, ab, yb);
-                double sv = (double)s[j];
+                real sv = (real)s[j];
                 for (int64_t h = 0; h < H; ++h) o[h] += sv * yb[h];
-                if (g) memcpy(g + j * I, gb, sizeof(double) * I);
-                if (u) memcpy(u + j * I, ub, sizeof(double) * I);
-                if (a) memcpy(a + j * I, ab, sizeof(double) * I);
-                if (y) memcpy(y + j * H, yb, sizeof(double) * H);
+                if (g) memcpy(g + j * I, gb, sizeof(real) * I);
+                if (u) memcpy(u + j * I, ub, sizeof(real) * I);
+                if (a) memcpy(a + j * I, ab, sizeof(real) * I);
+                if (y) memcpy(y + j * H, yb, sizeof(real) * H);
             }
         }
         free(gb); free(ub); free(ab); free(yb);
@@ -354,48 +366,48 @@ void orc_forward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const in
  * dW sums run over each expert's slots in ascending slot order. */
 void orc_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const int32_t *ids, const float *s,
                   const uint16_t *x, const uint16_t *Wg, const uint16_t *Wu, const uint16_t *Wd, const uint16_t *dY,
-                  double *dX, double *dWg, double *dWu, double *dWd, double *dS, double *dScheck) {
+                  real *dX, real *dWg, real *dWu, real *dWd, real *dS, real *dScheck) {
     layer_t L = make_layer(T, H, I, E, K, ids, s, x, Wg, Wu, Wd, dY);
     const int64_t R = T * (int64_t)K;
-    double *G = malloc(sizeof(double) * R * I), *U = malloc(sizeof(double) * R * I);
-    double *A = malloc(sizeof(double) * R * I), *DG = malloc(sizeof(double) * R * I);
-    double *DU = malloc(sizeof(double) * R * I);
+    real *G = malloc(sizeof(real) * R * I), *U = malloc(sizeof(real) * R * I);
+    real *A = malloc(sizeof(real) * R * I), *DG = malloc(sizeof(real) * R * I);
+    real *DU = malloc(sizeof(real) * R * I);
     /* per-slot quantities */
 #pragma omp parallel
     {
-        double *dap = malloc(sizeof(double) * I), *yb = malloc(sizeof(double) * H);
+        real *dap = malloc(sizeof(real) * I), *yb = malloc(sizeof(real) * H);
 #pragma omp for schedule(dynamic, 1)
         for (int64_t j = 0; j < R; ++j) {
             int64_t t = j / K;
             int32_t e = ids[j];
             expert_up(&L, e, t, G + j * I, U + j * I, A + j * I);
             expert_down_t(&L, e, t, dap);
-            double acc = 0.0;
+            real acc = (real)0;
             for (int64_t i = 0; i < I; ++i) acc += dap[i] * A[j * I + i];
             dS[j] = acc;
             if (dScheck) {
                 expert_down(&L, e, A + j * I, yb);
-                double c = 0.0;
-                for (int64_t h = 0; h < H; ++h) c += orc_bf16_value(dY[t * H + h]) * yb[h];
+                real c = (real)0;
+                for (int64_t h = 0; h < H; ++h) c += bf16r(dY[t * H + h]) * yb[h];
                 dScheck[j] = c;
             }
-            swiglu_bwd(I, (double)s[j], G + j * I, U + j * I, dap, DG + j * I, DU + j * I);
+            swiglu_bwd(I, (real)s[j], G + j * I, U + j * I, dap, DG + j * I, DU + j * I);
         }
         free(dap); free(yb);
     }
     /* dX per token, k ascending */
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t t = 0; t < T; ++t) {
-        double *d = dX + t * H;
-        for (int64_t h = 0; h < H; ++h) d[h] = 0.0;
+        real *d = dX + t * H;
+        for (int64_t h = 0; h < H; ++h) d[h] = (real)0;
         for (int32_t k = 0; k < K; ++k) {
             int64_t j = t * K + k;
             int32_t e = ids[j];
             for (int64_t i = 0; i < I; ++i) {
                 const uint16_t *wg = Wg + ((int64_t)e * I + i) * H;
                 const uint16_t *wu = Wu + ((int64_t)e * I + i) * H;
-                double cg = DG[j * I + i], cu = DU[j * I + i];
-                for (int64_t h = 0; h < H; ++h) d[h] += orc_bf16_value(wg[h]) * cg + orc_bf16_value(wu[h]) * cu;
+                real cg = DG[j * I + i], cu = DU[j * I + i];
+                for (int64_t h = 0; h < H; ++h) d[h] += bf16r(wg[h]) * cg + bf16r(wu[h]) * cu;
             }
         }
     }
@@ -403,14 +415,14 @@ void orc_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const i
 #pragma omp parallel for schedule(dynamic, 1) collapse(2)
     for (int32_t e = 0; e < E; ++e) {
         for (int64_t i = 0; i < I; ++i) {
-            double *rg = dWg + ((int64_t)e * I + i) * H, *ru = dWu + ((int64_t)e * I + i) * H;
-            for (int64_t h = 0; h < H; ++h) { rg[h] = 0.0; ru[h] = 0.0; }
+            real *rg = dWg + ((int64_t)e * I + i) * H, *ru = dWu + ((int64_t)e * I + i) * H;
+            for (int64_t h = 0; h < H; ++h) { rg[h] = (real)0; ru[h] = (real)0; }
             for (int64_t j = 0; j < R; ++j) {
                 if (ids[j] != e) continue;
                 const uint16_t *xt = x + (j / K) * H;
-                double cg = DG[j * I + i], cu = DU[j * I + i];
+                real cg = DG[j * I + i], cu = DU[j * I + i];
                 for (int64_t h = 0; h < H; ++h) {
-                    double xv = orc_bf16_value(xt[h]);
+                    real xv = bf16r(xt[h]);
                     rg[h] += cg * xv;
                     ru[h] += cu * xv;
                 }
@@ -420,11 +432,11 @@ void orc_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const i
 #pragma omp parallel for schedule(dynamic, 1) collapse(2)
     for (int32_t e = 0; e < E; ++e) {
         for (int64_t h = 0; h < H; ++h) {
-            double *rd = dWd + ((int64_t)e * H + h) * I;
-            for (int64_t i = 0; i < I; ++i) rd[i] = 0.0;
+            real *rd = dWd + ((int64_t)e * H + h) * I;
+            for (int64_t i = 0; i < I; ++i) rd[i] = (real)0;
             for (int64_t j = 0; j < R; ++j) {
                 if (ids[j] != e) continue;
-                double c = (double)s[j] * orc_bf16_value(dY[(j / K) * H + h]);
+                real c = (real)s[j] * bf16r(dY[(j / K) * H + h]);
                 for (int64_t i = 0; i < I; ++i) rd[i] += c * A[j * I + i];
             }
         }
@@ -432,6 +444,7 @@ void orc_backward(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const i
     free(G); free(U); free(A); free(DG); free(DU);
 }
 
+#ifndef ORC_TIMING_ONLY
 /* ------------------------------------------------------------------------------------------ */
 /* sampled outputs for full-size checks: the same definitions, one output at a time             */
 /* ------------------------------------------------------------------------------------------ */
@@ -537,6 +550,64 @@ void orc_dw_entries(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const
         val[n] = acc;
     }
 }
+
+/* One 32-column block [i0, i0+32) of I for expert e, against the nh sampled hidden columns hs:
+ *   dwg[ii * nh + n] = dWg[e, i0+ii, hs[n]], dwu likewise, dwd[n * 32 + ii] = dWd[e, hs[n], i0+ii].
+ * The same sums as orc_backward ([MTP] English summary: backward of the SwiGLU experts), over the
+ * expert's slots in ascending order; each slot's g, u and dA' are needed only on the block's 32
+ * columns, so a block costs the expert's rows times 96 H multiply-adds however many hidden columns
+ * are sampled. */
+void orc_dw_block(int64_t T, int32_t H, int32_t I, int32_t E, int32_t K, const int32_t *ids, const float *s,
+                  const uint16_t *x, const uint16_t *Wg, const uint16_t *Wu, const uint16_t *Wd, const uint16_t *dY,
+                  int32_t e, int32_t i0, int64_t nh, const int32_t *hs, double *dwg, double *dwu, double *dwd) {
+    (void)E;
+    const int64_t R = T * (int64_t)K;
+    int64_t *slots = malloc(sizeof(int64_t) * (R ? R : 1));
+    int64_t n = 0;
+    for (int64_t j = 0; j < R; ++j)
+        if (ids[j] == e) slots[n++] = j;
+    /* per slot: dg, du and s a on the block's 32 columns */
+    double *DG = malloc(sizeof(double) * 32 * (n ? n : 1)), *DU = malloc(sizeof(double) * 32 * (n ? n : 1));
+    double *SA = malloc(sizeof(double) * 32 * (n ? n : 1));
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t j = slots[r], t = j / K;
+        const uint16_t *xt = x + t * H, *dy = dY + t * H;
+        const double sv = (double)s[j];
+        for (int ii = 0; ii < 32; ++ii) {
+            const int64_t i = i0 + ii;
+            const uint16_t *wg = Wg + ((int64_t)e * I + i) * H, *wu = Wu + ((int64_t)e * I + i) * H;
+            double g = 0.0, u = 0.0, dap = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                const double xv = orc_bf16_value(xt[h]);
+                g += orc_bf16_value(wg[h]) * xv;
+                u += orc_bf16_value(wu[h]) * xv;
+                dap += orc_bf16_value(Wd[((int64_t)e * H + h) * I + i]) * orc_bf16_value(dy[h]);
+            }
+            const double sg = sigmoid(g), da = sv * dap;
+            DG[r * 32 + ii] = da * u * sg * (1.0 + g * (1.0 - sg));
+            DU[r * 32 + ii] = da * g * sg;
+            SA[r * 32 + ii] = sv * g * sg * u;
+        }
+    }
+    for (int ii = 0; ii < 32; ++ii)
+        for (int64_t q = 0; q < nh; ++q) {
+            double ag = 0.0, au = 0.0, ad = 0.0;
+            for (int64_t r = 0; r < n; ++r) {
+                const int64_t t = slots[r] / K;
+                const double xv = orc_bf16_value(x[t * H + hs[q]]), dv = orc_bf16_value(dY[t * H + hs[q]]);
+                ag += DG[r * 32 + ii] * xv;
+                au += DU[r * 32 + ii] * xv;
+                ad += dv * SA[r * 32 + ii];
+            }
+            dwg[ii * nh + q] = ag;
+            dwu[ii * nh + q] = au;
+            dwd[q * 32 + ii] = ad;
+        }
+    free(slots); free(DG); free(DU); free(SA);
+}
+
+#endif /* ORC_TIMING_ONLY */
 
 int orc_num_threads(void) {
 #ifdef _OPENMP

@@ -3,13 +3,15 @@
 Tolerance (BF16): max|gpu - oracle| / max|oracle| <= 2e-2 per output tensor; the GPU computes
 with bf16 operands, fp32 accumulation and bf16 intermediates (g, u, a, y, dg, du, dX rows), each
 rounding contributing about 2^-9 relative.  Small cases compare every element; the full-size
-workload compares sampled tokens and sampled weight-gradient entries the oracle computes one by
-one.  Determinism: repeats, grid sizes and minibatch settings must agree bitwise.
+workloads compare sampled tokens and sampled weight-gradient entries the oracle computes one by
+one (``fullsize.py``: 256 tokens and at least 4,096 entries of every weight gradient).
+Determinism: repeats, grid sizes and minibatch settings must agree bitwise.
 """
 import numpy as np
 import pytest
 import torch
 
+import fullsize
 import oracle
 from helpers import TOL_BF16, ctx_views, rel_err, to_f64
 from mixture_experts_layer_build_gb300 import inputs
@@ -132,27 +134,7 @@ def full_size(mok):
 
 def test_full_size_sampled_parity(mok, full_size):
     w, d, r = full_size
-    args = _np_args(d)
-    rng = np.random.default_rng(0)
-    tok = np.sort(rng.choice(w.T, size=48, replace=False))
-    ref_out = oracle.forward_tokens(*args, tok)
-    dX, dS = oracle.backward_tokens(*args, inputs.bits(d["dY"]), tok)
-    tk = torch.from_numpy(tok).cuda()
-    errs = dict(out=rel_err(to_f64(r["out"][tk]), ref_out), dX=rel_err(to_f64(r["dx"][tk]), dX),
-                dS=rel_err(to_f64(r["ds"][tk]), dS))
-    n = 96
-    for which, key, M, N in ((0, "dwg", w.I, w.H), (1, "dwu", w.I, w.H), (2, "dwd", w.H, w.I)):
-        t = r[key]
-        # the sample always holds the entry where the GPU tensor peaks, so a wrong peak cannot
-        # hide behind the denominator
-        flat = int(t.abs().argmax())
-        pe, pm, pc = np.unravel_index(flat, t.shape)
-        e = np.concatenate([[pe], rng.integers(0, w.E, n)])
-        m = np.concatenate([[pm], rng.integers(0, M, n)])
-        c = np.concatenate([[pc], rng.integers(0, N, n)])
-        ref = oracle.dw_entries(*args, inputs.bits(d["dY"]), np.full(n + 1, which), e, m, c)
-        got = t[torch.from_numpy(e).cuda(), torch.from_numpy(m).cuda(), torch.from_numpy(c).cuda()]
-        errs[key] = rel_err(to_f64(got), ref)
+    errs = fullsize.bf16_sampled_errors(d, w, r)
     bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
     assert not bad, errs
 
@@ -180,41 +162,15 @@ def test_determinism_repeats_grids_and_minibatches(mok, full_size):
             assert torch.equal(v, r[k]), (i, k)
 
 
-def _sampled_errors(d, w, r, ntok=16, n=64, seed=0):
-    """Sampled parity of one full-size run: tokens for out / dX / dS, entries of every dW tensor
-    (always including the GPU tensor's peak entry)."""
-    args = _np_args(d)
-    dy = inputs.bits(d["dY"])
-    rng = np.random.default_rng(seed)
-    tok = np.sort(rng.choice(w.T, size=ntok, replace=False))
-    tk = torch.from_numpy(tok).cuda()
-    ref_out = oracle.forward_tokens(*args, tok)
-    dX, dS = oracle.backward_tokens(*args, dy, tok)
-    errs = dict(out=rel_err(to_f64(r["out"][tk]), ref_out), dX=rel_err(to_f64(r["dx"][tk]), dX),
-                dS=rel_err(to_f64(r["ds"][tk]), dS))
-    ids = d["topk_ids"].numpy().reshape(-1)
-    used = np.unique(ids)
-    for which, key, M, N in ((0, "dwg", w.I, w.H), (1, "dwu", w.I, w.H), (2, "dwd", w.H, w.I)):
-        t = r[key]
-        pe, pm, pc = np.unravel_index(int(t.abs().argmax()), t.shape)
-        e = np.concatenate([[pe], rng.choice(used, n)])
-        m = np.concatenate([[pm], rng.integers(0, M, n)])
-        c = np.concatenate([[pc], rng.integers(0, N, n)])
-        ref = oracle.dw_entries(*args, dy, np.full(n + 1, which), e, m, c)
-        got = t[torch.from_numpy(e).cuda(), torch.from_numpy(m).cuda(), torch.from_numpy(c).cuda()]
-        errs[key] = rel_err(to_f64(got), ref)
-    return errs
-
-
-@pytest.mark.parametrize("name", ["dsv3_e256", "sweep_zipf0", "sweep_zipf2"])
-def test_workload_sampled_parity_and_grid_determinism(mok, name):
+@pytest.mark.parametrize("name", ["dsv3_e256", "sweep_zipf0", "sweep_zipf1", "sweep_zipf2"])
+def test_workload_sampled_parity_and_determinism(mok, name):
+    """Full-size workloads (the DeepSeek-V3-style layer with 256 resident experts; the T=8192,
+    E=128, top-8 sweep at Zipf s = 0, 1, 2): sampled parity, ten bitwise-identical repeats, and the
+    same bits on other grids and at every minibatch size of the granularity sweep."""
     w = inputs.WORKLOADS[name]
     d = inputs.make(w, seed=0, weight_device="cuda")
-    _, out, g = _run(mok, d, w, mok.make_config(512, 2048))
-    r = dict(out=out.clone(), dx=g.dx.clone(), dwg=g.dw_gate.clone(), dwu=g.dw_up.clone(), dwd=g.dw_down.clone(),
-             ds=g.d_topk_weights.clone())
-    del g
-    errs = _sampled_errors(d, w, r)
+    r = fullsize.run_layer(mok, w, d, mok.make_config(512, 2048), repeats=10)
+    errs = fullsize.bf16_sampled_errors(d, w, r)
     bad = {k: v for k, v in errs.items() if not v <= TOL_BF16}
     assert not bad, errs
     # other grids and every minibatch size of the granularity sweep (128 .. 2048 rows) must give
@@ -223,10 +179,9 @@ def test_workload_sampled_parity_and_grid_determinism(mok, name):
     if name.startswith("sweep"):
         cfgs += [mok.make_config(mb, 2 * mb) for mb in (256, 1024, 2048)]
     for cfg in cfgs:
-        _, out2, g2 = _run(mok, d, w, cfg)
-        for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down,
-                         ds=g2.d_topk_weights).items():
+        r2 = fullsize.run_layer(mok, w, d, cfg)
+        for k, v in r2.items():
             assert torch.equal(v, r[k]), (cfg.minibatch_rows, k)
-        del g2
+        del r2
     del r, d
     torch.cuda.empty_cache()

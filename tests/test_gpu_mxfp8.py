@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import fullsize
 import oracle
 from helpers import rel_err, to_f64
 from mixture_experts_layer_build_gb300 import inputs
@@ -51,6 +52,9 @@ SMALL = [
     ("h384", inputs.custom(T=300, H=384, I=256, E=3, K=2)),  # H not a multiple of 256: 128-wide tiles
     # H above 4096: the first data-gradient GEMM runs its other epilogue (four warps)
     ("long_h", inputs.custom(T=160, H=4224, I=256, E=3, K=2)),
+    # H above 4096 and a multiple of 256: the four-warp first data-gradient epilogue together with
+    # the 128 x 256 tiles of the other GEMMs (the EP64 shard's combination, H = 7168)
+    ("long_h_wide", inputs.custom(T=160, H=4352, I=256, E=3, K=2)),
 ]
 
 
@@ -74,33 +78,17 @@ def test_mxfp8_full_parity(mok, name, w):
 
 def test_mxfp8_ep64_shard_sampled_parity_and_determinism(mok):
     """The per-GPU shard of an EP64 layer: 16,384 routed rows onto 4 experts (Zipf 1.2),
-    H=7168, I=2048, top-1."""
+    H=7168, I=2048, top-1: sampled parity (256 rows, dW blocks of the heaviest and the lightest
+    expert and of each tensor's peak), ten bitwise-identical repeats, other grids."""
     w = inputs.WORKLOADS["mxfp8_ep64_shard"]
     d = inputs.make(w, seed=0)
     mx_gpu = _mx_inputs(mok, d)
     mx_ref = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]))
-    for k in ("q_gate", "st_down"):  # spot-check two copies bit for bit
+    for k in oracle.MX_KEYS:  # the weight copies the GPU reads are the oracle's bytes
         assert np.array_equal(mx_gpu[k].cpu().numpy(), mx_ref[k]), k
     cfg = mok.make_config(512, 2048, precision=mok.MOK_MXFP8)
-    out, g = _run_mx(mok, d, w, cfg, mx_gpu)
-    r = dict(out=out.clone(), dx=g.dx.clone(), dwg=g.dw_gate.clone(), dwu=g.dw_up.clone(), dwd=g.dw_down.clone(),
-             ds=g.d_topk_weights.clone())
-    args = (d["topk_ids"].numpy(), d["topk_weights"].numpy(), inputs.bits(d["x"]), inputs.bits(d["dY"]))
-    rng = np.random.default_rng(0)
-    tok = np.sort(rng.choice(w.T, size=8, replace=False))
-    ro, rdx, rds = oracle.tokens_mx(*args, mx_ref, w.E, w.I, tok)
-    tk = torch.from_numpy(tok).cuda()
-    errs = dict(out=rel_err(to_f64(r["out"][tk]), ro), dX=rel_err(to_f64(r["dx"][tk]), rdx),
-                dS=rel_err(to_f64(r["ds"][tk]), rds))
-    counts = np.bincount(args[0].reshape(-1), minlength=w.E)
-    e = int(np.argmin(counts))
-    i0 = 32 * int(rng.integers(0, w.I // 32))
-    hs = np.sort(rng.choice(w.H, size=8, replace=False))
-    dwg, dwu, dwd = oracle.dw_block_mx(*args, mx_ref, w.E, w.I, e, i0, hs)
-    hk = torch.from_numpy(hs).cuda()
-    errs["dWg"] = rel_err(to_f64(r["dwg"][e, i0:i0 + 32][:, hk]), dwg)
-    errs["dWu"] = rel_err(to_f64(r["dwu"][e, i0:i0 + 32][:, hk]), dwu)
-    errs["dWd"] = rel_err(to_f64(r["dwd"][e][hk, i0:i0 + 32]), dwd)
+    r = fullsize.run_layer(mok, w, d, cfg, mx_gpu=mx_gpu, repeats=10)
+    errs = fullsize.mx_sampled_errors(d, w, r)
     bad = {k: v for k, v in errs.items() if not v <= TOL_MX}
     assert not bad, errs
     for k, v in r.items():
@@ -108,9 +96,8 @@ def test_mxfp8_ep64_shard_sampled_parity_and_determinism(mok):
     # bitwise identical on another grid and minibatch size, and with static tile scheduling
     for cfg in (mok.make_config(256, 512, 37, precision=mok.MOK_MXFP8),
                 mok.make_config(512, 2048, 37, precision=mok.MOK_MXFP8, flags=mok.MOK_FLAG_STATIC_TILES)):
-        out2, g2 = _run_mx(mok, d, w, cfg, mx_gpu)
-        for k, v in dict(out=out2, dx=g2.dx, dwg=g2.dw_gate, dwu=g2.dw_up, dwd=g2.dw_down,
-                         ds=g2.d_topk_weights).items():
+        r2 = fullsize.run_layer(mok, w, d, cfg, mx_gpu=mx_gpu)
+        for k, v in r2.items():
             assert torch.equal(v, r[k]), k
 
 
@@ -260,36 +247,23 @@ def test_mxfp8_operand_copies(mok, name, w):
         err = np.abs(dec - refq)
         assert np.all(err <= step * (1 + 1e-6) + 1e-30), (name_, float((err / step).max()))
         assert not dec[:, ~valid].any(), name_
-@pytest.mark.parametrize("name", ["sweep_zipf0_mx", "sweep_zipf2_mx"])
-def test_mxfp8_sweep_sampled_parity(mok, name):
-    """T=8192, H=4096, I=1536, E=128, top-8, Zipf-skewed routing, MXFP8.  The oracle quantises only
-    the experts its sampled tokens and its dW block touch."""
+@pytest.mark.parametrize("name", ["sweep_zipf0_mx", "sweep_zipf1_mx", "sweep_zipf2_mx"])
+def test_mxfp8_sweep_sampled_parity_and_determinism(mok, name):
+    """T=8192, H=4096, I=1536, E=128, top-8, Zipf-skewed routing, MXFP8: sampled parity and ten
+    bitwise-identical repeats.  On the skewed sweeps the sampled tokens are drawn among those routed
+    only to the 32 heaviest experts, so the oracle quantises about 35 experts' weights instead of
+    128; the dW blocks still cover the lightest expert.  The uniform sweep (s = 0) has no such
+    tokens and samples from all of them."""
     w = inputs.WORKLOADS[name]
     d = inputs.make(w, seed=0, weight_device="cuda")
     mx_gpu = _mx_inputs(mok, d)
-    out, g = _run_mx(mok, d, w, mok.make_config(512, 2048, precision=mok.MOK_MXFP8), mx_gpu)
-    ids = d["topk_ids"].numpy()
-    rng = np.random.default_rng(1)
-    tok = np.sort(rng.choice(w.T, size=4, replace=False))
-    counts = np.bincount(ids.reshape(-1), minlength=w.E)
-    e = int(np.argmax(counts))  # the heaviest expert for the weight-gradient block
-    experts = np.unique(np.concatenate([ids[tok].reshape(-1), [e]]))
-    mx_ref = oracle.mx_weights(inputs.bits(d["Wg"]), inputs.bits(d["Wu"]), inputs.bits(d["Wd"]), experts=experts)
-    args = (ids, d["topk_weights"].numpy(), inputs.bits(d["x"]), inputs.bits(d["dY"]))
-    ro, rdx, rds = oracle.tokens_mx(*args, mx_ref, w.E, w.I, tok)
-    tk = torch.from_numpy(tok).cuda()
-    errs = dict(out=rel_err(to_f64(out[tk]), ro), dX=rel_err(to_f64(g.dx[tk]), rdx),
-                dS=rel_err(to_f64(g.d_topk_weights[tk]), rds))
-    i0 = 32 * int(rng.integers(0, w.I // 32))
-    hs = np.sort(rng.choice(w.H, size=4, replace=False))
-    dwg, dwu, dwd = oracle.dw_block_mx(*args, mx_ref, w.E, w.I, e, i0, hs)
-    hk = torch.from_numpy(hs).cuda()
-    errs["dWg"] = rel_err(to_f64(g.dw_gate[e, i0:i0 + 32][:, hk]), dwg)
-    errs["dWu"] = rel_err(to_f64(g.dw_up[e, i0:i0 + 32][:, hk]), dwu)
-    errs["dWd"] = rel_err(to_f64(g.dw_down[e][hk, i0:i0 + 32]), dwd)
+    r = fullsize.run_layer(mok, w, d, mok.make_config(512, 2048, precision=mok.MOK_MXFP8), mx_gpu=mx_gpu,
+                           repeats=10)
+    pool = fullsize.tokens_within_heaviest(d, w, 32)
+    errs = fullsize.mx_sampled_errors(d, w, r, seed=1, token_pool=pool if pool.size >= 64 else None)
     bad = {k: v for k, v in errs.items() if not v <= TOL_MX}
     assert not bad, errs
-    del out, g
+    del r, mx_gpu
     torch.cuda.empty_cache()
 
 

@@ -185,6 +185,21 @@ def test_sampled_entry_points_match_full():
     full = [g["dWg"], g["dWu"], g["dWd"]]
     ref = np.array([full[wh][ee, mm, cc] for wh, ee, mm, cc in zip(which, e, m, c)])
     np.testing.assert_allclose(val, ref, rtol=1e-11, atol=1e-14)
+    # the block entry point: one 32-column block of I against sampled hidden columns, every expert
+    # (expert 6 may have no slot: exact zeros)
+    hs = np.array([0, 5, 63, 31, 32])
+    for ee in range(7):
+        dwg, dwu, dwd = oracle.dw_block(ids, s, x, Wg, Wu, Wd, dY, ee, 0, hs)
+        np.testing.assert_allclose(dwg, g["dWg"][ee, 0:32][:, hs], rtol=1e-11, atol=1e-14)
+        np.testing.assert_allclose(dwu, g["dWu"][ee, 0:32][:, hs], rtol=1e-11, atol=1e-14)
+        np.testing.assert_allclose(dwd, g["dWd"][ee][hs, 0:32], rtol=1e-11, atol=1e-14)
+    w2 = inputs.custom(T=30, H=64, I=96, E=3, K=2)
+    ids, s, x, Wg, Wu, Wd, dY = _np_inputs(w2, seed=10)
+    g = oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
+    dwg, dwu, dwd = oracle.dw_block(ids, s, x, Wg, Wu, Wd, dY, 1, 64, hs)
+    np.testing.assert_allclose(dwg, g["dWg"][1, 64:96][:, hs], rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(dwu, g["dWu"][1, 64:96][:, hs], rtol=1e-11, atol=1e-14)
+    np.testing.assert_allclose(dwd, g["dWd"][1][hs, 64:96], rtol=1e-11, atol=1e-14)
 
 
 def test_intermediates_consistent():
@@ -196,3 +211,19 @@ def test_intermediates_consistent():
     np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-15)
     g, u = it["g"], it["u"]
     np.testing.assert_allclose(it["a"], g / (1 + np.exp(-g)) * u, rtol=1e-13, atol=1e-16)
+
+
+def test_fp32_timing_build_computes_the_same_layer():
+    """The fp32 -O3 build of the layer loops (the timed CPU baseline) computes the same layer as
+    the fp64 reference, to fp32 rounding."""
+    w = inputs.custom(T=40, H=128, I=64, E=4, K=2)
+    ids, s, x, Wg, Wu, Wd, dY = _np_inputs(w, seed=12)
+    out = oracle.forward(ids, s, x, Wg, Wu, Wd)
+    ref = oracle.backward(ids, s, x, Wg, Wu, Wd, dY)
+    got = oracle.step_f32(ids, s, x, Wg, Wu, Wd, dY)
+    assert got["out"].dtype == np.float32
+    rel = lambda a, b: np.abs(a.astype(np.float64) - b).max() / np.abs(b).max()  # noqa: E731
+    assert rel(got["out"], out) < 1e-5
+    for k in ("dX", "dWg", "dWu", "dWd", "dS"):
+        assert rel(got[k], ref[k]) < 1e-5, k
+        assert not np.array_equal(got[k].astype(np.float64), ref[k]), k  # really computed in fp32
