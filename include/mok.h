@@ -355,6 +355,63 @@ MOK_API mok_status mok_router_backward(const mok_schedule* sched, const void* x,
                                        const float* d_topk_weights, float* dw_router, float* d_bias, void* dx,
                                        int32_t accumulate_dx, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Expert parallelism ("Mixture-of-Kittens(MoK)란? ..." (alltoptrend), section 4 (1): destination
+ * ranks pull the token rows of their experts, expert outputs are pushed back to the ranks holding
+ * the tokens, and the backward runs the opposite directions, all driven by one schedule table).
+ * A group of `world` ranks: rank r holds tokens_per_rank tokens (the group's token t lives on rank
+ * t / tokens_per_rank) and owns experts [r * E, (r + 1) * E), E = the shape's expert count per
+ * rank.  Each call takes per-rank buffer tables (arrays of `world` DEVICE pointers, host arrays):
+ * on one GPU every entry is local memory; across GPUs the entries for other ranks must be
+ * addresses this GPU can load from and store to (peer-mapped memory).  Rows move with plain loads
+ * and stores, no multicast.  Results are bitwise those of the single-rank layer on the
+ * concatenated tokens and experts.  Order: every rank's mok_ep_forward, then (after all of them
+ * have completed: stream order on one GPU, a group barrier across GPUs) every rank's
+ * mok_ep_combine of its y rows; the same for mok_ep_backward and the dX combine.
+ * ------------------------------------------------------------------------------------------- */
+#define MOK_EP_MAX_RANKS 8
+typedef struct {
+  int32_t world;            /* ranks in the group, 1 .. MOK_EP_MAX_RANKS */
+  int32_t rank;             /* this rank */
+  int64_t tokens_per_rank;  /* tokens on every rank; the group's T = world * tokens_per_rank */
+} mok_ep_group;
+
+/* This rank's schedule over the group's slots (slot j = t * K + k of the group's token t).  It
+ * reads every rank's routing -- topk_ids[r], topk_weights[r]: rank r's [tokens_per_rank, K] int32
+ * global expert ids and fp32 weights -- and keeps the slots of its own experts; slots of other
+ * ranks' experts are skipped silently, ids outside [0, world * E) set MOK_ERR_BAD_EXPERT_ID.
+ * shape: T = world * tokens_per_rank, E = experts per rank.  ws as for mok_build_schedule (size
+ * mok_workspace_bytes of the same shape). */
+MOK_API mok_status mok_ep_build_schedule(const mok_config* cfg, const mok_shape* shape, const mok_ep_group* ep,
+                                         const int32_t* const* topk_ids, const float* const* topk_weights, void* ws,
+                                         size_t ws_bytes, mok_schedule* sched_out, void* stream);
+
+/* This rank's forward: pulls the token rows of its experts from x[r] (rank r's [tokens_per_rank,
+ * H] bf16), runs its experts (w: its E experts' weights, as for mok_forward), and pushes each
+ * expert output row y(t, k) to the token's rank: y_recv[r] is rank r's [tokens_per_rank * K, H]
+ * bf16 receive buffer, row t_local * K + k.  fwd_ctx as for mok_forward (mok_fwd_ctx_bytes). */
+MOK_API mok_status mok_ep_forward(const mok_schedule* sched, const mok_ep_group* ep, const void* const* x,
+                                  const mok_weights* w, void* const* y_recv, void* fwd_ctx, size_t fwd_ctx_bytes,
+                                  void* stream);
+
+/* This rank's backward: pulls dY rows of its experts' slots from dy[r] ([tokens_per_rank, H] bf16
+ * per rank), writes the weight gradients of its E experts (dw_gate, dw_up [E, I, H], dw_down [E, H,
+ * I] fp32, overwritten), and pushes per slot the dX row to dx_recv[r] ([tokens_per_rank * K, H] bf16,
+ * row t_local * K + k) and the router-weight gradient to d_topk_weights[r] ([tokens_per_rank, K]
+ * fp32).  Slots with an invalid id get dS = 0 from their token's own rank. */
+MOK_API mok_status mok_ep_backward(const mok_schedule* sched, const mok_ep_group* ep, const void* fwd_ctx,
+                                   const void* const* dy, const mok_weights* w, float* dw_gate, float* dw_up,
+                                   float* dw_down, void* const* dx_recv, float* const* d_topk_weights,
+                                   void* stream);
+
+/* The token owner's fixed-order combine of the rows pushed to it: out[t] = sum over k ascending of
+ * topk_weights[t,k] * recv[t * K + k] in fp32, rounded once to bf16, over the slots whose id lies
+ * in [0, world * E) (topk_weights NULL: weight 1, the dX reduction).  topk_ids, topk_weights: this
+ * rank's [tokens_per_rank, K]; recv [tokens_per_rank * K, H]; out [tokens_per_rank, H] bf16.  Only
+ * shape->H, K and E are read. */
+MOK_API mok_status mok_ep_combine(const mok_shape* shape, const mok_ep_group* ep, const int32_t* topk_ids,
+                                  const float* topk_weights, const void* recv, void* out, void* stream);
+
 /* Copy the schedule's device status word to *out (host pointer) after synchronising the stream.
  * The only call that blocks. */
 MOK_API mok_status mok_read_device_status(const mok_schedule* sched, uint32_t* out, void* stream);

@@ -336,7 +336,7 @@ mok_status mok_build_schedule(const mok_config* cfg, const mok_shape* shape, con
   s.topk_weights = topk_weights;
   s.ws = ws;
   s.ws_bytes = ws_bytes;
-  const int rc = launch_schedule(z, topk_ids, topk_weights, s, st, as_stream(stream));
+  const int rc = launch_schedule(z, plain_route(topk_ids, topk_weights), s, st, as_stream(stream));
   if (rc) return MOK_ERR_CUDA;
   *out = s;
   return MOK_OK;
@@ -368,8 +368,23 @@ static bool all4(std::initializer_list<const void*> ps) {
   return true;
 }
 
-mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weights* w, void* out, void* fwd_ctx,
-                       size_t fwd_ctx_bytes, void* stream) {
+}  // extern "C"
+
+namespace mok {
+namespace {
+
+// Where a pass's per-slot results go: the plain layer combines them itself; expert parallelism
+// pushes them to the ranks holding the tokens, which combine them afterwards.
+struct SlotOut {
+  const RowDst* rows;  // expert parallelism: y (forward) or dX rows (backward) per slot
+  const RowDst* ds;    // expert parallelism: d_topk_weights per slot (backward)
+  int32_t rank;
+};
+
+// The forward through the down projection (or the combine, plain layer): gather (dispatch), the
+// gate/up and down GEMMs, then the combine into out (plain) or the push of each y row (EP).
+mok_status forward_impl(const mok_schedule* sched, const RowSrc& x, const mok_weights* w, void* out, void* fwd_ctx,
+                        size_t fwd_ctx_bytes, const SlotOut* ep, void* stream) {
   Sizes z;
   Staging st;
   mok_status rc = check_sched(sched, &z, &st);
@@ -378,7 +393,9 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
   Ctx ctx;
   if (fwd_ctx_bytes < carve_ctx(z, static_cast<char*>(fwd_ctx), &ctx)) return MOK_ERR_WORKSPACE_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(fwd_ctx) % kAlign) return MOK_ERR_INVALID_ARG;
-  if (z.T > 0 && (!x || !out || !aligned16(x) || !aligned16(out))) return MOK_ERR_INVALID_ARG;
+  for (int r = 0; r < (x.n ? x.n : 1); ++r)
+    if (z.T > 0 && (!x.p[r] || !aligned16(x.p[r]))) return MOK_ERR_INVALID_ARG;
+  if (!ep && z.T > 0 && (!out || !aligned16(out))) return MOK_ERR_INVALID_ARG;
   if (z.mx) {
     if (!all16({w->q_gate, w->q_up, w->q_down}) || !all4({w->s_gate, w->s_up, w->s_down})) return MOK_ERR_INVALID_ARG;
   } else if (!all16({w->w_gate, w->w_up, w->w_down})) {
@@ -391,11 +408,10 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
     const ScaleJob jobs[2] = {{w->s_gate, w->s_up, st.sw_gu, EI / 128, z.H / 128, 2, 1},
                               {w->s_down, nullptr, st.sw_d, EH / (128 * ad), z.I / 128, ad, 0}};
     if (launch_mx_scale_atoms(jobs, 2, s)) return MOK_ERR_CUDA;
-    if (launch_gather_rows_mx(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
-                              st.xq, st.xs, ctx.xr, ctx.xrs, z.rcap(), z.mx_bn_h() / 128, K_GATHER_X, s))
+    if (launch_gather_rows_mx(x, sched->row_token, sched->meta, z.rpad_max, z.H, st.xq, st.xs, ctx.xr, ctx.xrs,
+                              z.rcap(), z.mx_bn_h() / 128, K_GATHER_X, s))
       return MOK_ERR_CUDA;
-  } else if (launch_gather_rows(static_cast<const uint16_t*>(x), sched->row_token, sched->meta, z.rpad_max, z.H,
-                                ctx.xg, K_GATHER_X, s)) {
+  } else if (launch_gather_rows(x, sched->row_token, sched->meta, z.rpad_max, z.H, ctx.xg, K_GATHER_X, s)) {
     return MOK_ERR_CUDA;
   }
   const int g = grid_of(sched);
@@ -403,20 +419,25 @@ mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weigh
   int e = launch_fwd_gemms(z, *sched, ctx, st, *w, g, s);
   if (e < 0) return MOK_ERR_INVALID_ARG;
   if (e) return MOK_ERR_CUDA;
+  if (ep) return from_cuda(launch_push_rows(st.ybuf, sched->perm, sched->meta, z.rpad_max, z.H, *ep->rows, K_PUSH_Y, s));
   return from_cuda(launch_combine(st.ybuf, sched->inv, sched->topk_weights, z.T, z.K, z.H,
                                   static_cast<uint16_t*>(out), K_COMBINE, s));
 }
 
-mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const void* dy, const mok_weights* w,
-                        const mok_grads* g, void* stream) {
+// The backward: gather dY, the first data-gradient GEMM (SwiGLU backward, dS partials), the dS
+// reduction, the second data-gradient GEMM, the dX reduction (plain) or the push of each dX row (EP),
+// and the weight gradients.
+mok_status backward_impl(const mok_schedule* sched, const void* fwd_ctx, const RowSrc& dy, const mok_weights* w,
+                         const mok_grads* g, const SlotOut* ep, void* stream) {
   Sizes z;
   Staging st;
   mok_status rc = check_sched(sched, &z, &st);
   if (rc != MOK_OK) return rc;
   if (!w || !g || !fwd_ctx || (reinterpret_cast<uintptr_t>(fwd_ctx) % kAlign)) return MOK_ERR_INVALID_ARG;
   if (!all16({g->dw_gate, g->dw_up, g->dw_down})) return MOK_ERR_INVALID_ARG;
-  if (z.T > 0 && (!dy || !g->dx || !g->d_topk_weights || !aligned16(dy) || !aligned16(g->dx)))
-    return MOK_ERR_INVALID_ARG;
+  for (int r = 0; r < (dy.n ? dy.n : 1); ++r)
+    if (z.T > 0 && (!dy.p[r] || !aligned16(dy.p[r]))) return MOK_ERR_INVALID_ARG;
+  if (!ep && z.T > 0 && (!g->dx || !g->d_topk_weights || !aligned16(g->dx))) return MOK_ERR_INVALID_ARG;
   if (z.mx) {
     if (!all16({w->qt_gate, w->qt_up, w->qt_down}) || !all4({w->st_gate, w->st_up, w->st_down}))
       return MOK_ERR_INVALID_ARG;
@@ -435,11 +456,10 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
                               {w->st_gate, nullptr, st.swt_g, EH / (128 * ag), z.I / 128, ag, 0},
                               {w->st_up, nullptr, st.swt_u, EH / (128 * ag), z.I / 128, ag, 0}};
     if (launch_mx_scale_atoms(jobs, 3, s)) return MOK_ERR_CUDA;
-    if (launch_gather_rows_mx(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
-                              st.dyq, st.dys, st.dyr, st.dyrs, z.rcap(), 1, K_GATHER_DY, s))
+    if (launch_gather_rows_mx(dy, sched->row_token, sched->meta, z.rpad_max, z.H, st.dyq, st.dys, st.dyr, st.dyrs,
+                              z.rcap(), 1, K_GATHER_DY, s))
       return MOK_ERR_CUDA;
-  } else if (launch_gather_rows(static_cast<const uint16_t*>(dy), sched->row_token, sched->meta, z.rpad_max, z.H,
-                                st.dyg, K_GATHER_DY, s)) {
+  } else if (launch_gather_rows(dy, sched->row_token, sched->meta, z.rpad_max, z.H, st.dyg, K_GATHER_DY, s)) {
     return MOK_ERR_CUDA;
   }
   int e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 1, s);
@@ -447,14 +467,144 @@ mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const vo
   // dS partials per row: one per N tile of the first data-gradient GEMM (two per 128-column tile
   // when the block-scaled one splits its columns between two warps)
   const int n_tiles1 = z.mx ? z.I / (z.mx_dg1_split() ? 64 : 128) : z.I / (z.I % 256 == 0 ? 256 : 128);
-  if (launch_ds_reduce(st.dspart, sched->inv, z.R, n_tiles1, g->d_topk_weights, s)) return MOK_ERR_CUDA;
+  if (ep ? launch_ds_push(st.dspart, sched->inv, z.R, n_tiles1, *ep->ds, ep->rank, s)
+         : launch_ds_reduce(st.dspart, sched->inv, z.R, n_tiles1, g->d_topk_weights, s))
+    return MOK_ERR_CUDA;
   e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 2, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
-  if (launch_combine(st.ybuf, sched->inv, nullptr, z.T, z.K, z.H, static_cast<uint16_t*>(g->dx), K_DX_REDUCE, s))
+  if (ep ? launch_push_rows(st.ybuf, sched->perm, sched->meta, z.rpad_max, z.H, *ep->rows, K_PUSH_DX, s)
+         : launch_combine(st.ybuf, sched->inv, nullptr, z.T, z.K, z.H, static_cast<uint16_t*>(g->dx), K_DX_REDUCE, s))
     return MOK_ERR_CUDA;
   e = launch_wgrad_gemms(z, *sched, ctx, st, *g, grid, s);
   if (e) return e < 0 ? MOK_ERR_INVALID_ARG : MOK_ERR_CUDA;
   return MOK_OK;
+}
+
+// Expert-parallel group description -> tables; false when the description is unusable.
+bool ep_ok(const mok_ep_group* ep) {
+  return ep && ep->world >= 1 && ep->world <= MOK_EP_MAX_RANKS && ep->rank >= 0 && ep->rank < ep->world &&
+         ep->tokens_per_rank >= 0;
+}
+
+// Copy a host table of `world` per-rank device pointers; every entry must be set when `need`.
+template <class D, class S>
+bool fill_table(const S* src, int world, bool need, D* out) {
+  for (int r = 0; r < MOK_EP_MAX_RANKS; ++r) out[r] = nullptr;
+  if (!src) return !need;
+  for (int r = 0; r < world; ++r) {
+    out[r] = (D)(src[r]);
+    if (need && !out[r]) return false;
+  }
+  return true;
+}
+
+}  // namespace
+}  // namespace mok
+
+extern "C" {
+
+mok_status mok_forward(const mok_schedule* sched, const void* x, const mok_weights* w, void* out, void* fwd_ctx,
+                       size_t fwd_ctx_bytes, void* stream) {
+  return forward_impl(sched, plain_rows(x), w, out, fwd_ctx, fwd_ctx_bytes, nullptr, stream);
+}
+
+mok_status mok_backward(const mok_schedule* sched, const void* fwd_ctx, const void* dy, const mok_weights* w,
+                        const mok_grads* g, void* stream) {
+  return backward_impl(sched, fwd_ctx, plain_rows(dy), w, g, nullptr, stream);
+}
+
+mok_status mok_ep_build_schedule(const mok_config* cfg, const mok_shape* shape, const mok_ep_group* ep,
+                                 const int32_t* const* topk_ids, const float* const* topk_weights, void* ws,
+                                 size_t ws_bytes, mok_schedule* out, void* stream) {
+  Sizes z;
+  if (!out || !ep_ok(ep) || !make_sizes(cfg, shape, &z)) return MOK_ERR_INVALID_ARG;
+  if (z.T != static_cast<int64_t>(ep->world) * ep->tokens_per_rank) return MOK_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(z.E) * ep->world > 1 << 30) return MOK_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return MOK_ERR_INVALID_ARG;
+  RouteSrc route{};
+  if (!fill_table(topk_ids, ep->world, z.R > 0, route.ids) || !fill_table(topk_weights, ep->world, z.R > 0, route.w))
+    return MOK_ERR_INVALID_ARG;
+  route.n = ep->world;
+  route.slots_per = ep->tokens_per_rank * z.K;
+  route.e0 = ep->rank * z.E;
+  route.e_total = ep->world * z.E;
+  if (route.slots_per == 0) route.slots_per = 1;
+  Staging st;
+  mok_schedule s{};
+  const size_t need = carve_workspace(z, static_cast<char*>(ws), &s, &st);
+  if (ws_bytes < need) return MOK_ERR_WORKSPACE_TOO_SMALL;
+  s.shape = *shape;
+  s.config = *cfg;
+  s.config.minibatch_rows = z.mb;
+  s.config.macrobatch_rows = z.MB;
+  s.rpad_max = z.rpad_max;
+  s.tiles_max = z.tiles_max;
+  s.mblocks_max = z.mblocks_max;
+  s.topk_weights = nullptr;  // the weights stay with the token owners; the rows carry them
+  s.ws = ws;
+  s.ws_bytes = ws_bytes;
+  if (launch_schedule(z, route, s, st, as_stream(stream))) return MOK_ERR_CUDA;
+  *out = s;
+  return MOK_OK;
+}
+
+mok_status mok_ep_forward(const mok_schedule* sched, const mok_ep_group* ep, const void* const* x,
+                          const mok_weights* w, void* const* y_recv, void* fwd_ctx, size_t fwd_ctx_bytes,
+                          void* stream) {
+  if (!sched || !ep_ok(ep) || sched->shape.T != static_cast<int64_t>(ep->world) * ep->tokens_per_rank)
+    return MOK_ERR_INVALID_ARG;
+  const bool any = sched->shape.T > 0;
+  RowSrc src{};
+  if (!fill_table(x, ep->world, any, src.p))
+    return MOK_ERR_INVALID_ARG;
+  src.n = ep->world;
+  src.rows_per = ep->tokens_per_rank > 0 ? ep->tokens_per_rank : 1;
+  RowDst dst{};
+  if (!fill_table(y_recv, ep->world, any, dst.p)) return MOK_ERR_INVALID_ARG;
+  for (int r = 0; r < ep->world; ++r)
+    if (dst.p[r] && !aligned16(dst.p[r])) return MOK_ERR_INVALID_ARG;
+  dst.n = ep->world;
+  dst.slots_per = src.rows_per * sched->shape.K;
+  const SlotOut so{&dst, nullptr, ep->rank};
+  return forward_impl(sched, src, w, nullptr, fwd_ctx, fwd_ctx_bytes, &so, stream);
+}
+
+mok_status mok_ep_backward(const mok_schedule* sched, const mok_ep_group* ep, const void* fwd_ctx,
+                           const void* const* dy, const mok_weights* w, float* dw_gate, float* dw_up, float* dw_down,
+                           void* const* dx_recv, float* const* d_topk_weights, void* stream) {
+  if (!sched || !ep_ok(ep) || sched->shape.T != static_cast<int64_t>(ep->world) * ep->tokens_per_rank)
+    return MOK_ERR_INVALID_ARG;
+  const bool any = sched->shape.T > 0;
+  RowSrc src{};
+  if (!fill_table(dy, ep->world, any, src.p))
+    return MOK_ERR_INVALID_ARG;
+  src.n = ep->world;
+  src.rows_per = ep->tokens_per_rank > 0 ? ep->tokens_per_rank : 1;
+  RowDst rows{}, ds{};
+  if (!fill_table(dx_recv, ep->world, any, rows.p) || !fill_table(d_topk_weights, ep->world, any, ds.p))
+    return MOK_ERR_INVALID_ARG;
+  for (int r = 0; r < ep->world; ++r)
+    if (rows.p[r] && !aligned16(rows.p[r])) return MOK_ERR_INVALID_ARG;
+  rows.n = ds.n = ep->world;
+  rows.slots_per = ds.slots_per = src.rows_per * sched->shape.K;
+  const SlotOut so{&rows, &ds, ep->rank};
+  mok_grads g{};
+  g.dw_gate = dw_gate;
+  g.dw_up = dw_up;
+  g.dw_down = dw_down;
+  return backward_impl(sched, fwd_ctx, src, w, &g, &so, stream);
+}
+
+mok_status mok_ep_combine(const mok_shape* shape, const mok_ep_group* ep, const int32_t* topk_ids,
+                          const float* topk_weights, const void* recv, void* out, void* stream) {
+  if (!shape || !ep_ok(ep) || shape->K <= 0 || shape->H <= 0 || shape->H % 8 != 0 || shape->E <= 0)
+    return MOK_ERR_INVALID_ARG;
+  const int64_t Tl = ep->tokens_per_rank;
+  if (Tl == 0) return MOK_OK;
+  if (!topk_ids || !recv || !out || !aligned16(recv) || !aligned16(out)) return MOK_ERR_INVALID_ARG;
+  return from_cuda(launch_combine_slots(static_cast<const uint16_t*>(recv), topk_ids, ep->world * shape->E,
+                                       topk_weights, Tl, shape->K, shape->H, static_cast<uint16_t*>(out),
+                                       topk_weights ? K_EP_COMBINE : K_EP_DX_REDUCE, as_stream(stream)));
 }
 
 mok_status mok_set_trace(mok_trace* trace) {
@@ -470,7 +620,8 @@ const char* mok_kernel_name(int32_t kind) {
       "gemm_fwd_down",   "combine",       "gather_dy",     "gemm_dgrad1",    "ds_reduce",
       "gemm_dgrad2",     "dx_reduce",     "gemm_wgrad_gu", "gemm_wgrad_d",   "mxfp8_quantize",
       "mx_scale_atoms",  "router_logits", "router_topk",   "router_transpose", "router_dx",
-      "router_dw",       "selftest_wait"};
+      "router_dw",       "selftest_wait", "push_y",        "push_dx",        "ep_combine",
+      "ep_dx_reduce",    "ds_push"};
   return (kind >= 0 && kind < K_NUM_KINDS) ? names[kind] : "?";
 }
 

@@ -12,6 +12,33 @@ constexpr int kRowTile = 128;       // GEMM row tile: each expert's segment is p
 constexpr int kSchedChunk = 512;    // slots per warp in the schedule histogram / scatter
 constexpr int kSchedWarps = 8;      // warps per CTA in the schedule kernels
 
+// Expert parallelism: buffers of the group's ranks, read (or written) through tables of device
+// pointers.  Token t of the group's global order lives on rank t / rows_per at row t % rows_per;
+// slot j = t * K + k likewise at j % (rows_per * K).  n == 0: one plain buffer, p[0].
+constexpr int kEpMax = 8;
+struct RouteSrc {             // the routing the schedule reads
+  const int32_t* ids[kEpMax];
+  const float* w[kEpMax];
+  int64_t slots_per;          // slots per rank (tokens per rank * K)
+  int32_t n;                  // ranks, 0 = plain
+  int32_t e0;                 // first global expert of this rank: local id = global id - e0
+  int32_t e_total;            // experts of the group: global ids outside [0, e_total) are invalid
+};
+struct RowSrc {               // token rows the gathers read
+  const uint16_t* p[kEpMax];
+  int64_t rows_per;
+  int32_t n;
+};
+struct RowDst {               // per-slot rows / values the pushes write ([rows_per * K] per rank)
+  void* p[kEpMax];
+  int64_t slots_per;
+  int32_t n;
+};
+// Slot codes of the schedule's inv[] besides a row index: a slot whose expert another rank owns
+// (expert parallelism), and a slot whose id is invalid (outside [0, E) or the group's experts).
+constexpr int32_t kSlotForeign = -1;
+constexpr int32_t kSlotInvalid = -2;
+
 // Derived sizes of one (shape, config) pair.
 struct Sizes {
   int64_t T, R, rpad_max, tiles_max, mblocks_max, nchunks;
@@ -105,20 +132,36 @@ enum KernelKind : int {
   K_ROUTER_DX,
   K_ROUTER_DW,
   K_SELFTEST_WAIT,
+  K_PUSH_Y,
+  K_PUSH_DX,
+  K_EP_COMBINE,
+  K_EP_DX_REDUCE,
+  K_DS_PUSH,
   K_NUM_KINDS
 };
 void trace_begin(cudaStream_t s, int kind);  // no-ops unless a trace is set
 void trace_end(cudaStream_t s);
 
 // launchers (return a cudaError_t as int)
-int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mok_schedule& s, const Staging& st,
+int launch_schedule(const Sizes& z, const RouteSrc& route, const mok_schedule& s, const Staging& st,
                     cudaStream_t stream);
-int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+inline RouteSrc plain_route(const int32_t* ids, const float* w) {
+  RouteSrc r{};
+  r.ids[0] = ids;
+  r.w[0] = w;
+  return r;
+}
+inline RowSrc plain_rows(const void* p) {
+  RowSrc r{};
+  r.p[0] = static_cast<const uint16_t*>(p);
+  return r;
+}
+int launch_gather_rows(const RowSrc& src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                        int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
 // MX gather of 32-row blocks: dst_q / dst_sf = rows quantised along H (row-major, A-operand atoms);
 // dstR_q / dstR_sf = the same rows quantised along the rows, transposed [H, rcap] (atoms grouped gT
 // at a time).
-int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+int launch_gather_rows_mx(const RowSrc& src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                           int32_t H, uint8_t* dst_q, uint8_t* dst_sf, uint8_t* dstR_q, uint8_t* dstR_sf,
                           int64_t rcap, int gT, int kind, cudaStream_t stream);
 // Re-tile row-major E8M0 scales [rows, 4 kq] into groups of `atoms` 512-byte atoms (up to three
@@ -137,8 +180,20 @@ struct ScaleJob {
 int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream);
 int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
                    uint16_t* out, int kind, cudaStream_t stream);
+// Expert parallelism, the token owner's combine: out[t] = sum over k ascending of s[t,k] * rows[t*K+k]
+// (s == nullptr: weight 1), over the slots whose global id lies in [0, e_total).
+int launch_combine_slots(const uint16_t* rows, const int32_t* ids, int32_t e_total, const float* s, int64_t T,
+                         int32_t K, int32_t H, uint16_t* out, int kind, cudaStream_t stream);
 int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, float* ds,
                      cudaStream_t stream);
+// Expert parallelism: dS of this rank's slots into the token owners' [slots_per] buffers; this
+// rank also writes 0 for its own tokens' invalid slots (rank = own index in dst).
+int launch_ds_push(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, const RowDst& dst, int32_t rank,
+                   cudaStream_t stream);
+// Expert parallelism: row r of src ([Rpad, H] bf16, r < meta[0]) holding slot j = perm[r] goes to
+// the slot's owner, dst.p[j / slots_per] + (j % slots_per) * H.
+int launch_push_rows(const uint16_t* src, const int32_t* perm, const int32_t* meta, int64_t rpad_max, int32_t H,
+                     const RowDst& dst, int kind, cudaStream_t stream);
 int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_t* q, uint8_t* sc,
                           cudaStream_t stream);
 

@@ -13,10 +13,20 @@ namespace {
 
 constexpr int kMoveThreads = 256;
 
+// Token t's row in the token buffers: one plain buffer, or (expert parallelism) the buffer of the
+// rank holding t, at its row t % rows_per -- a peer's memory when the ranks are separate GPUs.
+__device__ __forceinline__ const uint16_t* token_row(const RowSrc& src, int64_t t, int64_t H) {
+  if (src.n == 0) return src.p[0] + t * H;
+  const int64_t r = t / src.rows_per;
+  return src.p[r] + (t - r * src.rows_per) * H;
+}
+
 // dst[row] = src[row_token[row]] for row < Rpad (= meta[0]); zero rows where row_token < 0.
 // One warp per row, 16-byte vectors, lanes striding along the row (coalesced).  The gathered rows
-// are written evict-first so that the source rows, read K times, stay in L2.
-__global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* __restrict__ src,
+// are written evict-first so that the source rows, read K times, stay in L2.  With expert
+// parallelism this is the pull dispatch of the pages: the rank owning the experts reads the token
+// rows from the ranks holding them.
+__global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const RowSrc src,
                                                                   const int32_t* __restrict__ row_token,
                                                                   const int32_t* __restrict__ meta, int64_t vecs,
                                                                   uint4* __restrict__ dst) {
@@ -28,7 +38,7 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* 
     const int t = row_token[row];
     uint4* d = dst + row * vecs;
     if (t >= 0) {
-      const uint4* s = src + static_cast<int64_t>(t) * vecs;
+      const uint4* s = reinterpret_cast<const uint4*>(token_row(src, t, vecs * 8));
       int64_t c = lane;
       for (; c + 96 < vecs; c += 128) {
         const uint4 v0 = __ldg(s + c), v1 = __ldg(s + c + 32), v2 = __ldg(s + c + 64), v3 = __ldg(s + c + 96);
@@ -46,13 +56,16 @@ __global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const uint4* 
 }
 
 // out[t] = bf16( sum_{k = 0..K-1 ascending} w[t,k] * y[inv[t*K+k]] ), fp32 accumulation; w == nullptr
-// means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.  Each
+// means weight 1 (the dX reduction).  Slots with inv < 0 (invalid ids) contribute nothing.  With
+// inv == nullptr the rows are per slot (row t*K+k: the token owner's receive buffer under expert
+// parallelism) and a slot counts when its id lies in [0, e_total).  Each
 // lane keeps eight 16-byte row loads in flight: U column vectors x (8 / U) of the K rows, issued
 // together before the fixed-order FMA chains (U = 8 for top-1 ... U = 1 for K >= 8).  Rows are
 // read once and written once: both streams are marked evict-first.
 template <int U>
 __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __restrict__ y,
                                                               const int32_t* __restrict__ inv,
+                                                              const int32_t* __restrict__ ids, int e_total,
                                                               const float* __restrict__ w, int64_t T, int K,
                                                               int64_t vecs, uint4* __restrict__ out) {
   constexpr int kBatch = 8 / U;
@@ -73,7 +86,14 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __re
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
           const int k = k0 + b;
-          row[b] = k < K ? __ldg(inv + t * K + k) : -1;
+          if (k >= K) {
+            row[b] = -1;
+          } else if (inv) {
+            row[b] = __ldg(inv + t * K + k);
+          } else {
+            const int g = __ldg(ids + t * K + k);
+            row[b] = (g >= 0 && g < e_total) ? static_cast<int>(t * K + k) : -1;
+          }
           wk[b] = (row[b] >= 0 && w) ? __ldg(w + t * K + k) : 1.0f;
         }
 #pragma unroll
@@ -123,6 +143,55 @@ __global__ void __launch_bounds__(kMoveThreads) ds_reduce_kernel(const float* __
     for (int n = 0; n < n_tiles; ++n) acc += p[n];
   }
   ds[j] = acc;
+}
+
+// Expert parallelism: the dS of this rank's slots, sum over N tiles (ascending) of part[inv[j], :],
+// pushed to the token owner's [slots_per] buffer; this rank's own tokens' invalid slots get 0 (no
+// expert owns them).  Every slot of the group is written by exactly one rank.
+__global__ void __launch_bounds__(kMoveThreads) ds_push_kernel(const float* __restrict__ part,
+                                                              const int32_t* __restrict__ inv, int64_t R,
+                                                              int n_tiles, const RowDst dst, int rank) {
+  const int64_t j = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x;
+  if (j >= R) return;
+  const int row = inv[j];
+  const int64_t r = j / dst.slots_per;
+  if (row >= 0) {
+    const float* p = part + static_cast<int64_t>(row) * n_tiles;
+    float acc = 0.0f;
+    for (int n = 0; n < n_tiles; ++n) acc += p[n];
+    static_cast<float*>(dst.p[r])[j - r * dst.slots_per] = acc;
+  } else if (row == kSlotInvalid && r == rank) {
+    static_cast<float*>(dst.p[r])[j - r * dst.slots_per] = 0.0f;
+  }
+}
+
+// Expert parallelism, the push combine of the pages: row r of the expert-grouped rows (r < Rpad),
+// holding slot j = perm[r], goes to the rank holding slot j, at its row j % slots_per.  One warp per
+// row, 16-byte vectors; both streams single-use (evict-first).
+__global__ void __launch_bounds__(kMoveThreads) push_rows_kernel(const uint4* __restrict__ src,
+                                                                const int32_t* __restrict__ perm,
+                                                                const int32_t* __restrict__ meta, int64_t vecs,
+                                                                const RowDst dst) {
+  const int64_t rpad = meta[0];
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); row < rpad;
+       row += nwarps) {
+    const int64_t j = perm[row];
+    if (j < 0) continue;  // padding row
+    const int64_t r = j / dst.slots_per;
+    const uint4* s = src + row * vecs;
+    uint4* d = static_cast<uint4*>(dst.p[r]) + (j - r * dst.slots_per) * vecs;
+    int64_t c = lane;
+    for (; c + 96 < vecs; c += 128) {
+      const uint4 v0 = __ldcs(s + c), v1 = __ldcs(s + c + 32), v2 = __ldcs(s + c + 64), v3 = __ldcs(s + c + 96);
+      __stcs(d + c, v0);
+      __stcs(d + c + 32, v1);
+      __stcs(d + c + 64, v2);
+      __stcs(d + c + 96, v3);
+    }
+    for (; c < vecs; c += 32) __stcs(d + c, __ldcs(s + c));
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -283,7 +352,7 @@ __device__ __forceinline__ uint32_t gmx_quant(const uint32_t (&w)[N], uint32_t (
 }
 
 // Five CTAs per SM (48 registers; the packed-word quantisation keeps that free of spills).
-__global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const uint16_t* __restrict__ src,
+__global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src,
                                                             const int32_t* __restrict__ row_token,
                                                             const int32_t* __restrict__ meta, int32_t H,
                                                             uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf,
@@ -302,7 +371,7 @@ __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const uint16_t* 
     for (int i = 0; i < 8; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 16 i
       const int r = t / 16 + 16 * i;
       const int tok = __ldg(row_token + r0 + r);
-      val[i] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<int64_t>(tok) * H + c0) + t % 16)
+      val[i] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(token_row(src, tok, H) + c0) + t % 16)
                         : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
@@ -389,18 +458,17 @@ int grid_for(int64_t items, int per_block) {
 
 }  // namespace
 
-int launch_gather_rows(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+int launch_gather_rows(const RowSrc& src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                        int32_t H, uint16_t* dst, int kind, cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
   const int grid = grid_for(rpad_max, kMoveThreads / 32);
   trace_begin(stream, kind);
-  gather_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), row_token, meta,
-                                                        H / 8, reinterpret_cast<uint4*>(dst));
+  gather_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(src, row_token, meta, H / 8, reinterpret_cast<uint4*>(dst));
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
 
-int launch_gather_rows_mx(const uint16_t* src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
+int launch_gather_rows_mx(const RowSrc& src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
                           int32_t H, uint8_t* dst_q, uint8_t* dst_sf, uint8_t* dstR_q, uint8_t* dstR_sf,
                           int64_t rcap, int gT, int kind, cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
@@ -431,21 +499,51 @@ int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream) 
   return static_cast<int>(cudaGetLastError());
 }
 
-int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
-                   uint16_t* out, int kind, cudaStream_t stream) {
+static int combine_any(const uint16_t* y, const int32_t* inv, const int32_t* ids, int32_t e_total, const float* s,
+                       int64_t T, int32_t K, int32_t H, uint16_t* out, int kind, cudaStream_t stream) {
   if (T <= 0) return 0;
   const int grid = grid_for(T, kMoveThreads / 32);
   trace_begin(stream, kind);
   const uint4* yv = reinterpret_cast<const uint4*>(y);
   uint4* ov = reinterpret_cast<uint4*>(out);
   if (K == 1)
-    combine_kernel<8><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
+    combine_kernel<8><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else if (K == 2)
-    combine_kernel<4><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
+    combine_kernel<4><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else if (K <= 4)
-    combine_kernel<2><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
+    combine_kernel<2><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else
-    combine_kernel<1><<<grid, kMoveThreads, 0, stream>>>(yv, inv, s, T, K, H / 8, ov);
+    combine_kernel<1><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+  trace_end(stream);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_combine(const uint16_t* y, const int32_t* inv, const float* s, int64_t T, int32_t K, int32_t H,
+                   uint16_t* out, int kind, cudaStream_t stream) {
+  return combine_any(y, inv, nullptr, 0, s, T, K, H, out, kind, stream);
+}
+
+int launch_combine_slots(const uint16_t* rows, const int32_t* ids, int32_t e_total, const float* s, int64_t T,
+                         int32_t K, int32_t H, uint16_t* out, int kind, cudaStream_t stream) {
+  return combine_any(rows, nullptr, ids, e_total, s, T, K, H, out, kind, stream);
+}
+
+int launch_push_rows(const uint16_t* src, const int32_t* perm, const int32_t* meta, int64_t rpad_max, int32_t H,
+                     const RowDst& dst, int kind, cudaStream_t stream) {
+  if (rpad_max <= 0) return 0;
+  const int grid = grid_for(rpad_max, kMoveThreads / 32);
+  trace_begin(stream, kind);
+  push_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), perm, meta, H / 8, dst);
+  trace_end(stream);
+  return static_cast<int>(cudaGetLastError());
+}
+
+int launch_ds_push(const float* part, const int32_t* inv, int64_t R, int32_t n_tiles, const RowDst& dst, int32_t rank,
+                   cudaStream_t stream) {
+  if (R <= 0) return 0;
+  const int grid = static_cast<int>((R + kMoveThreads - 1) / kMoveThreads);
+  trace_begin(stream, K_DS_PUSH);
+  ds_push_kernel<<<grid, kMoveThreads, 0, stream>>>(part, inv, R, n_tiles, dst, rank);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }

@@ -73,6 +73,6 @@ extern "C" MOK_API mok_status mok_build_schedule_noalloc(const mok_config* cfg, 
   sched->ws_bytes = 0;
   Staging st{};
   st.chunk_hist = scratch;  // every entry the schedule reads is written first: nothing to clear
-  const int rc = launch_schedule(z, topk_ids, topk_weights, *sched, st, static_cast<cudaStream_t>(stream));
+  const int rc = launch_schedule(z, plain_route(topk_ids, topk_weights), *sched, st, static_cast<cudaStream_t>(stream));
   return rc ? MOK_ERR_CUDA : MOK_OK;
 }

@@ -25,11 +25,30 @@ namespace mok {
 namespace {
 
 constexpr int kHistWarps = 2;                    // warps per CTA of the histogram / scatter launches
+
+// The local expert of slot j, or kSlotInvalid (an id outside the experts), or kSlotForeign (expert
+// parallelism: an expert another rank owns).  Plain routing: ids in [0, E) are local.
+__device__ __forceinline__ int route_id(const RouteSrc& r, int64_t j, int E) {
+  if (r.n == 0) {
+    const int e = __ldg(r.ids[0] + j);
+    return (e < 0 || e >= E) ? kSlotInvalid : e;
+  }
+  const int64_t s = j / r.slots_per;
+  const int g = __ldg(r.ids[s] + (j - s * r.slots_per));
+  if (g < 0 || g >= r.e_total) return kSlotInvalid;
+  const int e = g - r.e0;
+  return (e < 0 || e >= E) ? kSlotForeign : e;
+}
+__device__ __forceinline__ float route_w(const RouteSrc& r, int64_t j) {
+  if (r.n == 0) return __ldg(r.w[0] + j);
+  const int64_t s = j / r.slots_per;
+  return __ldg(r.w[s] + (j - s * r.slots_per));
+}
 constexpr int kPieces = kSchedChunk / 32;        // 32-slot pieces per chunk
 constexpr int kBatch = 8;                        // pieces whose loads are in flight together
 
-__global__ void __launch_bounds__(kHistWarps * 32) sched_hist_kernel(const int32_t* __restrict__ ids, int64_t R,
-                                                                    int E, int64_t nchunks,
+__global__ void __launch_bounds__(kHistWarps * 32) sched_hist_kernel(const RouteSrc route, int64_t R, int E,
+                                                                    int64_t nchunks,
                                                                     int32_t* __restrict__ chunk_hist) {
   extern __shared__ int32_t sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -44,12 +63,12 @@ __global__ void __launch_bounds__(kHistWarps * 32) sched_hist_kernel(const int32
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int64_t j = j0 + (p0 + b) * 32 + lane;
-      ev[b] = j < R ? __ldg(ids + j) : INT32_MIN;
+      ev[b] = j < R ? route_id(route, j, E) : INT32_MIN;
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
-      if (ev[b] == INT32_MIN) continue;
-      const int e = (ev[b] < 0 || ev[b] >= E) ? E : ev[b];  // column E counts invalid ids
+      if (ev[b] == INT32_MIN || ev[b] == kSlotForeign) continue;  // another rank counts its slots
+      const int e = ev[b] == kSlotInvalid ? E : ev[b];  // column E counts invalid ids
       atomicAdd(&h[e], 1);
     }
   }
@@ -218,7 +237,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
 }
 
 __global__ void __launch_bounds__(kHistWarps * 32) sched_scatter_kernel(
-    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t R, int K, int E, int64_t nchunks,
+    const RouteSrc route, int64_t R, int K, int E, int64_t nchunks,
     const int32_t* __restrict__ chunk_first, const int32_t* __restrict__ meta, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
   extern __shared__ int32_t sh[];
@@ -236,18 +255,17 @@ __global__ void __launch_bounds__(kHistWarps * 32) sched_scatter_kernel(
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int64_t j = j0 + (p0 + b) * 32 + lane;
-      ev[b] = -1;
+      ev[b] = kSlotForeign;
       wv[b] = 0.0f;
       if (j < R) {
-        const int e0 = __ldg(ids + j);
-        ev[b] = (e0 < 0 || e0 >= E) ? -1 : e0;
-        wv[b] = __ldg(w + j);
+        ev[b] = route_id(route, j, E);
+        wv[b] = route_w(route, j);
       }
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int64_t j = j0 + (p0 + b) * 32 + lane;
-      const int e = ev[b];
+      const int e = ev[b] >= 0 ? ev[b] : -1;
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       const int base = (e >= 0) ? run[e] : 0;
@@ -260,7 +278,9 @@ __global__ void __launch_bounds__(kHistWarps * 32) sched_scatter_kernel(
         row_weight[row] = wv[b];
         if (lane == 31 - __clz(peers)) run[e] = base + __popc(peers);
       } else if (j < R) {
-        inv[j] = -1;  // an invalid id: the slot is skipped (status word says so)
+        // skipped: another rank's expert, or an invalid id (the status word says so; with
+        // expert parallelism it is marked apart, since its token's owner zeroes its dS)
+        inv[j] = (route.n != 0 && ev[b] == kSlotInvalid) ? kSlotInvalid : kSlotForeign;
       }
       __syncwarp();
     }
@@ -269,7 +289,7 @@ __global__ void __launch_bounds__(kHistWarps * 32) sched_scatter_kernel(
 
 }  // namespace
 
-int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mok_schedule& s, const Staging& st,
+int launch_schedule(const Sizes& z, const RouteSrc& route, const mok_schedule& s, const Staging& st,
                     cudaStream_t stream) {
   static DeviceOnce once;  // the scan's group sums need up to 32 x 1025 int32 of shared memory, on each device
   const int se = once.run([](int* d) { return static_cast<int>(cudaGetDevice(d)); },
@@ -285,7 +305,7 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
   if (blocks > 0) {
     const size_t sh = sizeof(int32_t) * kHistWarps * (z.E + 1);
     trace_begin(stream, K_SCHED_HIST);
-    sched_hist_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(ids, z.R, z.E, nchunks, st.chunk_hist);
+    sched_hist_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(route, z.R, z.E, nchunks, st.chunk_hist);
     trace_end(stream);
   }
   trace_begin(stream, K_SCHED_SCAN);
@@ -296,7 +316,7 @@ int launch_schedule(const Sizes& z, const int32_t* ids, const float* w, const mo
   if (blocks > 0) {
     const size_t sh = sizeof(int32_t) * kHistWarps * z.E;
     trace_begin(stream, K_SCHED_SCATTER);
-    sched_scatter_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(ids, w, z.R, z.K, z.E, nchunks, st.chunk_hist,
+    sched_scatter_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(route, z.R, z.K, z.E, nchunks, st.chunk_hist,
                                                                    s.meta, s.perm, s.inv, s.row_token, s.row_weight);
     trace_end(stream);
   }

@@ -123,7 +123,8 @@ _lib.mok_mx_operands_of.argtypes = [ctypes.POINTER(mok_schedule), _P, ctypes.POI
 EXPORTED = ("mok_version", "mok_status_string", "mok_workspace_bytes", "mok_fwd_ctx_bytes", "mok_mxfp8_quantize",
             "mok_build_schedule", "mok_forward", "mok_backward", "mok_read_device_status", "mok_set_trace",
             "mok_kernel_name", "mok_build_schedule_noalloc", "mok_mx_operands_of", "mok_router_workspace_bytes",
-            "mok_router_forward", "mok_router_backward", "mok_selftest_wait_timeout")
+            "mok_router_forward", "mok_router_backward", "mok_selftest_wait_timeout", "mok_ep_build_schedule",
+            "mok_ep_forward", "mok_ep_backward", "mok_ep_combine")
 _lib.mok_router_workspace_bytes.restype = ctypes.c_size_t
 _lib.mok_router_workspace_bytes.argtypes = [ctypes.POINTER(mok_shape)]
 _lib.mok_router_forward.restype = ctypes.c_int
@@ -134,6 +135,29 @@ _lib.mok_router_backward.argtypes = [ctypes.POINTER(mok_schedule), _P, _P, _P, _
 _lib.mok_build_schedule_noalloc.restype = ctypes.c_int
 _lib.mok_build_schedule_noalloc.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape), _P, _P,
                                             ctypes.POINTER(mok_schedule), _P]
+
+
+# ---- expert parallelism ----
+MOK_EP_MAX_RANKS = 8
+
+
+class mok_ep_group(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int32), ("rank", ctypes.c_int32), ("tokens_per_rank", ctypes.c_int64)]
+
+
+_PT = ctypes.POINTER(_P)
+_lib.mok_ep_build_schedule.restype = ctypes.c_int
+_lib.mok_ep_build_schedule.argtypes = [ctypes.POINTER(mok_config), ctypes.POINTER(mok_shape),
+                                       ctypes.POINTER(mok_ep_group), _PT, _PT, _P, ctypes.c_size_t,
+                                       ctypes.POINTER(mok_schedule), _P]
+_lib.mok_ep_forward.restype = ctypes.c_int
+_lib.mok_ep_forward.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(mok_ep_group), _PT,
+                                ctypes.POINTER(mok_weights), _PT, _P, ctypes.c_size_t, _P]
+_lib.mok_ep_backward.restype = ctypes.c_int
+_lib.mok_ep_backward.argtypes = [ctypes.POINTER(mok_schedule), ctypes.POINTER(mok_ep_group), _P, _PT,
+                                 ctypes.POINTER(mok_weights), _P, _P, _P, _PT, _PT, _P]
+_lib.mok_ep_combine.restype = ctypes.c_int
+_lib.mok_ep_combine.argtypes = [ctypes.POINTER(mok_shape), ctypes.POINTER(mok_ep_group), _P, _P, _P, _P, _P]
 
 
 def _check(rc: int, where: str):
@@ -342,6 +366,58 @@ def mok_backward(sched: Schedule, fwd_ctx: torch.Tensor, dy: torch.Tensor, weigh
     _check(_lib.mok_backward(ctypes.byref(sched.c), _ptr(fwd_ctx, None, "fwd_ctx"), _ptr(dy, torch.bfloat16, "dy"),
                              ctypes.byref(weights), ctypes.byref(gs), _stream(stream)), "mok_backward")
     return grads
+
+
+def make_ep_group(world: int, rank: int, tokens_per_rank: int) -> mok_ep_group:
+    return mok_ep_group(world, rank, tokens_per_rank)
+
+
+def _table(tensors, dtype, name):
+    """Host array of per-rank device pointers (one per rank of the group)."""
+    if len(tensors) > MOK_EP_MAX_RANKS:
+        raise ValueError(f"at most {MOK_EP_MAX_RANKS} ranks")
+    arr = (_P * MOK_EP_MAX_RANKS)()
+    for r, t in enumerate(tensors):
+        arr[r] = _ptr(t, dtype, f"{name}[{r}]")
+    return arr
+
+
+def mok_ep_build_schedule(cfg: mok_config, shape: mok_shape, ep: mok_ep_group, topk_ids: list, topk_weights: list,
+                          ws: torch.Tensor, stream=None) -> Schedule:
+    """This rank's schedule over the group's slots, from every rank's routing (lists of tensors)."""
+    s = mok_schedule()
+    ids_t, w_t = _table(topk_ids, torch.int32, "topk_ids"), _table(topk_weights, torch.float32, "topk_weights")
+    _check(_lib.mok_ep_build_schedule(ctypes.byref(cfg), ctypes.byref(shape), ctypes.byref(ep), ids_t, w_t,
+                                      _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), ctypes.byref(s),
+                                      _stream(stream)), "mok_ep_build_schedule")
+    return Schedule(s, ws, topk_ids[ep.rank], topk_weights[ep.rank])
+
+
+def mok_ep_forward(sched: Schedule, ep: mok_ep_group, x: list, weights: mok_weights, y_recv: list,
+                   fwd_ctx: torch.Tensor, stream=None) -> None:
+    _check(_lib.mok_ep_forward(ctypes.byref(sched.c), ctypes.byref(ep), _table(x, torch.bfloat16, "x"),
+                               ctypes.byref(weights), _table(y_recv, torch.bfloat16, "y_recv"),
+                               _ptr(fwd_ctx, None, "fwd_ctx"), fwd_ctx.numel() * fwd_ctx.element_size(),
+                               _stream(stream)), "mok_ep_forward")
+
+
+def mok_ep_backward(sched: Schedule, ep: mok_ep_group, fwd_ctx: torch.Tensor, dy: list, weights: mok_weights,
+                    dw_gate: torch.Tensor, dw_up: torch.Tensor, dw_down: torch.Tensor, dx_recv: list,
+                    d_topk_weights: list, stream=None) -> None:
+    _check(_lib.mok_ep_backward(ctypes.byref(sched.c), ctypes.byref(ep), _ptr(fwd_ctx, None, "fwd_ctx"),
+                                _table(dy, torch.bfloat16, "dy"), ctypes.byref(weights),
+                                _ptr(dw_gate, torch.float32, "dw_gate"), _ptr(dw_up, torch.float32, "dw_up"),
+                                _ptr(dw_down, torch.float32, "dw_down"), _table(dx_recv, torch.bfloat16, "dx_recv"),
+                                _table(d_topk_weights, torch.float32, "d_topk_weights"), _stream(stream)),
+           "mok_ep_backward")
+
+
+def mok_ep_combine(shape: mok_shape, ep: mok_ep_group, topk_ids: torch.Tensor, topk_weights: torch.Tensor | None,
+                   recv: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    _check(_lib.mok_ep_combine(ctypes.byref(shape), ctypes.byref(ep), _ptr(topk_ids, torch.int32, "topk_ids"),
+                               _ptr(topk_weights, torch.float32, "topk_weights"), _ptr(recv, torch.bfloat16, "recv"),
+                               _ptr(out, torch.bfloat16, "out"), _stream(stream)), "mok_ep_combine")
+    return out
 
 
 def mok_read_device_status(sched: Schedule, stream=None) -> int:
