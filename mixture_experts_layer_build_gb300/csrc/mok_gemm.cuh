@@ -162,7 +162,7 @@ __device__ __forceinline__ int gemm_num_units(const GemmArgs& a) {
 // CTA pairs (row-tiled variants; rank = this CTA's place in the pair): the same enumeration over
 // pairs of row blocks (N tiles outer, pairs inner, within each minibatch tile).  A CTA without rows
 // gets row0 = -1.
-template <int VAR, bool MX, bool PAIR = false>
+template <int VAR, bool MX, bool PAIR = false, int BN = 256>
 __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u, int rank = 0) {
   Unit w;
   w.peer_rows = true;
@@ -171,8 +171,16 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u, int rank =
     const int per_e = a.m_tiles * a.n_tiles;
     w.e = u / per_e;
     const int r = u - w.e * per_e;
-    w.mt = r / a.n_tiles;
-    w.nt = r - w.mt * a.n_tiles;
+    if (MX && a.m_tiles * kBM <= a.n_tiles * BN) {
+      // the smaller operand's tiles fastest: the tiles running together sweep all of its slices,
+      // which then stay in L2 while the larger operand streams through once (with the larger one
+      // fastest, a long expert's slices of it were re-read from DRAM for every group of tiles)
+      w.nt = r / a.m_tiles;
+      w.mt = r - w.nt * a.m_tiles;
+    } else {
+      w.mt = r / a.n_tiles;
+      w.nt = r - w.mt * a.n_tiles;
+    }
     const int p0 = __ldg(a.poff + w.e), p1 = __ldg(a.poff + w.e + 1);
     w.row0 = p0;
     w.kblocks = (p1 - p0) / (MX ? 128 : kBK);
@@ -335,7 +343,7 @@ struct Stager {
   }
   // Lane r writes its row (ROW / 16 chunks of 16 bytes) and the warp stores the tile at (c0, c1).
   template <int ROW>
-  __device__ __forceinline__ void put(const uint4* ch, const CUtensorMap* tm, int c0, int c1) {
+  __device__ __forceinline__ void put(const uint4* ch, const CUtensorMap* tm, int c0, int c1, bool ef = false) {
     static_assert(ROW == 128 || ROW == 64 || ROW == 32, "row size with a TMA swizzle mode");
     static_assert(32 * ROW <= BUFBYTES, "tile fits the staging buffer");
     const uint32_t b = acquire();
@@ -346,7 +354,8 @@ struct Stager {
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(tm, b, c0, c1);
+      if (ef) tma_store_2d_evict_first(tm, b, c0, c1);
+      else tma_store_2d(tm, b, c0, c1);
       bulk_commit();
     }
   }
@@ -375,7 +384,7 @@ struct GroupStager {
     return true;
   }
   __device__ __forceinline__ bool put(const uint4 (&ch)[8], const CUtensorMap* tm, int c0, int row0,
-                                      volatile int* abort, uint32_t* status) {
+                                      volatile int* abort, uint32_t* status, bool ef = false) {
     const uint32_t tile = base + static_cast<uint32_t>(cur) * 16384u;
     const uint32_t r = tile + static_cast<uint32_t>(row) * 128u;
 #pragma unroll
@@ -383,7 +392,8 @@ struct GroupStager {
     fence_proxy_async_smem();
     if (!sync(abort, status)) return false;  // all 128 rows are in the tile
     if (leader) {
-      tma_store_2d(tm, tile, c0, row0);
+      if (ef) tma_store_2d_evict_first(tm, tile, c0, row0);
+      else tma_store_2d(tm, tile, c0, row0);
       bulk_commit();
       bulk_wait_read<1>();  // the other tile's store has read it
     }
@@ -467,7 +477,7 @@ __device__ __forceinline__ void quant_rows_store(const float (&v)[32], uint32_t 
   const uint32_t sb = mx_quant32(col, codes);
   const uint4 ch[2] = {make_uint4(codes[0], codes[1], codes[2], codes[3]),
                        make_uint4(codes[4], codes[5], codes[6], codes[7])};
-  stg.template put<32>(ch, tm, rowc, f0);
+  stg.template put<32>(ch, tm, rowc, f0, true);  // read by the weight gradients, after the next GEMM
   sf[sf_atom_offset_p2(f0 + lane, rowc >> 5, kq, gl)] = static_cast<uint8_t>(sb);
 }
 
@@ -505,12 +515,12 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
         for (int j = 0; j < 4; ++j)
           ch[j] = make_uint4(gr[c + c16 + 4 * j], gr[c + c16 + 4 * j + 1], gr[c + c16 + 4 * j + 2],
                              gr[c + c16 + 4 * j + 3]);
-        stg.template put<64>(ch, tO0, i0 + c + c16, rowc);
+        stg.template put<64>(ch, tO0, i0 + c + c16, rowc, true);  // context: read in the backward
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           ch[j] = make_uint4(ur[c + c16 + 4 * j], ur[c + c16 + 4 * j + 1], ur[c + c16 + 4 * j + 2],
                              ur[c + c16 + 4 * j + 3]);
-        stg.template put<64>(ch, tO0, a.I + i0 + c + c16, rowc);
+        stg.template put<64>(ch, tO0, a.I + i0 + c + c16, rowc, true);
       }
       float v[32];
 #pragma unroll
@@ -555,10 +565,10 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       tmem_ld64(taddr + BN / 2 + c, u);
       if (c + 64 >= BN / 2) release_acc<PAIR>(tempty);
       uint4 ch[8];
-      pack_bf16<64>(g, ch);
-      if (!gs.put(ch, tO0, i0 + c, w.row0, abort_flag, a.status)) return;
+      pack_bf16<64>(g, ch);  // g, u: the context, read in the backward
+      if (!gs.put(ch, tO0, i0 + c, w.row0, abort_flag, a.status, true)) return;
       pack_bf16<64>(u, ch);
-      if (!gs.put(ch, tO0, a.I + i0 + c, w.row0, abort_flag, a.status)) return;
+      if (!gs.put(ch, tO0, a.I + i0 + c, w.row0, abort_flag, a.status, true)) return;
 #pragma unroll
       for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
       pack_bf16<64>(g, ch);
@@ -731,7 +741,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         ch[j] = make_uint4(r[c + 4 * j], r[c + 4 * j + 1], r[c + 4 * j + 2], r[c + 4 * j + 3]);
-      stg.template put<64>(ch, tm, w.nt * BN + 128 * h + c, r0);
+      stg.template put<64>(ch, tm, w.nt * BN + 128 * h + c, r0, true);  // dW: not read again
     }
   } else {
     // weight gradients, fp32 out in 128-row x 32-column tiles of the group stager (a quarter of the
@@ -763,7 +773,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
       uint4 ch[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) ch[j] = make_uint4(rv[4 * j], rv[4 * j + 1], rv[4 * j + 2], rv[4 * j + 3]);
-      if (!gs.put(ch, tm, w.nt * BN + c, rt, abort_flag, a.status)) return;
+      if (!gs.put(ch, tm, w.nt * BN + c, rt, abort_flag, a.status, true)) return;  // dW: not read again
     }
   }
 }
@@ -910,7 +920,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR, SPLIT>::kThreads, 1
         } else if (u >= num_units) {
           break;
         }
-        const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
+        const Unit w = gemm_decode<VAR, MX, PAIR, BN>(args, u, rank);
         for (int kb = 0; kb < w.kblocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, args.status)) {
             ok = false;
@@ -981,7 +991,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR, SPLIT>::kThreads, 1
         } else if (u >= num_units) {
           break;
         }
-        const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
+        const Unit w = gemm_decode<VAR, MX, PAIR, BN>(args, u, rank);
         if (!mbar_wait<PAIR>(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -1058,7 +1068,7 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR, SPLIT>::kThreads, 1
       } else if (u >= num_units) {
         break;
       }
-      const Unit w = gemm_decode<VAR, MX, PAIR>(args, u, rank);
+      const Unit w = gemm_decode<VAR, MX, PAIR, BN>(args, u, rank);
       const uint32_t tempty = PAIR ? mapa_shared(tempty_bar(acc), 0) : tempty_bar(acc);
       Dg1Chunk pre;
       if constexpr (VAR == V_DGRAD1 && !MX) {  // before the wait
