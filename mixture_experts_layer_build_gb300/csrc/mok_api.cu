@@ -411,7 +411,8 @@ mok_status forward_impl(const mok_schedule* sched, const RowSrc& x, const mok_we
     if (launch_gather_rows_mx(x, sched->row_token, sched->meta, z.rpad_max, z.H, st.xq, st.xs, ctx.xr, ctx.xrs,
                               z.rcap(), z.mx_bn_h() / 128, K_GATHER_X, s))
       return MOK_ERR_CUDA;
-  } else if (launch_gather_rows(x, sched->row_token, sched->meta, z.rpad_max, z.H, ctx.xg, K_GATHER_X, s)) {
+  } else if (launch_gather_rows(x, sched->inv, sched->row_token, sched->meta, z.T, z.K, z.rpad_max, z.H,
+                                     ctx.xg, K_GATHER_X, s)) {
     return MOK_ERR_CUDA;
   }
   const int g = grid_of(sched);
@@ -459,7 +460,8 @@ mok_status backward_impl(const mok_schedule* sched, const void* fwd_ctx, const R
     if (launch_gather_rows_mx(dy, sched->row_token, sched->meta, z.rpad_max, z.H, st.dyq, st.dys, st.dyr, st.dyrs,
                               z.rcap(), 1, K_GATHER_DY, s))
       return MOK_ERR_CUDA;
-  } else if (launch_gather_rows(dy, sched->row_token, sched->meta, z.rpad_max, z.H, st.dyg, K_GATHER_DY, s)) {
+  } else if (launch_gather_rows(dy, sched->inv, sched->row_token, sched->meta, z.T, z.K, z.rpad_max, z.H,
+                                     st.dyg, K_GATHER_DY, s)) {
     return MOK_ERR_CUDA;
   }
   int e = launch_dgrad_gemms(z, *sched, ctx, st, *w, grid, 1, s);

@@ -156,8 +156,9 @@ inline RowSrc plain_rows(const void* p) {
   r.p[0] = static_cast<const uint16_t*>(p);
   return r;
 }
-int launch_gather_rows(const RowSrc& src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                       int32_t H, uint16_t* dst, int kind, cudaStream_t stream);
+int launch_gather_rows(const RowSrc& src, const int32_t* inv, const int32_t* row_token, const int32_t* meta,
+                       int64_t T, int32_t K, int64_t rpad_max, int32_t H, uint16_t* dst, int kind,
+                       cudaStream_t stream);
 // MX gather of 32-row blocks: dst_q / dst_sf = rows quantised along H (row-major, A-operand atoms);
 // dstR_q / dstR_sf = the same rows quantised along the rows, transposed [H, rcap] (atoms grouped gT
 // at a time).

@@ -21,35 +21,63 @@ __device__ __forceinline__ const uint16_t* token_row(const RowSrc& src, int64_t 
   return src.p[r] + (t - r * src.rows_per) * H;
 }
 
-// dst[row] = src[row_token[row]] for row < Rpad (= meta[0]); zero rows where row_token < 0.
-// One warp per row, 16-byte vectors, lanes striding along the row (coalesced).  The gathered rows
-// are written evict-first so that the source rows, read K times, stay in L2.  With expert
-// parallelism this is the pull dispatch of the pages: the rank owning the experts reads the token
-// rows from the ranks holding them.
-__global__ void __launch_bounds__(kMoveThreads) gather_rows_kernel(const RowSrc src,
-                                                                  const int32_t* __restrict__ row_token,
-                                                                  const int32_t* __restrict__ meta, int64_t vecs,
-                                                                  uint4* __restrict__ dst) {
-  const int64_t rpad = meta[0];
+// The dispatch gather in token order: token t's row is read once and written to the rows of its
+// K slots (row inv[t*K+k]; a slot with inv < 0 -- an invalid id, or an expert another rank owns --
+// is skipped), then every padding row (row_token < 0, row < Rpad = meta[0]) is zeroed.  A warp's
+// work item is one chunk of 32 * U 16-byte vectors of one token row (chunks fastest, so warps
+// running together read whole rows), lanes striding along it: U loads per lane, then the K stores
+// of each.  Walking the rows in expert order instead re-reads each token row K times from wherever
+// L2 has let it go; in token order HBM sees one read of the token rows and one write of the
+// gathered ones, and both streams are marked evict-first.  Padding rows are dealt out to the
+// warps by a row stride (padding sits in runs at the end of each expert's rows): each lane looks
+// up one of the warp's next 32 rows, and the warp zeroes the ones that are padding.  With expert
+// parallelism this is the pull dispatch of the pages: the rank owning the experts reads, from the
+// ranks holding them, the rows of the tokens with a slot on one of its experts.
+template <int U>
+__global__ void __launch_bounds__(kMoveThreads) gather_tokens_kernel(const RowSrc src,
+                                                                    const int32_t* __restrict__ inv,
+                                                                    const int32_t* __restrict__ row_token,
+                                                                    const int32_t* __restrict__ meta, int64_t T,
+                                                                    int K, int64_t vecs, uint4* __restrict__ dst) {
+  constexpr int64_t kChunk = 32 * U;
   const int lane = threadIdx.x & 31;
+  const int64_t warp = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5);
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
-  for (int64_t row = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); row < rpad;
-       row += nwarps) {
-    const int t = row_token[row];
-    uint4* d = dst + row * vecs;
-    if (t >= 0) {
-      const uint4* s = reinterpret_cast<const uint4*>(token_row(src, t, vecs * 8));
-      int64_t c = lane;
-      for (; c + 96 < vecs; c += 128) {
-        const uint4 v0 = __ldg(s + c), v1 = __ldg(s + c + 32), v2 = __ldg(s + c + 64), v3 = __ldg(s + c + 96);
-        __stcs(d + c, v0);
-        __stcs(d + c + 32, v1);
-        __stcs(d + c + 64, v2);
-        __stcs(d + c + 96, v3);
+  const int64_t chunks = (vecs + kChunk - 1) / kChunk;
+  // every loop bound and branch condition below is the same on all 32 lanes, so each
+  // __ballot_sync / __shfl_sync is reached by the whole warp
+  for (int64_t item = warp; item < T * chunks; item += nwarps) {
+    const int64_t t = item / chunks;
+    const int64_t c0 = (item - t * chunks) * kChunk;
+    const uint4* s = reinterpret_cast<const uint4*>(token_row(src, t, vecs * 8));
+    for (int k0 = 0; k0 < K; k0 += 32) {
+      const int row = k0 + lane < K ? __ldg(inv + t * K + k0 + lane) : -1;
+      const unsigned live = __ballot_sync(0xffffffffu, row >= 0);
+      if (!live) continue;
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t c = c0 + 32 * u + lane;
+        v[u] = c < vecs ? __ldcs(s + c) : make_uint4(0, 0, 0, 0);
       }
-      for (; c < vecs; c += 32) __stcs(d + c, __ldg(s + c));
-    } else {
-      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (unsigned m = live; m; m &= m - 1) {
+        const int64_t r = __shfl_sync(0xffffffffu, row, __ffs(m) - 1);
+        uint4* d = dst + r * vecs;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t c = c0 + 32 * u + lane;
+          if (c < vecs) __stcs(d + c, v[u]);
+        }
+      }
+    }
+  }
+  const int64_t rpad = meta[0];
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t r0 = warp; r0 < rpad; r0 += 32 * nwarps) {  // rows r0 + j * nwarps, j = 0..31
+    const int64_t r = r0 + lane * nwarps;
+    const bool pad = r < rpad && __ldg(row_token + r) < 0;
+    for (unsigned m = __ballot_sync(0xffffffffu, pad); m; m &= m - 1) {
+      uint4* d = dst + (r0 + static_cast<int64_t>(__ffs(m) - 1) * nwarps) * vecs;
       for (int64_t c = lane; c < vecs; c += 32) __stcs(d + c, z);
     }
   }
@@ -458,12 +486,18 @@ int grid_for(int64_t items, int per_block) {
 
 }  // namespace
 
-int launch_gather_rows(const RowSrc& src, const int32_t* row_token, const int32_t* meta, int64_t rpad_max,
-                       int32_t H, uint16_t* dst, int kind, cudaStream_t stream) {
+int launch_gather_rows(const RowSrc& src, const int32_t* inv, const int32_t* row_token, const int32_t* meta,
+                       int64_t T, int32_t K, int64_t rpad_max, int32_t H, uint16_t* dst, int kind,
+                       cudaStream_t stream) {
   if (rpad_max <= 0) return 0;
-  const int grid = grid_for(rpad_max, kMoveThreads / 32);
+  const int64_t vecs = H / 8;
+  const int grid = grid_for(T * ((vecs + 127) / 128) + rpad_max / 32, kMoveThreads / 32);
   trace_begin(stream, kind);
-  gather_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(src, row_token, meta, H / 8, reinterpret_cast<uint4*>(dst));
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  if (vecs >= 32 * 4)
+    gather_tokens_kernel<4><<<grid, kMoveThreads, 0, stream>>>(src, inv, row_token, meta, T, K, vecs, d);
+  else
+    gather_tokens_kernel<1><<<grid, kMoveThreads, 0, stream>>>(src, inv, row_token, meta, T, K, vecs, d);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
