@@ -49,6 +49,8 @@ SMALL = [
     ("multi_tile", inputs.custom(T=700, H=512, I=384, E=3, K=2)),
     ("one_expert", inputs.custom(T=64, H=128, I=128, E=1, K=1)),
     ("wide", inputs.custom(T=96, H=1024, I=512, E=6, K=2)),
+    # more than 32 slots per token: the token-order gather takes its slot rows 32 at a time
+    ("many_slots", inputs.custom(T=48, H=256, I=128, E=48, K=40)),
 ]
 
 
