@@ -566,8 +566,8 @@ def ours(args, rank, ws, local_rank, name, with_router=True):
     recs = tr.records()
     launches_per_step = len(recs) / args.steps
     per = {}
-    for name, t in recs:
-        p = per.setdefault(name, [0.0, 0])
+    for kname, t in recs:
+        p = per.setdefault(kname, [0.0, 0])
         p[0] += t
         p[1] += 1
     traced_total = sum(v[0] for v in per.values())
