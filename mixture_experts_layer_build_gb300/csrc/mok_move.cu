@@ -90,8 +90,8 @@ __global__ void __launch_bounds__(kMoveThreads) gather_tokens_kernel(const RowSr
 // lane keeps eight 16-byte row loads in flight: U column vectors x (8 / U) of the K rows, issued
 // together before the fixed-order FMA chains (U = 8 for top-1 ... U = 1 for K >= 8).  Rows are
 // read once and written once: both streams are marked evict-first.
-template <int U>
-__global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __restrict__ y,
+template <int U, bool ONE>
+__global__ void __launch_bounds__(kMoveThreads, 4) combine_kernel(const uint4* __restrict__ y,
                                                               const int32_t* __restrict__ inv,
                                                               const int32_t* __restrict__ ids, int e_total,
                                                               const float* __restrict__ w, int64_t T, int K,
@@ -102,6 +102,57 @@ __global__ void __launch_bounds__(kMoveThreads) combine_kernel(const uint4* __re
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5); t < T;
        t += nwarps) {
     for (int64_t c0 = lane; c0 < vecs; c0 += 32 * U) {
+      if constexpr (ONE) {
+        // all K slots in one batch (K <= 8 / U): each column vector is reduced and stored as soon
+        // as its loads land, so no U x 8 accumulator array stays live across a runtime k loop (the
+        // top-1 instance: 95 -> 62 registers, four blocks per SM instead of two, enough warps to
+        // cover the HBM latency).  Same fused multiply-adds in the same ascending k order as the
+        // general path.
+        uint4 v[U][kBatch];
+        float wk[kBatch];
+        int row[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          if (b >= K) {
+            row[b] = -1;
+          } else if (inv) {
+            row[b] = __ldg(inv + t * K + b);
+          } else {
+            const int g = __ldg(ids + t * K + b);
+            row[b] = (g >= 0 && g < e_total) ? static_cast<int>(t * K + b) : -1;
+          }
+          wk[b] = (row[b] >= 0 && w) ? __ldg(w + t * K + b) : 1.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            const int64_t c = c0 + 32 * u;
+            v[u][b] = (row[b] >= 0 && c < vecs) ? __ldcs(y + static_cast<int64_t>(row[b]) * vecs + c)
+                                                : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          float acc[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            if (row[b] < 0) continue;
+            const uint32_t p[4] = {v[u][b].x, v[u][b].y, v[u][b].z, v[u][b].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              acc[2 * i] = fmaf(wk[b], bf16_lo(p[i]), acc[2 * i]);
+              acc[2 * i + 1] = fmaf(wk[b], bf16_hi(p[i]), acc[2 * i + 1]);
+            }
+          }
+          const int64_t c = c0 + 32 * u;
+          if (c < vecs)
+            __stcs(out + t * vecs + c, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+        }
+        continue;
+      }
       float acc[U][8];
 #pragma unroll
       for (int u = 0; u < U; ++u)
@@ -541,13 +592,13 @@ static int combine_any(const uint16_t* y, const int32_t* inv, const int32_t* ids
   const uint4* yv = reinterpret_cast<const uint4*>(y);
   uint4* ov = reinterpret_cast<uint4*>(out);
   if (K == 1)
-    combine_kernel<8><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+    combine_kernel<8, true><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else if (K == 2)
-    combine_kernel<4><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+    combine_kernel<4, true><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else if (K <= 4)
-    combine_kernel<2><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
-  else
-    combine_kernel<1><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+    combine_kernel<2, true><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+  else  // one column vector, up to eight rows per batch (64 registers as it is)
+    combine_kernel<1, false><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
