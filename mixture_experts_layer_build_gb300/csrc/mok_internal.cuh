@@ -34,6 +34,18 @@ struct RowDst {               // per-slot rows / values the pushes write ([rows_
   int64_t slots_per;
   int32_t n;
 };
+#ifdef __CUDACC__
+// Entry r of a per-rank table held in a kernel parameter, chosen by an unrolled select: indexing the
+// parameter array with a run-time r makes the compiler copy the whole struct to local memory in
+// every thread.
+template <class P>
+__device__ __forceinline__ P pick_rank(const P (&tab)[kEpMax], int64_t r) {
+  P v = tab[0];
+#pragma unroll
+  for (int i = 1; i < kEpMax; ++i) v = r == i ? tab[i] : v;
+  return v;
+}
+#endif
 // Slot codes of the schedule's inv[] besides a row index: a slot whose expert another rank owns
 // (expert parallelism), and a slot whose id is invalid (outside [0, E) or the group's experts).
 constexpr int32_t kSlotForeign = -1;

@@ -18,7 +18,7 @@ constexpr int kMoveThreads = 256;
 __device__ __forceinline__ const uint16_t* token_row(const RowSrc& src, int64_t t, int64_t H) {
   if (src.n == 0) return src.p[0] + t * H;
   const int64_t r = t / src.rows_per;
-  return src.p[r] + (t - r * src.rows_per) * H;
+  return pick_rank(src.p, r) + (t - r * src.rows_per) * H;
 }
 
 // The dispatch gather in token order: token t's row is read once and written to the rows of its
@@ -238,9 +238,9 @@ __global__ void __launch_bounds__(kMoveThreads) ds_push_kernel(const float* __re
     const float* p = part + static_cast<int64_t>(row) * n_tiles;
     float acc = 0.0f;
     for (int n = 0; n < n_tiles; ++n) acc += p[n];
-    static_cast<float*>(dst.p[r])[j - r * dst.slots_per] = acc;
+    static_cast<float*>(pick_rank(dst.p, r))[j - r * dst.slots_per] = acc;
   } else if (row == kSlotInvalid && r == rank) {
-    static_cast<float*>(dst.p[r])[j - r * dst.slots_per] = 0.0f;
+    static_cast<float*>(pick_rank(dst.p, r))[j - r * dst.slots_per] = 0.0f;
   }
 }
 
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kMoveThreads) push_rows_kernel(const uint4* __
     if (j < 0) continue;  // padding row
     const int64_t r = j / dst.slots_per;
     const uint4* s = src + row * vecs;
-    uint4* d = static_cast<uint4*>(dst.p[r]) + (j - r * dst.slots_per) * vecs;
+    uint4* d = static_cast<uint4*>(pick_rank(dst.p, r)) + (j - r * dst.slots_per) * vecs;
     int64_t c = lane;
     for (; c + 96 < vecs; c += 128) {
       const uint4 v0 = __ldcs(s + c), v1 = __ldcs(s + c + 32), v2 = __ldcs(s + c + 64), v3 = __ldcs(s + c + 96);

@@ -34,7 +34,7 @@ __device__ __forceinline__ int route_id(const RouteSrc& r, int64_t j, int E) {
     return (e < 0 || e >= E) ? kSlotInvalid : e;
   }
   const int64_t s = j / r.slots_per;
-  const int g = __ldg(r.ids[s] + (j - s * r.slots_per));
+  const int g = __ldg(pick_rank(r.ids, s) + (j - s * r.slots_per));
   if (g < 0 || g >= r.e_total) return kSlotInvalid;
   const int e = g - r.e0;
   return (e < 0 || e >= E) ? kSlotForeign : e;
@@ -42,7 +42,7 @@ __device__ __forceinline__ int route_id(const RouteSrc& r, int64_t j, int E) {
 __device__ __forceinline__ float route_w(const RouteSrc& r, int64_t j) {
   if (r.n == 0) return __ldg(r.w[0] + j);
   const int64_t s = j / r.slots_per;
-  return __ldg(r.w[s] + (j - s * r.slots_per));
+  return __ldg(pick_rank(r.w, s) + (j - s * r.slots_per));
 }
 constexpr int kPieces = kSchedChunk / 32;        // 32-slot pieces per chunk
 constexpr int kBatch = 8;                        // pieces whose loads are in flight together
