@@ -15,10 +15,13 @@ constexpr int kMoveThreads = 256;
 
 // Token t's row in the token buffers: one plain buffer, or (expert parallelism) the buffer of the
 // rank holding t, at its row t % rows_per -- a peer's memory when the ranks are separate GPUs.
+// (Token and slot indices fit in 32 bits -- the schedule's tables are int32 -- so the rank is a
+// 32-bit division, not the much longer 64-bit one.)
 __device__ __forceinline__ const uint16_t* token_row(const RowSrc& src, int64_t t, int64_t H) {
   if (src.n == 0) return src.p[0] + t * H;
-  const int64_t r = t / src.rows_per;
-  return pick_rank(src.p, r) + (t - r * src.rows_per) * H;
+  const uint32_t per = static_cast<uint32_t>(src.rows_per);
+  const uint32_t r = static_cast<uint32_t>(t) / per;
+  return pick_rank(src.p, r) + (static_cast<uint32_t>(t) - r * per) * H;
 }
 
 // The dispatch gather in token order: token t's row is read once and written to the rows of its
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kMoveThreads) ds_push_kernel(const float* __re
   const int64_t j = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x;
   if (j >= R) return;
   const int row = inv[j];
-  const int64_t r = j / dst.slots_per;
+  const int64_t r = static_cast<uint32_t>(j) / static_cast<uint32_t>(dst.slots_per);
   if (row >= 0) {
     const float* p = part + static_cast<int64_t>(row) * n_tiles;
     float acc = 0.0f;
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(kMoveThreads) push_rows_kernel(const uint4* __
        row += nwarps) {
     const int64_t j = perm[row];
     if (j < 0) continue;  // padding row
-    const int64_t r = j / dst.slots_per;
+    const int64_t r = static_cast<uint32_t>(j) / static_cast<uint32_t>(dst.slots_per);
     const uint4* s = src + row * vecs;
     uint4* d = static_cast<uint4*>(pick_rank(dst.p, r)) + (j - r * dst.slots_per) * vecs;
     int64_t c = lane;
