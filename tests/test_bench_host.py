@@ -46,3 +46,34 @@ def test_counter_key_ignores_comments_but_not_code(bench):
     assert bench._code_only(src) == bench._code_only(commented)
     assert bench._code_only(src) != bench._code_only(changed)
     assert len(bench.src_hash()) == 16
+
+
+def test_stored_counters_are_found_by_workload_and_kernel_and_dropped_when_the_code_changed(bench, tmp_path,
+                                                                                            monkeypatch):
+    import json
+    path = tmp_path / "traffic.json"
+    h = bench.src_hash()
+    path.write_text(json.dumps({"sweep_zipf1": {"gemm_wgrad_gu": {"dram_bytes_per_launch": 7.6e9, "src_hash": h,
+                                                                   "note": "one pass"}},
+                                "bf16_e64": {"gemm_wgrad_gu": {"dram_bytes_per_launch": 1.2e9,
+                                                               "src_hash": "0000000000000000"}}}))
+    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(path))
+    assert bench.traffic_for("gemm_wgrad_gu", "sweep_zipf1") == (7.6e9, "one pass")
+    assert bench.traffic_for("gemm_wgrad_d", "sweep_zipf1") == (None, "kernel not captured")
+    assert bench.traffic_for("gemm_wgrad_gu", "dsv3_e256") == (None, "kernel not captured")
+    assert bench.traffic_for("gemm_wgrad_gu", "bf16_e64")[0] is None
+    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "absent.json"))
+    assert bench.traffic_for("gemm_wgrad_gu", "sweep_zipf1")[0] is None
+
+
+def test_the_timed_step_keeps_its_workload_name_for_the_counter_lookup():
+    """The per-kernel loop of the timed step once reused the variable holding the workload's name,
+    so the stored counters were looked up under a kernel's name and never found: nothing in the
+    function may rebind it."""
+    import ast
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    fn = next(n for n in ast.walk(tree) if isinstance(n, ast.FunctionDef) and n.name == "ours")
+    assert "name" in [a.arg for a in fn.args.args]
+    rebound = [n.lineno for n in ast.walk(fn) if isinstance(n, ast.Name) and n.id == "name"
+               and isinstance(n.ctx, ast.Store)]
+    assert rebound == []
