@@ -6,6 +6,7 @@
 // expert-grouped layout, and each token's K expert outputs are summed back in ascending k in fp32
 // and rounded once to bf16, so the result does not depend on any scheduling order.
 #include "mok_internal.cuh"
+#include "mok_once.h"
 #include "mok_ptx.cuh"
 
 namespace mok {
@@ -505,30 +506,39 @@ __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src
   }
 }
 
-// Scale atoms: thread t writes line (t % 32) of atom t / 32 of the destination -- rows l, l+32,
-// l+64, l+96 of the atom's 128-row tile, four k-groups each.  blockIdx.y selects the job.
+// Scale atoms.  One block per 128-row slab of a source scale matrix (group g, atom j of the group):
+// the slab's rows (kq 32-bit words each: four k-groups per word) are read with coalesced 4-byte
+// loads into shared memory, then its kq atoms leave as 32 lines of 16 bytes each -- line l of atom
+// q holds word q of rows l, l+32, l+64, l+96, the order tcgen05.cp's 32x128b.warpx4 shape expects.
+// (Reading the four words of a line straight from global memory took 4 bytes from each of 32 rows
+// per load instruction.)  The staged rows are an odd number of words apart, so the column reads of
+// the 32 lanes fall in 32 different banks.  blockIdx.y selects the job.
 struct ScaleJobs {
   ScaleJob j[3];
 };
 __global__ void __launch_bounds__(kMoveThreads) mx_scale_atoms_kernel(const ScaleJobs jobs) {
+  extern __shared__ uint32_t slab_words[];
   const ScaleJob jb = jobs.j[blockIdx.y];
-  const int64_t lines = jb.groups * jb.kq * jb.atoms * 32;
-  const int64_t kg = 4 * static_cast<int64_t>(jb.kq);  // source row length in bytes
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; t < lines; t += stride) {
-    const int l = static_cast<int>(t & 31);
-    const int64_t atom = t >> 5;  // ((g * kq + q) * atoms + j)
-    const int j = static_cast<int>(atom % jb.atoms);
-    const int64_t gq = atom / jb.atoms;
-    const int64_t g = gq / jb.kq;
-    const int64_t q = gq - g * jb.kq;
-    const uint8_t* srcp = (jb.two_src && j) ? jb.src1 : jb.src0;
-    const int64_t row0 = jb.two_src ? g * 128 : (g * jb.atoms + j) * 128;
-    uint32_t wv[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      wv[c] = __ldg(reinterpret_cast<const uint32_t*>(srcp + (row0 + l + 32 * c) * kg + 4 * q));
-    reinterpret_cast<uint4*>(jb.dst)[t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+  const int64_t slab = blockIdx.x;
+  if (slab >= jb.groups * jb.atoms) return;
+  const int64_t g = slab / jb.atoms;
+  const int j = static_cast<int>(slab - g * jb.atoms);
+  const int kq = jb.kq;
+  const int stride = kq % 2 == 0 ? kq + 1 : kq;
+  const uint8_t* srcp = (jb.two_src && j) ? jb.src1 : jb.src0;
+  const int64_t row0 = jb.two_src ? g * 128 : slab * 128;
+  const uint32_t* rows = reinterpret_cast<const uint32_t*>(srcp + row0 * 4 * kq);
+  for (int w = threadIdx.x; w < 128 * kq; w += kMoveThreads) {
+    const int r = w / kq;
+    slab_words[r * stride + (w - r * kq)] = __ldg(rows + w);
+  }
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>(jb.dst);
+  for (int x = threadIdx.x; x < 32 * kq; x += kMoveThreads) {
+    const int q = x >> 5, l = x & 31;
+    const int64_t atom = (g * kq + q) * jb.atoms + j;
+    dst[atom * 32 + l] = make_uint4(slab_words[l * stride + q], slab_words[(l + 32) * stride + q],
+                                    slab_words[(l + 64) * stride + q], slab_words[(l + 96) * stride + q]);
   }
 }
 
@@ -572,17 +582,29 @@ int launch_gather_rows_mx(const RowSrc& src, const int32_t* row_token, const int
 
 int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream) {
   if (njobs <= 0 || njobs > 3) return static_cast<int>(cudaErrorInvalidValue);
+  static DeviceOnce once;  // slabs of wide scale rows need more than the default 48 KB, on each device
+  const int se = once.run([](int* d) { return static_cast<int>(cudaGetDevice(d)); },
+                          [] {
+                            return static_cast<int>(cudaFuncSetAttribute(
+                                mx_scale_atoms_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+                          },
+                          static_cast<int>(cudaErrorInvalidDevice));
+  if (se) return se;
   ScaleJobs p{};
-  int64_t most = 0;
+  int64_t slabs = 0;
+  int kq = 0;
   for (int i = 0; i < njobs; ++i) {
     p.j[i] = jobs[i];
-    const int64_t lines = jobs[i].groups * jobs[i].kq * jobs[i].atoms * 32;
-    most = lines > most ? lines : most;
+    const int64_t n = jobs[i].groups * jobs[i].atoms;
+    slabs = n > slabs ? n : slabs;
+    kq = jobs[i].kq > kq ? jobs[i].kq : kq;
   }
-  if (most <= 0) return 0;
-  const dim3 grid(static_cast<unsigned>(grid_for(most, kMoveThreads)), static_cast<unsigned>(njobs));
+  if (slabs <= 0 || kq <= 0) return 0;
+  const size_t smem = sizeof(uint32_t) * 128 * static_cast<size_t>(kq + 1);
+  if (smem > 227 * 1024 || slabs > 0x7fffffff) return static_cast<int>(cudaErrorInvalidValue);
+  const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(njobs));
   trace_begin(stream, K_MX_SCALE_ATOMS);
-  mx_scale_atoms_kernel<<<grid, kMoveThreads, 0, stream>>>(p);
+  mx_scale_atoms_kernel<<<grid, kMoveThreads, smem, stream>>>(p);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
