@@ -239,7 +239,8 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
                   uint32_t box_outer, int swizzle_bytes) {
   const CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                                      : CU_TENSOR_MAP_SWIZZLE_32B;
+                                : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                      : CU_TENSOR_MAP_SWIZZLE_NONE;
   return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, inner, outer, box_inner, box_outer, sw);
 }
 

@@ -112,21 +112,23 @@ constexpr int kUnitRing = 8;
 template <int VAR, int BN, bool MX, bool PAIR = false, bool SPLIT = false>
 struct GemmCfg {
   static_assert(!MX || BN == 128 || BN == 256, "block-scaled tiles are 128 x 128 or 128 x 256");
-  static_assert(!(MX && PAIR), "block-scaled tiles run on single CTAs");
+  // block-scaled tiles run on single CTAs, except the weight gradients of long experts
+  static_assert(!(MX && PAIR) || VAR == V_WGRAD_GU || VAR == V_WGRAD_D, "block-scaled pairs: weight gradients");
   static constexpr bool kWide = MX && BN == 256;
   // SPLIT (block-scaled DGRAD1 only): eight epilogue warps, two per lane quarter, 64 columns each
   static_assert(!SPLIT || (MX && VAR == V_DGRAD1 && BN == 128), "split epilogue: block-scaled DGRAD1");
   static constexpr bool kSplitEpi = SPLIT;
   static constexpr bool kDg1Mx = MX && VAR == V_DGRAD1;
   static constexpr int kAccBufs = kWide ? 1 : 2;
-  static constexpr int kStages = MX ? (kWide ? 4 : 5) : PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : 6);
+  static constexpr int kStages = MX ? (kWide ? (PAIR ? 6 : 4) : 5) : PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : 6);
   static constexpr int kEpiWarps = kWide || kSplitEpi ? 8 : 4;  // warp w accesses TMEM lane quarter w % 4
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = (PAIR ? BN / 2 : BN) * 128;  // the B rows this CTA holds
   static constexpr uint32_t kSfBytes = MX ? 512 + BN * 4 : 0;  // A atom, then B's BN / 128 atoms
-  // bytes landing per stage (a pair counts both CTAs' loads on the first CTA's barrier)
-  static constexpr uint32_t kTxBytes = (PAIR ? 2 : 1) * (kABytes + kBBytes) + kSfBytes;
+  // bytes landing per stage (a pair counts both CTAs' loads, scale atoms included, on the first
+  // CTA's barrier)
+  static constexpr uint32_t kTxBytes = (PAIR ? 2 : 1) * (kABytes + kBBytes + kSfBytes);
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;           // multiple of 1024: swizzle atoms
   static constexpr uint32_t kTmemCols = MX ? 512 : 2 * BN;
   static constexpr uint32_t kSfCol0 = kAccBufs * BN;
@@ -143,6 +145,7 @@ struct GemmCfg {
   static constexpr uint32_t kScratchOff = kStagingOff + kStagingBytes;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kScratchOff) + kScratchBytes + 512;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(!MX || kSfCol0 + kStages * kSfCols <= kTmemCols, "scale words fit in TMEM");
 };
 
 struct Unit {
@@ -153,7 +156,7 @@ struct Unit {
 // Units of work: one per CTA, or (PAIR) one per CTA pair.
 template <int VAR, bool PAIR>
 __device__ __forceinline__ int gemm_num_units(const GemmArgs& a) {
-  if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) return a.E * a.m_tiles * a.n_tiles;
+  if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) return a.E * (PAIR ? a.m_tiles / 2 : a.m_tiles) * a.n_tiles;
   else return (PAIR ? a.meta[3] : a.meta[2]) * a.n_tiles;
 }
 
@@ -167,20 +170,22 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u, int rank =
   Unit w;
   w.peer_rows = true;
   if constexpr (VAR == V_WGRAD_GU || VAR == V_WGRAD_D) {
-    static_assert(!PAIR, "weight gradients run on single CTAs");
-    const int per_e = a.m_tiles * a.n_tiles;
+    // CTA pairs (block-scaled, long experts): a unit is two consecutive M tiles, one per CTA
+    const int mts = PAIR ? a.m_tiles / 2 : a.m_tiles;
+    const int per_e = mts * a.n_tiles;
     w.e = u / per_e;
     const int r = u - w.e * per_e;
     if (MX && a.m_tiles * kBM <= a.n_tiles * BN) {
       // the smaller operand's tiles fastest: the tiles running together sweep all of its slices,
       // which then stay in L2 while the larger operand streams through once (with the larger one
       // fastest, a long expert's slices of it were re-read from DRAM for every group of tiles)
-      w.nt = r / a.m_tiles;
-      w.mt = r - w.nt * a.m_tiles;
+      w.nt = r / mts;
+      w.mt = r - w.nt * mts;
     } else {
       w.mt = r / a.n_tiles;
       w.nt = r - w.mt * a.n_tiles;
     }
+    if constexpr (PAIR) w.mt = 2 * w.mt + rank;
     const int p0 = __ldg(a.poff + w.e), p1 = __ldg(a.poff + w.e + 1);
     w.row0 = p0;
     w.kblocks = (p1 - p0) / (MX ? 128 : kBK);
@@ -314,6 +319,23 @@ __device__ __forceinline__ void gemm_load_pair(const GemmArgs& a, const Unit& w,
 #pragma unroll
     for (int j = 0; j < HB / 64; ++j) tma_load_2d_pair(sb + j * 8192, tm, bar, w.nt * BN + rank * HB + j * 64, krow);
   }
+}
+
+// CTA pair, block-scaled weight gradients: this CTA's loads of one K block (128 routed rows), all
+// completing on the first CTA's barrier `bar` (shared::cluster address): A = its own 128 M rows, B =
+// its half of the pair's N tile, then the scale atoms -- its A rows' atom, and the atoms of all N
+// rows of B (each CTA's TMEM must hold all of them) -- through pair-form loads over [atoms x 4, 128
+// bytes] views of the atom arrays (tSfa: one atom per box; tSfb: BN / 128 atoms per box).
+template <int BN>
+__device__ __forceinline__ void gemm_load_pair_mx(const GemmArgs& a, const Unit& w, int kb, uint32_t sa, uint32_t sb,
+                                                  uint32_t sf, uint32_t bar, const CUtensorMap* tA,
+                                                  const CUtensorMap* tB, const CUtensorMap* tSfa,
+                                                  const CUtensorMap* tSfb, int rank) {
+  const int k0 = w.row0 + kb * 128;
+  tma_load_2d_pair(sa, tA, bar, k0, w.mt * kBM);
+  tma_load_2d_pair(sb, tB, bar, k0, w.nt * BN + rank * (BN / 2));
+  tma_load_2d_pair(sf, tSfa, bar, 0, (w.mt * a.sf_kq + (k0 >> 7)) * 4);
+  tma_load_2d_pair(sf + 512, tSfb, bar, 0, (w.nt * a.sf_kq + (k0 >> 7)) * 4 * (BN / 128));
 }
 
 // SwiGLU pieces in fp32 with the fast approximate division (about 2 ulp; the results are rounded to
@@ -927,7 +949,11 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR, SPLIT>::kThreads, 1
             break;
           }
           const uint32_t sa = base + stage * C::kStageBytes;
-          if constexpr (PAIR) {
+          if constexpr (PAIR && MX) {  // block-scaled weight gradients (the scale maps ride in B2 and O2)
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::kTxBytes);
+            gemm_load_pair_mx<BN>(args, w, kb, sa, sa + C::kABytes, sf_ring + stage * C::kSfBytes,
+                                  mapa_shared(full_bar(stage), 0), &tmA, &tmB, &tmB2, &tmO2, rank);
+          } else if constexpr (PAIR) {
             if (rank == 0)
               mbar_arrive_expect_tx(full_bar(stage), w.peer_rows ? C::kTxBytes : C::kTxBytes - C::kABytes);
             gemm_load_pair<VAR, BN>(args, w, kb, sa, sa + C::kABytes, mapa_shared(full_bar(stage), 0), &tmA, &tmB,
@@ -1007,14 +1033,25 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR, SPLIT>::kThreads, 1
             // and the MMAs that read them execute in issue order
             const uint32_t sf = sf_ring + stage * C::kSfBytes;
             const uint32_t tsf = tmem_base + C::kSfCol0 + static_cast<uint32_t>(stage) * C::kSfCols;
-            tmem_cp_sf_atom(tsf, sdesc_plain(sf));
+            if constexpr (PAIR) {  // both CTAs' atoms, each into its own TMEM
+              tmem_cp_sf_atom_pair(tsf, sdesc_plain(sf));
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j)  // B row n's word lands in column n / 32
-              tmem_cp_sf_atom(tsf + 4 + 4 * j, sdesc_plain(sf + 512 + 512 * j));
+              for (int j = 0; j < BN / 128; ++j) tmem_cp_sf_atom_pair(tsf + 4 + 4 * j, sdesc_plain(sf + 512 + 512 * j));
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)  // K = 32 e4m3 (32 bytes) per instruction; k-group ks
-              umma_mxf8(d_tmem, sdesc_sw128(sa + ks * 32, 16, 1024), sdesc_sw128(sb + ks * 32, 16, 1024),
-                        idesc_mx(kBM, BN, static_cast<uint32_t>(ks)), (kb | ks) != 0 ? 1u : 0u, tsf, tsf + 4);
+              for (int ks = 0; ks < 4; ++ks)
+                umma_mxf8_pair(d_tmem, sdesc_sw128(sa + ks * 32, 16, 1024), sdesc_sw128(sb + ks * 32, 16, 1024),
+                               idesc_mx(2 * kBM, BN, static_cast<uint32_t>(ks)), (kb | ks) != 0 ? 1u : 0u, tsf,
+                               tsf + 4);
+            } else {
+              tmem_cp_sf_atom(tsf, sdesc_plain(sf));
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j)  // B row n's word lands in column n / 32
+                tmem_cp_sf_atom(tsf + 4 + 4 * j, sdesc_plain(sf + 512 + 512 * j));
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)  // K = 32 e4m3 (32 bytes) per instruction; k-group ks
+                umma_mxf8(d_tmem, sdesc_sw128(sa + ks * 32, 16, 1024), sdesc_sw128(sb + ks * 32, 16, 1024),
+                          idesc_mx(kBM, BN, static_cast<uint32_t>(ks)), (kb | ks) != 0 ? 1u : 0u, tsf, tsf + 4);
+            }
           } else {
 #pragma unroll
             for (int ks = 0; ks < kBK / kUmmaK; ++ks) {
@@ -1124,7 +1161,7 @@ bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
                    uint32_t box_outer);
 bool make_tmap_f32_sw64(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                         uint32_t box_outer);
-// bytes (E4M3 codes); swizzle_bytes 128, 64 or 32
+// bytes (E4M3 codes); swizzle_bytes 128, 64, 32, or 0 for none
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                   uint32_t box_outer, int swizzle_bytes);
 

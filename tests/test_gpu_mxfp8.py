@@ -55,6 +55,10 @@ SMALL = [
     # H above 4096 and a multiple of 256: the four-warp first data-gradient epilogue together with
     # the 128 x 256 tiles of the other GEMMs (the EP64 shard's combination, H = 7168)
     ("long_h_wide", inputs.custom(T=160, H=4352, I=256, E=3, K=2)),
+    # 2,048 routed rows per expert: the weight gradients run on CTA pairs (128 x 256 tiles per CTA;
+    # with H = 384 the gate/up one takes 128-column tiles and the down one stays on single CTAs)
+    ("long_experts", inputs.custom(T=4096, H=256, I=256, E=2, K=1)),
+    ("long_experts_h384", inputs.custom(T=4096, H=384, I=128, E=2, K=1)),
 ]
 
 
