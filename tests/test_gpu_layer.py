@@ -51,6 +51,8 @@ SMALL = [
     ("wide", inputs.custom(T=96, H=1024, I=512, E=6, K=2)),
     # more than 32 slots per token: the token-order gather takes its slot rows 32 at a time
     ("many_slots", inputs.custom(T=48, H=256, I=128, E=48, K=40)),
+    # the most experts the library takes: about two rows each, most padding, 176 experts unused
+    ("max_experts", inputs.custom(T=256, H=128, I=128, E=1024, K=8)),
 ]
 
 

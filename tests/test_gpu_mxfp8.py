@@ -59,6 +59,8 @@ SMALL = [
     # with H = 384 the gate/up one takes 128-column tiles and the down one stays on single CTAs)
     ("long_experts", inputs.custom(T=4096, H=256, I=256, E=2, K=1)),
     ("long_experts_h384", inputs.custom(T=4096, H=384, I=128, E=2, K=1)),
+    # the most experts the library takes: per-expert scale atoms at the limit, most experts short
+    ("max_experts", inputs.custom(T=256, H=128, I=128, E=1024, K=8)),
 ]
 
 
