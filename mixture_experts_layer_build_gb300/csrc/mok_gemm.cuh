@@ -56,6 +56,8 @@ struct GemmArgs {
   const int32_t* tiles;    // minibatch tiles {expert, first row, valid, macro}
   const int32_t* meta;     // meta[2] = number of 128-row blocks
   const int32_t* poff;     // weight-gradient variants: padded expert offsets
+  const int32_t* counts;   // BF16 weight gradients: routed rows per expert (the K loop stops at the
+                           // last 64-row block holding one; the rest of the padding adds only zeros)
   int32_t E, I, H;
   int32_t n_tiles;         // N / BN
   int32_t m_tiles;         // weight-gradient variants: M / 128
@@ -188,7 +190,8 @@ __device__ __forceinline__ Unit gemm_decode(const GemmArgs& a, int u, int rank =
     if constexpr (PAIR) w.mt = 2 * w.mt + rank;
     const int p0 = __ldg(a.poff + w.e), p1 = __ldg(a.poff + w.e + 1);
     w.row0 = p0;
-    w.kblocks = (p1 - p0) / (MX ? 128 : kBK);
+    if constexpr (MX) w.kblocks = (p1 - p0) / 128;  // block-scaled K blocks are the 128-row padding unit
+    else w.kblocks = (__ldg(a.counts + w.e) + kBK - 1) / kBK;
   } else if constexpr (PAIR) {
     const int4 pe = __ldg(a.pairs + u / a.n_tiles);
     const int4 tl = __ldg(reinterpret_cast<const int4*>(a.tiles) + pe.z);

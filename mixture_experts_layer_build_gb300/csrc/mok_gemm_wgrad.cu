@@ -93,6 +93,7 @@ int launch_wgrad_gemms(const Sizes& z, const mok_schedule& s, const Ctx& ctx, co
   CUtensorMap tA, tB, tO0, tO1;
   GemmArgs a{};
   a.poff = s.poff;
+  a.counts = s.counts;
   a.E = z.E;
   a.I = z.I;
   a.H = z.H;
