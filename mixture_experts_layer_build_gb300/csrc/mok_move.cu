@@ -385,6 +385,8 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
 //   along the routed rows: each thread quantises two adjacent columns over one 32-row block
 //     (reading both as one 32-bit word per row) -- 32 consecutive bytes per column of the
 //     transposed copy [H, rcap] the weight-gradient GEMM reads K-major, atoms grouped gT at a time.
+// Both passes keep the values as packed bf16 pairs: the block maxima and the power-of-two scaling
+// take one instruction per two values, and only the final E4M3 conversion widens them to fp32.
 // The scale bytes are collected in shared memory and leave as one 32-bit word per row (its four
 // 32-column blocks) and per column (its four 32-row blocks): in both atom layouts these four
 // bytes are adjacent.
@@ -393,48 +395,91 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
 // multiples of 128.
 constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
 
-// E4M3 codes and scale byte of one 32-value MX block of bf16 values held as packed words, without
-// 32 fp32 registers: MODE 0 / 1 = value i is the low / high half of w[i] (32 words, one column
-// of a staged pair of columns), MODE 2 = values 2i, 2i + 1 are the low, high halves of w[i] (16
-// words along a row).  The same codes and scale as mx_quant32 on the fp32 values: a bf16
-// magnitude's bits order like the value, and its exponent field is the fp32 one.
-template <int MODE, int N>
-__device__ __forceinline__ uint32_t gmx_quant(const uint32_t (&w)[N], uint32_t (&codes)[8]) {
-  static_assert((MODE < 2 && N == 32) || (MODE == 2 && N == 16), "32 values");
-  uint32_t amax = 0;
+// Packed bf16 arithmetic for the quantising gather: two values per 32-bit word, one instruction each.
+// absmax: per 16-bit half the larger magnitude, NaN if either operand is NaN; the sign bits of the
+// result (the XOR of the operands') mean nothing and are masked off at the end.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Per half, a value times a power of two.  Exact while the product is a normal bf16; a product
+// below that is under half of E4M3's smallest subnormal and encodes as a zero of its sign.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Per-half magnitude maxima of N packed words (a pairwise tree), sign bits cleared.
+template <int N>
+__device__ __forceinline__ uint32_t bf16x2_absmax_words(const uint32_t (&w)[N]) {
+  static_assert(N >= 2 && (N & (N - 1)) == 0, "power of two");
+  uint32_t m[N / 2];
 #pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const uint32_t m = MODE == 0 ? w[i] & 0x7FFFu : MODE == 1 ? (w[i] >> 16) & 0x7FFFu
-                                                              : max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu);
-    amax = max(amax, m);
+  for (int i = 0; i < N / 2; ++i) m[i] = bf16x2_absmax(w[i], w[i + N / 2]);
+#pragma unroll
+  for (int s = N / 4; s >= 1; s >>= 1) {
+#pragma unroll
+    for (int i = 0; i < s; ++i) m[i] = bf16x2_absmax(m[i], m[i + s]);
   }
-  if (amax >= 0x7F80u) {  // an Inf or NaN in the block
+  return m[0] & 0x7FFF7FFFu;
+}
+// The shared exponent of a block from its 15-bit bf16 magnitude maximum (finite): floor(log2 amax)
+// - 8, clamped below at -127 (zero and subnormal maxima give -127).  Its bf16 multiplier 2^-shared
+// is the exponent field 127 - shared in [8, 254]: always a normal number.
+__device__ __forceinline__ int gmx_shared(uint32_t amax) {
+  const int s = static_cast<int>(amax >> 7) - 135;
+  return s < -127 ? -127 : s;
+}
+__device__ __forceinline__ uint32_t gmx_mult(int shared) { return static_cast<uint32_t>(127 - shared) << 7; }
+// E4M3 codes of the two bf16 halves of word w (low half in the low byte).
+__device__ __forceinline__ uint32_t e4m3x2_of_bf16x2(uint32_t w) {
+  uint16_t q;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(__uint_as_float(w & 0xFFFF0000u)),
+      "f"(__uint_as_float(w << 16)));
+  return q;
+}
+// Same, for the low halves (COL 0) or the high halves (COL 1) of two words: value of w0, then w1.
+template <int COL>
+__device__ __forceinline__ uint32_t e4m3x2_of_halves(uint32_t w0, uint32_t w1) {
+  uint16_t q;
+  if constexpr (COL == 0)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(__uint_as_float(w1 << 16)),
+        "f"(__uint_as_float(w0 << 16)));
+  else
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(__uint_as_float(w1 & 0xFFFF0000u)),
+        "f"(__uint_as_float(w0 & 0xFFFF0000u)));
+  return q;
+}
+// 32 bytes to global memory in one instruction, streaming (p 32-byte aligned).
+__device__ __forceinline__ void st_cs_32B(void* p, const uint32_t (&c)[8]) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(c[0]), "r"(c[1]),
+               "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(c[5]), "r"(c[6]), "r"(c[7])
+               : "memory");
+}
+
+// One 32-value block along a row, held as 16 packed words (values 2i, 2i + 1 = low, high half of
+// w[i]); w is scaled in place.  Returns the scale byte.  The codes and the byte are those of
+// mx_quant32 on the same values: a bf16 magnitude's bits order like the value, its exponent field is
+// the fp32 one, and scaling by a power of two is exact (see bf16x2_mul).
+__device__ __forceinline__ uint32_t gmx_quant_row(uint32_t (&w)[16], uint32_t (&codes)[8]) {
+  uint32_t m = bf16x2_absmax_words(w);
+  m = bf16x2_absmax(m, m >> 16) & 0x7FFFu;
+  if (m >= 0x7F80u) {  // an Inf or NaN in the block
 #pragma unroll
     for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
     return 0xFFu;
   }
-  int shared = static_cast<int>(amax >> 7) - 127 - 8;
-  shared = shared < -127 ? -127 : shared;
-  const float dn = pow2f(-shared);
+  const int shared = gmx_shared(m);
+  const uint32_t dn2 = gmx_mult(shared) * 0x10001u;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {  // values 2i, 2i + 1
-    float v0, v1;
-    if constexpr (MODE == 2) {
-      v0 = __uint_as_float(w[i] << 16);
-      v1 = __uint_as_float(w[i] & 0xFFFF0000u);
-    } else {
-      v0 = MODE ? __uint_as_float(w[2 * i] & 0xFFFF0000u) : __uint_as_float(w[2 * i] << 16);
-      v1 = MODE ? __uint_as_float(w[2 * i + 1] & 0xFFFF0000u) : __uint_as_float(w[2 * i + 1] << 16);
-    }
-    uint16_t q;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(v1 * dn), "f"(v0 * dn));
-    if (i & 1) codes[i >> 1] |= static_cast<uint32_t>(q) << 16;
-    else codes[i >> 1] = q;
-  }
+  for (int i = 0; i < 16; ++i) w[i] = bf16x2_mul(w[i], dn2);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) codes[i] = e4m3x2_of_bf16x2(w[2 * i]) | (e4m3x2_of_bf16x2(w[2 * i + 1]) << 16);
   return static_cast<uint32_t>(shared + 127);
 }
 
-// Five CTAs per SM (48 registers; the packed-word quantisation keeps that free of spills).
+// Five CTAs per SM (48 registers or fewer, no spills).
 __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src,
                                                             const int32_t* __restrict__ row_token,
                                                             const int32_t* __restrict__ meta, int32_t H,
@@ -463,8 +508,10 @@ __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {  // along H: row it / 4, columns c0 + 32 (it % 4) ... + 31
-    const int it = t + 256 * k, r = it / 4, b = it % 4;
+  for (int k = 0; k < 2; ++k) {
+    // along H: a warp takes 8 rows x the 4 blocks of 32 columns, the 8 lanes of a quarter warp 8
+    // rows of one block (their 16-byte reads fall in 8 different bank groups)
+    const int it = t + 256 * k, r = 8 * (it >> 5) + (it & 7), b = (it & 31) >> 3;
     uint32_t wr[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -472,25 +519,36 @@ __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src
       wr[4 * i] = v.x, wr[4 * i + 1] = v.y, wr[4 * i + 2] = v.z, wr[4 * i + 3] = v.w;
     }
     uint32_t codes[8];
-    sc_row[4 * r + b] = static_cast<uint8_t>(gmx_quant<2>(wr, codes));
-    uint4* dq = reinterpret_cast<uint4*>(dst_q + (r0 + r) * H + c0 + 32 * b);
-    __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-    __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+    sc_row[4 * r + b] = static_cast<uint8_t>(gmx_quant_row(wr, codes));
+    st_cs_32B(dst_q + (r0 + r) * H + c0 + 32 * b, codes);
   }
-  {  // along the rows: columns c0 + 2 (t % 64) and the next one, row block t / 64
+  {  // along the rows: columns c0 + 2 (t % 64) and the next one (the low and high halves of each
+     // staged word), row block t / 64; both columns' maxima and scaling share the packed words
     const int cp = t % 64, rb = t / 64;
     uint32_t w2[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r)
       w2[r] = *reinterpret_cast<const uint32_t*>(tile + (32 * rb + r) * kGmxStride + 4 * cp);
+    const uint32_t m = bf16x2_absmax_words(w2);
+    const uint32_t m0 = m & 0xFFFFu, m1 = m >> 16;
+    const int s0 = gmx_shared(m0), s1 = gmx_shared(m1);
+    const uint32_t dn2 = gmx_mult(s0) | (gmx_mult(s1) << 16);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) w2[r] = bf16x2_mul(w2[r], dn2);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       uint32_t codes[8];
-      const uint32_t sb = j ? gmx_quant<1>(w2, codes) : gmx_quant<0>(w2, codes);
-      sc_col[4 * (2 * cp + j) + rb] = static_cast<uint8_t>(sb);
-      uint4* dq = reinterpret_cast<uint4*>(dstR_q + static_cast<int64_t>(c0 + 2 * cp + j) * rcap + r0 + 32 * rb);
-      __stcs(dq, make_uint4(codes[0], codes[1], codes[2], codes[3]));
-      __stcs(dq + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+      const bool bad = (j ? m1 : m0) >= 0x7F80u;  // an Inf or NaN in this column's block
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = j ? e4m3x2_of_halves<1>(w2[4 * i], w2[4 * i + 1])
+                              : e4m3x2_of_halves<0>(w2[4 * i], w2[4 * i + 1]);
+        const uint32_t hi = j ? e4m3x2_of_halves<1>(w2[4 * i + 2], w2[4 * i + 3])
+                              : e4m3x2_of_halves<0>(w2[4 * i + 2], w2[4 * i + 3]);
+        codes[i] = bad ? 0x7F7F7F7Fu : lo | (hi << 16);
+      }
+      sc_col[4 * (2 * cp + j) + rb] = static_cast<uint8_t>(bad ? 0xFFu : (j ? s1 : s0) + 127);
+      st_cs_32B(dstR_q + static_cast<int64_t>(c0 + 2 * cp + j) * rcap + r0 + 32 * rb, codes);
     }
   }
   __syncthreads();

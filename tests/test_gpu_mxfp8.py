@@ -168,6 +168,23 @@ def test_mxfp8_gather_quantises_x_bit_exactly(mok):
     x[3] = x[3] * 1e-30  # tiny block exponents
     x[4] = x[4] * 1e30   # large ones
     x[5, :64] = 0        # zero blocks
+    # bit patterns: every finite class at random (subnormals, both signs, every exponent); blocks of
+    # bf16 subnormals and tiny normals only (scaled up by 2^127); Inf and NaN blocks; blocks whose
+    # small values underflow after scaling and must keep their sign (E4M3 -0 is 0x80)
+    rng = np.random.default_rng(11)
+    xb = x.view(torch.int16).numpy()
+    pat = rng.integers(0, 1 << 16, size=w.H, dtype=np.uint32)
+    pat = np.where((pat & 0x7F80) == 0x7F80, pat & 0xBFFF, pat)
+    xb[6] = pat.astype(np.uint16).view(np.int16)
+    tiny = (rng.integers(0, 3, size=w.H) << 7) | rng.integers(0, 128, size=w.H) | (rng.integers(0, 2, size=w.H) << 15)
+    xb[7] = tiny.astype(np.uint16).view(np.int16)
+    row8 = np.full(w.H, 0x3F80, np.uint16)
+    row8[5], row8[40], row8[70], row8[100] = 0x7F80, 0x7FC1, 0xFF80, 0xFFFF  # +Inf, NaN, -Inf, -NaN
+    xb[8] = row8.view(np.int16)
+    row9 = np.full(w.H, 0x8001, np.uint16)  # -(smallest subnormal)
+    row9[::32] = 0x7100                      # about 6.3e29: the block's maximum
+    row9[1::32] = 0xB000                     # -4.7e-10
+    xb[9] = row9.view(np.int16)
     d["x"] = x
     mx_gpu = _mx_inputs(mok, d)
     cfg = mok.make_config(128, 256, precision=mok.MOK_MXFP8)
