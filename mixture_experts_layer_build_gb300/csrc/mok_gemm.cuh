@@ -898,6 +898,8 @@ __global__ void __launch_bounds__(GemmCfg<VAR, BN, MX, PAIR, SPLIT>::kThreads, 1
   tc_fence_before();
   if constexpr (PAIR) cluster_sync();  // the peer's barriers are initialised before any remote arrive
   else __syncthreads();
+  // the set-up above touches no global memory; from here on the producers' results are needed
+  pdl_wait();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_units = gemm_num_units<VAR, PAIR>(args);
@@ -1214,13 +1216,15 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel calls pdl_wait()
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;
+  cfg.numAttrs = PAIR ? 2 : 1;
   const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_kernel<VAR, BN, MX, PAIR, SPLIT>, a, b, b2, o0, o1, o2, args);
   trace_end(stream);
   return le != cudaSuccess ? static_cast<int>(le) : static_cast<int>(cudaGetLastError());

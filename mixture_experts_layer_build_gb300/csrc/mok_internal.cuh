@@ -154,6 +154,25 @@ enum KernelKind : int {
 void trace_begin(cudaStream_t s, int kind);  // no-ops unless a trace is set
 void trace_end(cudaStream_t s);
 
+// A kernel launch with programmatic stream serialisation: the grid may start launching as the
+// previous kernel's last CTAs exit.  Only for kernels that begin with pdl_wait() (mok_ptx.cuh), so
+// nothing they read or write is touched before their producer has completed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // launchers (return a cudaError_t as int)
 int launch_schedule(const Sizes& z, const RouteSrc& route, const mok_schedule& s, const Staging& st,
                     cudaStream_t stream);

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kMoveThreads) gather_tokens_kernel(const RowSr
                                                                     const int32_t* __restrict__ row_token,
                                                                     const int32_t* __restrict__ meta, int64_t T,
                                                                     int K, int64_t vecs, uint4* __restrict__ dst) {
+  pdl_wait();
   constexpr int64_t kChunk = 32 * U;
   const int lane = threadIdx.x & 31;
   const int64_t warp = static_cast<int64_t>(blockIdx.x) * (kMoveThreads / 32) + (threadIdx.x >> 5);
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(kMoveThreads, 4) combine_kernel(const uint4* _
                                                               const int32_t* __restrict__ ids, int e_total,
                                                               const float* __restrict__ w, int64_t T, int K,
                                                               int64_t vecs, uint4* __restrict__ out) {
+  pdl_wait();
   constexpr int kBatch = 8 / U;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(kMoveThreads, 4) combine_kernel(const uint4* _
 __global__ void __launch_bounds__(kMoveThreads) ds_reduce_kernel(const float* __restrict__ part,
                                                                 const int32_t* __restrict__ inv, int64_t R,
                                                                 int n_tiles, float* __restrict__ ds) {
+  pdl_wait();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x;
   if (j >= R) return;
   const int row = inv[j];
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(kMoveThreads) ds_reduce_kernel(const float* __
 __global__ void __launch_bounds__(kMoveThreads) ds_push_kernel(const float* __restrict__ part,
                                                               const int32_t* __restrict__ inv, int64_t R,
                                                               int n_tiles, const RowDst dst, int rank) {
+  pdl_wait();
   const int64_t j = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x;
   if (j >= R) return;
   const int row = inv[j];
@@ -255,6 +259,7 @@ __global__ void __launch_bounds__(kMoveThreads) push_rows_kernel(const uint4* __
                                                                 const int32_t* __restrict__ perm,
                                                                 const int32_t* __restrict__ meta, int64_t vecs,
                                                                 const RowDst dst) {
+  pdl_wait();
   const int64_t rpad = meta[0];
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kMoveThreads / 32);
@@ -334,6 +339,7 @@ __device__ __forceinline__ uint32_t e4m3_code(uint32_t mag, int shared) {
 __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint4* __restrict__ in,
                                                                      int64_t nblocks, uint4* __restrict__ q,
                                                                      uint8_t* __restrict__ sc) {
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; b < nblocks; b += stride) {
     uint32_t w[16];
@@ -486,6 +492,7 @@ __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src
                                                             uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf,
                                                             uint8_t* __restrict__ dstR_q,
                                                             uint8_t* __restrict__ dstR_sf, int64_t rcap, int gT) {
+  pdl_wait();
   __shared__ __align__(16) uint8_t tile[128 * kGmxStride];
   __shared__ __align__(4) uint8_t sc_row[128 * 4];  // [row][32-column block]
   __shared__ __align__(4) uint8_t sc_col[128 * 4];  // [column][32-row block]
@@ -575,6 +582,7 @@ struct ScaleJobs {
   ScaleJob j[3];
 };
 __global__ void __launch_bounds__(kMoveThreads) mx_scale_atoms_kernel(const ScaleJobs jobs) {
+  pdl_wait();
   extern __shared__ uint32_t slab_words[];
   const ScaleJob jb = jobs.j[blockIdx.y];
   const int64_t slab = blockIdx.x;
@@ -617,9 +625,9 @@ int launch_gather_rows(const RowSrc& src, const int32_t* inv, const int32_t* row
   trace_begin(stream, kind);
   uint4* d = reinterpret_cast<uint4*>(dst);
   if (vecs >= 32 * 4)
-    gather_tokens_kernel<4><<<grid, kMoveThreads, 0, stream>>>(src, inv, row_token, meta, T, K, vecs, d);
+    launch_pdl(gather_tokens_kernel<4>, dim3(grid), dim3(kMoveThreads), 0, stream, src, inv, row_token, meta, T, K, vecs, d);
   else
-    gather_tokens_kernel<1><<<grid, kMoveThreads, 0, stream>>>(src, inv, row_token, meta, T, K, vecs, d);
+    launch_pdl(gather_tokens_kernel<1>, dim3(grid), dim3(kMoveThreads), 0, stream, src, inv, row_token, meta, T, K, vecs, d);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
@@ -633,7 +641,7 @@ int launch_gather_rows_mx(const RowSrc& src, const int32_t* row_token, const int
   if ((rpad_max + 127) / 128 > 65535) return static_cast<int>(cudaErrorInvalidValue);
   const dim3 grid(static_cast<unsigned>(H / 128), static_cast<unsigned>((rpad_max + 127) / 128));
   trace_begin(stream, kind);
-  gather_rows_mx_kernel<<<grid, 256, 0, stream>>>(src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
+  launch_pdl(gather_rows_mx_kernel, dim3(grid), dim3(256), 0, stream, src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
@@ -662,7 +670,7 @@ int launch_mx_scale_atoms(const ScaleJob* jobs, int njobs, cudaStream_t stream) 
   if (smem > 227 * 1024 || slabs > 0x7fffffff) return static_cast<int>(cudaErrorInvalidValue);
   const dim3 grid(static_cast<unsigned>(slabs), static_cast<unsigned>(njobs));
   trace_begin(stream, K_MX_SCALE_ATOMS);
-  mx_scale_atoms_kernel<<<grid, kMoveThreads, smem, stream>>>(p);
+  launch_pdl(mx_scale_atoms_kernel, dim3(grid), dim3(kMoveThreads), smem, stream, p);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
@@ -675,13 +683,13 @@ static int combine_any(const uint16_t* y, const int32_t* inv, const int32_t* ids
   const uint4* yv = reinterpret_cast<const uint4*>(y);
   uint4* ov = reinterpret_cast<uint4*>(out);
   if (K == 1)
-    combine_kernel<8, true><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+    launch_pdl(combine_kernel<8, true>, dim3(grid), dim3(kMoveThreads), 0, stream, yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else if (K == 2)
-    combine_kernel<4, true><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+    launch_pdl(combine_kernel<4, true>, dim3(grid), dim3(kMoveThreads), 0, stream, yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else if (K <= 4)
-    combine_kernel<2, true><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+    launch_pdl(combine_kernel<2, true>, dim3(grid), dim3(kMoveThreads), 0, stream, yv, inv, ids, e_total, s, T, K, H / 8, ov);
   else  // one column vector, up to eight rows per batch (64 registers as it is)
-    combine_kernel<1, false><<<grid, kMoveThreads, 0, stream>>>(yv, inv, ids, e_total, s, T, K, H / 8, ov);
+    launch_pdl(combine_kernel<1, false>, dim3(grid), dim3(kMoveThreads), 0, stream, yv, inv, ids, e_total, s, T, K, H / 8, ov);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
@@ -701,7 +709,7 @@ int launch_push_rows(const uint16_t* src, const int32_t* perm, const int32_t* me
   if (rpad_max <= 0) return 0;
   const int grid = grid_for(rpad_max, kMoveThreads / 32);
   trace_begin(stream, kind);
-  push_rows_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(src), perm, meta, H / 8, dst);
+  launch_pdl(push_rows_kernel, dim3(grid), dim3(kMoveThreads), 0, stream, reinterpret_cast<const uint4*>(src), perm, meta, H / 8, dst);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
@@ -711,7 +719,7 @@ int launch_ds_push(const float* part, const int32_t* inv, int64_t R, int32_t n_t
   if (R <= 0) return 0;
   const int grid = static_cast<int>((R + kMoveThreads - 1) / kMoveThreads);
   trace_begin(stream, K_DS_PUSH);
-  ds_push_kernel<<<grid, kMoveThreads, 0, stream>>>(part, inv, R, n_tiles, dst, rank);
+  launch_pdl(ds_push_kernel, dim3(grid), dim3(kMoveThreads), 0, stream, part, inv, R, n_tiles, dst, rank);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
@@ -721,7 +729,7 @@ int launch_ds_reduce(const float* part, const int32_t* inv, int64_t R, int32_t n
   if (R <= 0) return 0;
   const int grid = static_cast<int>((R + kMoveThreads - 1) / kMoveThreads);
   trace_begin(stream, K_DS_REDUCE);
-  ds_reduce_kernel<<<grid, kMoveThreads, 0, stream>>>(part, inv, R, n_tiles, ds);
+  launch_pdl(ds_reduce_kernel, dim3(grid), dim3(kMoveThreads), 0, stream, part, inv, R, n_tiles, ds);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
@@ -732,7 +740,7 @@ int launch_mxfp8_quantize(const uint16_t* in, int64_t rows, int64_t cols, uint8_
   if (nblocks <= 0) return 0;
   const int grid = grid_for(nblocks, kMoveThreads);
   trace_begin(stream, K_MXFP8_QUANTIZE);
-  mxfp8_quantize_kernel<<<grid, kMoveThreads, 0, stream>>>(reinterpret_cast<const uint4*>(in), nblocks,
+  launch_pdl(mxfp8_quantize_kernel, dim3(grid), dim3(kMoveThreads), 0, stream, reinterpret_cast<const uint4*>(in), nblocks,
                                                            reinterpret_cast<uint4*>(q), sc);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());

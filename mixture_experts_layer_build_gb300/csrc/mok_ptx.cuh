@@ -26,6 +26,14 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  Every kernel of the layer step starts with pdl_wait() and is
+// launched with programmatic stream serialisation, so its CTAs may start launching as the previous
+// kernel's last CTAs exit, before that grid's completion has been processed; pdl_wait() then holds
+// them until the previous grid has completed and its memory is visible (it returns at once when
+// there is no such dependency).  No kernel signals its dependents earlier than its exit: CTAs
+// launched ahead of time to wait on an SM slowed the graph-replayed step.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Deadline of any single wait inside a kernel (ns).  Legitimate waits last microseconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
                                                             const uint16_t* __restrict__ w,
                                                             const float* __restrict__ bias, int64_t T, int H, int E,
                                                             float* __restrict__ logits) {
+  pdl_wait();
   __shared__ __align__(16) float xs[kLgTokens][kLgChunk + 4];
   __shared__ __align__(16) float ws[kLgChunk][kLgExperts];
   const int tid = threadIdx.x;
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(128) router_logits_kernel(const uint16_t* __re
 // weights are the softmax over the K chosen logits (the full softmax renormalised to the top K).
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int K,
                                                           int32_t* __restrict__ ids, float* __restrict__ wts) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (t >= T) return;  // whole warp
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 // wt[e, h] = w[h, e] (32 x 32 tiles through shared memory).
 __global__ void __launch_bounds__(256) router_transpose_kernel(const uint16_t* __restrict__ w, int H, int E,
                                                                uint16_t* __restrict__ wt) {
+  pdl_wait();
   __shared__ uint16_t tile[32][33];
   const int e0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += 8) {
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t* __restric
                                                         const uint16_t* __restrict__ wt, int64_t T, int H, int E,
                                                         int K, float* __restrict__ gbuf, uint16_t* __restrict__ dx,
                                                         int accumulate) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   if (t >= T) return;  // whole warp
@@ -281,6 +285,7 @@ __global__ void __launch_bounds__(256 * P) router_dw_kernel(const uint16_t* __re
                                                         const int32_t* __restrict__ poff,
                                                         const int32_t* __restrict__ perm, int H, int E, int K,
                                                         float* __restrict__ dw, float* __restrict__ db) {
+  pdl_wait();
   static_assert(P == 1 || P == 2, "one or two row parts");
   __shared__ int64_t s_tok[P][kDwRows];
   __shared__ float s_g[P][kDwRows];
@@ -359,12 +364,12 @@ extern "C" MOK_API mok_status mok_router_forward(const mok_shape* s, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dim3 g1((s->E + kLgExperts - 1) / kLgExperts, static_cast<unsigned>((s->T + kLgTokens - 1) / kLgTokens));
   trace_begin(st, K_ROUTER_LOGITS);
-  router_logits_kernel<<<g1, 128, 0, st>>>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w_router),
+  launch_pdl(router_logits_kernel, dim3(g1), dim3(128), 0, st, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(w_router),
                                            bias, s->T, s->H, s->E, logits);
   trace_end(st);
   trace_begin(st, K_ROUTER_TOPK);
-  router_topk_kernel<<<static_cast<unsigned>((s->T + 7) / 8), 256, 0, st>>>(logits, s->T, s->E, s->K, topk_ids,
-                                                                           topk_weights);
+  launch_pdl(router_topk_kernel, dim3(static_cast<unsigned>((s->T + 7) / 8)), dim3(256), 0, st, logits, s->T, s->E,
+             s->K, topk_ids, topk_weights);
   trace_end(st);
   return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
 }
@@ -388,22 +393,21 @@ extern "C" MOK_API mok_status mok_router_backward(const mok_schedule* sched, con
   float* gbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + align256(static_cast<size_t>(s.E) * s.H * 2));
   const dim3 gt((s.E + 31) / 32, (s.H + 31) / 32);
   trace_begin(st, K_ROUTER_TRANSPOSE);
-  router_transpose_kernel<<<gt, dim3(32, 8), 0, st>>>(static_cast<const uint16_t*>(w_router), s.H, s.E, wt);
+  launch_pdl(router_transpose_kernel, dim3(gt), dim3(32, 8), 0, st, static_cast<const uint16_t*>(w_router), s.H, s.E, wt);
   trace_end(st);
   if (s.T > 0) {
     trace_begin(st, K_ROUTER_DX);
-    router_dx_kernel<<<static_cast<unsigned>((s.T + 7) / 8), 256, 0, st>>>(
-        topk_ids, topk_weights, d_topk_weights, wt, s.T, s.H, s.E, s.K, gbuf, static_cast<uint16_t*>(dx),
-        accumulate_dx);
+    launch_pdl(router_dx_kernel, dim3(static_cast<unsigned>((s.T + 7) / 8)), dim3(256), 0, st, topk_ids, topk_weights,
+               d_topk_weights, wt, s.T, s.H, s.E, s.K, gbuf, static_cast<uint16_t*>(dx), accumulate_dx);
     trace_end(st);
   }
   const dim3 gw(s.E, (s.H + 511) / 512);
   trace_begin(st, K_ROUTER_DW);
   if (static_cast<int64_t>(gw.x) * gw.y < 2 * static_cast<int64_t>(sm_count()))  // small grid: two row parts
-    router_dw_kernel<2><<<gw, 512, 0, st>>>(static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
+    launch_pdl(router_dw_kernel<2>, dim3(gw), dim3(512), 0, st, static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
                                             sched->perm, s.H, s.E, s.K, dw_router, d_bias);
   else
-    router_dw_kernel<1><<<gw, 256, 0, st>>>(static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
+    launch_pdl(router_dw_kernel<1>, dim3(gw), dim3(256), 0, st, static_cast<const uint16_t*>(x), gbuf, sched->counts, sched->poff,
                                             sched->perm, s.H, s.E, s.K, dw_router, d_bias);
   trace_end(st);
   return cudaGetLastError() == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;

@@ -50,6 +50,7 @@ constexpr int kBatch = 8;                        // pieces whose loads are in fl
 __global__ void __launch_bounds__(kHistWarps * 32) sched_hist_kernel(const RouteSrc route, int64_t R, int E,
                                                                     int64_t nchunks,
                                                                     int32_t* __restrict__ chunk_hist) {
+  pdl_wait();
   extern __shared__ int32_t sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kHistWarps + warp;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(int E, int64_t nchunks
                                                          float* __restrict__ row_weight, int32_t* __restrict__ tiles,
                                                          int32_t* __restrict__ mblocks, int32_t* __restrict__ meta,
                                                          int4* __restrict__ pairs) {
+  pdl_wait();
   extern __shared__ int32_t part[];  // [32 chunk groups][E + 1]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int W = E + 1;
@@ -240,6 +242,7 @@ __global__ void __launch_bounds__(kHistWarps * 32) sched_scatter_kernel(
     const RouteSrc route, int64_t R, int K, int E, int64_t nchunks,
     const int32_t* __restrict__ chunk_first, const int32_t* __restrict__ meta, int32_t* __restrict__ perm,
     int32_t* __restrict__ inv, int32_t* __restrict__ row_token, float* __restrict__ row_weight) {
+  pdl_wait();
   extern __shared__ int32_t sh[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t chunk = static_cast<int64_t>(blockIdx.x) * kHistWarps + warp;
@@ -305,18 +308,18 @@ int launch_schedule(const Sizes& z, const RouteSrc& route, const mok_schedule& s
   if (blocks > 0) {
     const size_t sh = sizeof(int32_t) * kHistWarps * (z.E + 1);
     trace_begin(stream, K_SCHED_HIST);
-    sched_hist_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(route, z.R, z.E, nchunks, st.chunk_hist);
+    launch_pdl(sched_hist_kernel, dim3(blocks), dim3(kHistWarps * 32), sh, stream, route, z.R, z.E, nchunks, st.chunk_hist);
     trace_end(stream);
   }
   trace_begin(stream, K_SCHED_SCAN);
-  sched_scan_kernel<<<1, 1024, sizeof(int32_t) * 32 * (z.E + 1), stream>>>(
+  launch_pdl(sched_scan_kernel, dim3(1), dim3(1024), sizeof(int32_t) * 32 * (z.E + 1), stream, 
       z.E, nchunks, st.chunk_hist, z.mb, z.MB, z.rpad_max, z.tiles_max, z.mblocks_max, s.counts, s.offsets, s.poff,
       s.perm, s.row_token, s.row_weight, s.tiles, s.mblocks, s.meta, st.pairs);
   trace_end(stream);
   if (blocks > 0) {
     const size_t sh = sizeof(int32_t) * kHistWarps * z.E;
     trace_begin(stream, K_SCHED_SCATTER);
-    sched_scatter_kernel<<<blocks, kHistWarps * 32, sh, stream>>>(route, z.R, z.K, z.E, nchunks, st.chunk_hist,
+    launch_pdl(sched_scatter_kernel, dim3(blocks), dim3(kHistWarps * 32), sh, stream, route, z.R, z.K, z.E, nchunks, st.chunk_hist,
                                                                    s.meta, s.perm, s.inv, s.row_token, s.row_weight);
     trace_end(stream);
   }
