@@ -483,6 +483,38 @@ def time_router(args, mok, w, d, cfg, dev, stream, peaks) -> dict:
     return res
 
 
+def time_quantize(args, mok, Wg, Wu, Wd, stream, peaks) -> dict:
+    """mok_mxfp8_quantize on the forward weight copies (Wg, Wu along H; Wd along I), the call a
+    training loop makes after each optimiser step: CUDA events around K sets of the three calls
+    after W warm-ups, outputs preallocated.  Each element moves 2 bytes in and 1 + 1/32 out."""
+    mats = [Wg.reshape(-1, Wg.shape[-1]), Wu.reshape(-1, Wu.shape[-1]), Wd.reshape(-1, Wd.shape[-1])]
+    outs = [(torch.empty(m.shape, dtype=torch.uint8, device=m.device),
+             torch.empty((m.shape[0], m.shape[1] // 32), dtype=torch.uint8, device=m.device)) for m in mats]
+
+    def one():
+        for m, (q, sc) in zip(mats, outs):
+            mok.mok_mxfp8_quantize(m, q, sc, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    n = sum(m.numel() for m in mats)
+    nbytes = n * (2 + 1 + 1 / 32)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "mxfp8_quantize", "ms_per_set": ms, "elements": n, "bytes": nbytes, "gbs": gbs,
+            "bound": "hbm", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+            "what": "the three forward weight copies (Wg, Wu along H; Wd along I), inputs larger than L2"}
+
+
 def ours(args, rank, ws, local_rank, name, with_router=True):
     """Every measurement of one workload: the step from a CUDA graph and eagerly, the per-kernel
     event trace and roofline, the router step (workloads with a softmax router), and e2e through
@@ -594,6 +626,8 @@ def ours(args, rank, ws, local_rank, name, with_router=True):
 
     # ---- the router step before the layer (timed on its own; not part of the layer step) ----
     router = time_router(args, mok, w, d, cfg, dev, stream, peaks) if with_router and "Wr" in d else None
+    # ---- the weight quantiser (MXFP8; outside the layer step, like the router) ----
+    quant = time_quantize(args, mok, Wg.to(dev), Wu.to(dev), Wd.to(dev), stream, peaks) if mxfp8 else None
 
     # ---- end to end through the C ABI with host buffers ----
     # Every step copies its own inputs host->device and its results device->host inside the timed
@@ -698,6 +732,8 @@ def ours(args, rank, ws, local_rank, name, with_router=True):
         }
         if router is not None:
             result["router"] = router
+        if quant is not None:
+            result["quantize"] = quant
     return result, d, w
 
 
@@ -713,7 +749,7 @@ def parse_extra(spec: str):
 
 # keys of a further workload's object (its full kernel table stays on the headline only)
 EXTRA_KEYS = ("metric", "value", "unit", "ms_per_step", "dtype", "config", "tflops", "roofline", "e2e",
-              "gpu_launches", "launches_per_step", "clocks", "device_status", "step")
+              "gpu_launches", "launches_per_step", "clocks", "device_status", "step", "quantize")
 
 
 def main():

@@ -284,124 +284,13 @@ __global__ void __launch_bounds__(kMoveThreads) push_rows_kernel(const uint4* __
 
 // ---------------------------------------------------------------------------------------------
 // MXFP8: E4M3 elements with one E8M0 scale per 32 consecutive values ("Mixture-of-Kittens (MoK)"
-// project card, "Key concepts": ops.mxfp8_quantize).  Integer arithmetic on the bf16 bit pattern:
-// |v| = M * 2^X exactly (M < 256), so every rounding decision below is exact.
+// project card, "Key concepts": ops.mxfp8_quantize).  Per block: amax = max |v|; shared =
+// floor(log2 amax) - 8 (8 = the exponent of E4M3's largest normal), clamped below at -127; each
+// element is v * 2^-shared rounded to nearest even on the E4M3 grid, saturating at 448; a block
+// holding Inf or NaN gets scale byte 0xFF and every code 0x7F.
 // ---------------------------------------------------------------------------------------------
 
-// floor(log2 |v|) of a finite nonzero bf16 magnitude (15 bits).
-__device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
-  const uint32_t eb = mag >> 7, m = mag & 0x7Fu;
-  if (eb != 0) return static_cast<int>(eb) - 127;
-  return (31 - __clz(m)) - 133;  // subnormal: m * 2^-133
-}
-
-// E4M3 code (without sign) of |v| * 2^-shared, round to nearest even, saturating at 448.
-__device__ __forceinline__ uint32_t e4m3_code(uint32_t mag, int shared) {
-  const uint32_t eb = mag >> 7, mf = mag & 0x7Fu;
-  if (eb == 0 && mf == 0) return 0;
-  uint32_t M;
-  int X;
-  if (eb != 0) {
-    M = 0x80u | mf;
-    X = static_cast<int>(eb) - 134;
-  } else {
-    M = mf;
-    X = -133;
-  }
-  const int Y = X - shared;                          // value = M * 2^Y
-  const int p = 31 - __clz(M);                       // leading bit of M
-  const int Ep = p + Y;                              // unbiased exponent of the value
-  const int qe = (Ep > -6 ? Ep : -6) - 3;            // quantum: 2^qe (subnormal quantum 2^-9)
-  const int d = qe - Y;                              // right shift of M onto the quantum grid
-  uint32_t n;
-  if (d <= 0) {
-    n = M << (-d);                                   // exact (d >= -7 here)
-  } else if (d > 20) {
-    n = 0;                                           // far below half a quantum
-  } else {
-    n = M >> d;
-    const uint32_t rem = M & ((1u << d) - 1u), half = 1u << (d - 1);
-    if (rem > half || (rem == half && (n & 1u))) ++n;
-  }
-  int q = qe;
-  if (n == 16u) {                                    // mantissa overflow: next binade
-    n = 8u;
-    ++q;
-  }
-  if (q == -9 && n < 8u) return n;                   // subnormal (includes 0)
-  const int E = q + 10;                              // value = n * 2^q = (1 + (n-8)/8) * 2^(E-7)
-  if (E > 15) return 0x7Eu;
-  const uint32_t code = (static_cast<uint32_t>(E) << 3) | (n - 8u);
-  return code > 0x7Eu ? 0x7Eu : code;
-}
-
-// One thread per 32-element block; 64 bytes read, 32 + 1 bytes written.
-__global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint4* __restrict__ in,
-                                                                     int64_t nblocks, uint4* __restrict__ q,
-                                                                     uint8_t* __restrict__ sc) {
-  pdl_wait();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
-  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; b < nblocks; b += stride) {
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = __ldg(in + b * 4 + i);
-      w[4 * i] = v.x;
-      w[4 * i + 1] = v.y;
-      w[4 * i + 2] = v.z;
-      w[4 * i + 3] = v.w;
-    }
-    uint32_t amax = 0;
-    bool bad = false;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t mag = (i & 1 ? (w[i >> 1] >> 16) : w[i >> 1]) & 0x7FFFu;
-      bad |= mag >= 0x7F80u;
-      amax = mag > amax ? mag : amax;
-    }
-    uint32_t out[8];
-    uint8_t sbyte;
-    if (bad) {
-      sbyte = 0xFF;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) out[i] = 0x7F7F7F7Fu;
-    } else {
-      int shared = amax == 0 ? -127 : bf16_floor_log2(amax) - 8;
-      shared = shared < -127 ? -127 : (shared > 127 ? 127 : shared);
-      sbyte = static_cast<uint8_t>(shared + 127);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) out[i] = 0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t h = (i & 1 ? (w[i >> 1] >> 16) : w[i >> 1]) & 0xFFFFu;
-        const uint32_t c = e4m3_code(h & 0x7FFFu, shared) | ((h >> 8) & 0x80u);
-        out[i >> 2] |= c << (8 * (i & 3));
-      }
-    }
-    q[b * 2] = make_uint4(out[0], out[1], out[2], out[3]);
-    q[b * 2 + 1] = make_uint4(out[4], out[5], out[6], out[7]);
-    sc[b] = sbyte;
-  }
-}
-
-// MX gather, one CTA per (128-row block of the expert-grouped layout, 128 columns), 256 threads.
-// The 128 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
-//   along H: each thread quantises two 32-column blocks of rows -- row-major E4M3 codes for the
-//     forward / data-gradient GEMMs, A-operand atoms;
-//   along the routed rows: each thread quantises two adjacent columns over one 32-row block
-//     (reading both as one 32-bit word per row) -- 32 consecutive bytes per column of the
-//     transposed copy [H, rcap] the weight-gradient GEMM reads K-major, atoms grouped gT at a time.
-// Both passes keep the values as packed bf16 pairs: the block maxima and the power-of-two scaling
-// take one instruction per two values, and only the final E4M3 conversion widens them to fp32.
-// The scale bytes are collected in shared memory and leave as one 32-bit word per row (its four
-// 32-column blocks) and per column (its four 32-row blocks): in both atom layouts these four
-// bytes are adjacent.
-// The rounding is bit-exact with mxfp8_quantize_kernel (shared exponent from amax, E4M3
-// round-to-nearest-even, saturating).  Row blocks never straddle two experts: segments start at
-// multiples of 128.
-constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
-
-// Packed bf16 arithmetic for the quantising gather: two values per 32-bit word, one instruction each.
+// Packed bf16 arithmetic: two values per 32-bit word, one instruction each.
 // absmax: per 16-bit half the larger magnitude, NaN if either operand is NaN; the sign bits of the
 // result (the XOR of the operands') mean nothing and are masked off at the end.
 __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
@@ -484,6 +373,43 @@ __device__ __forceinline__ uint32_t gmx_quant_row(uint32_t (&w)[16], uint32_t (&
   for (int i = 0; i < 8; ++i) codes[i] = e4m3x2_of_bf16x2(w[2 * i]) | (e4m3x2_of_bf16x2(w[2 * i + 1]) << 16);
   return static_cast<uint32_t>(shared + 127);
 }
+
+// One thread per 32-element block; 64 bytes read, 32 + 1 bytes written.
+__global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint4* __restrict__ in,
+                                                                     int64_t nblocks, uint4* __restrict__ q,
+                                                                     uint8_t* __restrict__ sc) {
+  pdl_wait();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kMoveThreads;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * kMoveThreads + threadIdx.x; b < nblocks; b += stride) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(in + b * 4 + i);
+      w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+    }
+    uint32_t codes[8];
+    sc[b] = static_cast<uint8_t>(gmx_quant_row(w, codes));
+    __stcs(q + b * 2, make_uint4(codes[0], codes[1], codes[2], codes[3]));
+    __stcs(q + b * 2 + 1, make_uint4(codes[4], codes[5], codes[6], codes[7]));
+  }
+}
+
+// MX gather, one CTA per (128-row block of the expert-grouped layout, 128 columns), 256 threads.
+// The 128 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
+//   along H: each thread quantises two 32-column blocks of rows -- row-major E4M3 codes for the
+//     forward / data-gradient GEMMs, A-operand atoms;
+//   along the routed rows: each thread quantises two adjacent columns over one 32-row block
+//     (reading both as one 32-bit word per row) -- 32 consecutive bytes per column of the
+//     transposed copy [H, rcap] the weight-gradient GEMM reads K-major, atoms grouped gT at a time.
+// Both passes keep the values as packed bf16 pairs: the block maxima and the power-of-two scaling
+// take one instruction per two values, and only the final E4M3 conversion widens them to fp32.
+// The scale bytes are collected in shared memory and leave as one 32-bit word per row (its four
+// 32-column blocks) and per column (its four 32-row blocks): in both atom layouts these four
+// bytes are adjacent.
+// The rounding is bit-exact with mxfp8_quantize_kernel (shared exponent from amax, E4M3
+// round-to-nearest-even, saturating).  Row blocks never straddle two experts: segments start at
+// multiples of 128.
+constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
 
 // Five CTAs per SM (48 registers or fewer, no spills).
 __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src,
