@@ -141,8 +141,8 @@ struct GemmCfg {
   static constexpr uint32_t kStagingBytes = kEpiWarps * kStageBufs * kStageBufBytes;
   static constexpr uint32_t kSfRing = static_cast<uint32_t>(kStages) * kStageBytes;  // offset of the atom ring
   static constexpr uint32_t kStagingOff = kSfRing + static_cast<uint32_t>(kStages) * kSfBytes;
-  // MXFP8 dgrad1: a 32 x 33 fp32 transpose scratch per epilogue warp (quantisation along the rows)
-  static constexpr uint32_t kScratchWarp = 32u * 33u * 4u;
+  // MXFP8 dgrad1: a 32 x 36 fp32 transpose scratch per epilogue warp (quantisation along the rows)
+  static constexpr uint32_t kScratchWarp = 32u * 36u * 4u;
   static constexpr uint32_t kScratchBytes = kDg1Mx ? kEpiWarps * kScratchWarp : 0u;
   static constexpr uint32_t kScratchOff = kStagingOff + kStagingBytes;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(kScratchOff) + kScratchBytes + 512;
@@ -479,8 +479,9 @@ __device__ __forceinline__ void dgrad1_fetch(const GemmArgs& a, const Unit& w, i
 }
 
 // MX quantisation of one 32 x 32 block along the rows: lane = row, v[j] = column j (feature f0 + j).
-// The block is transposed through the warp's fp32 scratch (element (r, c) at r * 33 + c: both the
-// row writes and the column reads are free of bank conflicts, and every address is a per-lane base
+// The block is transposed through the warp's fp32 scratch (element (r, c) at r * 36 + c: each lane
+// writes its row with eight 16-byte stores, the 8 lanes of a quarter warp in 8 different bank
+// groups; the column reads of the 32 lanes hit 32 different banks; every address is a per-lane base
 // plus a constant, so no table of addresses stays live), lane j then quantises column j
 // over the 32 rows as one MX block, and its 32 codes leave as row j of a byte tile stored at
 // (row rowc, feature f0) of the transposed [features, rows] copy; lane j writes column j's scale
@@ -489,17 +490,20 @@ template <class Stg>
 __device__ __forceinline__ void quant_rows_store(const float (&v)[32], uint32_t scratch, Stg& stg,
                                                  const CUtensorMap* tm, uint8_t* sf, int rowc, int f0, int kq, int gl,
                                                  int lane) {
-  const uint32_t row = scratch + static_cast<uint32_t>(lane) * 132;
+  const uint32_t row = scratch + static_cast<uint32_t>(lane) * 144;
 #pragma unroll
-  for (int c = 0; c < 32; ++c) asm volatile("st.shared.f32 [%0], %1;" ::"r"(row + 4u * c), "f"(v[c]) : "memory");
+  for (int c = 0; c < 32; c += 4)
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(row + 4u * c), "f"(v[c]), "f"(v[c + 1]),
+                 "f"(v[c + 2]), "f"(v[c + 3])
+                 : "memory");
   __syncwarp();
   float col[32];
   const uint32_t colp = scratch + static_cast<uint32_t>(lane) * 4;
 #pragma unroll
-  for (int r = 0; r < 32; ++r) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(col[r]) : "r"(colp + 132u * r) : "memory");
+  for (int r = 0; r < 32; ++r) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(col[r]) : "r"(colp + 144u * r) : "memory");
   __syncwarp();
   uint32_t codes[8];
-  const uint32_t sb = mx_quant32(col, codes);
+  const uint32_t sb = mx_quant32<false>(col, codes);
   const uint4 ch[2] = {make_uint4(codes[0], codes[1], codes[2], codes[3]),
                        make_uint4(codes[4], codes[5], codes[6], codes[7])};
   stg.template put<32>(ch, tm, rowc, f0, true);  // read by the weight gradients, after the next GEMM
@@ -642,13 +646,18 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
           u[4 * j] = y.x, u[4 * j + 1] = y.y, u[4 * j + 2] = y.z, u[4 * j + 3] = y.w;
         }
       }
+      // the products below run two lanes of fp32 per instruction (mul / fma .f32x2)
       float sg[32];
       {
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sg[i] = sigmoid_f(g[i]);
-          v[i] = s * (g[i] * sg[i] * u[i]);
+        for (int i = 0; i < 32; ++i) sg[i] = sigmoid_f(g[i]);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {  // s * (g * sigmoid(g) * u)
+          float t0, t1;
+          mul_f32x2(t0, t1, g[i], g[i + 1], sg[i], sg[i + 1]);
+          mul_f32x2(t0, t1, t0, t1, u[i], u[i + 1]);
+          mul_f32x2(v[i], v[i + 1], s, s, t0, t1);
         }
         quant_rows_store(v, scratch, stg, tO1, a.out_sf3, rowc, i0 + c, a.sf_kq, sa_gl, lane);
       }
@@ -665,23 +674,28 @@ __device__ __forceinline__ void gemm_epilogue(const GemmArgs& a, const Unit& w, 
           for (int k = 0; k < 8; ++k) part = fmaf(__uint_as_float(rv[8 * j + k]), a8[k], part);
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float da = s * __uint_as_float(rv[i]);
-          const float dg = da * u[i] * sg[i] * (1.0f + g[i] * (1.0f - sg[i]));
-          g[i] = da * g[i] * sg[i];  // du
-          u[i] = dg;
+        for (int i = 0; i < 32; i += 2) {
+          // da = s dA'; x = da sigmoid(g); du = x g; dg = x u (1 + g (1 - sigmoid(g)))
+          float da0, da1, x0, x1, w0, w1, y0, y1;
+          mul_f32x2(da0, da1, s, s, __uint_as_float(rv[i]), __uint_as_float(rv[i + 1]));
+          mul_f32x2(x0, x1, da0, da1, sg[i], sg[i + 1]);
+          fma_f32x2(w0, w1, sg[i], sg[i + 1], -1.0f, -1.0f, 1.0f, 1.0f);
+          fma_f32x2(w0, w1, g[i], g[i + 1], w0, w1, 1.0f, 1.0f);
+          mul_f32x2(y0, y1, x0, x1, u[i], u[i + 1]);
+          mul_f32x2(g[i], g[i + 1], x0, x1, g[i], g[i + 1]);  // du
+          mul_f32x2(u[i], u[i + 1], y0, y1, w0, w1);          // dg
         }
       }
       uint4 ch[2];
       uint32_t codes[8];
       quant_rows_store(u, scratch, stg, tO0, a.out_sf2, rowc, i0 + c, a.sf_kq, 0, lane);
-      uint32_t sb = mx_quant32(u, codes);
+      uint32_t sb = mx_quant32<false>(u, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
       stg.template put<32>(ch, tO2, i0 + c, rowc);
       a.out_sf[sf_atom_offset(row, (i0 + c) >> 5, a.out_kq)] = static_cast<uint8_t>(sb);
       quant_rows_store(g, scratch, stg, tO0, a.out_sf2, rowc, a.I + i0 + c, a.sf_kq, 0, lane);
-      sb = mx_quant32(g, codes);
+      sb = mx_quant32<false>(g, codes);
       ch[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
       ch[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
       stg.template put<32>(ch, tO2, a.I + i0 + c, rowc);

@@ -396,75 +396,94 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 // ------------------------------------------------------------------------------------------------
 // MXFP8 helpers (OCP MX: E4M3 elements, one E8M0 scale per 32 values)
 // ------------------------------------------------------------------------------------------------
-// Two fp32 values -> E4M3 (round to nearest even, saturating to +-448) -> back to fp32, exactly.
-__device__ __forceinline__ void e4m3x2_round_trip(float& hi, float& lo) {
-  uint16_t q;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(hi), "f"(lo));
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q));
-  hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
-  lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
-}
-
 // 2^e exactly, for e in [-149, 127] (subnormal below -126).
 __device__ __forceinline__ float pow2f(int e) {
   return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(1 << (e + 149));
 }
 
-// Quantise-dequantise 2n values of one MX block with shared exponent `shared` (in [-127, 127]):
-// E4M3(v * 2^-shared) * 2^shared, exact scalings, hardware round-to-nearest-even with saturation.
-__device__ __forceinline__ void mx_qdq_pairs(float* v, int n2, int shared) {
-  const float dn = pow2f(-shared), up = pow2f(shared);
+// Larger magnitude of two fp32 values, NaN if either is NaN (one instruction); the sign of the
+// result is the XOR of the operands' and means nothing here.
+__device__ __forceinline__ float fmax_abs_nan(float a, float b) {
+  float d;
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+// Bits of max |v[i]| over 32 values (a pairwise tree): above 0x7F7FFFFF means an Inf or a NaN.
+__device__ __forceinline__ uint32_t absmax32_bits(const float* v) {
+  float m[16];
 #pragma unroll
-  for (int i = 0; i < n2; i += 2) {
-    float hi = v[i] * dn, lo = v[i + 1] * dn;
-    e4m3x2_round_trip(hi, lo);
-    v[i] = hi * up;
-    v[i + 1] = lo * up;
+  for (int i = 0; i < 16; ++i) m[i] = fmax_abs_nan(v[i], v[i + 16]);
+#pragma unroll
+  for (int s = 8; s >= 1; s >>= 1) {
+#pragma unroll
+    for (int i = 0; i < s; ++i) m[i] = fmax_abs_nan(m[i], m[i + s]);
   }
+  return __float_as_uint(m[0]) & 0x7FFFFFFFu;
+}
+// Two fp32 products in one instruction, each rounded as a single fp32 multiply.
+__device__ __forceinline__ void fmul2(float& a, float& b, uint64_t s2) {
+  asm("{\n\t.reg .b64 x;\n\tmov.b64 x, {%0, %1};\n\tmul.rn.f32x2 x, x, %2;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "l"(s2));
+}
+// (d0, d1) = (a0 * b0, a1 * b1) and (a0 * b0 + c0, a1 * b1 + c1) in one instruction each; every
+// lane is rounded exactly as the scalar fp32 multiply or fused multiply-add.
+__device__ __forceinline__ void mul_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmul.rn.f32x2 x, x, y;"
+      "\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                          float c1) {
+  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};"
+      "\n\tfma.rn.f32x2 x, x, y, z;\n\tmov.b64 {%0, %1}, x;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ uint64_t f32x2_splat(float s) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+  return r;
 }
 
-// MX quantise-dequantise of 32 fp32 values in place: shared = floor(log2 amax) - 8 clamped at
-// -127 (amax 0 or subnormal), elements E4M3(v / 2^shared) * 2^shared.
-__device__ __forceinline__ void mx_fakequant32(float* v) {
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  int shared = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
-  shared = shared < -127 ? -127 : shared;
-  mx_qdq_pairs(v, 32, shared);
-}
-
-// MX quantisation of 32 fp32 values (one block): returns the E8M0 scale byte, writes the E4M3 codes
-// (byte i of the 32 = element i) and replaces v by the dequantised values.  A block holding a NaN
-// or an infinity gets scale 0xFF and codes 0x7F (NaN), as the OCP MX format prescribes.
+// MX quantisation of 32 fp32 values (one block): returns the E8M0 scale byte and writes the E4M3
+// codes (byte i of the 32 = element i); with DEQ, v is replaced by the dequantised values.  shared
+// = floor(log2 amax) - 8 (8 = the exponent of E4M3's largest normal), clamped below at -127 (amax 0
+// or subnormal); codes = E4M3(v * 2^-shared), round to nearest even, saturating (the scaling by a
+// power of two is exact in fp32).  A block holding a NaN or an infinity gets scale 0xFF and codes
+// 0x7F (NaN), as the OCP MX format prescribes.
+template <bool DEQ = true>
 __device__ __forceinline__ uint32_t mx_quant32(float* v, uint32_t (&codes)[8]) {
-  float amax = 0.0f;
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float a = fabsf(v[i]);
-    bad |= !(a <= 3.402823466e38f);
-    amax = fmaxf(amax, a);
-  }
-  if (bad) {
+  const uint32_t amax = absmax32_bits(v);
+  if (amax > 0x7F7FFFFFu) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) codes[i] = 0x7F7F7F7Fu;
+    if constexpr (DEQ) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __int_as_float(0x7FC00000);
+      for (int i = 0; i < 32; ++i) v[i] = __int_as_float(0x7FC00000);
+    }
     return 0xFFu;
   }
-  int shared = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 8;
+  int shared = static_cast<int>(amax >> 23) - 127 - 8;
   shared = shared < -127 ? -127 : shared;
-  const float dn = pow2f(-shared), up = pow2f(shared);
+  const uint64_t dn2 = f32x2_splat(pow2f(-shared));
+  const uint64_t up2 = f32x2_splat(pow2f(shared));
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
+    float lo = v[2 * i], hi = v[2 * i + 1];
+    fmul2(lo, hi, dn2);
     uint16_t q;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(v[2 * i + 1] * dn), "f"(v[2 * i] * dn));
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q));
-    v[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))) * up;
-    v[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))) * up;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q) : "f"(hi), "f"(lo));
+    if constexpr (DEQ) {
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q));
+      lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+      hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+      fmul2(lo, hi, up2);
+      v[2 * i] = lo;
+      v[2 * i + 1] = hi;
+    }
     if (i & 1) codes[i >> 1] |= static_cast<uint32_t>(q) << 16;
     else codes[i >> 1] = q;
   }
