@@ -483,6 +483,29 @@ def time_router(args, mok, w, d, cfg, dev, stream, peaks) -> dict:
     return res
 
 
+def time_schedule_in_graph(mok, layer, ids, s, stream, step_ms, n=20, reps=10) -> dict:
+    """The schedule's cost as it runs inside the step's graph: one CUDA graph of n back-to-back
+    mok_build_schedule calls on the step's routing (three dependent launches each), replayed reps
+    times; per build, against the graph-replayed step (the pages' budget: under 3 %)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n):
+            layer.schedule(ids, s, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (reps * n)
+    return {"ms_per_build": ms, "share_of_step": ms / step_ms,
+            "how": f"graph of {n} builds in a row, {reps} replays"}
+
+
 def time_quantize(args, mok, Wg, Wu, Wd, stream, peaks) -> dict:
     """mok_mxfp8_quantize on the forward weight copies (Wg, Wu along H; Wd along I), the call a
     training loop makes after each optimiser step: CUDA events around K sets of the three calls
@@ -589,6 +612,8 @@ def ours(args, rank, ws, local_rank, name, with_router=True):
                  "eager_ms_per_step": eager_ms, "eager_value": aggregate_tokens_per_s(w.T, ws, eager_ms)}
     if graph_error:
         step_mode["graph_error"] = graph_error
+    if graph is not None:
+        step_mode["schedule"] = time_schedule_in_graph(mok, layer, ids, s, stream, ms_max)
 
     # ---- per-kernel times: the same K steps with the library's event trace ----
     tr = mok.Tracer(capacity=20 * args.steps + 64)
