@@ -394,8 +394,8 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
   }
 }
 
-// MX gather, one CTA per (128-row block of the expert-grouped layout, 128 columns), 256 threads.
-// The 128 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
+// MX gather, one CTA per (64-row block of the expert-grouped layout, 128 columns), 128 threads.
+// The 64 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
 //   along H: each thread quantises two 32-column blocks of rows -- row-major E4M3 codes for the
 //     forward / data-gradient GEMMs, A-operand atoms;
 //   along the routed rows: each thread quantises two adjacent columns over one 32-row block
@@ -404,47 +404,50 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
 // Both passes keep the values as packed bf16 pairs: the block maxima and the power-of-two scaling
 // take one instruction per two values, and only the final E4M3 conversion widens them to fp32.
 // The scale bytes are collected in shared memory and leave as one 32-bit word per row (its four
-// 32-column blocks) and per column (its four 32-row blocks): in both atom layouts these four
-// bytes are adjacent.
+// 32-column blocks) and one 16-bit half word per column (its two 32-row blocks): in both atom
+// layouts a row's or a column's four bytes are adjacent.  Half-height blocks (measured against
+// 128 rows and 256 threads: 0.220 -> 0.210 ms per gather on sweep_zipf1_mx) put ten CTAs on an SM,
+// so more of them are between their row loads and their quantisation at any time.
 // The rounding is bit-exact with mxfp8_quantize_kernel (shared exponent from amax, E4M3
 // round-to-nearest-even, saturating).  Row blocks never straddle two experts: segments start at
 // multiples of 128.
 constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
 
-// Five CTAs per SM (48 registers or fewer, no spills).
-__global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src,
+// 64-row blocks, 128 threads, ten CTAs per SM (48 registers, no spills).
+constexpr int kGmxRows = 64;
+__global__ void __launch_bounds__(128, 10) gather_rows_mx_kernel(const RowSrc src,
                                                             const int32_t* __restrict__ row_token,
                                                             const int32_t* __restrict__ meta, int32_t H,
                                                             uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf,
                                                             uint8_t* __restrict__ dstR_q,
                                                             uint8_t* __restrict__ dstR_sf, int64_t rcap, int gT) {
   pdl_wait();
-  __shared__ __align__(16) uint8_t tile[128 * kGmxStride];
-  __shared__ __align__(4) uint8_t sc_row[128 * 4];  // [row][32-column block]
-  __shared__ __align__(4) uint8_t sc_col[128 * 4];  // [column][32-row block]
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+  __shared__ __align__(16) uint8_t tile[kGmxRows * kGmxStride];
+  __shared__ __align__(4) uint8_t sc_row[kGmxRows * 4];  // [row][32-column block]
+  __shared__ __align__(4) uint8_t sc_col[128 * 2];       // [column][32-row block]
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kGmxRows;
   if (r0 >= meta[0]) return;
   const int c0 = static_cast<int>(blockIdx.x) * 128;
   const int t = threadIdx.x;
   {
     uint4 val[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 16 i
-      const int r = t / 16 + 16 * i;
+    for (int i = 0; i < 8; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 8 i
+      const int r = t / 16 + 8 * i;
       const int tok = __ldg(row_token + r0 + r);
       val[i] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(token_row(src, tok, H) + c0) + t % 16)
                         : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<uint4*>(tile + (t / 16 + 16 * i) * kGmxStride + (t % 16) * 16) = val[i];
+      *reinterpret_cast<uint4*>(tile + (t / 16 + 8 * i) * kGmxStride + (t % 16) * 16) = val[i];
   }
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     // along H: a warp takes 8 rows x the 4 blocks of 32 columns, the 8 lanes of a quarter warp 8
     // rows of one block (their 16-byte reads fall in 8 different bank groups)
-    const int it = t + 256 * k, r = 8 * (it >> 5) + (it & 7), b = (it & 31) >> 3;
+    const int it = t + 128 * k, r = 8 * (it >> 5) + (it & 7), b = (it & 31) >> 3;
     uint32_t wr[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -480,21 +483,19 @@ __global__ void __launch_bounds__(256, 5) gather_rows_mx_kernel(const RowSrc src
                               : e4m3x2_of_halves<0>(w2[4 * i + 2], w2[4 * i + 3]);
         codes[i] = bad ? 0x7F7F7F7Fu : lo | (hi << 16);
       }
-      sc_col[4 * (2 * cp + j) + rb] = static_cast<uint8_t>(bad ? 0xFFu : (j ? s1 : s0) + 127);
+      sc_col[2 * (2 * cp + j) + rb] = static_cast<uint8_t>(bad ? 0xFFu : (j ? s1 : s0) + 127);
       st_cs_32B(dstR_q + static_cast<int64_t>(c0 + 2 * cp + j) * rcap + r0 + 32 * rb, codes);
     }
   }
   __syncthreads();
-  // k-groups c0 / 32 ... + 3 of row r0 + t, and row groups r0 / 32 ... + 3 of column c0 + t - 128:
-  // both start at a multiple of 4 (c0 and r0 are multiples of 128), so each word is aligned
-  if (t < 128) {
+  // k-groups c0 / 32 ... + 3 of row r0 + t (t < 64: a 32-bit word); row groups r0 / 32 and the next
+  // of column c0 + t (two adjacent bytes of the column's word: r0 / 32 is even)
+  if (t < kGmxRows) {
     *reinterpret_cast<uint32_t*>(dst_sf + sf_atom_offset(r0 + t, c0 >> 5, H / 128)) =
         *reinterpret_cast<const uint32_t*>(sc_row + 4 * t);
-  } else {
-    const int c = t - 128;
-    *reinterpret_cast<uint32_t*>(dstR_sf + sf_atom_offset_g(c0 + c, r0 >> 5, rcap / 128, gT)) =
-        *reinterpret_cast<const uint32_t*>(sc_col + 4 * c);
   }
+  *reinterpret_cast<uint16_t*>(dstR_sf + sf_atom_offset_g(c0 + t, r0 >> 5, rcap / 128, gT)) =
+      *reinterpret_cast<const uint16_t*>(sc_col + 2 * t);
 }
 
 // Scale atoms.  One block per 128-row slab of a source scale matrix (group g, atom j of the group):
@@ -564,10 +565,10 @@ int launch_gather_rows_mx(const RowSrc& src, const int32_t* row_token, const int
   if (rpad_max <= 0) return 0;
   // column tiles fastest: blocks running together read whole source rows, not 256-byte pieces of
   // 128 scattered rows
-  if ((rpad_max + 127) / 128 > 65535) return static_cast<int>(cudaErrorInvalidValue);
-  const dim3 grid(static_cast<unsigned>(H / 128), static_cast<unsigned>((rpad_max + 127) / 128));
+  if ((rpad_max + kGmxRows - 1) / kGmxRows > 65535) return static_cast<int>(cudaErrorInvalidValue);
+  const dim3 grid(static_cast<unsigned>(H / 128), static_cast<unsigned>((rpad_max + kGmxRows - 1) / kGmxRows));
   trace_begin(stream, kind);
-  launch_pdl(gather_rows_mx_kernel, dim3(grid), dim3(256), 0, stream, src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
+  launch_pdl(gather_rows_mx_kernel, dim3(grid), dim3(128), 0, stream, src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
