@@ -394,28 +394,28 @@ __global__ void __launch_bounds__(kMoveThreads) mxfp8_quantize_kernel(const uint
   }
 }
 
-// MX gather, one CTA per (64-row block of the expert-grouped layout, 128 columns), 128 threads.
-// The 64 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
+// MX gather, one CTA per (32-row block of the expert-grouped layout, 128 columns), 64 threads.
+// The 32 gathered rows are staged in shared memory as bf16 (zero for padding rows); then
 //   along H: each thread quantises two 32-column blocks of rows -- row-major E4M3 codes for the
 //     forward / data-gradient GEMMs, A-operand atoms;
-//   along the routed rows: each thread quantises two adjacent columns over one 32-row block
+//   along the routed rows: each thread quantises two adjacent columns over the 32-row block
 //     (reading both as one 32-bit word per row) -- 32 consecutive bytes per column of the
 //     transposed copy [H, rcap] the weight-gradient GEMM reads K-major, atoms grouped gT at a time.
 // Both passes keep the values as packed bf16 pairs: the block maxima and the power-of-two scaling
 // take one instruction per two values, and only the final E4M3 conversion widens them to fp32.
 // The scale bytes are collected in shared memory and leave as one 32-bit word per row (its four
-// 32-column blocks) and one 16-bit half word per column (its two 32-row blocks): in both atom
-// layouts a row's or a column's four bytes are adjacent.  Half-height blocks (measured against
-// 128 rows and 256 threads: 0.220 -> 0.210 ms per gather on sweep_zipf1_mx) put ten CTAs on an SM,
-// so more of them are between their row loads and their quantisation at any time.
+// 32-column blocks) and one byte per column (its 32-row block).  Small blocks put twenty CTAs on
+// an SM, so more of them are between their row loads and their quantisation at any time
+// (measured per gather on sweep_zipf1_mx: 128 rows and 256 threads 0.220 ms, 64 rows 0.210, 32
+// rows 0.205).
 // The rounding is bit-exact with mxfp8_quantize_kernel (shared exponent from amax, E4M3
 // round-to-nearest-even, saturating).  Row blocks never straddle two experts: segments start at
 // multiples of 128.
 constexpr int kGmxStride = 128 * 2 + 16;  // bytes per staged bf16 row (the pad spreads banks)
 
-// 64-row blocks, 128 threads, ten CTAs per SM (48 registers, no spills).
-constexpr int kGmxRows = 64;
-__global__ void __launch_bounds__(128, 10) gather_rows_mx_kernel(const RowSrc src,
+// 32-row blocks, 64 threads, twenty CTAs per SM (48 registers, no spills).
+constexpr int kGmxRows = 32;
+__global__ void __launch_bounds__(64, 20) gather_rows_mx_kernel(const RowSrc src,
                                                             const int32_t* __restrict__ row_token,
                                                             const int32_t* __restrict__ meta, int32_t H,
                                                             uint8_t* __restrict__ dst_q, uint8_t* __restrict__ dst_sf,
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(128, 10) gather_rows_mx_kernel(const RowSrc sr
   pdl_wait();
   __shared__ __align__(16) uint8_t tile[kGmxRows * kGmxStride];
   __shared__ __align__(4) uint8_t sc_row[kGmxRows * 4];  // [row][32-column block]
-  __shared__ __align__(4) uint8_t sc_col[128 * 2];       // [column][32-row block]
+  __shared__ __align__(4) uint8_t sc_col[128];           // [column]
   const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kGmxRows;
   if (r0 >= meta[0]) return;
   const int c0 = static_cast<int>(blockIdx.x) * 128;
@@ -432,22 +432,22 @@ __global__ void __launch_bounds__(128, 10) gather_rows_mx_kernel(const RowSrc sr
   {
     uint4 val[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 8 i
-      const int r = t / 16 + 8 * i;
+    for (int i = 0; i < 8; ++i) {  // thread t: 16-byte vector t % 16 of rows t / 16 + 4 i
+      const int r = t / 16 + 4 * i;
       const int tok = __ldg(row_token + r0 + r);
       val[i] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(token_row(src, tok, H) + c0) + t % 16)
                         : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      *reinterpret_cast<uint4*>(tile + (t / 16 + 8 * i) * kGmxStride + (t % 16) * 16) = val[i];
+      *reinterpret_cast<uint4*>(tile + (t / 16 + 4 * i) * kGmxStride + (t % 16) * 16) = val[i];
   }
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     // along H: a warp takes 8 rows x the 4 blocks of 32 columns, the 8 lanes of a quarter warp 8
     // rows of one block (their 16-byte reads fall in 8 different bank groups)
-    const int it = t + 128 * k, r = 8 * (it >> 5) + (it & 7), b = (it & 31) >> 3;
+    const int it = t + 64 * k, r = 8 * (it >> 5) + (it & 7), b = (it & 31) >> 3;
     uint32_t wr[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(128, 10) gather_rows_mx_kernel(const RowSrc sr
   }
   {  // along the rows: columns c0 + 2 (t % 64) and the next one (the low and high halves of each
      // staged word), row block t / 64; both columns' maxima and scaling share the packed words
-    const int cp = t % 64, rb = t / 64;
+    const int cp = t, rb = 0;
     uint32_t w2[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r)
@@ -483,19 +483,19 @@ __global__ void __launch_bounds__(128, 10) gather_rows_mx_kernel(const RowSrc sr
                               : e4m3x2_of_halves<0>(w2[4 * i + 2], w2[4 * i + 3]);
         codes[i] = bad ? 0x7F7F7F7Fu : lo | (hi << 16);
       }
-      sc_col[2 * (2 * cp + j) + rb] = static_cast<uint8_t>(bad ? 0xFFu : (j ? s1 : s0) + 127);
+      sc_col[2 * cp + j] = static_cast<uint8_t>(bad ? 0xFFu : (j ? s1 : s0) + 127);
       st_cs_32B(dstR_q + static_cast<int64_t>(c0 + 2 * cp + j) * rcap + r0 + 32 * rb, codes);
     }
   }
   __syncthreads();
-  // k-groups c0 / 32 ... + 3 of row r0 + t (t < 64: a 32-bit word); row groups r0 / 32 and the next
-  // of column c0 + t (two adjacent bytes of the column's word: r0 / 32 is even)
+  // k-groups c0 / 32 ... + 3 of row r0 + t (t < 32: a 32-bit word); row group r0 / 32 of columns
+  // c0 + t and c0 + 64 + t (one byte each)
   if (t < kGmxRows) {
     *reinterpret_cast<uint32_t*>(dst_sf + sf_atom_offset(r0 + t, c0 >> 5, H / 128)) =
         *reinterpret_cast<const uint32_t*>(sc_row + 4 * t);
   }
-  *reinterpret_cast<uint16_t*>(dstR_sf + sf_atom_offset_g(c0 + t, r0 >> 5, rcap / 128, gT)) =
-      *reinterpret_cast<const uint16_t*>(sc_col + 2 * t);
+  dstR_sf[sf_atom_offset_g(c0 + t, r0 >> 5, rcap / 128, gT)] = sc_col[t];
+  dstR_sf[sf_atom_offset_g(c0 + 64 + t, r0 >> 5, rcap / 128, gT)] = sc_col[64 + t];
 }
 
 // Scale atoms.  One block per 128-row slab of a source scale matrix (group g, atom j of the group):
@@ -568,7 +568,7 @@ int launch_gather_rows_mx(const RowSrc& src, const int32_t* row_token, const int
   if ((rpad_max + kGmxRows - 1) / kGmxRows > 65535) return static_cast<int>(cudaErrorInvalidValue);
   const dim3 grid(static_cast<unsigned>(H / 128), static_cast<unsigned>((rpad_max + kGmxRows - 1) / kGmxRows));
   trace_begin(stream, kind);
-  launch_pdl(gather_rows_mx_kernel, dim3(grid), dim3(128), 0, stream, src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
+  launch_pdl(gather_rows_mx_kernel, dim3(grid), dim3(64), 0, stream, src, row_token, meta, H, dst_q, dst_sf, dstR_q, dstR_sf, rcap, gT);
   trace_end(stream);
   return static_cast<int>(cudaGetLastError());
 }
