@@ -346,10 +346,15 @@ __device__ __forceinline__ uint32_t e4m3x2_of_halves(uint32_t w0, uint32_t w1) {
         "f"(__uint_as_float(w0 & 0xFFFF0000u)));
   return q;
 }
-// 32 bytes to global memory in one instruction, streaming (p 32-byte aligned).
-__device__ __forceinline__ void st_cs_32B(void* p, const uint32_t (&c)[8]) {
-  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(c[0]), "r"(c[1]),
-               "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(c[5]), "r"(c[6]), "r"(c[7])
+// 32 bytes to global memory in one instruction (p 32-byte aligned), with an L2 evict-first policy:
+// the codes are read by later kernels from DRAM anyway, and the gathered x rows (read K times)
+// should be the lines L2 keeps.  Measured against plain streaming stores (.cs): 0.205 -> 0.202 ms
+// per gather on sweep_zipf1_mx.
+__device__ __forceinline__ void st_ef_32B(void* p, const uint32_t (&c)[8]) {
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(c[0]),
+               "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(c[5]), "r"(c[6]), "r"(c[7]), "l"(pol)
                : "memory");
 }
 
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(64, 20) gather_rows_mx_kernel(const RowSrc src
     }
     uint32_t codes[8];
     sc_row[4 * r + b] = static_cast<uint8_t>(gmx_quant_row(wr, codes));
-    st_cs_32B(dst_q + (r0 + r) * H + c0 + 32 * b, codes);
+    st_ef_32B(dst_q + (r0 + r) * H + c0 + 32 * b, codes);
   }
   {  // along the rows: columns c0 + 2 (t % 64) and the next one (the low and high halves of each
      // staged word), row block t / 64; both columns' maxima and scaling share the packed words
@@ -484,7 +489,7 @@ __global__ void __launch_bounds__(64, 20) gather_rows_mx_kernel(const RowSrc src
         codes[i] = bad ? 0x7F7F7F7Fu : lo | (hi << 16);
       }
       sc_col[2 * cp + j] = static_cast<uint8_t>(bad ? 0xFFu : (j ? s1 : s0) + 127);
-      st_cs_32B(dstR_q + static_cast<int64_t>(c0 + 2 * cp + j) * rcap + r0 + 32 * rb, codes);
+      st_ef_32B(dstR_q + static_cast<int64_t>(c0 + 2 * cp + j) * rcap + r0 + 32 * rb, codes);
     }
   }
   __syncthreads();
